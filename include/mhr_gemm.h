@@ -1,0 +1,122 @@
+/*
+ * mhr_gemm.h -- C ABI of the GB300 (sm_103a) dense matrix-multiply library
+ * libmhr_gemm.so.
+ *
+ * Operation (every gemm_* entry point):
+ *
+ *     C[i*ldc + j] = sum over k < K of A[i*lda + k] * B[k*ldb + j]
+ *     for 0 <= i < M, 0 <= j < N
+ *
+ * This is the product the pages compute -- "矩阵乘法 tiling:把分块搬进 shared
+ * memory,让 GFLOPS 翻百倍", sections 一 and 二 (C = A x B, row-major floats,
+ * each output tile built from a row strip of A and a column strip of B);
+ * "CUDA 深入浅出（二）：为什么分块可以减少 Global Memory 访问", section
+ * "naive kernel 怎么读数据" -- generalised from N x N to M x N x K with leading
+ * dimensions.  As on the pages, K-tiles of A and B are staged on chip so that
+ * each element read from HBM is reused across a whole output tile.
+ *
+ * Layout: all three matrices are row-major.  lda >= K, ldb >= N, ldc >= N
+ * (elements, not bytes).  C is overwritten (no accumulation into prior
+ * contents).  Elements of C outside the logical M x N block (the ld padding)
+ * are never written.  K == 0 writes zeros to C (the empty sum); M == 0 or
+ * N == 0 is a no-op.  Sizes that are not tile multiples are handled: inputs
+ * outside the matrix count as zero, outputs outside it are not written
+ * ("矩阵乘法 tiling", section 六; "CUDA 编程系列之三", section 7).
+ *
+ * Pointers: A, B and C are DEVICE pointers on the current CUDA device.  The
+ * caller owns them; the library never frees or retains them.  C must not
+ * overlap A or B (rejected with MHR_ERR_INVALID_ARG).
+ *
+ * Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ * default stream).  Calls enqueue their work on it and return without
+ * waiting.  A launch-time failure is returned at once; a device-side failure
+ * (a bounded wait that ran out) is recorded in a per-device status word that
+ * gemm_check() reads.
+ *
+ * Scratch: gemm_f32_3xtf32 (always) and gemm_bf16_f32acc (only when an
+ * operand's address or leading dimension is not 16-byte aligned) need a
+ * device workspace.  The library owns it: one buffer per (device, stream),
+ * grown with cudaMalloc on demand and kept until gemm_release().
+ *
+ * Errors: every entry point returns an int status (mhr_status below); none
+ * throws, none traps on the device.  Thread safety: calls from several host
+ * threads are serialised on an internal lock.
+ */
+#ifndef MHR_GEMM_H
+#define MHR_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mhr_status {
+  MHR_OK = 0,
+  MHR_ERR_INVALID_ARG = 1, /* NULL pointer with nonzero size, negative size,
+                              ld too small, size overflow, C overlapping A/B */
+  MHR_ERR_UNSUPPORTED = 2, /* current device is not sm_103 (GB300) */
+  MHR_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (launch,
+                              allocation, tensor-map encode) */
+  MHR_ERR_TIMEOUT = 4      /* a device-side bounded wait ran out; the kernel
+                              stopped early and C is not valid */
+} mhr_status;
+
+/*
+ * Strict-FP32 path: a register-tiled SIMT kernel (fp32 FMA, fp32
+ * accumulation).  128 x 128 output tile per block, K staged through a
+ * double-buffered shared-memory ring, each thread accumulating an 8 x 8
+ * register block ("矩阵乘法 tiling", sections 四 and 五: thread coarsening,
+ * accumulator in registers; "CUDA 编程系列之三", section 6: register tiling).
+ * Any alignment and any leading dimension are accepted.
+ */
+int gemm_f32(const float* A, const float* B, float* C, int64_t M, int64_t N, int64_t K,
+             int64_t lda, int64_t ldb, int64_t ldc, void* stream);
+
+/*
+ * FP32-accurate path on the tensor cores: each operand is split as
+ * x = big + small with big = tf32(x) and small = tf32(x - big) (round to
+ * nearest even), and C accumulates small*big + big*small + big*big with
+ * tcgen05.mma kind::tf32 into a TMEM accumulator (the small*small term is
+ * dropped).  A split pre-pass writes the four tf32 operands into the
+ * library's workspace (B transposed to K-major), then a TMA + mbarrier ring
+ * feeds the tensor cores.  Any alignment and leading dimension are accepted.
+ */
+int gemm_f32_3xtf32(const float* A, const float* B, float* C, int64_t M, int64_t N,
+                    int64_t K, int64_t lda, int64_t ldb, int64_t ldc, void* stream);
+
+/*
+ * bf16 tensor-core path: A and B hold bfloat16 bit patterns (uint16_t), C is
+ * fp32; products are accumulated in fp32 in TMEM (tcgen05.mma kind::f16).
+ * Fast path: A, B 16-byte aligned with lda, ldb multiples of 8 elements;
+ * otherwise the operands are first packed into the workspace.  C written with
+ * TMA stores when C is 16-byte aligned and ldc is a multiple of 4, else with
+ * masked vector stores.
+ */
+int gemm_bf16_f32acc(const uint16_t* A, const uint16_t* B, float* C, int64_t M, int64_t N,
+                     int64_t K, int64_t lda, int64_t ldb, int64_t ldc, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word.  Returns MHR_OK, MHR_ERR_TIMEOUT (some kernel since the last check hit
+ * a wait limit) or MHR_ERR_CUDA (the synchronisation itself failed).
+ */
+int gemm_check(void* stream);
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char* gemm_status_string(int status);
+
+/*
+ * Frees every workspace the library holds (all devices, all streams).  The
+ * caller must ensure no library work is still running on any stream.
+ */
+void gemm_release(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int gemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MHR_GEMM_H */

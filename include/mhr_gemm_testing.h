@@ -1,0 +1,45 @@
+/*
+ * mhr_gemm_testing.h -- test hooks of libmhr_gemm.so.  Not for production use.
+ *
+ * The pages have no counterpart: these hooks exist so the failure path of the
+ * tensor-core kernels (a bounded wait that runs out) can be exercised without
+ * faulting, trapping or hanging a GPU.
+ */
+#ifndef MHR_GEMM_TESTING_H
+#define MHR_GEMM_TESTING_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * Sets the limit, in nanoseconds, of every bounded wait inside the
+ * tensor-core kernels launched afterwards (process-wide; default 2 s).
+ * Values below 1 ms are raised to 1 ms.  Returns the previous limit.
+ */
+uint64_t gemm_testing_set_wait_limit_ns(uint64_t limit_ns);
+
+/*
+ * When `enable` is nonzero, the next tensor-core launches run with an
+ * injected stall: block 0 arms its first ring stage for a TMA load but never
+ * issues the load, so that stage never fills.  Its consumers' waits then run
+ * out, the kernel records MHR_ERR_TIMEOUT in the device status word, frees
+ * its TMEM and exits; gemm_check() reports the timeout.  No GPU fault occurs
+ * and the CUDA context stays usable.  Returns the previous setting.
+ */
+int gemm_testing_set_inject_stall(int enable);
+
+/*
+ * Synchronises `stream` and returns the raw bits of the current device's
+ * status word without clearing it (1: producer timeout, 2: MMA-issuer
+ * timeout, 4: epilogue timeout, 8: drain timeout).  Negative on a CUDA error.
+ */
+int64_t gemm_testing_peek_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MHR_GEMM_TESTING_H */

@@ -1,0 +1,339 @@
+// C-ABI front end of libmhr_gemm.so: argument validation, degenerate cases,
+// workspace management, tensor-map encoding and kernel dispatch.  The
+// operation and its contract are documented in include/mhr_gemm.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "mhr_gemm.h"
+#include "mhr_gemm_testing.h"
+#include "mhr_internal.h"
+
+#define MHR_API extern "C" __attribute__((visibility("default")))
+
+namespace mhr {
+namespace {
+
+constexpr int kVersion = 1 * 10000 + 0 * 100 + 0;
+constexpr int64_t kMaxDim = (int64_t{1} << 31) - 512;  // tile/TMA coordinates are int32
+
+// Per-device status word: tensor-core kernels OR their timeout bits into it.
+__device__ uint32_t g_status_word;
+
+struct DeviceState {
+  int checked = 0;  // 0 = not yet, 1 = sm_103, 2 = unsupported
+  uint32_t* status = nullptr;
+  int sm_count = 0;
+};
+
+struct Workspace {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+
+std::mutex g_mu;
+std::map<int, DeviceState> g_devices;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_workspaces;
+uint64_t g_wait_limit_ns = 2000000000ull;
+int g_inject_stall = 0;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// Current device: check it is sm_103 and find its status word (once).
+int device_state(DeviceState** out, int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MHR_ERR_CUDA;
+  DeviceState& st = g_devices[dev];
+  if (st.checked == 0) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MHR_ERR_CUDA;
+    if (major != 10 || minor != 3) {
+      st.checked = 2;
+    } else {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return MHR_ERR_CUDA;
+      st.status = static_cast<uint32_t*>(p);
+      st.sm_count = sms;
+      st.checked = 1;
+    }
+  }
+  if (st.checked != 1) return MHR_ERR_UNSUPPORTED;
+  *out = &st;
+  if (dev_out) *dev_out = dev;
+  return MHR_OK;
+}
+
+bool mul_ok(int64_t a, int64_t b, int64_t* r) { return !__builtin_mul_overflow(a, b, r); }
+
+// Byte extent [lo, hi) of a rows x cols row-major matrix with pitch ld.
+bool extent(const void* p, int64_t rows, int64_t cols, int64_t ld, int64_t esz, uintptr_t* lo,
+            uintptr_t* hi) {
+  int64_t span, bytes;
+  if (!mul_ok(rows - 1, ld, &span) || __builtin_add_overflow(span, cols, &span) ||
+      !mul_ok(span, esz, &bytes))
+    return false;
+  *lo = reinterpret_cast<uintptr_t>(p);
+  if (__builtin_add_overflow(*lo, static_cast<uintptr_t>(bytes), hi)) return false;
+  return true;
+}
+
+bool overlaps(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
+
+// Shared validation.  Returns MHR_OK with *noop set when there is nothing to do.
+int validate(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
+             int64_t lda, int64_t ldb, int64_t ldc, int64_t esz_ab, bool* noop) {
+  *noop = false;
+  if (M < 0 || N < 0 || K < 0) return MHR_ERR_INVALID_ARG;
+  if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return MHR_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) {
+    *noop = true;
+    return MHR_OK;
+  }
+  if (C == nullptr || ldc < N) return MHR_ERR_INVALID_ARG;
+  uintptr_t c0, c1;
+  if (!extent(C, M, N, ldc, 4, &c0, &c1)) return MHR_ERR_INVALID_ARG;
+  if (K == 0) return MHR_OK;
+  if (A == nullptr || B == nullptr || lda < K || ldb < N) return MHR_ERR_INVALID_ARG;
+  uintptr_t a0, a1, b0, b1;
+  if (!extent(A, M, K, lda, esz_ab, &a0, &a1) || !extent(B, K, N, ldb, esz_ab, &b0, &b1))
+    return MHR_ERR_INVALID_ARG;
+  if (overlaps(c0, c1, a0, a1) || overlaps(c0, c1, b0, b1)) return MHR_ERR_INVALID_ARG;
+  return MHR_OK;
+}
+
+// Workspace of at least `bytes` for (device, stream).  Growing frees the old
+// buffer first (cudaFree waits for the device), so earlier calls on the same
+// stream that still read it have finished.
+int workspace(int dev, cudaStream_t s, size_t bytes, void** out) {
+  Workspace& w = g_workspaces[{dev, s}];
+  if (w.bytes < bytes) {
+    if (w.ptr) {
+      cudaFree(w.ptr);
+      w.ptr = nullptr;
+      w.bytes = 0;
+    }
+    const size_t rounded = (bytes + (size_t{2} << 20) - 1) & ~((size_t{2} << 20) - 1);
+    if (cudaMalloc(&w.ptr, rounded) != cudaSuccess) {
+      cudaGetLastError();
+      w.ptr = nullptr;
+      return MHR_ERR_CUDA;
+    }
+    w.bytes = rounded;
+  }
+  *out = w.ptr;
+  return MHR_OK;
+}
+
+DeviceCtl make_ctl(const DeviceState& st) {
+  DeviceCtl c;
+  c.status = st.status;
+  c.wait_limit_ns = g_wait_limit_ns;
+  c.inject_stall = g_inject_stall;
+  c.sm_count = st.sm_count;
+  return c;
+}
+
+int from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return MHR_OK;
+  cudaGetLastError();  // clear the sticky-free launch error so later calls start clean
+  return MHR_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+}  // namespace
+
+CUresult encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                        uint64_t inner, uint64_t outer, uint64_t row_pitch_bytes,
+                        uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return CUDA_ERROR_NOT_FOUND;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_pitch_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace mhr
+
+using namespace mhr;
+
+MHR_API int gemm_f32(const float* A, const float* B, float* C, int64_t M, int64_t N, int64_t K,
+                     int64_t lda, int64_t ldb, int64_t ldc, void* stream) {
+  bool noop;
+  int rc = validate(A, B, C, M, N, K, lda, ldb, ldc, 4, &noop);
+  if (rc != MHR_OK || noop) return rc;
+  std::lock_guard<std::mutex> g(g_mu);
+  DeviceState* st;
+  if ((rc = device_state(&st, nullptr)) != MHR_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K == 0) return from_cuda(launch_zero_fill(C, M, N, ldc, s));
+  return from_cuda(launch_simt_f32(A, B, C, M, N, K, lda, ldb, ldc, s));
+}
+
+MHR_API int gemm_f32_3xtf32(const float* A, const float* B, float* C, int64_t M, int64_t N,
+                            int64_t K, int64_t lda, int64_t ldb, int64_t ldc, void* stream) {
+  bool noop;
+  int rc = validate(A, B, C, M, N, K, lda, ldb, ldc, 4, &noop);
+  if (rc != MHR_OK || noop) return rc;
+  std::lock_guard<std::mutex> g(g_mu);
+  DeviceState* st;
+  int dev;
+  if ((rc = device_state(&st, &dev)) != MHR_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K == 0) return from_cuda(launch_zero_fill(C, M, N, ldc, s));
+  // Split operands: a_big, a_small (M x Kp), bt_big, bt_small (N x Kp).
+  const int64_t Kp = round_up(K, 4);
+  const size_t a_bytes = static_cast<size_t>(M) * Kp * 4, b_bytes = static_cast<size_t>(N) * Kp * 4;
+  void* ws;
+  if ((rc = workspace(dev, s, 2 * (a_bytes + b_bytes), &ws)) != MHR_OK) return rc;
+  float* a_big = static_cast<float*>(ws);
+  float* a_small = a_big + M * Kp;
+  float* bt_big = a_small + M * Kp;
+  float* bt_small = bt_big + N * Kp;
+  cudaError_t e = launch_split_tf32(A, B, M, N, K, lda, ldb, Kp, a_big, a_small, bt_big, bt_small, s);
+  if (e != cudaSuccess) return from_cuda(e);
+  const bool c_tma = aligned16(C) && (ldc % 4) == 0;
+  return from_cuda(launch_tc_3xtf32(a_big, a_small, bt_big, bt_small, C, M, N, K, Kp, ldc, c_tma,
+                                    make_ctl(*st), s));
+}
+
+MHR_API int gemm_bf16_f32acc(const uint16_t* A, const uint16_t* B, float* C, int64_t M, int64_t N,
+                             int64_t K, int64_t lda, int64_t ldb, int64_t ldc, void* stream) {
+  bool noop;
+  int rc = validate(A, B, C, M, N, K, lda, ldb, ldc, 2, &noop);
+  if (rc != MHR_OK || noop) return rc;
+  std::lock_guard<std::mutex> g(g_mu);
+  DeviceState* st;
+  int dev;
+  if ((rc = device_state(&st, &dev)) != MHR_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K == 0) return from_cuda(launch_zero_fill(C, M, N, ldc, s));
+  const bool a_ok = aligned16(A) && (lda % 8) == 0;
+  const bool b_ok = aligned16(B) && (ldb % 8) == 0;
+  if (!a_ok || !b_ok) {
+    // TMA needs 16-byte aligned rows: repack the offending operand(s).
+    const int64_t lda_p = round_up(K, 8), ldb_p = round_up(N, 8);
+    const size_t a_bytes = a_ok ? 0 : static_cast<size_t>(M) * lda_p * 2;
+    const size_t b_bytes = b_ok ? 0 : static_cast<size_t>(K) * ldb_p * 2;
+    void* ws;
+    if ((rc = workspace(dev, s, round_up(a_bytes, 256) + b_bytes, &ws)) != MHR_OK) return rc;
+    uint16_t* pa = static_cast<uint16_t*>(ws);
+    uint16_t* pb = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + round_up(a_bytes, 256));
+    cudaError_t e;
+    if (!a_ok) {
+      if ((e = launch_pack_u16(A, M, K, lda, pa, lda_p, s)) != cudaSuccess) return from_cuda(e);
+      A = pa;
+      lda = lda_p;
+    }
+    if (!b_ok) {
+      if ((e = launch_pack_u16(B, K, N, ldb, pb, ldb_p, s)) != cudaSuccess) return from_cuda(e);
+      B = pb;
+      ldb = ldb_p;
+    }
+  }
+  const bool c_tma = aligned16(C) && (ldc % 4) == 0;
+  return from_cuda(launch_tc_bf16(A, B, C, M, N, K, lda, ldb, ldc, c_tma, make_ctl(*st), s));
+}
+
+MHR_API int gemm_check(void* stream) {
+  std::lock_guard<std::mutex> g(g_mu);
+  DeviceState* st;
+  int rc;
+  if ((rc = device_state(&st, nullptr)) != MHR_OK) return rc;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return MHR_ERR_CUDA;
+  }
+  uint32_t bits = 0;
+  if (cudaMemcpy(&bits, st->status, sizeof(bits), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(st->status, 0, sizeof(bits)) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    return MHR_ERR_CUDA;
+  }
+  return bits ? MHR_ERR_TIMEOUT : MHR_OK;
+}
+
+MHR_API const char* gemm_status_string(int status) {
+  switch (status) {
+    case MHR_OK: return "MHR_OK";
+    case MHR_ERR_INVALID_ARG: return "MHR_ERR_INVALID_ARG: invalid argument";
+    case MHR_ERR_UNSUPPORTED: return "MHR_ERR_UNSUPPORTED: device is not sm_103 (GB300)";
+    case MHR_ERR_CUDA: return "MHR_ERR_CUDA: a CUDA call failed";
+    case MHR_ERR_TIMEOUT: return "MHR_ERR_TIMEOUT: a device-side bounded wait ran out";
+    default: return "unknown mhr_status";
+  }
+}
+
+MHR_API void gemm_release(void) {
+  std::lock_guard<std::mutex> g(g_mu);
+  int cur = 0;
+  cudaGetDevice(&cur);
+  for (auto& kv : g_workspaces) {
+    if (kv.second.ptr) {
+      cudaSetDevice(kv.first.first);
+      cudaFree(kv.second.ptr);
+    }
+  }
+  g_workspaces.clear();
+  cudaSetDevice(cur);
+}
+
+MHR_API int gemm_version(void) { return kVersion; }
+
+MHR_API uint64_t gemm_testing_set_wait_limit_ns(uint64_t limit_ns) {
+  std::lock_guard<std::mutex> g(g_mu);
+  const uint64_t old = g_wait_limit_ns;
+  g_wait_limit_ns = limit_ns < 1000000ull ? 1000000ull : limit_ns;
+  return old;
+}
+
+MHR_API int gemm_testing_set_inject_stall(int enable) {
+  std::lock_guard<std::mutex> g(g_mu);
+  const int old = g_inject_stall;
+  g_inject_stall = enable ? 1 : 0;
+  return old;
+}
+
+MHR_API int64_t gemm_testing_peek_status(void* stream) {
+  std::lock_guard<std::mutex> g(g_mu);
+  DeviceState* st;
+  if (device_state(&st, nullptr) != MHR_OK) return -1;
+  uint32_t bits = 0;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess ||
+      cudaMemcpy(&bits, st->status, sizeof(bits), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  return bits;
+}

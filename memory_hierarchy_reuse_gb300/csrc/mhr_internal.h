@@ -1,0 +1,59 @@
+// Launchers shared between the C-ABI front end (api.cu) and the kernel
+// translation units.  Every launcher assumes validated arguments (sizes >= 1,
+// pointers non-null) and returns the launch's cudaError_t.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace mhr {
+
+// Knobs read by the tensor-core kernels; set by the C-ABI front end.
+struct DeviceCtl {
+  uint32_t* status = nullptr;          // device address of the status word
+  uint64_t wait_limit_ns = 2000000000ull;
+  int inject_stall = 0;                // test hook: block 0 arms one TMA stage and never loads it
+  int sm_count = 0;
+};
+
+cudaError_t launch_simt_f32(const float* A, const float* B, float* C, int64_t M, int64_t N,
+                            int64_t K, int64_t lda, int64_t ldb, int64_t ldc, cudaStream_t s);
+
+// C[M x N] = 0 (the K == 0 case).
+cudaError_t launch_zero_fill(float* C, int64_t M, int64_t N, int64_t ldc, cudaStream_t s);
+
+// Copy a rows x cols matrix of 2-byte elements to a buffer with leading
+// dimension dst_ld (used when a bf16 operand is not TMA-aligned).
+cudaError_t launch_pack_u16(const uint16_t* src, int64_t rows, int64_t cols, int64_t src_ld,
+                            uint16_t* dst, int64_t dst_ld, cudaStream_t s);
+
+// 3xTF32 split: A (M x K, lda) -> a_big, a_small (M x Kp, K-contiguous);
+// B (K x N, ldb) -> bt_big, bt_small (N x Kp, K-contiguous, i.e. B transposed).
+cudaError_t launch_split_tf32(const float* A, const float* B, int64_t M, int64_t N, int64_t K,
+                              int64_t lda, int64_t ldb, int64_t Kp, float* a_big, float* a_small,
+                              float* bt_big, float* bt_small, cudaStream_t s);
+
+// Shared-memory bytes the tensor-core kernels request (for cudaFuncSetAttribute).
+size_t tc_bf16_smem_bytes();
+size_t tc_3xtf32_smem_bytes();
+
+// bf16 x bf16 -> fp32 on tcgen05.  A: M x K bf16 (row pitch lda, 16-byte
+// aligned rows), B: K x N bf16 (pitch ldb, aligned).  C via TMA store when
+// c_tma is true (C 16-byte aligned, ldc % 4 == 0), else direct stores.
+cudaError_t launch_tc_bf16(const uint16_t* A, const uint16_t* B, float* C, int64_t M, int64_t N,
+                           int64_t K, int64_t lda, int64_t ldb, int64_t ldc, bool c_tma,
+                           const DeviceCtl& ctl, cudaStream_t s);
+
+// 3xTF32 main loop over the split operands (pitch Kp floats).
+cudaError_t launch_tc_3xtf32(const float* a_big, const float* a_small, const float* bt_big,
+                             const float* bt_small, float* C, int64_t M, int64_t N, int64_t K,
+                             int64_t Kp, int64_t ldc, bool c_tma, const DeviceCtl& ctl,
+                             cudaStream_t s);
+
+// Tensor-map encoding through the driver entry point (no libcuda link).
+CUresult encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                        uint64_t inner, uint64_t outer, uint64_t row_pitch_bytes,
+                        uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
+
+}  // namespace mhr

@@ -1,0 +1,180 @@
+// Strict-FP32 GEMM on the SIMT pipes: C = A * B, all row-major, fp32 FMA with
+// fp32 accumulation.
+//
+// This is the pages' shared-memory tiled kernel ("矩阵乘法 tiling", section 四;
+// "CUDA 编程系列之三", section 6) taken two levels further, as the pages point
+// to in "矩阵乘法 tiling", sections 三 and 五 (one thread owns several outputs,
+// the accumulator lives in registers):
+//   * a 128 x 128 output tile per block: each A element staged in shared
+//     memory feeds 128 outputs and each B element 128 outputs, so global
+//     traffic is MNK (1/128 + 1/128) elements instead of 2MNK;
+//   * an 8 x 8 register block per thread (register tiling): every value read
+//     from shared memory feeds 8 FMAs;
+//   * a double-buffered K ring (BK = 8): the next K-tile is fetched into
+//     registers while the current one is consumed, so each K step needs one
+//     __syncthreads() instead of the pages' two (the second barrier's job --
+//     "do not overwrite a tile still being read" -- is done by writing the
+//     other buffer);
+//   * edge tiles: elements outside the matrix are loaded as zero and outputs
+//     outside it are not stored ("矩阵乘法 tiling", section 六;
+//     "CUDA 编程系列之三", section 7).
+//
+// Loads are coalesced where the tile crosses the global-memory boundary (a
+// warp reads consecutive addresses of one row), the A tile is stored
+// transposed (k-major) in shared memory with 4 floats of row padding so the
+// transposing stores do not conflict, and the compute loop reads shared memory
+// as float4 (two distinct A vectors per warp, broadcast; sixteen consecutive B
+// vectors per warp).
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "mhr_internal.h"
+
+namespace mhr {
+namespace {
+
+constexpr int BM = 128, BN = 128, BK = 8, NT = 256, APAD = 4;
+constexpr int GROUP_M = 8;  // tile rows swept together (L2 reuse of B column strips)
+
+template <bool VA, bool VB, bool VC>
+__global__ void __launch_bounds__(NT, 2)
+    simt_f32_kernel(const float* __restrict__ A, const float* __restrict__ B,
+                    float* __restrict__ C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                    int64_t ldb, int64_t ldc, int64_t tiles_m, int64_t tiles_n) {
+  __shared__ __align__(16) float As[2][BK][BM + APAD];
+  __shared__ __align__(16) float Bs[2][BK][BN];
+
+  const int tid = threadIdx.x;
+  // Grouped raster over a 1-D grid: blocks launched together cover GROUP_M
+  // tile rows, column by column.
+  const int64_t t = blockIdx.x;
+  const int64_t group_size = GROUP_M * tiles_n;
+  const int64_t first_m = (t / group_size) * GROUP_M;
+  const int64_t gm = tiles_m - first_m < GROUP_M ? tiles_m - first_m : GROUP_M;
+  const int64_t r = t % group_size;
+  const int64_t m0 = (first_m + r % gm) * BM;
+  const int64_t n0 = (r / gm) * BN;
+
+  // Load mapping: A tile 128 rows x 8 k, 4 consecutive k per thread; B tile
+  // 8 k x 128 cols, 4 consecutive columns per thread.
+  const int a_row = tid >> 1, a_k = (tid & 1) * 4;
+  const int b_k = tid >> 5, b_col = (tid & 31) * 4;
+  const bool a_row_ok = m0 + a_row < M;
+  const int64_t b_col_g = n0 + b_col;
+  const float* a_ptr = A + (a_row_ok ? (m0 + a_row) * lda : 0) + a_k;
+  const float* b_ptr = B + static_cast<int64_t>(b_k) * ldb + b_col_g;
+
+  // Compute mapping: thread (ty, tx) owns rows {4ty..4ty+3, 64+4ty..64+4ty+3}
+  // and columns {4tx..4tx+3, 64+4tx..64+4tx+3} of the tile.
+  const int ty = tid >> 4, tx = tid & 15;
+
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+  float ra[4], rb[4];
+  auto fetch = [&](int64_t k0) {
+    const int64_t ka = k0 + a_k;
+    if (VA && a_row_ok && ka + 4 <= K) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(a_ptr + k0));
+      ra[0] = v.x; ra[1] = v.y; ra[2] = v.z; ra[3] = v.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ra[i] = (a_row_ok && ka + i < K) ? __ldg(a_ptr + k0 + i) : 0.f;
+    }
+    const int64_t kb = k0 + b_k;
+    const float* bp = b_ptr + k0 * ldb;
+    if (VB && kb < K && b_col_g + 4 <= N) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(bp));
+      rb[0] = v.x; rb[1] = v.y; rb[2] = v.z; rb[3] = v.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) rb[i] = (kb < K && b_col_g + i < N) ? __ldg(bp + i) : 0.f;
+    }
+  };
+  auto stash = [&](int buf) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) As[buf][a_k + i][a_row] = ra[i];
+    *reinterpret_cast<float4*>(&Bs[buf][b_k][b_col]) = make_float4(rb[0], rb[1], rb[2], rb[3]);
+  };
+
+  const int64_t nk = (K + BK - 1) / BK;
+  fetch(0);
+  stash(0);
+  __syncthreads();
+
+  for (int64_t kt = 0; kt < nk; ++kt) {
+    const int cur = static_cast<int>(kt & 1);
+    if (kt + 1 < nk) fetch((kt + 1) * BK);
+#pragma unroll
+    for (int k = 0; k < BK; ++k) {
+      const float4 a0 = *reinterpret_cast<const float4*>(&As[cur][k][ty * 4]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&As[cur][k][64 + ty * 4]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[cur][k][tx * 4]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[cur][k][64 + tx * 4]);
+      const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    if (kt + 1 < nk) stash(cur ^ 1);
+    __syncthreads();
+  }
+
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int64_t row = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
+    if (row >= M) continue;
+    float* crow = C + row * ldc;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int64_t col = n0 + h * 64 + tx * 4;
+      if (VC && col + 4 <= N) {
+        *reinterpret_cast<float4*>(crow + col) =
+            make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2], acc[i][4 * h + 3]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (col + j < N) crow[col + j] = acc[i][4 * h + j];
+      }
+    }
+  }
+}
+
+template <bool VA, bool VB, bool VC>
+cudaError_t launch_t(const float* A, const float* B, float* C, int64_t M, int64_t N, int64_t K,
+                     int64_t lda, int64_t ldb, int64_t ldc, cudaStream_t s) {
+  const int64_t tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
+  simt_f32_kernel<VA, VB, VC><<<static_cast<unsigned>(tiles_m * tiles_n), NT, 0, s>>>(
+      A, B, C, M, N, K, lda, ldb, ldc, tiles_m, tiles_n);
+  return cudaGetLastError();
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+// Requires M, N, K >= 1 and ceil(M/128) * ceil(N/128) < 2^31.  Validation is the caller's.
+cudaError_t launch_simt_f32(const float* A, const float* B, float* C, int64_t M, int64_t N,
+                            int64_t K, int64_t lda, int64_t ldb, int64_t ldc, cudaStream_t s) {
+  const bool va = aligned16(A) && (lda % 4) == 0;
+  const bool vb = aligned16(B) && (ldb % 4) == 0;
+  const bool vc = aligned16(C) && (ldc % 4) == 0;
+  const int key = (va ? 4 : 0) | (vb ? 2 : 0) | (vc ? 1 : 0);
+  switch (key) {
+    case 7: return launch_t<true, true, true>(A, B, C, M, N, K, lda, ldb, ldc, s);
+    case 6: return launch_t<true, true, false>(A, B, C, M, N, K, lda, ldb, ldc, s);
+    case 5: return launch_t<true, false, true>(A, B, C, M, N, K, lda, ldb, ldc, s);
+    case 4: return launch_t<true, false, false>(A, B, C, M, N, K, lda, ldb, ldc, s);
+    case 3: return launch_t<false, true, true>(A, B, C, M, N, K, lda, ldb, ldc, s);
+    case 2: return launch_t<false, true, false>(A, B, C, M, N, K, lda, ldb, ldc, s);
+    case 1: return launch_t<false, false, true>(A, B, C, M, N, K, lda, ldb, ldc, s);
+    default: return launch_t<false, false, false>(A, B, C, M, N, K, lda, ldb, ldc, s);
+  }
+}
+
+}  // namespace mhr

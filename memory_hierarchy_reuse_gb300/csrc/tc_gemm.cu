@@ -1,0 +1,561 @@
+// Tensor-core GEMM for sm_103a: TMA -> mbarrier shared-memory ring ->
+// tcgen05.mma with a TMEM accumulator -> TMA-store epilogue.
+//
+// The method is the pages' tiling ("矩阵乘法 tiling", sections 二-四;
+// "CUDA 深入浅出（二）", sections "分块之后怎么读" and "推广到整个 N×N 矩阵"):
+// one output tile per work unit, K walked in BK-wide steps, each step staging
+// an A box (BM x BK) and a B box (BK x BN) on chip and reusing every staged
+// element across the whole tile.  What differs from the pages' 2016-era SIMT
+// kernel is how each step is executed on Blackwell:
+//
+//   step                    pages                         here
+//   ----------------------  ----------------------------  ------------------------------
+//   global -> shared        each thread loads 1 element   one TMA box copy per operand,
+//                                                          128-byte swizzle (no bank
+//                                                          conflicts), OOB zero-fill
+//   barrier one / two       __syncthreads() x 2           full[s] / empty[s] mbarriers
+//                                                          of a STAGES-deep ring
+//   multiply-accumulate     scalar FMA, acc in a register tcgen05.mma 128 x BN x K_instr,
+//                                                          accumulator in TMEM
+//   write C                 one store per thread          TMEM -> registers -> swizzled
+//                                                          smem -> TMA store
+//
+// Warp roles (192 threads, one CTA per SM, persistent over tiles):
+//   warp 0     TMA producer (lane 0 issues)
+//   warp 1     TMEM allocator + MMA issuer (lane 0 issues)
+//   warps 2-5  epilogue; warp w reads TMEM lanes 32*(w%4) .. 32*(w%4)+31
+// The accumulator is double-buffered in TMEM so the epilogue of tile i runs
+// while the MMAs of tile i+1 are issued.
+//
+// Two kinds:
+//   KIND_BF16:   A bf16 K-major (row-major M x K), B bf16 MN-major (row-major
+//                K x N), BM x BN x BK = 128 x 256 x 64, 4 stages, kind::f16.
+//   KIND_3XTF32: A_big, A_small K-major; B_big^T, B_small^T K-major (N x K),
+//                128 x 128 x 32, 3 stages, kind::tf32, three MMAs per
+//                instruction-K step (small*big, big*small, big*big).
+//
+// Every wait is bounded (DeviceCtl::wait_limit_ns).  A role that runs out of
+// time sets its bit in the device status word and an abort flag in shared
+// memory; the other roles see the flag and unwind; the CTA then waits
+// (bounded) for its own copies and MMAs in flight, frees its TMEM and exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "mhr_device.cuh"
+#include "mhr_internal.h"
+
+namespace mhr {
+namespace {
+
+constexpr int KIND_BF16 = 0;
+constexpr int KIND_3XTF32 = 1;
+
+template <int KIND>
+struct Cfg;
+
+template <>
+struct Cfg<KIND_BF16> {
+  static constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+  static constexpr int A_BYTES = BM * BK * 2;              // 16 KB
+  static constexpr int B_BOX_BYTES = 64 * BK * 2;          // 64 cols x 64 k = 8 KB
+  static constexpr int B_BYTES = BK * BN * 2;              // 32 KB
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;    // 48 KB
+  static constexpr int INSTR_K = 16;
+  static constexpr uint32_t IDESC = make_idesc(1, false, true, BM, BN);
+  static constexpr uint32_t TMEM_COLS = 2 * BN;            // 512
+};
+
+template <>
+struct Cfg<KIND_3XTF32> {
+  static constexpr int BM = 128, BN = 128, BK = 32, STAGES = 3;
+  static constexpr int A_BYTES = BM * BK * 4;              // 16 KB each (big, small)
+  static constexpr int B_BYTES = BN * BK * 4;              // 16 KB each (big, small)
+  static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;  // 64 KB
+  static constexpr int INSTR_K = 8;
+  static constexpr uint32_t IDESC = make_idesc(2, false, false, BM, BN);
+  static constexpr uint32_t TMEM_COLS = 2 * BN;            // 256
+};
+
+constexpr int EPI_WARPS = 4;
+constexpr int EPI_BUF_BYTES = 32 * 32 * 4;                 // 32 rows x 32 fp32
+constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;   // 32 KB
+constexpr int NUM_THREADS = 192;
+constexpr int GROUP_M = 16;                                // tile rows per raster group
+
+template <int KIND>
+struct Layout {
+  using C = Cfg<KIND>;
+  static constexpr int EPI_OFF = C::STAGES * C::STAGE_BYTES;
+  static constexpr int BAR_OFF = EPI_OFF + EPI_BYTES;
+  static constexpr int NUM_BARS = 2 * C::STAGES + 5;        // full, empty, acc_full x2, acc_empty x2, drain
+  static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;   // tmem slot, abort flag
+  static constexpr int USED = MISC_OFF + 16;
+  static constexpr int ALLOC = USED + 1024;                 // slack for 1024-byte alignment
+};
+
+struct TcParams {
+  int32_t M, N, K;
+  int32_t tiles_m, tiles_n, num_tiles, num_kb;
+  float* C;
+  int64_t ldc;
+  uint32_t* status;
+  uint64_t wait_limit_ns;
+  int32_t inject_stall;
+};
+
+// Grouped raster: consecutive work units sweep GROUP_M tile rows column by
+// column, so the CTAs resident at one time share A row strips and B column
+// strips in L2 (a second level of the pages' reuse argument, one level up
+// from shared memory).
+__device__ __forceinline__ void tile_coords(int t, const TcParams& p, int& tm, int& tn) {
+  const int group_size = GROUP_M * p.tiles_n;
+  const int g = t / group_size;
+  const int first_m = g * GROUP_M;
+  const int gm = min(p.tiles_m - first_m, GROUP_M);
+  const int r = t - g * group_size;
+  tm = first_m + r % gm;
+  tn = r / gm;
+}
+
+// Warp-uniform bounded wait: every lane polls; the warp agrees on the outcome.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_t limit,
+                                          volatile int* abort_flag) {
+  const bool ok = mbar_wait_bounded(bar, parity, limit, abort_flag);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void give_up(const TcParams& p, volatile int* abort_flag, uint32_t bit,
+                                        int lane) {
+  if (lane == 0) {
+    if (!*abort_flag) atomicOr(p.status, bit);  // the first role to give up records why
+    *abort_flag = 1;
+  }
+  __syncwarp();
+}
+
+template <int KIND, bool TMA_STORE>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+                   const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
+                   const __grid_constant__ CUtensorMap tmC, const TcParams p) {
+  using Cf = Cfg<KIND>;
+  using L = Layout<KIND>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + L::BAR_OFF;
+  auto full_bar = [&](uint32_t s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (Cf::STAGES + s); };
+  auto accf_bar = [&](uint32_t b) { return bar0 + 8u * (2 * Cf::STAGES + b); };
+  auto acce_bar = [&](uint32_t b) { return bar0 + 8u * (2 * Cf::STAGES + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * Cf::STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Cf::STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf_bar(b), 1);
+      mbar_init(acce_bar(b), EPI_WARPS);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA0);
+    tma_prefetch_desc(&tmB0);
+    if constexpr (KIND == KIND_3XTF32) {
+      tma_prefetch_desc(&tmA1);
+      tma_prefetch_desc(&tmB1);
+    }
+    if (TMA_STORE) tma_prefetch_desc(&tmC);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), Cf::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint64_t limit = p.wait_limit_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    uint32_t it = 0;
+    uint32_t inflight = 0;  // bit s: the latest fill of stage s had a TMA issued
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+      int tm, tn;
+      tile_coords(t, p, tm, tn);
+      const int m0 = tm * Cf::BM, n0 = tn * Cf::BN;
+      for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+        const uint32_t s = it % Cf::STAGES, ph = (it / Cf::STAGES) & 1u;
+        if (!warp_wait(empty_bar(s), ph ^ 1u, limit, abort_flag)) {
+          give_up(p, abort_flag, kErrTimeoutProducer, lane);
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t st = sbase + s * Cf::STAGE_BYTES;
+          const int k0 = kb * Cf::BK;
+          mbar_arrive_expect_tx(full_bar(s), Cf::STAGE_BYTES);
+          const bool stall = p.inject_stall && blockIdx.x == 0 && it == 0;
+          if (!stall) {
+            if constexpr (KIND == KIND_BF16) {
+              tma_load_2d(st, &tmA0, full_bar(s), k0, m0);
+#pragma unroll
+              for (int j = 0; j < Cf::BN / 64; ++j)
+                tma_load_2d(st + Cf::A_BYTES + j * Cf::B_BOX_BYTES, &tmB0, full_bar(s), n0 + 64 * j,
+                            k0);
+            } else {
+              tma_load_2d(st, &tmA0, full_bar(s), k0, m0);
+              tma_load_2d(st + Cf::A_BYTES, &tmA1, full_bar(s), k0, m0);
+              tma_load_2d(st + 2 * Cf::A_BYTES, &tmB0, full_bar(s), k0, n0);
+              tma_load_2d(st + 2 * Cf::A_BYTES + Cf::B_BYTES, &tmB1, full_bar(s), k0, n0);
+            }
+            inflight |= 1u << s;
+          } else {
+            inflight &= ~(1u << s);
+          }
+        }
+        __syncwarp();
+      }
+    }
+    // Drain: every TMA this CTA issued must have landed before it exits.
+    if (lane == 0) {
+      for (uint32_t s = 0; s < static_cast<uint32_t>(Cf::STAGES) && s < it; ++s) {
+        if (!(inflight & (1u << s))) continue;
+        const uint32_t last = it - 1 - ((it - 1 - s) % Cf::STAGES);  // latest fill of stage s
+        volatile int never = 0;
+        if (!mbar_wait_bounded(full_bar(s), (last / Cf::STAGES) & 1u, limit, &never))
+          atomicOr(p.status, kErrTimeoutDrain);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    uint32_t it = 0, tcount = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++tcount) {
+      const uint32_t buf = tcount & 1u, aph = (tcount >> 1) & 1u;
+      if (!warp_wait(acce_bar(buf), aph ^ 1u, limit, abort_flag)) {
+        give_up(p, abort_flag, kErrTimeoutMma, lane);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + buf * Cf::BN;
+      for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+        const uint32_t s = it % Cf::STAGES, ph = (it / Cf::STAGES) & 1u;
+        if (!warp_wait(full_bar(s), ph, limit, abort_flag)) {
+          give_up(p, abort_flag, kErrTimeoutMma, lane);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t st = sbase + s * Cf::STAGE_BYTES;
+          if constexpr (KIND == KIND_BF16) {
+            // A: 128 rows x 128 B, K-major, 8-row groups 1024 B apart.
+            // B: four 64-column boxes (8 KB apart) of 64 k-rows x 128 B,
+            //    MN-major: LBO = next 64 columns, SBO = next 8 k-rows.
+#pragma unroll
+            for (int kk = 0; kk < Cf::BK / Cf::INSTR_K; ++kk) {
+              const uint64_t ad = smem_desc_sw128(st + kk * 32, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(st + Cf::A_BYTES + kk * 2048, Cf::B_BOX_BYTES, 1024);
+              mma_f16(d_tmem, ad, bd, Cf::IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+            }
+          } else {
+            // All four operands K-major, 128 B rows (32 floats), 8-row groups
+            // 1024 B apart; one instruction-K step (8 tf32) = 32 B.
+            const uint32_t a_big = st, a_small = st + Cf::A_BYTES;
+            const uint32_t b_big = st + 2 * Cf::A_BYTES, b_small = b_big + Cf::B_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < Cf::BK / Cf::INSTR_K; ++kk) {
+              const uint32_t off = kk * 32;
+              const uint64_t abd = smem_desc_sw128(a_big + off, 16, 1024);
+              const uint64_t asd = smem_desc_sw128(a_small + off, 16, 1024);
+              const uint64_t bbd = smem_desc_sw128(b_big + off, 16, 1024);
+              const uint64_t bsd = smem_desc_sw128(b_small + off, 16, 1024);
+              mma_tf32(d_tmem, asd, bbd, Cf::IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+              mma_tf32(d_tmem, abd, bsd, Cf::IDESC, 1u);
+              mma_tf32(d_tmem, abd, bbd, Cf::IDESC, 1u);
+            }
+          }
+          mma_commit(empty_bar(s));  // stage s may be refilled once these MMAs finish
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (lane == 0) mma_commit(accf_bar(buf));  // accumulator `buf` complete
+      __syncwarp();
+    }
+    // Drain: all MMAs issued by this thread complete before TMEM is freed.
+    if (lane == 0) {
+      mma_commit(drain_bar);
+      volatile int never = 0;
+      if (!mbar_wait_bounded(drain_bar, 0, limit, &never)) atomicOr(p.status, kErrTimeoutDrain);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;           // TMEM lane quarter this warp may access
+    const int ew = warp - 2;          // epilogue warp index 0..3
+    uint32_t tcount = 0, chunk = 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++tcount) {
+      const uint32_t buf = tcount & 1u, aph = (tcount >> 1) & 1u;
+      if (!warp_wait(accf_bar(buf), aph, limit, abort_flag)) {
+        give_up(p, abort_flag, kErrTimeoutEpilogue, lane);
+        break;
+      }
+      tc_fence_after();
+      int tm, tn;
+      tile_coords(t, p, tm, tn);
+      const int m0 = tm * Cf::BM, n0 = tn * Cf::BN;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * Cf::BN;
+#pragma unroll 1
+      for (int c = 0; c < Cf::BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32cols(taddr + c * 32, r);
+        tmem_ld_wait();
+        if constexpr (TMA_STORE) {
+          const uint32_t stg = sbase + L::EPI_OFF + (ew * 2 + (chunk & 1u)) * EPI_BUF_BYTES;
+          if (lane == 0) bulk_wait_group_read<1>();  // the store that last used this buffer has read it
+          __syncwarp();
+          // Row `lane` of the 32 x 32 box, 128-byte swizzle: 16-byte chunk j
+          // of row r sits at chunk position j ^ (r % 8).
+          const uint32_t row_addr = stg + lane * 128;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t a = row_addr + ((j ^ (lane & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(r[4 * j]),
+                         "r"(r[4 * j + 1]), "r"(r[4 * j + 2]), "r"(r[4 * j + 3])
+                         : "memory");
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmC, stg, n0 + c * 32, m0 + q * 32);
+            bulk_commit_group();
+          }
+          ++chunk;
+        } else {
+          const int row = m0 + q * 32 + lane;
+          if (row < p.M) {
+            float* crow = p.C + static_cast<int64_t>(row) * p.ldc;
+            const int col0 = n0 + c * 32;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (col0 + j < p.N) crow[col0 + j] = __uint_as_float(r[j]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce_bar(buf));  // TMEM buffer `buf` may be overwritten
+    }
+    if constexpr (TMA_STORE) {
+      if (lane == 0) bulk_wait_group<0>();
+      __syncwarp();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cf::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ pre-passes
+
+__global__ void zero_fill_kernel(float* C, int64_t M, int64_t N, int64_t ldc) {
+  for (int64_t r = blockIdx.y; r < M; r += gridDim.y)
+    for (int64_t c = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; c < N;
+         c += static_cast<int64_t>(gridDim.x) * blockDim.x)
+      C[r * ldc + c] = 0.f;
+}
+
+__global__ void pack_u16_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t cols,
+                                int64_t src_ld, uint16_t* __restrict__ dst, int64_t dst_ld) {
+  for (int64_t r = blockIdx.y; r < rows; r += gridDim.y)
+    for (int64_t c = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; c < cols;
+         c += static_cast<int64_t>(gridDim.x) * blockDim.x)
+      dst[r * dst_ld + c] = src[r * src_ld + c];
+}
+
+// Round an fp32 value to tf32 (10 explicit mantissa bits) to nearest, ties to
+// even, by integer arithmetic on the bit pattern; Inf and NaN pass unchanged.
+__device__ __forceinline__ float tf32_rne(float x) {
+  uint32_t u = __float_as_uint(x);
+  if ((u & 0x7F800000u) == 0x7F800000u) return x;
+  u += 0x0FFFu + ((u >> 13) & 1u);
+  return __uint_as_float(u & 0xFFFFE000u);
+}
+
+__device__ __forceinline__ void split_tf32(float x, float& big, float& small) {
+  big = tf32_rne(x);
+  const float rest = x - big;  // exact: the discarded low bits
+  small = isfinite(x) ? tf32_rne(rest) : 0.f;
+}
+
+// A: row-major M x K -> big/small M x Kp (same orientation).
+__global__ void split_a_kernel(const float* __restrict__ A, int64_t M, int64_t K, int64_t lda,
+                               int64_t Kp, float* __restrict__ big, float* __restrict__ small) {
+  for (int64_t r = blockIdx.y; r < M; r += gridDim.y) {
+    for (int64_t k = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; k < K;
+         k += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+      float b, s;
+      split_tf32(__ldg(A + r * lda + k), b, s);
+      big[r * Kp + k] = b;
+      small[r * Kp + k] = s;
+    }
+  }
+}
+
+// B: row-major K x N -> big/small N x Kp (transposed, K-contiguous) through a
+// 32 x 33 shared tile so both the read (along n) and the write (along k) are
+// coalesced.
+__global__ void split_bt_kernel(const float* __restrict__ B, int64_t K, int64_t N, int64_t ldb,
+                                int64_t Kp, float* __restrict__ big, float* __restrict__ small) {
+  __shared__ float tb[32][33];
+  __shared__ float ts[32][33];
+  const int64_t tiles_n = (N + 31) / 32, tiles_k = (K + 31) / 32;
+  for (int64_t tile = blockIdx.x; tile < tiles_n * tiles_k; tile += gridDim.x) {
+    const int64_t n0 = (tile % tiles_n) * 32, k0 = (tile / tiles_n) * 32;
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+      const int64_t k = k0 + i, n = n0 + threadIdx.x;
+      float b = 0.f, s = 0.f;
+      if (k < K && n < N) split_tf32(__ldg(B + k * ldb + n), b, s);
+      tb[i][threadIdx.x] = b;
+      ts[i][threadIdx.x] = s;
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+      const int64_t n = n0 + i, k = k0 + threadIdx.x;
+      if (n < N && k < K) {
+        big[n * Kp + k] = tb[threadIdx.x][i];
+        small[n * Kp + k] = ts[threadIdx.x][i];
+      }
+    }
+    __syncthreads();
+  }
+}
+
+template <int KIND, bool TMA_STORE>
+cudaError_t prepare_kernel() {
+  // cudaFuncSetAttribute is per device; callers run it on every launch (cheap).
+  return cudaFuncSetAttribute(tc_gemm_kernel<KIND, TMA_STORE>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<KIND>::ALLOC);
+}
+
+template <int KIND>
+cudaError_t launch_tc(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
+                      const CUtensorMap& b1, const CUtensorMap& cm, float* C, int64_t M, int64_t N,
+                      int64_t K, int64_t ldc, bool c_tma, const DeviceCtl& ctl, cudaStream_t s) {
+  using Cf = Cfg<KIND>;
+  TcParams p;
+  p.M = static_cast<int32_t>(M);
+  p.N = static_cast<int32_t>(N);
+  p.K = static_cast<int32_t>(K);
+  p.tiles_m = static_cast<int32_t>((M + Cf::BM - 1) / Cf::BM);
+  p.tiles_n = static_cast<int32_t>((N + Cf::BN - 1) / Cf::BN);
+  p.num_tiles = p.tiles_m * p.tiles_n;
+  p.num_kb = static_cast<int32_t>((K + Cf::BK - 1) / Cf::BK);
+  p.C = C;
+  p.ldc = ldc;
+  p.status = ctl.status;
+  p.wait_limit_ns = ctl.wait_limit_ns;
+  p.inject_stall = ctl.inject_stall;
+  const int grid = p.num_tiles < ctl.sm_count ? p.num_tiles : ctl.sm_count;
+  cudaError_t e;
+  if (c_tma) {
+    if ((e = prepare_kernel<KIND, true>()) != cudaSuccess) return e;
+    tc_gemm_kernel<KIND, true><<<grid, NUM_THREADS, Layout<KIND>::ALLOC, s>>>(a0, a1, b0, b1, cm, p);
+  } else {
+    if ((e = prepare_kernel<KIND, false>()) != cudaSuccess) return e;
+    tc_gemm_kernel<KIND, false><<<grid, NUM_THREADS, Layout<KIND>::ALLOC, s>>>(a0, a1, b0, b1, cm, p);
+  }
+  return cudaGetLastError();
+}
+
+unsigned grid_rows(int64_t rows) { return static_cast<unsigned>(rows < 65535 ? rows : 65535); }
+
+CUresult encode_c_map(CUtensorMap* cm, float* C, int64_t M, int64_t N, int64_t ldc, bool c_tma) {
+  if (!c_tma) return CUDA_SUCCESS;
+  return encode_tmap_2d(cm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, N, M, ldc * 4, 32, 32,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+}  // namespace
+
+size_t tc_bf16_smem_bytes() { return Layout<KIND_BF16>::ALLOC; }
+size_t tc_3xtf32_smem_bytes() { return Layout<KIND_3XTF32>::ALLOC; }
+
+cudaError_t launch_zero_fill(float* C, int64_t M, int64_t N, int64_t ldc, cudaStream_t s) {
+  const unsigned gx = static_cast<unsigned>((N + 255) / 256 < 64 ? (N + 255) / 256 : 64);
+  zero_fill_kernel<<<dim3(gx, grid_rows(M)), 256, 0, s>>>(C, M, N, ldc);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_u16(const uint16_t* src, int64_t rows, int64_t cols, int64_t src_ld,
+                            uint16_t* dst, int64_t dst_ld, cudaStream_t s) {
+  const unsigned gx = static_cast<unsigned>((cols + 255) / 256 < 64 ? (cols + 255) / 256 : 64);
+  pack_u16_kernel<<<dim3(gx, grid_rows(rows)), 256, 0, s>>>(src, rows, cols, src_ld, dst, dst_ld);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split_tf32(const float* A, const float* B, int64_t M, int64_t N, int64_t K,
+                              int64_t lda, int64_t ldb, int64_t Kp, float* a_big, float* a_small,
+                              float* bt_big, float* bt_small, cudaStream_t s) {
+  const unsigned gx = static_cast<unsigned>((K + 255) / 256 < 64 ? (K + 255) / 256 : 64);
+  split_a_kernel<<<dim3(gx, grid_rows(M)), 256, 0, s>>>(A, M, K, lda, Kp, a_big, a_small);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t tiles = ((N + 31) / 32) * ((K + 31) / 32);
+  const unsigned gb = static_cast<unsigned>(tiles < (1 << 20) ? tiles : (1 << 20));
+  split_bt_kernel<<<gb, dim3(32, 8), 0, s>>>(B, K, N, ldb, Kp, bt_big, bt_small);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tc_bf16(const uint16_t* A, const uint16_t* B, float* C, int64_t M, int64_t N,
+                           int64_t K, int64_t lda, int64_t ldb, int64_t ldc, bool c_tma,
+                           const DeviceCtl& ctl, cudaStream_t s) {
+  CUtensorMap a, b, cm;
+  if (encode_tmap_2d(&a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, K, M, lda * 2, 64, 128,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
+      encode_tmap_2d(&b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, N, K, ldb * 2, 64, 64,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
+      encode_c_map(&cm, C, M, N, ldc, c_tma) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  if (!c_tma) cm = a;  // unused by the kernel
+  return launch_tc<KIND_BF16>(a, a, b, b, cm, C, M, N, K, ldc, c_tma, ctl, s);
+}
+
+cudaError_t launch_tc_3xtf32(const float* a_big, const float* a_small, const float* bt_big,
+                             const float* bt_small, float* C, int64_t M, int64_t N, int64_t K,
+                             int64_t Kp, int64_t ldc, bool c_tma, const DeviceCtl& ctl,
+                             cudaStream_t s) {
+  CUtensorMap a0, a1, b0, b1, cm;
+  const auto f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  if (encode_tmap_2d(&a0, f32, a_big, K, M, Kp * 4, 32, 128, sw) != CUDA_SUCCESS ||
+      encode_tmap_2d(&a1, f32, a_small, K, M, Kp * 4, 32, 128, sw) != CUDA_SUCCESS ||
+      encode_tmap_2d(&b0, f32, bt_big, K, N, Kp * 4, 32, 128, sw) != CUDA_SUCCESS ||
+      encode_tmap_2d(&b1, f32, bt_small, K, N, Kp * 4, 32, 128, sw) != CUDA_SUCCESS ||
+      encode_c_map(&cm, C, M, N, ldc, c_tma) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  if (!c_tma) cm = a0;
+  return launch_tc<KIND_3XTF32>(a0, a1, b0, b1, cm, C, M, N, K, ldc, c_tma, ctl, s);
+}
+
+}  // namespace mhr

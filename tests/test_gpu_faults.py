@@ -1,0 +1,37 @@
+"""Failure detection on the GPU without a fault (GB300 only).
+
+A test hook makes block 0 of a tensor-core kernel arm one ring stage without
+loading it, so its consumers' bounded waits run out. The kernel must record
+the timeout, free its TMEM and exit; gemm_check() must report
+MHR_ERR_TIMEOUT; and the context must stay usable (a following call is
+correct). Nothing traps, faults or hangs.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from parity_util import TOL, DeviceCall, normalised_error, operands
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("path", ["3xtf32", "bf16"])
+def test_injected_stall_reports_timeout(mhr, path):
+    A, B, Ab, Bb = operands(300, 520, 700, 6001, "normal", path)
+    call = DeviceCall(path, A, B, Ab, Bb)
+    old_limit = mhr.gemm_testing_set_wait_limit_ns(50_000_000)  # 50 ms
+    mhr.gemm_testing_set_inject_stall(1)
+    try:
+        call.run(mhr, check=False)
+        bits = mhr.gemm_testing_peek_status(None)
+        assert bits > 0 and (bits & 0x8) == 0, bits  # a timeout, and nothing left in flight
+        assert mhr.gemm_check(None) == mhr.MHR_ERR_TIMEOUT
+        assert mhr.gemm_check(None) == mhr.MHR_OK  # the check clears the word
+    finally:
+        mhr.gemm_testing_set_inject_stall(0)
+        mhr.gemm_testing_set_wait_limit_ns(old_limit)
+    # the context is still healthy: the same call now succeeds
+    C = call.run(mhr).result()
+    Cref, S = oracle.gemm(A, B, with_abs=True)
+    assert normalised_error(C, Cref, S) <= TOL[path]
+

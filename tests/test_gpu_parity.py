@@ -1,0 +1,185 @@
+"""Parity of every CUDA path with the CPU oracle, through the C ABI (GB300 only).
+
+Small and ragged shapes are compared element by element with the full oracle;
+the full-size workloads (4096^3, 8192^3, 3000 x 2050 x 1000) in the exact
+launch configuration the benchmark times are compared on sampled outputs that
+the oracle computes one by one. Integer-valued inputs must match bit for bit;
+real-valued inputs must meet the normalised-error tolerance of each path.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from parity_util import TOL, DeviceCall, normalised_error, operands, sample_indices
+
+pytestmark = pytest.mark.gpu
+
+PATHS = ["f32", "3xtf32", "bf16"]
+
+# (M, N, K): single elements, thin shapes, several tiles with ragged tails in
+# every dimension, and K long enough to wrap every ring several times
+# (bf16: 64-wide K steps x 4 stages; tf32: 32-wide x 3; SIMT: 8-wide x 2).
+SMALL_SHAPES = [
+    (1, 1, 1), (1, 300, 7), (7, 1, 300), (2, 3, 5), (127, 129, 65), (129, 257, 127),
+    (256, 256, 256), (300, 520, 200), (255, 513, 1000), (130, 260, 769), (200, 200, 289),
+    (64, 1100, 33),
+]
+
+
+def check_full(mhr, path, M, N, K, seed, dist="normal", **kw):
+    A, B, Ab, Bb = operands(M, N, K, seed, dist, path)
+    C = DeviceCall(path, A, B, Ab, Bb, **kw).run(mhr).result()
+    Cref, S = oracle.gemm(A, B, with_abs=True)
+    err = normalised_error(C, Cref, S)
+    assert err <= TOL[path], (path, M, N, K, err)
+    return err
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("shape", SMALL_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_small_shapes(mhr, path, shape):
+    check_full(mhr, path, *shape, seed=1000 + sum(shape))
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_config1_uniform_256(mhr, path):
+    """256^3, uniform[-1, 1), seeds (1001, 1002)."""
+    check_full(mhr, path, 256, 256, 256, seed=1001, dist="uniform")
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("shape", [(256, 256, 256), (300, 520, 1000), (8, 8, 8)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_integer_twin_bit_exact(mhr, path, shape):
+    """Integers in {-2..2}: every product and partial sum is exact in fp32, tf32
+    and bf16, so every path must reproduce the oracle bit for bit."""
+    M, N, K = shape
+    A, B, Ab, Bb = operands(M, N, K, 1011, "int", path)
+    C = DeviceCall(path, A, B, Ab, Bb).run(mhr).result()
+    assert np.array_equal(C, oracle.gemm(A, B))
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_block_decomposition_n8_tile4(mhr, path):
+    """The pages' N=8, TILE=4 example on the GPU: C00 = A00*B00 + A01*B10 on
+    integer inputs, each product computed by the same entry point."""
+    A, B, Ab, Bb = operands(8, 8, 8, 11, "int", path)
+    C = DeviceCall(path, A, B, Ab, Bb).run(mhr).result()
+    T = 4
+    for bi in range(2):
+        for bj in range(2):
+            acc = np.zeros((T, T), np.float32)
+            for t in range(2):
+                a = np.ascontiguousarray(A[bi * T:(bi + 1) * T, t * T:(t + 1) * T])
+                b = np.ascontiguousarray(B[t * T:(t + 1) * T, bj * T:(bj + 1) * T])
+                ab = bb = None
+                if path == "bf16":
+                    ab = np.ascontiguousarray(Ab[bi * T:(bi + 1) * T, t * T:(t + 1) * T])
+                    bb = np.ascontiguousarray(Bb[t * T:(t + 1) * T, bj * T:(bj + 1) * T])
+                acc += DeviceCall(path, a, b, ab, bb).run(mhr).result()
+            assert np.array_equal(C[bi * T:(bi + 1) * T, bj * T:(bj + 1) * T], acc)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_identity_and_ones(mhr, path):
+    import seeded_inputs as si
+
+    M, N = 200, 300
+    B = si.matrix(M, N, 77, "int")
+    eye = np.eye(M, dtype=np.float32)
+    ab = bb = None
+    if path == "bf16":
+        ab, _ = si.bf16_rne(eye)
+        bb, _ = si.bf16_rne(B)
+    assert np.array_equal(DeviceCall(path, eye, B, ab, bb).run(mhr).result(), B)
+    K = 1000
+    ones_a, ones_b = np.ones((64, K), np.float32), np.ones((K, 96), np.float32)
+    if path == "bf16":
+        ab, _ = si.bf16_rne(ones_a)
+        bb, _ = si.bf16_rne(ones_b)
+    assert np.all(DeviceCall(path, ones_a, ones_b, ab, bb).run(mhr).result() == K)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_padded_leading_dims_nan_poison(mhr, path):
+    """ld > width with NaN in every pad: a read outside the logical matrix
+    poisons C; a write outside it breaks the guard band (checked in result())."""
+    check_full(mhr, path, 131, 250, 77, seed=2201, lda=77 + 5, ldb=250 + 3, ldc=250 + 7)
+    check_full(mhr, path, 131, 256, 128, seed=2202, lda=136, ldb=264, ldc=260)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_misaligned_pointers(mhr, path):
+    """Operands and output shifted one element off 16-byte alignment: the SIMT
+    path falls back to scalar accesses, the tensor-core paths repack/split the
+    operands and store C without TMA."""
+    check_full(mhr, path, 150, 270, 90, seed=2301, offset=1)
+    check_full(mhr, path, 150, 270, 90, seed=2302, offset=1, lda=91, ldb=271, ldc=271)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_deterministic(mhr, path):
+    """Fixed MMA order: repeated calls give bit-identical results (a missing
+    ring barrier would show up here as run-to-run differences)."""
+    A, B, Ab, Bb = operands(384, 640, 1217, 2401, "normal", path)
+    call = DeviceCall(path, A, B, Ab, Bb)
+    first = call.run(mhr).result()
+    for _ in range(5):
+        assert np.array_equal(call.run(mhr).result(), first)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_degenerate_sizes(mhr, path):
+    import torch
+
+    ent = {"f32": mhr.gemm_f32, "3xtf32": mhr.gemm_f32_3xtf32, "bf16": mhr.gemm_bf16_f32acc}[path]
+    C = torch.full((5, 7), float("nan"), device="cuda")
+    # K == 0: C becomes the empty sum, zero
+    assert ent(None, None, C.data_ptr(), 5, 7, 0, 0, 0, 7, None) == mhr.MHR_OK
+    assert mhr.gemm_check(None) == mhr.MHR_OK
+    assert torch.all(C == 0)
+    # M == 0 / N == 0: nothing written
+    C.fill_(3.0)
+    assert ent(None, None, C.data_ptr(), 0, 7, 4, 4, 7, 7, None) == mhr.MHR_OK
+    assert ent(None, None, C.data_ptr(), 5, 0, 4, 4, 0, 7, None) == mhr.MHR_OK
+    assert torch.all(C == 3.0)
+
+
+def test_config3_rectangular_full(mhr):
+    """3000 x 2050 x 1000, normal(0,1), seeds (3001, 3002): none of the sizes is
+    a tile multiple and B's row pitch (2050 floats) is not 16-byte aligned.
+    Full comparison for both fp32 paths."""
+    M, N, K = 3000, 2050, 1000
+    A, B, _, _ = operands(M, N, K, 3001, "normal", "f32")
+    Cref, S = oracle.gemm(A, B, with_abs=True)
+    for path in ("f32", "3xtf32"):
+        C = DeviceCall(path, A, B).run(mhr).result()
+        err = normalised_error(C, Cref, S)
+        assert err <= TOL[path], (path, err)
+
+
+def sampled_check(mhr, path, M, N, K, seed, dist):
+    A, B, Ab, Bb = operands(M, N, K, seed, dist, path)
+    C = DeviceCall(path, A, B, Ab, Bb).run(mhr).result()
+    rows, cols = sample_indices(M, N, seed, rows=(0, M // 2 + 1, M - 1), cols=(0, N - 1))
+    ref, S = oracle.gemm_entries(A, B, rows, cols, M, N, K)
+    err = normalised_error(C[rows, cols], ref, S)
+    assert err <= TOL[path], (path, M, N, K, err)
+    return err
+
+
+@pytest.mark.parametrize("path", ["f32", "3xtf32"])
+def test_config2_4096_sampled(mhr, path):
+    """4096^3 fp32, uniform[-1, 1), seeds (2001, 2002)."""
+    sampled_check(mhr, path, 4096, 4096, 4096, 2001, "uniform")
+
+
+def test_config4_8192_3xtf32_sampled(mhr):
+    """8192^3 fp32 through 3xTF32, uniform[-1, 1), seeds (4001, 4002)."""
+    sampled_check(mhr, "3xtf32", 8192, 8192, 8192, 4001, "uniform")
+
+
+def test_config5_8192_bf16_sampled(mhr):
+    """8192^3 bf16 inputs (normal(0,1) rounded to bf16), fp32 accumulate and
+    output, seeds (5001, 5002); the oracle runs on the bf16 values."""
+    sampled_check(mhr, "bf16", 8192, 8192, 8192, 5001, "normal")
