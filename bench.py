@@ -1,0 +1,454 @@
+"""Benchmark of the GEMM hot path: C = A * B through the C ABI on one GB300.
+
+One step = one call of the library entry point on one seeded synthetic
+problem, with inputs resident in HBM. The default workload is 4096^3 fp32
+(uniform[-1, 1), seeds 2001/2002) through gemm_f32_3xtf32 -- the split
+pre-pass, TMA ring, tcgen05 main loop and epilogue -- and the same problem
+through the strict-fp32 SIMT path is reported beside it. Other workloads:
+--workload c1 (256^3), c3 (3000 x 2050 x 1000), c4 (8192^3 3xTF32),
+c5 (8192^3 bf16).
+
+Prints ONE JSON line (rank 0). Metric: 2MNK / t in TFLOPS. L2 is flushed
+(a 256 MiB write) between timed steps, outside the per-step CUDA events.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c2]
+    python bench.py --impl reference ...   # the CPU oracle, timed as it stands
+
+Under torchrun (N > 1) every rank runs its own independent problem on its own
+GPU (weak scaling, no collective on the data path); the reported time is the
+max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOPS (2MNK/t) at N=4096/8192 on 1 GB300; % of pipe roofline"
+
+WORKLOADS = {
+    "c1": dict(M=256, N=256, K=256, dist="uniform", seeds=(1001, 1002), path="3xtf32",
+               also="f32", desc="fp32 square 256^3, uniform[-1,1)"),
+    "c2": dict(M=4096, N=4096, K=4096, dist="uniform", seeds=(2001, 2002), path="3xtf32",
+               also="f32", desc="fp32 square 4096^3, uniform[-1,1) (the pages' worked size)"),
+    "c3": dict(M=3000, N=2050, K=1000, dist="normal", seeds=(3001, 3002), path="3xtf32",
+               also="f32", desc="fp32 rectangular 3000x2050x1000, normal(0,1), ragged edges"),
+    "c4": dict(M=8192, N=8192, K=8192, dist="uniform", seeds=(4001, 4002), path="3xtf32",
+               also=None, desc="fp32-accurate 8192^3 via 3xTF32, uniform[-1,1)"),
+    "c5": dict(M=8192, N=8192, K=8192, dist="normal", seeds=(5001, 5002), path="bf16",
+               also=None, desc="bf16 inputs (normal(0,1) rounded), fp32 accumulate, 8192^3"),
+}
+ENTRY = {"f32": "gemm_f32", "3xtf32": "gemm_f32_3xtf32", "bf16": "gemm_bf16_f32acc"}
+DTYPE = {"f32": "f32", "3xtf32": "tf32x3", "bf16": "bf16"}
+# our kernel launches per call (split A, split B^T, main; pack kernels only for
+# unaligned bf16 operands, never in these workloads)
+LAUNCHES = {"f32": 1, "3xtf32": 3, "bf16": 1}
+TF32_OVER_BF16 = 1.1 / 2.25   # nominal dense tensor rates (PFLOP/s) of GB300
+FP32_LANES_PER_SM = 128
+L2_FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained"),
+                    sm_max_mhz=d.get("sm_max_mhz", 2070.0), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0,
+                sm_max_mhz=2070.0, source="fallback")
+
+
+def source_digest() -> str:
+    """Hash of the kernel sources, to tell whether stored ncu counters still apply."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "memory_hierarchy_reuse_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(f.encode())
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        e = d[kernel][workload]
+        if e.get("source_digest") != source_digest():
+            return None
+        return e["dram_bytes_per_launch"]
+    except (KeyError, ValueError, TypeError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons, sampled every 100 ms in the background."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.rows = []
+        self.proc = None
+        import torch
+
+        ident = []
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            ident = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            ident = []
+        cmd = ["nvidia-smi", *ident, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == 7:
+                self.rows.append((time.time(), parts))
+
+    def window(self, t0, t1):
+        return [r for (t, r) in self.rows if t0 <= t <= t1]
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    @staticmethod
+    def summary(rows):
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def oracle_rows(A, B, rows, nthreads=0):
+    """CPU oracle on the first `rows` rows of C (the bounded CPU sample)."""
+    import oracle
+
+    t0 = time.perf_counter()
+    C = oracle.gemm(A[:rows], B, nthreads=nthreads)
+    return C, time.perf_counter() - t0
+
+
+def calibrate_rows(A, B, budget_s, max_rows):
+    """Rows of C the oracle computes in about budget_s seconds on this host."""
+    r = 2
+    _, t = oracle_rows(A, B, r)
+    while t < 0.5 and r < max_rows:
+        r = min(max_rows, r * 4)
+        _, t = oracle_rows(A, B, r)
+    return max(1, min(max_rows, int(r * budget_s / max(t, 1e-6)))), t / r
+
+
+def host_operands(w):
+    import seeded_inputs as si
+
+    A = si.matrix(w["M"], w["K"], w["seeds"][0], w["dist"])
+    B = si.matrix(w["K"], w["N"], w["seeds"][1], w["dist"])
+    if w["path"] == "bf16":
+        Ab, A = si.bf16_rne(A)
+        Bb, B = si.bf16_rne(B)
+        return A.reshape(w["M"], w["K"]), B.reshape(w["K"], w["N"]), Ab, Bb
+    return A, B, None, None
+
+
+def run_reference(args, w, world, rank):
+    """The oracle as it stands, timed on this host's cores: each step computes a
+    bounded sample of rows of C; TFLOPS = 2 * rows * N * K / t."""
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    A, B, _, _ = host_operands(w)
+    steps = args.steps
+    per_step_budget = max(0.5, 100.0 / (steps + args.warmup))
+    rows, _ = calibrate_rows(A, B, per_step_budget, w["M"])
+    for _ in range(args.warmup):
+        oracle_rows(A, B, rows)
+    times = [oracle_rows(A, B, rows)[1] for _ in range(steps)]
+    t = sum(times) / len(times)
+    value = 2.0 * rows * w["N"] * w["K"] / t / 1e12
+    cores = oracle.max_threads()
+    sample = f"rows 0..{rows - 1} of C ({rows} x {w['N']} outputs, K={w['K']}) per step"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w["desc"], "M": w["M"], "N": w["N"], "K": w["K"],
+                   "entry": "CPU oracle (fp64 accumulate)", "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="c2", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="mhr", choices=["mhr", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle work for the cpu_baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    w = WORKLOADS[args.workload]
+    world, rank, local = dist_setup()
+
+    if args.impl == "reference":
+        run_reference(args, w, world, rank)
+        return
+
+    import numpy as np
+    import torch
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    from memory_hierarchy_reuse_gb300 import build as mbuild
+
+    mbuild.build()
+    import memory_hierarchy_reuse_gb300 as mhr
+    from memory_hierarchy_reuse_gb300 import model
+
+    lib = mhr.load()
+    M, N, K = w["M"], w["N"], w["K"]
+    A_h, B_h, Ab_h, Bb_h = host_operands(w)
+    path = w["path"]
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    def device_operands(p):
+        if p == "bf16":
+            a = torch.from_numpy(Ab_h.view(np.int16).reshape(M, K)).pin_memory()
+            b = torch.from_numpy(Bb_h.view(np.int16).reshape(K, N)).pin_memory()
+        else:
+            a = torch.from_numpy(A_h).pin_memory()
+            b = torch.from_numpy(B_h).pin_memory()
+        return a, b, a.to(dev), b.to(dev)
+
+    a_pin, b_pin, a_d, b_d = device_operands(path)
+    c_d = torch.empty((M, N), dtype=torch.float32, device=dev)
+    c_pin = torch.empty((M, N), dtype=torch.float32).pin_memory()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    entry = getattr(lib, ENTRY[path])
+
+    def call(p=path, a=None, b=None):
+        a = a_d if a is None else a
+        b = b_d if b is None else b
+        rc = getattr(lib, ENTRY[p])(a.data_ptr(), b.data_ptr(), c_d.data_ptr(), M, N, K, K, N, N, sh)
+        if rc != mhr.MHR_OK:
+            raise mhr.GemmError(rc, ENTRY[p])
+
+    def timed_steps(p, steps, a=None, b=None):
+        """Per-step CUDA events around each call (L2 flushed before each, outside
+        the events), plus events around the main kernel of each call."""
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+               torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for e in ev:  # create the underlying events
+            for x in e:
+                x.record(stream)
+        torch.cuda.synchronize(dev)
+        for s0, s1, k0, k1 in ev:
+            flush.zero_()
+            lib.gemm_testing_set_main_kernel_events(k0.cuda_event, k1.cuda_event)
+            s0.record(stream)
+            call(p, a, b)
+            s1.record(stream)
+        lib.gemm_testing_set_main_kernel_events(None, None)
+        torch.cuda.synchronize(dev)
+        step_ms = [s0.elapsed_time(s1) for s0, s1, _, _ in ev]
+        kern_ms = [k0.elapsed_time(k1) for _, _, k0, k1 in ev]
+        return step_ms, kern_ms
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        t = torch.tensor([x], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    # ---------------------------------------------------------------- warm-up
+    for _ in range(args.warmup):
+        call()
+    rc = lib.gemm_check(sh)
+    if rc != mhr.MHR_OK:
+        raise mhr.GemmError(rc, "warm-up")
+
+    # ---------------------------------------------------------------- timed
+    time.sleep(0.5)  # let the clock sampler start
+    barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    step_ms, kern_ms = timed_steps(path, args.steps)
+    torch.cuda.synchronize(dev)
+    barrier()
+    t_wall1 = time.time()
+    rc = lib.gemm_check(sh)
+    if rc != mhr.MHR_OK:
+        raise mhr.GemmError(rc, "timed region")
+    ms_step = max_over_ranks(sum(step_ms) / len(step_ms))
+    ms_kern = max_over_ranks(sum(kern_ms) / len(kern_ms))
+    flop = model.flops(M, N, K)
+    value = world * flop / (ms_step * 1e-3) / 1e12
+
+    # ------------------------------------------------- end to end (host buffers)
+    e2e_steps = max(3, min(args.steps, 20))
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        a_d.copy_(a_pin, non_blocking=True)
+        b_d.copy_(b_pin, non_blocking=True)
+        call()
+        c_pin.copy_(c_d, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps)
+    h2d = a_pin.numel() * a_pin.element_size() + b_pin.numel() * b_pin.element_size()
+    d2h = c_pin.numel() * 4
+
+    # ------------------------------------- the strict-fp32 SIMT path, same problem
+    extra = {}
+    if w["also"]:
+        also = w["also"]
+        call(also)
+        s_ms, s_k = timed_steps(also, max(3, min(args.steps, 50)))
+        simt_ms = max_over_ranks(sum(s_ms) / len(s_ms))
+        simt_k = max_over_ranks(sum(s_k) / len(s_k))
+        clock_mhz = peaks()["sm_max_mhz"]
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        fp32_peak = sms * FP32_LANES_PER_SM * 2 * clock_mhz * 1e6 / 1e12
+        extra[ENTRY[also]] = {
+            "value": world * flop / (simt_ms * 1e-3) / 1e12, "unit": "TFLOPS", "ms_per_step": simt_ms,
+            "roofline": {"bound": "alu", "achieved": flop / (simt_k * 1e-3) / 1e12,
+                         "peak": fp32_peak, "unit": "TFLOP/s",
+                         "frac": flop / (simt_k * 1e-3) / 1e12 / fp32_peak,
+                         "peak_note": f"{sms} SMs x {FP32_LANES_PER_SM} fp32 lanes x 2 x "
+                                      f"{clock_mhz:.0f} MHz (max SM clock)"},
+        }
+
+    clocks = None
+    if sampler:
+        sampler.stop()
+        clocks = ClockSampler.summary(sampler.window(t_wall0, t_wall1))
+
+    # ---------------------------------------------------------------- roofline
+    pk = peaks()
+    if path == "bf16":
+        tensor_flop, peak_tf, peak_note = flop, pk["bf16_tflops"], "bf16 dense, burst"
+    elif path == "3xtf32":
+        tensor_flop = 3 * flop
+        peak_tf = pk["bf16_tflops"] * TF32_OVER_BF16
+        peak_note = "tf32 = bf16 burst x 1.1/2.25 (nominal tf32/bf16 ratio); 3 MMAs per product"
+    else:
+        tensor_flop, peak_tf, peak_note = flop, None, ""
+    kernel_name = {"3xtf32": "tc_gemm_kernel<3xtf32>", "bf16": "tc_gemm_kernel<bf16>",
+                   "f32": "simt_f32_kernel"}[path]
+    achieved = tensor_flop / (ms_kern * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": achieved / peak_tf if peak_tf else None,
+                "traffic": stored_traffic(kernel_name, args.workload),
+                "kernel": kernel_name, "kernel_ms": ms_kern,
+                "peak_source": f"{pk['source']} ({peak_note})"}
+
+    # ---------------------------------------------------------------- CPU baseline
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+
+        oracle.build()
+        rows, _ = calibrate_rows(A_h, B_h, args.cpu_budget, M)
+        C_ref, t_cpu = oracle_rows(A_h, B_h, rows)
+        # the same rows from the GPU (last timed call's output)
+        call()
+        torch.cuda.synchronize(dev)
+        c_rows = c_d[:rows].cpu().numpy()
+        S = np.abs(A_h[:rows].astype(np.float64)) @ np.abs(B_h.astype(np.float64))
+        nerr = float(np.max(np.abs(c_rows.astype(np.float64) - C_ref) / np.maximum(S, 1e-300)))
+        cpu = {"value": 2.0 * rows * N * K / t_cpu / 1e12, "unit": "TFLOPS",
+               "cores": oracle.max_threads(), "kind": "oracle",
+               "sample": f"rows 0..{rows - 1} of C ({rows} x {N} outputs, K={K}), "
+                         f"{t_cpu:.1f} s of CPU work",
+               "gpu_vs_sample_normalised_error": nerr}
+
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": DTYPE[path], "data": "synthetic",
+            "config": {"workload": w["desc"], "M": M, "N": N, "K": K, "entry": ENTRY[path],
+                       "dist": w["dist"], "seeds": list(w["seeds"]),
+                       "l2": "flushed before every timed step (256 MiB write, outside the step events)",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * flop / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "note": "pinned host A, B -> device, C API call, C -> pinned host, per step"},
+            "gpu_launches": LAUNCHES[path] * args.steps,
+            "clocks": clocks,
+            "paths": extra,
+            "source_digest": source_digest(),
+        }
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

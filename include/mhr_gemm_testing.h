@@ -38,6 +38,16 @@ int gemm_testing_set_inject_stall(int enable);
  */
 int64_t gemm_testing_peek_status(void* stream);
 
+/*
+ * Profiling hook.  When `start` and `stop` are both non-NULL cudaEvent_t
+ * handles, every following gemm_* call records `start` on its stream just
+ * before it launches its main GEMM kernel (after any split or pack pre-pass)
+ * and `stop` just after, so the caller can time that kernel alone with
+ * cudaEventElapsedTime.  Passing NULL for either turns the hook off.  The
+ * events stay owned by the caller.
+ */
+void gemm_testing_set_main_kernel_events(void* start, void* stop);
+
 #ifdef __cplusplus
 }
 #endif

@@ -40,7 +40,7 @@ PATHS = ("f32", "3xtf32", "bf16")
 EXPORTS = ("gemm_f32", "gemm_f32_3xtf32", "gemm_bf16_f32acc", "gemm_check",
            "gemm_status_string", "gemm_release", "gemm_version",
            "gemm_testing_set_wait_limit_ns", "gemm_testing_set_inject_stall",
-           "gemm_testing_peek_status")
+           "gemm_testing_peek_status", "gemm_testing_set_main_kernel_events")
 
 _lib = None
 
@@ -81,6 +81,8 @@ def load(path: str | None = None):
     lib.gemm_testing_set_inject_stall.restype = ctypes.c_int
     lib.gemm_testing_peek_status.argtypes = [vp]
     lib.gemm_testing_peek_status.restype = ctypes.c_int64
+    lib.gemm_testing_set_main_kernel_events.argtypes = [vp, vp]
+    lib.gemm_testing_set_main_kernel_events.restype = None
     _lib = lib
     return lib
 
@@ -123,6 +125,11 @@ def gemm_testing_set_inject_stall(enable: int) -> int:
 
 def gemm_testing_peek_status(stream=None) -> int:
     return load().gemm_testing_peek_status(stream)
+
+
+def gemm_testing_set_main_kernel_events(start=None, stop=None) -> None:
+    """start/stop: cudaEvent_t handles as ints (torch.cuda.Event().cuda_event) or None."""
+    load().gemm_testing_set_main_kernel_events(start, stop)
 
 
 _ENTRY = {"f32": "gemm_f32", "3xtf32": "gemm_f32_3xtf32", "bf16": "gemm_bf16_f32acc"}

@@ -42,6 +42,18 @@ std::map<int, DeviceState> g_devices;
 std::map<std::pair<int, cudaStream_t>, Workspace> g_workspaces;
 uint64_t g_wait_limit_ns = 2000000000ull;
 int g_inject_stall = 0;
+cudaEvent_t g_main_start = nullptr, g_main_stop = nullptr;
+
+// Brackets the main kernel launch with the caller's profiling events, if set.
+struct MainKernelEvents {
+  cudaStream_t s;
+  explicit MainKernelEvents(cudaStream_t st) : s(st) {
+    if (g_main_start && g_main_stop) cudaEventRecord(g_main_start, s);
+  }
+  ~MainKernelEvents() {
+    if (g_main_start && g_main_stop) cudaEventRecord(g_main_stop, s);
+  }
+};
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -197,6 +209,7 @@ MHR_API int gemm_f32(const float* A, const float* B, float* C, int64_t M, int64_
   if ((rc = device_state(&st, nullptr)) != MHR_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (K == 0) return from_cuda(launch_zero_fill(C, M, N, ldc, s));
+  MainKernelEvents ev(s);
   return from_cuda(launch_simt_f32(A, B, C, M, N, K, lda, ldb, ldc, s));
 }
 
@@ -223,6 +236,7 @@ MHR_API int gemm_f32_3xtf32(const float* A, const float* B, float* C, int64_t M,
   cudaError_t e = launch_split_tf32(A, B, M, N, K, lda, ldb, Kp, a_big, a_small, bt_big, bt_small, s);
   if (e != cudaSuccess) return from_cuda(e);
   const bool c_tma = aligned16(C) && (ldc % 4) == 0;
+  MainKernelEvents ev(s);
   return from_cuda(launch_tc_3xtf32(a_big, a_small, bt_big, bt_small, C, M, N, K, Kp, ldc, c_tma,
                                     make_ctl(*st), s));
 }
@@ -262,6 +276,7 @@ MHR_API int gemm_bf16_f32acc(const uint16_t* A, const uint16_t* B, float* C, int
     }
   }
   const bool c_tma = aligned16(C) && (ldc % 4) == 0;
+  MainKernelEvents ev(s);
   return from_cuda(launch_tc_bf16(A, B, C, M, N, K, lda, ldb, ldc, c_tma, make_ctl(*st), s));
 }
 
@@ -323,6 +338,12 @@ MHR_API int gemm_testing_set_inject_stall(int enable) {
   const int old = g_inject_stall;
   g_inject_stall = enable ? 1 : 0;
   return old;
+}
+
+MHR_API void gemm_testing_set_main_kernel_events(void* start, void* stop) {
+  std::lock_guard<std::mutex> g(g_mu);
+  g_main_start = static_cast<cudaEvent_t>(start);
+  g_main_stop = static_cast<cudaEvent_t>(stop);
 }
 
 MHR_API int64_t gemm_testing_peek_status(void* stream) {
