@@ -97,6 +97,32 @@ int gemm_bf16_f32acc(const uint16_t* A, const uint16_t* B, float* C, int64_t M, 
                      int64_t K, int64_t lda, int64_t ldb, int64_t ldc, void* stream);
 
 /*
+ * The 3xTF32 GEMM without any device allocation.  The pages have no
+ * counterpart: this entry point exists for callers that must not allocate
+ * device memory inside a library call -- programs whose device memory is
+ * owned by their own pool allocator (an outside cudaMalloc may fail or
+ * fragment it), latency-critical loops (cudaMalloc and cudaFree synchronise
+ * the device), and programs in which only one owner thread allocates.
+ *
+ * Same arguments, result and numerics as gemm_f32_3xtf32 (same kernels).  The
+ * split operands live in a 64 MiB static device array inside the library
+ * instead of the allocated workspace:
+ *   - problems for which 8 * Kp * (M + N) bytes exceed 64 MiB, Kp = K
+ *     rounded up to a multiple of 4 (e.g. larger than M = N = K = 2048), are
+ *     rejected with MHR_ERR_INVALID_ARG before any work is enqueued;
+ *   - every GPU on which the library is loaded holds those 64 MiB until exit;
+ *   - all calls on a device share the one array.  Calls whose work overlaps
+ *     on the GPU (streams with no ordering between them) race on it and give
+ *     wrong results: order them on one stream or with events.  The array
+ *     keeps the last call's contents; nothing in it needs to start at zero;
+ *   - the first call on each device looks up the array's device address;
+ *     make that first call before any stream capture begins.
+ * The caller still passes (and owns) A, B and C.
+ */
+int gemm_f32_3xtf32_noalloc(const float* A, const float* B, float* C, int64_t M, int64_t N,
+                            int64_t K, int64_t lda, int64_t ldb, int64_t ldc, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's status
  * word.  Returns MHR_OK, MHR_ERR_TIMEOUT (some kernel since the last check hit
  * a wait limit) or MHR_ERR_CUDA (the synchronisation itself failed).

@@ -11,6 +11,7 @@ Raw entry points (same names and arguments as the C ABI; pointers are ints,
     gemm_f32(A, B, C, M, N, K, lda, ldb, ldc, stream) -> status
     gemm_f32_3xtf32(...)                               -> status
     gemm_bf16_f32acc(...)                              -> status
+    gemm_f32_3xtf32_noalloc(...)                       -> status
     gemm_check(stream) -> status
     gemm_status_string(status) -> str
     gemm_release()
@@ -37,7 +38,8 @@ MHR_ERR_TIMEOUT = 4
 PATHS = ("f32", "3xtf32", "bf16")
 
 #: every symbol the public headers declare
-EXPORTS = ("gemm_f32", "gemm_f32_3xtf32", "gemm_bf16_f32acc", "gemm_check",
+EXPORTS = ("gemm_f32", "gemm_f32_3xtf32", "gemm_bf16_f32acc", "gemm_f32_3xtf32_noalloc",
+           "gemm_check",
            "gemm_status_string", "gemm_release", "gemm_version",
            "gemm_testing_set_wait_limit_ns", "gemm_testing_set_inject_stall",
            "gemm_testing_peek_status", "gemm_testing_set_main_kernel_events")
@@ -63,7 +65,7 @@ def load(path: str | None = None):
             "(there is no fallback implementation)")
     lib = ctypes.CDLL(path)
     vp, i64 = ctypes.c_void_p, ctypes.c_int64
-    for name in ("gemm_f32", "gemm_f32_3xtf32", "gemm_bf16_f32acc"):
+    for name in ("gemm_f32", "gemm_f32_3xtf32", "gemm_bf16_f32acc", "gemm_f32_3xtf32_noalloc"):
         f = getattr(lib, name)
         f.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, vp]
         f.restype = ctypes.c_int
@@ -97,6 +99,12 @@ def gemm_f32_3xtf32(A, B, C, M, N, K, lda, ldb, ldc, stream=None) -> int:
 
 def gemm_bf16_f32acc(A, B, C, M, N, K, lda, ldb, ldc, stream=None) -> int:
     return load().gemm_bf16_f32acc(A, B, C, M, N, K, lda, ldb, ldc, stream)
+
+
+def gemm_f32_3xtf32_noalloc(A, B, C, M, N, K, lda, ldb, ldc, stream=None) -> int:
+    """gemm_f32_3xtf32 with its scratch in a 64 MiB static device array: no
+    device allocation in the call (for callers that must not allocate)."""
+    return load().gemm_f32_3xtf32_noalloc(A, B, C, M, N, K, lda, ldb, ldc, stream)
 
 
 def gemm_check(stream=None) -> int:

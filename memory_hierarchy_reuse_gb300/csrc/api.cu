@@ -195,6 +195,19 @@ CUresult encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void*
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+int check_gemm_args(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
+                    int64_t lda, int64_t ldb, int64_t ldc, int64_t esz_ab, bool* noop) {
+  return validate(A, B, C, M, N, K, lda, ldb, ldc, esz_ab, noop);
+}
+
+int current_device_ctl(DeviceCtl* ctl, int* dev) {
+  std::lock_guard<std::mutex> g(g_mu);
+  DeviceState* st;
+  const int rc = device_state(&st, dev);
+  if (rc == MHR_OK) *ctl = make_ctl(*st);
+  return rc;
+}
+
 }  // namespace mhr
 
 using namespace mhr;

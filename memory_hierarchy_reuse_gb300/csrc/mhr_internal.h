@@ -56,4 +56,13 @@ CUresult encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void*
                         uint64_t inner, uint64_t outer, uint64_t row_pitch_bytes,
                         uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
 
+// The C-ABI front end's argument checks (api.cu), for entry points defined in
+// other translation units.  Returns an mhr_status; *noop is set when M or N is 0.
+int check_gemm_args(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
+                    int64_t lda, int64_t ldb, int64_t ldc, int64_t esz_ab, bool* noop);
+
+// The current device's kernel controls (status word, wait limit, SM count);
+// MHR_ERR_UNSUPPORTED unless the device is sm_103.
+int current_device_ctl(DeviceCtl* ctl, int* dev);
+
 }  // namespace mhr
