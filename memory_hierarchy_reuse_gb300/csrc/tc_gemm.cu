@@ -451,6 +451,96 @@ __global__ void split_bt_kernel(const float* __restrict__ B, int64_t K, int64_t 
   }
 }
 
+// Vectorised split of both operands in one launch (A, B and C pointers
+// 16-byte aligned, K, N, lda, ldb multiples of 4, so Kp == K).  Blocks
+// [0, a_blocks) split rows of A in place-order; the remaining blocks split
+// 64 x 64 tiles of B and write them transposed.  Each thread keeps four
+// 16-byte loads in flight.
+constexpr int SPLIT_THREADS = 256;
+constexpr int SPLIT_TILE = 64;
+
+__device__ __forceinline__ void split4(const float4 v, float4& b, float4& s) {
+  split_tf32(v.x, b.x, s.x);
+  split_tf32(v.y, b.y, s.y);
+  split_tf32(v.z, b.z, s.z);
+  split_tf32(v.w, b.w, s.w);
+}
+
+__global__ void __launch_bounds__(SPLIT_THREADS)
+    split_vec_kernel(const float* __restrict__ A, const float* __restrict__ B, int64_t M,
+                     int64_t N, int64_t K, int64_t lda, int64_t ldb, int a_blocks,
+                     float* __restrict__ a_big, float* __restrict__ a_small,
+                     float* __restrict__ bt_big, float* __restrict__ bt_small) {
+  __shared__ float tb[SPLIT_TILE][SPLIT_TILE + 1];
+  __shared__ float ts[SPLIT_TILE][SPLIT_TILE + 1];
+  const int t = threadIdx.x;
+  if (static_cast<int>(blockIdx.x) < a_blocks) {
+    const int64_t k4 = K / 4;
+    for (int64_t r = blockIdx.x; r < M; r += a_blocks) {
+      const float4* src = reinterpret_cast<const float4*>(A + r * lda);
+      float4* db = reinterpret_cast<float4*>(a_big + r * K);
+      float4* ds = reinterpret_cast<float4*>(a_small + r * K);
+      for (int64_t c0 = t; c0 < k4; c0 += 4 * SPLIT_THREADS) {
+        float4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int64_t c = c0 + j * SPLIT_THREADS;
+          if (c < k4) v[j] = __ldg(src + c);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int64_t c = c0 + j * SPLIT_THREADS;
+          if (c < k4) {
+            float4 b, s;
+            split4(v[j], b, s);
+            db[c] = b;
+            ds[c] = s;
+          }
+        }
+      }
+    }
+    return;
+  }
+  // B role: tile (k0, n0) of 64 x 64.
+  const int64_t tiles_n = (N + SPLIT_TILE - 1) / SPLIT_TILE;
+  const int64_t tiles = tiles_n * ((K + SPLIT_TILE - 1) / SPLIT_TILE);
+  const int64_t nb = gridDim.x - a_blocks;
+  for (int64_t tile = blockIdx.x - a_blocks; tile < tiles; tile += nb) {
+    const int64_t n0 = (tile % tiles_n) * SPLIT_TILE, k0 = (tile / tiles_n) * SPLIT_TILE;
+    float4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {  // read: 64 k-rows x 16 float4 along n
+      const int idx = t + j * SPLIT_THREADS;
+      const int64_t k = k0 + (idx >> 4), n = n0 + (idx & 15) * 4;
+      v[j] = (k < K && n < N) ? __ldg(reinterpret_cast<const float4*>(B + k * ldb + n))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int idx = t + j * SPLIT_THREADS;
+      const int kr = idx >> 4, nc = (idx & 15) * 4;
+      float4 b, s;
+      split4(v[j], b, s);
+      tb[kr][nc] = b.x; tb[kr][nc + 1] = b.y; tb[kr][nc + 2] = b.z; tb[kr][nc + 3] = b.w;
+      ts[kr][nc] = s.x; ts[kr][nc + 1] = s.y; ts[kr][nc + 2] = s.z; ts[kr][nc + 3] = s.w;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {  // write: 64 n-rows x 16 float4 along k
+      const int idx = t + j * SPLIT_THREADS;
+      const int nr = idx >> 4, kc = (idx & 15) * 4;
+      const int64_t n = n0 + nr, k = k0 + kc;
+      if (n < N && k < K) {
+        *reinterpret_cast<float4*>(bt_big + n * K + k) =
+            make_float4(tb[kc][nr], tb[kc + 1][nr], tb[kc + 2][nr], tb[kc + 3][nr]);
+        *reinterpret_cast<float4*>(bt_small + n * K + k) =
+            make_float4(ts[kc][nr], ts[kc + 1][nr], ts[kc + 2][nr], ts[kc + 3][nr]);
+      }
+    }
+    __syncthreads();
+  }
+}
+
 template <int KIND, bool TMA_STORE>
 cudaError_t prepare_kernel() {
   // cudaFuncSetAttribute is per device; callers run it on every launch (cheap).
@@ -517,6 +607,27 @@ cudaError_t launch_pack_u16(const uint16_t* src, int64_t rows, int64_t cols, int
 cudaError_t launch_split_tf32(const float* A, const float* B, int64_t M, int64_t N, int64_t K,
                               int64_t lda, int64_t ldb, int64_t Kp, float* a_big, float* a_small,
                               float* bt_big, float* bt_small, cudaStream_t s) {
+  auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  const bool vec = Kp == K && K % 4 == 0 && N % 4 == 0 && lda % 4 == 0 && ldb % 4 == 0 &&
+                   al16(A) && al16(B) && al16(a_big) && al16(a_small) && al16(bt_big) &&
+                   al16(bt_small);
+  if (vec) {
+    // One wave of resident blocks (6 per SM fit), shared between the operands
+    // in proportion to their sizes.
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t total = static_cast<int64_t>(sms) * 6;
+    const int64_t b_tiles = ((N + SPLIT_TILE - 1) / SPLIT_TILE) * ((K + SPLIT_TILE - 1) / SPLIT_TILE);
+    const double a_share = static_cast<double>(M) / static_cast<double>(M + N);
+    int64_t a_blocks = static_cast<int64_t>(a_share * total);
+    a_blocks = a_blocks < 1 ? 1 : (a_blocks > M ? M : a_blocks);
+    int64_t b_blocks = total - a_blocks;
+    b_blocks = b_blocks < 1 ? 1 : (b_blocks > b_tiles ? b_tiles : b_blocks);
+    split_vec_kernel<<<static_cast<unsigned>(a_blocks + b_blocks), SPLIT_THREADS, 0, s>>>(
+        A, B, M, N, K, lda, ldb, static_cast<int>(a_blocks), a_big, a_small, bt_big, bt_small);
+    return cudaGetLastError();
+  }
   const unsigned gx = static_cast<unsigned>((K + 255) / 256 < 64 ? (K + 255) / 256 : 64);
   split_a_kernel<<<dim3(gx, grid_rows(M)), 256, 0, s>>>(A, M, K, lda, Kp, a_big, a_small);
   cudaError_t e = cudaGetLastError();
