@@ -39,6 +39,15 @@ int gemm_testing_set_inject_stall(int enable);
 int64_t gemm_testing_peek_status(void* stream);
 
 /*
+ * Chooses the tensor-core kernel variant of the following calls
+ * (process-wide): 0 = automatic (the CTA-pair kernel when its 256-row tiles
+ * fill the GPU, else the single-CTA kernel), 1 = always the single-CTA
+ * kernel, 2 = always the CTA-pair kernel.  Other values mean 0.  Returns the
+ * previous mode.
+ */
+int gemm_testing_set_cta_pair_mode(int mode);
+
+/*
  * Profiling hook.  When `start` and `stop` are both non-NULL cudaEvent_t
  * handles, every following gemm_* call records `start` on its stream just
  * before it launches its main GEMM kernel (after any split or pack pre-pass)

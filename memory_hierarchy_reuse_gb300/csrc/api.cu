@@ -42,6 +42,7 @@ std::map<int, DeviceState> g_devices;
 std::map<std::pair<int, cudaStream_t>, Workspace> g_workspaces;
 uint64_t g_wait_limit_ns = 2000000000ull;
 int g_inject_stall = 0;
+int g_pair_mode = 0;
 cudaEvent_t g_main_start = nullptr, g_main_stop = nullptr;
 
 // Brackets the main kernel launch with the caller's profiling events, if set.
@@ -167,6 +168,7 @@ DeviceCtl make_ctl(const DeviceState& st) {
   c.wait_limit_ns = g_wait_limit_ns;
   c.inject_stall = g_inject_stall;
   c.sm_count = st.sm_count;
+  c.pair_mode = g_pair_mode;
   return c;
 }
 
@@ -350,6 +352,13 @@ MHR_API int gemm_testing_set_inject_stall(int enable) {
   std::lock_guard<std::mutex> g(g_mu);
   const int old = g_inject_stall;
   g_inject_stall = enable ? 1 : 0;
+  return old;
+}
+
+MHR_API int gemm_testing_set_cta_pair_mode(int mode) {
+  std::lock_guard<std::mutex> g(g_mu);
+  const int old = g_pair_mode;
+  g_pair_mode = (mode == 1 || mode == 2) ? mode : 0;
   return old;
 }
 

@@ -15,10 +15,12 @@ from parity_util import TOL, DeviceCall, normalised_error, operands
 pytestmark = pytest.mark.gpu
 
 
+@pytest.mark.parametrize("mode", [1, 2], ids=["1cta", "pair"])
 @pytest.mark.parametrize("path", ["3xtf32", "bf16"])
-def test_injected_stall_reports_timeout(mhr, path):
+def test_injected_stall_reports_timeout(mhr, path, mode):
     A, B, Ab, Bb = operands(300, 520, 700, 6001, "normal", path)
     call = DeviceCall(path, A, B, Ab, Bb)
+    old_mode = mhr.gemm_testing_set_cta_pair_mode(mode)
     old_limit = mhr.gemm_testing_set_wait_limit_ns(50_000_000)  # 50 ms
     mhr.gemm_testing_set_inject_stall(1)
     try:
@@ -31,7 +33,10 @@ def test_injected_stall_reports_timeout(mhr, path):
         mhr.gemm_testing_set_inject_stall(0)
         mhr.gemm_testing_set_wait_limit_ns(old_limit)
     # the context is still healthy: the same call now succeeds
-    C = call.run(mhr).result()
+    try:
+        C = call.run(mhr).result()
+    finally:
+        mhr.gemm_testing_set_cta_pair_mode(old_mode)
     Cref, S = oracle.gemm(A, B, with_abs=True)
     assert normalised_error(C, Cref, S) <= TOL[path]
 

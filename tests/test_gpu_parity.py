@@ -15,10 +15,24 @@ from parity_util import TOL, DeviceCall, normalised_error, operands, sample_indi
 pytestmark = pytest.mark.gpu
 
 PATHS = ["f32", "3xtf32", "bf16"]
+# Each tensor-core path has two kernels: the single-CTA kernel (128-row tiles)
+# and the CTA-pair kernel (256-row tiles over a cluster of 2). Both are forced
+# in turn on every small shape; full-size checks use the automatic choice, as
+# the benchmark does.
+VARIANTS = [("f32", 0), ("3xtf32", 1), ("3xtf32", 2), ("bf16", 1), ("bf16", 2)]
+VARIANT_IDS = ["f32", "3xtf32-1cta", "3xtf32-pair", "bf16-1cta", "bf16-pair"]
+
+
+@pytest.fixture(params=VARIANTS, ids=VARIANT_IDS)
+def path(request, mhr):
+    name, mode = request.param
+    old = mhr.gemm_testing_set_cta_pair_mode(mode)
+    yield name
+    mhr.gemm_testing_set_cta_pair_mode(old)
 
 # (M, N, K): single elements, thin shapes, several tiles with ragged tails in
 # every dimension, and K long enough to wrap every ring several times
-# (bf16: 64-wide K steps x 4 stages; tf32: 32-wide x 3; SIMT: 8-wide x 2).
+# (bf16: 64-wide K steps x 4 or 6 stages; tf32: 32-wide x 3; SIMT: 8-wide x 2).
 SMALL_SHAPES = [
     (1, 1, 1), (1, 300, 7), (7, 1, 300), (2, 3, 5), (127, 129, 65), (129, 257, 127),
     (256, 256, 256), (300, 520, 200), (255, 513, 1000), (130, 260, 769), (200, 200, 289),
@@ -35,19 +49,16 @@ def check_full(mhr, path, M, N, K, seed, dist="normal", **kw):
     return err
 
 
-@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("shape", SMALL_SHAPES, ids=lambda s: "x".join(map(str, s)))
 def test_small_shapes(mhr, path, shape):
     check_full(mhr, path, *shape, seed=1000 + sum(shape))
 
 
-@pytest.mark.parametrize("path", PATHS)
 def test_config1_uniform_256(mhr, path):
     """256^3, uniform[-1, 1), seeds (1001, 1002)."""
     check_full(mhr, path, 256, 256, 256, seed=1001, dist="uniform")
 
 
-@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("shape", [(256, 256, 256), (300, 520, 1000), (8, 8, 8)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_integer_twin_bit_exact(mhr, path, shape):
@@ -59,7 +70,6 @@ def test_integer_twin_bit_exact(mhr, path, shape):
     assert np.array_equal(C, oracle.gemm(A, B))
 
 
-@pytest.mark.parametrize("path", PATHS)
 def test_block_decomposition_n8_tile4(mhr, path):
     """The pages' N=8, TILE=4 example on the GPU: C00 = A00*B00 + A01*B10 on
     integer inputs, each product computed by the same entry point."""
@@ -80,7 +90,6 @@ def test_block_decomposition_n8_tile4(mhr, path):
             assert np.array_equal(C[bi * T:(bi + 1) * T, bj * T:(bj + 1) * T], acc)
 
 
-@pytest.mark.parametrize("path", PATHS)
 def test_identity_and_ones(mhr, path):
     import seeded_inputs as si
 
@@ -100,7 +109,6 @@ def test_identity_and_ones(mhr, path):
     assert np.all(DeviceCall(path, ones_a, ones_b, ab, bb).run(mhr).result() == K)
 
 
-@pytest.mark.parametrize("path", PATHS)
 def test_padded_leading_dims_nan_poison(mhr, path):
     """ld > width with NaN in every pad: a read outside the logical matrix
     poisons C; a write outside it breaks the guard band (checked in result())."""
@@ -108,7 +116,6 @@ def test_padded_leading_dims_nan_poison(mhr, path):
     check_full(mhr, path, 131, 256, 128, seed=2202, lda=136, ldb=264, ldc=260)
 
 
-@pytest.mark.parametrize("path", PATHS)
 def test_misaligned_pointers(mhr, path):
     """Operands and output shifted one element off 16-byte alignment: the SIMT
     path falls back to scalar accesses, the tensor-core paths repack/split the
@@ -117,7 +124,6 @@ def test_misaligned_pointers(mhr, path):
     check_full(mhr, path, 150, 270, 90, seed=2302, offset=1, lda=91, ldb=271, ldc=271)
 
 
-@pytest.mark.parametrize("path", PATHS)
 def test_deterministic(mhr, path):
     """Fixed MMA order: repeated calls give bit-identical results (a missing
     ring barrier would show up here as run-to-run differences)."""
@@ -128,7 +134,6 @@ def test_deterministic(mhr, path):
         assert np.array_equal(call.run(mhr).result(), first)
 
 
-@pytest.mark.parametrize("path", PATHS)
 def test_degenerate_sizes(mhr, path):
     import torch
 
