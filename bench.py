@@ -191,6 +191,35 @@ def host_operands(w):
     return A, B, None, None
 
 
+def cublas_reference(path, M, N, K, dev, stream, achieved):
+    """cuBLAS (torch.matmul) on the same shape in the same run, for context: tf32
+    for the 3xTF32 path (one tf32 pass), bf16 for the bf16 path. Best of 10
+    launches, L2 not flushed. Not a roofline denominator: the recipe's peak is."""
+    import torch
+
+    old = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        dt = torch.bfloat16 if path == "bf16" else torch.float32
+        a = torch.randn(M, K, device=dev).to(dt)
+        b = torch.randn(K, N, device=dev).to(dt)
+        for _ in range(3):
+            torch.matmul(a, b)
+        best = float("inf")
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            torch.matmul(a, b)
+            e1.record(stream)
+            e1.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        tflops = 2.0 * M * N * K / (best * 1e-3) / 1e12
+        return {"kind": "tf32" if path != "bf16" else "bf16", "tflops": tflops,
+                "frac": achieved / tflops}
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = old
+
+
 def run_reference(args, w, world, rank):
     """The oracle as it stands, timed on this host's cores: each step computes a
     bounded sample of rows of C; TFLOPS = 2 * rows * N * K / t."""
@@ -326,6 +355,7 @@ def main():
     rc = lib.gemm_check(sh)
     if rc != mhr.MHR_OK:
         raise mhr.GemmError(rc, "warm-up")
+    main_kernel = lib.gemm_testing_last_main_kernel().decode()
 
     # ---------------------------------------------------------------- timed
     time.sleep(0.5)  # let the clock sampler start
@@ -396,14 +426,15 @@ def main():
         peak_note = "tf32 = bf16 burst x 1.1/2.25 (nominal tf32/bf16 ratio); 3 MMAs per product"
     else:
         tensor_flop, peak_tf, peak_note = flop, None, ""
-    kernel_name = {"3xtf32": "tc_gemm_kernel<3xtf32>", "bf16": "tc_gemm_kernel<bf16>",
-                   "f32": "simt_f32_kernel"}[path]
+    kernel_name = main_kernel.split(" ")[0]
     achieved = tensor_flop / (ms_kern * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
                 "frac": achieved / peak_tf if peak_tf else None,
                 "traffic": stored_traffic(kernel_name, args.workload),
-                "kernel": kernel_name, "kernel_ms": ms_kern,
+                "kernel": main_kernel, "kernel_ms": ms_kern,
                 "peak_source": f"{pk['source']} ({peak_note})"}
+    if path in ("3xtf32", "bf16"):
+        roofline["cublas_same_run"] = cublas_reference(path, M, N, K, dev, stream, achieved)
 
     # ---------------------------------------------------------------- CPU baseline
     cpu = None

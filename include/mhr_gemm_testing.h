@@ -48,6 +48,14 @@ int64_t gemm_testing_peek_status(void* stream);
 int gemm_testing_set_cta_pair_mode(int mode);
 
 /*
+ * Name, grid size and tile count of the main kernel that the most recent
+ * gemm_* call launched, e.g. "tc_gemm_pair_kernel<3xtf32> grid=148
+ * tiles=256" ("none" before the first launch).  Static storage, overwritten
+ * by the next call.
+ */
+const char* gemm_testing_last_main_kernel(void);
+
+/*
  * Profiling hook.  When `start` and `stop` are both non-NULL cudaEvent_t
  * handles, every following gemm_* call records `start` on its stream just
  * before it launches its main GEMM kernel (after any split or pack pre-pass)

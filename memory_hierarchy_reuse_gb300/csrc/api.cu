@@ -6,6 +6,7 @@
 
 #include <climits>
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -197,6 +198,18 @@ CUresult encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void*
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+namespace {
+char g_last_kernel[160] = "none";
+std::mutex g_last_kernel_mu;
+}  // namespace
+
+void note_main_kernel(const char* name, int grid, int tiles) {
+  std::lock_guard<std::mutex> g(g_last_kernel_mu);
+  snprintf(g_last_kernel, sizeof(g_last_kernel), "%s grid=%d tiles=%d", name, grid, tiles);
+}
+
+const char* last_main_kernel() { return g_last_kernel; }
+
 int check_gemm_args(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
                     int64_t lda, int64_t ldb, int64_t ldc, int64_t esz_ab, bool* noop) {
   return validate(A, B, C, M, N, K, lda, ldb, ldc, esz_ab, noop);
@@ -353,6 +366,11 @@ MHR_API int gemm_testing_set_inject_stall(int enable) {
   const int old = g_inject_stall;
   g_inject_stall = enable ? 1 : 0;
   return old;
+}
+
+MHR_API const char* gemm_testing_last_main_kernel(void) {
+  std::lock_guard<std::mutex> g(g_last_kernel_mu);
+  return last_main_kernel();
 }
 
 MHR_API int gemm_testing_set_cta_pair_mode(int mode) {

@@ -57,6 +57,11 @@ CUresult encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void*
                         uint64_t inner, uint64_t outer, uint64_t row_pitch_bytes,
                         uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
 
+// Name of the main kernel the last tensor-core or SIMT launch used, with its
+// grid (for profiling labels; static storage).
+void note_main_kernel(const char* name, int grid, int tiles);
+const char* last_main_kernel();
+
 // The C-ABI front end's argument checks (api.cu), for entry points defined in
 // other translation units.  Returns an mhr_status; *noop is set when M or N is 0.
 int check_gemm_args(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,

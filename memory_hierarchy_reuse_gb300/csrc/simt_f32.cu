@@ -149,6 +149,8 @@ template <bool VA, bool VB, bool VC>
 cudaError_t launch_t(const float* A, const float* B, float* C, int64_t M, int64_t N, int64_t K,
                      int64_t lda, int64_t ldb, int64_t ldc, cudaStream_t s) {
   const int64_t tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
+  note_main_kernel("simt_f32_kernel", static_cast<int>(tiles_m * tiles_n),
+                   static_cast<int>(tiles_m * tiles_n));
   simt_f32_kernel<VA, VB, VC><<<static_cast<unsigned>(tiles_m * tiles_n), NT, 0, s>>>(
       A, B, C, M, N, K, lda, ldb, ldc, tiles_m, tiles_n);
   return cudaGetLastError();

@@ -97,6 +97,10 @@ struct Layout {
 struct TcParams {
   int32_t M, N, K;
   int32_t tiles_m, tiles_n, num_tiles, num_kb;
+  // Work units of the pair kernel: tiles [0, full_units) whole; tiles
+  // [full_units, num_tiles) split into two K halves, [0, kb_mid) and
+  // [kb_mid, num_kb), whose results are reduce-added into a zeroed C.
+  int32_t full_units, num_units, kb_mid;
   float* C;
   int64_t ldc;
   uint32_t* status;
@@ -116,6 +120,29 @@ __device__ __forceinline__ void tile_coords(int t, const TcParams& p, int& tm, i
   const int r = t - g * group_size;
   tm = first_m + r % gm;
   tn = r / gm;
+}
+
+// Work unit u of the pair kernel -> tile, K-block range, and whether its
+// result is added into C (split unit) rather than stored.
+struct Unit {
+  int tile, kb0, kb1;
+  bool reduce;
+};
+__device__ __forceinline__ Unit unit_of(int u, const TcParams& p) {
+  Unit w;
+  if (u < p.full_units) {
+    w.tile = u;
+    w.kb0 = 0;
+    w.kb1 = p.num_kb;
+    w.reduce = false;
+  } else {
+    const int v = u - p.full_units;
+    w.tile = p.full_units + (v >> 1);
+    w.kb0 = (v & 1) ? p.kb_mid : 0;
+    w.kb1 = (v & 1) ? p.num_kb : p.kb_mid;
+    w.reduce = true;
+  }
+  return w;
 }
 
 // Warp-uniform bounded wait: every lane polls; the warp agrees on the outcome.
@@ -513,12 +540,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------------ producers (both CTAs)
     uint32_t it = 0, inflight = 0;
     bool ok = true;
-    for (int t = cluster; ok && t < p.num_tiles; t += num_clusters) {
+    for (int u = cluster; ok && u < p.num_units; u += num_clusters) {
+      const Unit w = unit_of(u, p);
       int tm, tn;
-      tile_coords(t, p, tm, tn);
+      tile_coords(w.tile, p, tm, tn);
       const int m0 = tm * 2 * Cf::BM + static_cast<int>(rank) * Cf::BM;
       const int nb0 = tn * Cf::BN + static_cast<int>(rank) * Cf::BN_HALF;
-      for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+      for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
         const uint32_t s = it % Cf::STAGES, ph = (it / Cf::STAGES) & 1u;
         if (!warp_wait(empty_bar(s), ph ^ 1u, limit, abort_flag)) {
           give_up_pair(kErrTimeoutProducer);
@@ -573,7 +601,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (leader) {
       uint32_t it = 0, tcount = 0;
       bool ok = true;
-      for (int t = cluster; ok && t < p.num_tiles; t += num_clusters, ++tcount) {
+      for (int u = cluster; ok && u < p.num_units; u += num_clusters, ++tcount) {
+        const Unit w = unit_of(u, p);
         const uint32_t buf = tcount & 1u, aph = (tcount >> 1) & 1u;
         if (!warp_wait(acce_bar(buf), aph ^ 1u, limit, abort_flag)) {
           give_up_pair(kErrTimeoutMma);
@@ -582,7 +611,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * Cf::BN;
-        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
           const uint32_t s = it % Cf::STAGES, ph = (it / Cf::STAGES) & 1u;
           if (!warp_wait(full_bar(s), ph, limit, abort_flag)) {
             give_up_pair(kErrTimeoutMma);
@@ -600,7 +629,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const uint64_t ad = smem_desc_sw128(st + kk * 32, 16, 1024);
                 const uint64_t bd =
                     smem_desc_sw128(st + Cf::A_BYTES + kk * 2048, Cf::B_BOX_BYTES, 1024);
-                mma_f16_pair(d_tmem, ad, bd, Cf::IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+                mma_f16_pair(d_tmem, ad, bd, Cf::IDESC, (kb > w.kb0 || kk > 0) ? 1u : 0u);
               }
             } else {
               const uint32_t a_big = st, a_small = st + Cf::A_BYTES;
@@ -612,7 +641,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const uint64_t asd = smem_desc_sw128(a_small + off, 16, 1024);
                 const uint64_t bbd = smem_desc_sw128(b_big + off, 16, 1024);
                 const uint64_t bsd = smem_desc_sw128(b_small + off, 16, 1024);
-                mma_tf32_pair(d_tmem, asd, bbd, Cf::IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+                mma_tf32_pair(d_tmem, asd, bbd, Cf::IDESC, (kb > w.kb0 || kk > 0) ? 1u : 0u);
                 mma_tf32_pair(d_tmem, abd, bsd, Cf::IDESC, 1u);
                 mma_tf32_pair(d_tmem, abd, bbd, Cf::IDESC, 1u);
               }
@@ -637,7 +666,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int q = warp & 3;
     const int ew = warp - 2;
     uint32_t tcount = 0, chunk = 0;
-    for (int t = cluster; t < p.num_tiles; t += num_clusters, ++tcount) {
+    for (int u = cluster; u < p.num_units; u += num_clusters, ++tcount) {
+      const Unit w = unit_of(u, p);
       const uint32_t buf = tcount & 1u, aph = (tcount >> 1) & 1u;
       if (!warp_wait(accf_bar(buf), aph, limit, abort_flag)) {
         give_up_pair(kErrTimeoutEpilogue);
@@ -645,7 +675,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       tc_fence_after();
       int tm, tn;
-      tile_coords(t, p, tm, tn);
+      tile_coords(w.tile, p, tm, tn);
       const int m0 = tm * 2 * Cf::BM + static_cast<int>(rank) * Cf::BM;
       const int n0 = tn * Cf::BN;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * Cf::BN;
@@ -669,7 +699,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tmC, stg, n0 + c * 32, m0 + q * 32);
+            if (w.reduce)
+              tma_reduce_add_2d(&tmC, stg, n0 + c * 32, m0 + q * 32);
+            else
+              tma_store_2d(&tmC, stg, n0 + c * 32, m0 + q * 32);
             bulk_commit_group();
           }
           ++chunk;
@@ -679,8 +712,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             float* crow = p.C + static_cast<int64_t>(row) * p.ldc;
             const int col0 = n0 + c * 32;
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (col0 + j < p.N) crow[col0 + j] = __uint_as_float(r[j]);
+            for (int j = 0; j < 32; ++j) {
+              if (col0 + j < p.N) {
+                if (w.reduce)
+                  atomicAdd(crow + col0 + j, __uint_as_float(r[j]));
+                else
+                  crow[col0 + j] = __uint_as_float(r[j]);
+              }
+            }
           }
         }
       }
@@ -704,6 +743,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 // ------------------------------------------------------------------ pre-passes
+
+// Zero the C tiles of the split work units (pair tiles [full_units,
+// num_tiles)), which both K halves then add into.
+__global__ void zero_split_tiles_kernel(TcParams p, int tile_rows, int tile_cols) {
+  const int tile = p.full_units + blockIdx.x;
+  int tm, tn;
+  tile_coords(tile, p, tm, tn);
+  const int64_t r0 = static_cast<int64_t>(tm) * tile_rows, c0 = static_cast<int64_t>(tn) * tile_cols;
+  for (int r = threadIdx.y; r < tile_rows; r += blockDim.y) {
+    const int64_t row = r0 + r;
+    if (row >= p.M) break;
+    for (int c = threadIdx.x; c < tile_cols; c += blockDim.x) {
+      const int64_t col = c0 + c;
+      if (col < p.N) p.C[row * p.ldc + col] = 0.f;
+    }
+  }
+}
 
 __global__ void zero_fill_kernel(float* C, int64_t M, int64_t N, int64_t ldc) {
   for (int64_t r = blockIdx.y; r < M; r += gridDim.y)
@@ -888,12 +944,17 @@ cudaError_t launch_tc(const CUtensorMap& a0, const CUtensorMap& a1, const CUtens
   p.tiles_n = static_cast<int32_t>((N + Cf::BN - 1) / Cf::BN);
   p.num_tiles = p.tiles_m * p.tiles_n;
   p.num_kb = static_cast<int32_t>((K + Cf::BK - 1) / Cf::BK);
+  p.full_units = p.num_tiles;
+  p.num_units = p.num_tiles;
+  p.kb_mid = p.num_kb;
   p.C = C;
   p.ldc = ldc;
   p.status = ctl.status;
   p.wait_limit_ns = ctl.wait_limit_ns;
   p.inject_stall = ctl.inject_stall;
   const int grid = p.num_tiles < ctl.sm_count ? p.num_tiles : ctl.sm_count;
+  note_main_kernel(KIND == KIND_BF16 ? "tc_gemm_kernel<bf16>" : "tc_gemm_kernel<3xtf32>", grid,
+                   p.num_tiles);
   cudaError_t e;
   if (c_tma) {
     if ((e = prepare_kernel<KIND, true>()) != cudaSuccess) return e;
@@ -932,8 +993,23 @@ cudaError_t launch_pair_t(const CUtensorMap& a0, const CUtensorMap& a1, const CU
   if (e != cudaSuccess) return e;
   if (max_clusters < 1) return cudaErrorInvalidConfiguration;
   const int clusters = p.num_tiles < max_clusters ? p.num_tiles : max_clusters;
+  // A last round that would leave more than half of the clusters idle is
+  // split along K: its tiles become two half-K units each, reduce-added into
+  // C (zeroed first).  Two addends onto zero give the same sum in either
+  // order, so results stay bit-reproducible.
+  TcParams q = p;
+  const int rem = p.num_tiles % clusters;
+  if (p.num_tiles > clusters && rem > 0 && 2 * rem <= clusters && p.num_kb >= 2) {
+    q.full_units = p.num_tiles - rem;
+    q.num_units = q.full_units + 2 * rem;
+    q.kb_mid = p.num_kb / 2;
+    zero_split_tiles_kernel<<<rem, dim3(64, 8), 0, s>>>(q, 2 * PairCfg<KIND>::BM, PairCfg<KIND>::BN);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   cfg.gridDim = dim3(2 * clusters);
-  e = cudaLaunchKernelEx(&cfg, kern, a0, a1, b0, b1, cm, p);
+  note_main_kernel(KIND == KIND_BF16 ? "tc_gemm_pair_kernel<bf16>" : "tc_gemm_pair_kernel<3xtf32>",
+                   2 * clusters, p.num_tiles);
+  e = cudaLaunchKernelEx(&cfg, kern, a0, a1, b0, b1, cm, q);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -960,6 +1036,9 @@ cudaError_t launch_tc_any(const CUtensorMap& a0, const CUtensorMap& a1, const CU
   p.tiles_n = static_cast<int32_t>((N + Pc::BN - 1) / Pc::BN);
   p.num_tiles = p.tiles_m * p.tiles_n;
   p.num_kb = static_cast<int32_t>((K + Pc::BK - 1) / Pc::BK);
+  p.full_units = p.num_tiles;
+  p.num_units = p.num_tiles;
+  p.kb_mid = p.num_kb;
   p.C = C;
   p.ldc = ldc;
   p.status = ctl.status;

@@ -188,3 +188,35 @@ def test_config5_8192_bf16_sampled(mhr):
     """8192^3 bf16 inputs (normal(0,1) rounded to bf16), fp32 accumulate and
     output, seeds (5001, 5002); the oracle runs on the bf16 values."""
     sampled_check(mhr, "bf16", 8192, 8192, 8192, 5001, "normal")
+
+
+@pytest.mark.parametrize("path", ["3xtf32", "bf16"])
+def test_pair_kernel_split_last_round(mhr, path):
+    """The CTA-pair kernel splits a sparse last round of tiles into two K halves
+    that are reduce-added into C. Build a problem with 3 more pair tiles than
+    co-resident clusters, so exactly 3 tiles are split, and compare it in full
+    with the oracle, through the TMA reduce path (aligned C) and the atomic
+    path (ldc odd), and for bitwise repeatability."""
+    import re
+
+    old = mhr.gemm_testing_set_cta_pair_mode(2)
+    try:
+        A, B, Ab, Bb = operands(4096, 4096, 64, 3101, "normal", path)
+        DeviceCall(path, A, B, Ab, Bb).run(mhr)
+        label = mhr.gemm_testing_last_main_kernel()
+        clusters = int(re.search(r"grid=(\d+)", label).group(1)) // 2
+        assert clusters >= 8, label
+        M, N, K = 256 * (clusters + 3), 256, 320
+        for ldc in (None, N + 1):
+            A, B, Ab, Bb = operands(M, N, K, 3103, "normal", path)
+            call = DeviceCall(path, A, B, Ab, Bb, ldc=ldc)
+            C = call.run(mhr).result()
+            assert f"tiles={clusters + 3}" in mhr.gemm_testing_last_main_kernel()
+            Cref, S = oracle.gemm(A, B, with_abs=True)
+            assert normalised_error(C, Cref, S) <= TOL[path]
+            assert np.array_equal(call.run(mhr).result(), C)
+        # integer inputs: the two halves' sum is exact, so still bit-exact
+        A, B, Ab, Bb = operands(M, N, K, 3105, "int", path)
+        assert np.array_equal(DeviceCall(path, A, B, Ab, Bb).run(mhr).result(), oracle.gemm(A, B))
+    finally:
+        mhr.gemm_testing_set_cta_pair_mode(old)
