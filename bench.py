@@ -69,11 +69,21 @@ def peaks():
                 sm_max_mhz=2070.0, source="fallback")
 
 
-def source_digest() -> str:
-    """Hash of the kernel sources, to tell whether stored ncu counters still apply."""
+KERNEL_SOURCES = {  # the files whose text determines each kernel
+    "tc_gemm_pair_kernel": ["tc_gemm.cu", "mhr_device.cuh"],
+    "tc_gemm_kernel": ["tc_gemm.cu", "mhr_device.cuh"],
+    "simt_f32_kernel": ["simt_f32.cu"],
+}
+
+
+def source_digest(kernel: str | None = None) -> str:
+    """Hash of a kernel's source files (all sources if kernel is None), to
+    tell whether stored ncu counters still apply."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "memory_hierarchy_reuse_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    base = kernel.split("<")[0] if kernel else None
+    files = KERNEL_SOURCES.get(base) if base else None
+    for f in sorted(files or os.listdir(csrc)):
         h.update(f.encode())
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
@@ -88,7 +98,7 @@ def stored_traffic(kernel: str, workload: str):
     try:
         d = json.load(open(p))
         e = d[kernel][workload]
-        if e.get("source_digest") != source_digest():
+        if e.get("source_digest") != source_digest(kernel):
             return None
         return e["dram_bytes_per_launch"]
     except (KeyError, ValueError, TypeError):
@@ -220,6 +230,70 @@ def cublas_reference(path, M, N, K, dev, stream, achieved):
         torch.backends.cuda.matmul.allow_tf32 = old
 
 
+def run_ladder(args):
+    """The pages' ladder on this GPU at 4096^3 fp32 (uniform[-1, 1), seeds
+    2001/2002): naive, 16x16 and 32x32 shared-memory tiles, the register-tiled
+    SIMT kernel and the 3xTF32 tensor-core path, each timed with per-call
+    CUDA events after warm-up (L2 flushed before each call), with the pages'
+    global-load model 2MNK/T beside it. One JSON line."""
+    import torch
+
+    from memory_hierarchy_reuse_gb300 import build as mbuild
+
+    mbuild.build()
+    import memory_hierarchy_reuse_gb300 as mhr
+    from memory_hierarchy_reuse_gb300 import model
+
+    lib = mhr.load()
+    w = WORKLOADS["c2"]
+    M, N, K = w["M"], w["N"], w["K"]
+    A_h, B_h, _, _ = host_operands(w)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    a, b = torch.from_numpy(A_h).to(dev), torch.from_numpy(B_h).to(dev)
+    c = torch.empty((M, N), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    sh = stream.cuda_stream
+    rungs = [("naive", lambda: lib.gemm_f32_ladder(0, a.data_ptr(), b.data_ptr(), c.data_ptr(),
+                                                   M, N, K, K, N, N, sh), 1),
+             ("tiled16", lambda: lib.gemm_f32_ladder(1, a.data_ptr(), b.data_ptr(), c.data_ptr(),
+                                                     M, N, K, K, N, N, sh), 16),
+             ("tiled32", lambda: lib.gemm_f32_ladder(2, a.data_ptr(), b.data_ptr(), c.data_ptr(),
+                                                     M, N, K, K, N, N, sh), 32),
+             ("simt_f32", lambda: lib.gemm_f32(a.data_ptr(), b.data_ptr(), c.data_ptr(),
+                                               M, N, K, K, N, N, sh), 128),
+             ("tc_3xtf32", lambda: lib.gemm_f32_3xtf32(a.data_ptr(), b.data_ptr(), c.data_ptr(),
+                                                       M, N, K, K, N, N, sh), 256)]
+    out = {}
+    flop = model.flops(M, N, K)
+    for name, fn, T in rungs:
+        for _ in range(args.warmup):
+            assert fn() == 0
+        torch.cuda.synchronize(dev)
+        times = []
+        steps = max(3, min(args.steps, 10 if name == "naive" else 30))
+        for _ in range(steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            assert fn() == 0
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            times.append(e0.elapsed_time(e1))
+        assert lib.gemm_check(sh) == 0
+        ms = sum(times) / len(times)
+        out[name] = {"tflops": flop / (ms * 1e-3) / 1e12, "ms": ms, "tile": T,
+                     "model_global_load_bytes": 4 * (model.naive_loads(M, N, K) if T == 1
+                                                     else model.tiled_loads(M, N, K, T))}
+    base = out["naive"]["tflops"]
+    for v in out.values():
+        v["speedup_vs_naive"] = v["tflops"] / base
+    print(json.dumps({"metric": METRIC, "mode": "ladder", "unit": "TFLOPS", "n_gpus": 1,
+                      "config": {"workload": w["desc"], "M": M, "N": N, "K": K,
+                                 "l2": "flushed before every call"},
+                      "ladder": out}), flush=True)
+
+
 def run_reference(args, w, world, rank):
     """The oracle as it stands, timed on this host's cores: each step computes a
     bounded sample of rows of C; TFLOPS = 2 * rows * N * K / t."""
@@ -261,11 +335,16 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ladder", action="store_true",
+                    help="time the pages' naive/tiled kernels beside the build's paths at 4096^3")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     w = WORKLOADS[args.workload]
     world, rank, local = dist_setup()
+    if args.ladder:
+        run_ladder(args)
+        return
 
     if args.impl == "reference":
         run_reference(args, w, world, rank)
@@ -456,6 +535,20 @@ def main():
                          f"{t_cpu:.1f} s of CPU work",
                "gpu_vs_sample_normalised_error": nerr}
 
+    # the pages' tiling on the host caches: a realistic CPU comparator (full problem)
+    cpu_tiled_line = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import cpu_tiled
+
+        cpu_tiled.build()
+        cpu_tiled.gemm(A_h[:64], B_h)  # warm the threads and caches
+        t0 = time.perf_counter()
+        cpu_tiled.gemm(A_h, B_h)
+        t_ct = time.perf_counter() - t0
+        cpu_tiled_line = {"value": flop / t_ct / 1e12, "unit": "TFLOPS",
+                          "cores": cpu_tiled.max_threads(), "kind": "cache-blocked fp32 CPU GEMM",
+                          "sample": f"the whole {M}x{N}x{K} product, {t_ct:.2f} s"}
+
     if rank == 0:
         out = {
             "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
@@ -468,6 +561,7 @@ def main():
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": roofline,
             "cpu_baseline": cpu,
+            "cpu_tiled": cpu_tiled_line,
             "e2e": {"value": world * flop / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "note": "pinned host A, B -> device, C API call, C -> pinned host, per step"},

@@ -123,6 +123,23 @@ int gemm_f32_3xtf32_noalloc(const float* A, const float* B, float* C, int64_t M,
                             int64_t K, int64_t lda, int64_t ldb, int64_t ldc, void* stream);
 
 /*
+ * The pages' optimisation ladder, kept for measuring their claims on this
+ * GPU (fp32 FMA, fp32 accumulation, one output per thread):
+ *   rung 0  one thread per output reading a row of A and a column of B from
+ *           global memory: 2MNK element loads ("矩阵乘法 tiling", section 一;
+ *           "CUDA 深入浅出（二）", section "naive kernel 怎么读数据");
+ *   rung 1  16 x 16 blocks staging 16 x 16 tiles of A and B in shared memory
+ *           with two barriers per K step: 2MNK/16 loads ("矩阵乘法 tiling",
+ *           sections 二-四; "CUDA 编程系列之三", section 6);
+ *   rung 2  the same with 32 x 32 tiles: 2MNK/32 loads.
+ * Edges are zero-filled (inputs) and masked (outputs), which the pages'
+ * listings omit.  Same arguments and contract as gemm_f32, plus `rung`;
+ * MHR_ERR_INVALID_ARG for another rung or for M > 65535 * T.
+ */
+int gemm_f32_ladder(int rung, const float* A, const float* B, float* C, int64_t M, int64_t N,
+                    int64_t K, int64_t lda, int64_t ldb, int64_t ldc, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's status
  * word.  Returns MHR_OK, MHR_ERR_TIMEOUT (some kernel since the last check hit
  * a wait limit) or MHR_ERR_CUDA (the synchronisation itself failed).

@@ -12,6 +12,7 @@ Raw entry points (same names and arguments as the C ABI; pointers are ints,
     gemm_f32_3xtf32(...)                               -> status
     gemm_bf16_f32acc(...)                              -> status
     gemm_f32_3xtf32_noalloc(...)                       -> status
+    gemm_f32_ladder(rung, A, B, C, ...)                -> status
     gemm_check(stream) -> status
     gemm_status_string(status) -> str
     gemm_release()
@@ -39,6 +40,7 @@ PATHS = ("f32", "3xtf32", "bf16")
 
 #: every symbol the public headers declare
 EXPORTS = ("gemm_f32", "gemm_f32_3xtf32", "gemm_bf16_f32acc", "gemm_f32_3xtf32_noalloc",
+           "gemm_f32_ladder",
            "gemm_check",
            "gemm_status_string", "gemm_release", "gemm_version",
            "gemm_testing_set_wait_limit_ns", "gemm_testing_set_inject_stall",
@@ -70,6 +72,8 @@ def load(path: str | None = None):
         f = getattr(lib, name)
         f.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, vp]
         f.restype = ctypes.c_int
+    lib.gemm_f32_ladder.argtypes = [ctypes.c_int, vp, vp, vp, i64, i64, i64, i64, i64, i64, vp]
+    lib.gemm_f32_ladder.restype = ctypes.c_int
     lib.gemm_check.argtypes = [vp]
     lib.gemm_check.restype = ctypes.c_int
     lib.gemm_status_string.argtypes = [ctypes.c_int]
@@ -110,6 +114,11 @@ def gemm_f32_3xtf32_noalloc(A, B, C, M, N, K, lda, ldb, ldc, stream=None) -> int
     """gemm_f32_3xtf32 with its scratch in a 64 MiB static device array: no
     device allocation in the call (for callers that must not allocate)."""
     return load().gemm_f32_3xtf32_noalloc(A, B, C, M, N, K, lda, ldb, ldc, stream)
+
+
+def gemm_f32_ladder(rung, A, B, C, M, N, K, lda, ldb, ldc, stream=None) -> int:
+    """The pages' kernels: rung 0 naive, 1 tiled 16x16, 2 tiled 32x32."""
+    return load().gemm_f32_ladder(int(rung), A, B, C, M, N, K, lda, ldb, ldc, stream)
 
 
 def gemm_check(stream=None) -> int:

@@ -241,6 +241,24 @@ MHR_API int gemm_f32(const float* A, const float* B, float* C, int64_t M, int64_
   return from_cuda(launch_simt_f32(A, B, C, M, N, K, lda, ldb, ldc, s));
 }
 
+MHR_API int gemm_f32_ladder(int rung, const float* A, const float* B, float* C, int64_t M,
+                            int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                            void* stream) {
+  if (rung < 0 || rung > 2) return MHR_ERR_INVALID_ARG;
+  bool noop;
+  int rc = validate(A, B, C, M, N, K, lda, ldb, ldc, 4, &noop);
+  if (rc != MHR_OK || noop) return rc;
+  const int64_t T = rung == 2 ? 32 : 16;
+  if ((M + T - 1) / T > 65535) return MHR_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> g(g_mu);
+  DeviceState* st;
+  if ((rc = device_state(&st, nullptr)) != MHR_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K == 0) return from_cuda(launch_zero_fill(C, M, N, ldc, s));
+  MainKernelEvents ev(s);
+  return from_cuda(launch_ladder(rung, A, B, C, M, N, K, lda, ldb, ldc, s));
+}
+
 MHR_API int gemm_f32_3xtf32(const float* A, const float* B, float* C, int64_t M, int64_t N,
                             int64_t K, int64_t lda, int64_t ldb, int64_t ldc, void* stream) {
   bool noop;

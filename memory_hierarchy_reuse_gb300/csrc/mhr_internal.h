@@ -21,6 +21,11 @@ struct DeviceCtl {
 cudaError_t launch_simt_f32(const float* A, const float* B, float* C, int64_t M, int64_t N,
                             int64_t K, int64_t lda, int64_t ldb, int64_t ldc, cudaStream_t s);
 
+// The pages' ladder: rung 0 = one thread per output, 1 = 16 x 16 shared tiles,
+// 2 = 32 x 32 shared tiles.  Requires ceil(M / T) <= 65535.
+cudaError_t launch_ladder(int rung, const float* A, const float* B, float* C, int64_t M, int64_t N,
+                          int64_t K, int64_t lda, int64_t ldb, int64_t ldc, cudaStream_t s);
+
 // C[M x N] = 0 (the K == 0 case).
 cudaError_t launch_zero_fill(float* C, int64_t M, int64_t N, int64_t ldc, cudaStream_t s);
 

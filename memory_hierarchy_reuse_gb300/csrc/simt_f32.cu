@@ -25,6 +25,13 @@
 // transposing stores do not conflict, and the compute loop reads shared memory
 // as float4 (two distinct A vectors per warp, broadcast; sixteen consecutive B
 // vectors per warp).
+//
+// The multiply-adds use Blackwell's packed fp32 instruction fma.rn.f32x2: one
+// instruction performs two independent fp32 fused multiply-adds (here
+// acc[i][j] and acc[i][j+1] with the same a[i]), so the 64 FMAs per k step
+// take 32 issue slots instead of 64 and the FMA pipe, not instruction issue,
+// sets the pace.  Each lane is an ordinary round-to-nearest fp32 FMA, so the
+// results are bit-identical to scalar fmaf in the same order.
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -35,6 +42,23 @@ namespace {
 
 constexpr int BM = 128, BN = 128, BK = 8, NT = 256, APAD = 4;
 constexpr int GROUP_M = 8;  // tile rows swept together (L2 reuse of B column strips)
+
+// d = a * b + c on two fp32 lanes packed in 64-bit registers.
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t dup2(float x) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(d) : "f"(x));
+  return d;
+}
+__device__ __forceinline__ float2 unpack2(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
 
 template <bool VA, bool VB, bool VC>
 __global__ void __launch_bounds__(NT, 2)
@@ -68,11 +92,12 @@ __global__ void __launch_bounds__(NT, 2)
   // and columns {4tx..4tx+3, 64+4tx..64+4tx+3} of the tile.
   const int ty = tid >> 4, tx = tid & 15;
 
-  float acc[8][8];
+  // acc2[i][p] holds outputs (i, 2p) and (i, 2p + 1) of the 8 x 8 block.
+  uint64_t acc2[8][4];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    for (int p = 0; p < 4; ++p) acc2[i][p] = 0ull;
 
   float ra[4], rb[4];
   auto fetch = [&](int64_t k0) {
@@ -112,19 +137,30 @@ __global__ void __launch_bounds__(NT, 2)
     for (int k = 0; k < BK; ++k) {
       const float4 a0 = *reinterpret_cast<const float4*>(&As[cur][k][ty * 4]);
       const float4 a1 = *reinterpret_cast<const float4*>(&As[cur][k][64 + ty * 4]);
-      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[cur][k][tx * 4]);
-      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[cur][k][64 + tx * 4]);
+      const ulonglong2 b0 = *reinterpret_cast<const ulonglong2*>(&Bs[cur][k][tx * 4]);
+      const ulonglong2 b1 = *reinterpret_cast<const ulonglong2*>(&Bs[cur][k][64 + tx * 4]);
       const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-      const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+      const uint64_t b[4] = {b0.x, b0.y, b1.x, b1.y};
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < 8; ++i) {
+        const uint64_t ai = dup2(a[i]);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        for (int p = 0; p < 4; ++p) acc2[i][p] = ffma2(ai, b[p], acc2[i][p]);
+      }
     }
     if (kt + 1 < nk) stash(cur ^ 1);
     __syncthreads();
   }
 
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const float2 v = unpack2(acc2[i][p]);
+      acc[i][2 * p] = v.x;
+      acc[i][2 * p + 1] = v.y;
+    }
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int64_t row = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));

@@ -745,20 +745,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // ------------------------------------------------------------------ pre-passes
 
 // Zero the C tiles of the split work units (pair tiles [full_units,
-// num_tiles)), which both K halves then add into.
-__global__ void zero_split_tiles_kernel(TcParams p, int tile_rows, int tile_cols) {
+// num_tiles)), which both K halves then add into.  Block (x, y) clears rows
+// [8y, 8y + 8) of split tile x.
+__global__ void zero_split_tiles_kernel(TcParams p, int tile_cols) {
   const int tile = p.full_units + blockIdx.x;
   int tm, tn;
   tile_coords(tile, p, tm, tn);
-  const int64_t r0 = static_cast<int64_t>(tm) * tile_rows, c0 = static_cast<int64_t>(tn) * tile_cols;
-  for (int r = threadIdx.y; r < tile_rows; r += blockDim.y) {
-    const int64_t row = r0 + r;
-    if (row >= p.M) break;
-    for (int c = threadIdx.x; c < tile_cols; c += blockDim.x) {
-      const int64_t col = c0 + c;
-      if (col < p.N) p.C[row * p.ldc + col] = 0.f;
-    }
-  }
+  const int64_t row = static_cast<int64_t>(tm) * (8 * gridDim.y) + 8 * blockIdx.y + threadIdx.y;
+  if (row >= p.M) return;
+  const int64_t c0 = static_cast<int64_t>(tn) * tile_cols;
+  float* crow = p.C + row * p.ldc;
+  for (int c = threadIdx.x; c < tile_cols; c += blockDim.x)
+    if (c0 + c < p.N) crow[c0 + c] = 0.f;
 }
 
 __global__ void zero_fill_kernel(float* C, int64_t M, int64_t N, int64_t ldc) {
@@ -1003,7 +1001,8 @@ cudaError_t launch_pair_t(const CUtensorMap& a0, const CUtensorMap& a1, const CU
     q.full_units = p.num_tiles - rem;
     q.num_units = q.full_units + 2 * rem;
     q.kb_mid = p.num_kb / 2;
-    zero_split_tiles_kernel<<<rem, dim3(64, 8), 0, s>>>(q, 2 * PairCfg<KIND>::BM, PairCfg<KIND>::BN);
+    zero_split_tiles_kernel<<<dim3(rem, 2 * PairCfg<KIND>::BM / 8), dim3(128, 8), 0, s>>>(
+        q, PairCfg<KIND>::BN);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   cfg.gridDim = dim3(2 * clusters);

@@ -59,9 +59,14 @@ def test_version_and_strings(lib):
     assert lib.gemm_status_string(99) == "unknown mhr_status"
 
 
-@pytest.mark.parametrize("entry", ["gemm_f32", "gemm_f32_3xtf32", "gemm_bf16_f32acc"])
+@pytest.mark.parametrize("entry", ["gemm_f32", "gemm_f32_3xtf32", "gemm_bf16_f32acc",
+                                   "gemm_f32_3xtf32_noalloc", "ladder0", "ladder2"])
 def test_argument_validation_without_gpu(lib, entry):
-    f = getattr(lib, entry)
+    if entry.startswith("ladder"):
+        rung = int(entry[-1])
+        f = lambda *a: lib.gemm_f32_ladder(rung, *a)  # noqa: E731
+    else:
+        f = getattr(lib, entry)
     P, Q, R = 0x10000, 0x20000000, 0x40000000  # fake, disjoint, 16-byte aligned addresses
     bad = [
         (P, Q, R, -1, 4, 4, 4, 4, 4),          # negative M
@@ -85,6 +90,14 @@ def test_argument_validation_without_gpu(lib, entry):
     assert f(None, None, None, 5, 0, 5, 5, 5, 5, None) == lib.MHR_OK
     # K == 0 needs C but not A or B; it is checked, then needs the device
     assert f(None, None, None, 2, 2, 0, 0, 0, 2, None) == lib.MHR_ERR_INVALID_ARG
+
+
+def test_ladder_rejects_unknown_rungs_and_huge_m(lib):
+    P, Q, R = 0x10000, 0x20000000, 0x40000000
+    for rung in (-1, 3):
+        assert lib.gemm_f32_ladder(rung, P, Q, R, 4, 4, 4, 4, 4, 4, None) == lib.MHR_ERR_INVALID_ARG
+    assert lib.gemm_f32_ladder(0, P, Q, 1 << 45, 65535 * 16 + 1, 1, 1, 1, 1, 1, None) == \
+        lib.MHR_ERR_INVALID_ARG
 
 
 def test_oracle_and_library_are_independent():
