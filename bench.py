@@ -54,6 +54,9 @@ DTYPE = {"f32": "f32", "3xtf32": "tf32x3", "bf16": "bf16"}
 # unaligned bf16 operands, never in these workloads)
 LAUNCHES = {"f32": 1, "3xtf32": 3, "bf16": 1}
 TF32_OVER_BF16 = 1.1 / 2.25   # nominal dense tensor rates (PFLOP/s) of GB300
+# Dense tensor-core rate of one Blackwell SM per clock: 2.25 PFLOP/s bf16 over
+# 152 SMs is 8192 FLOP/clk at ~1.8 GHz; tf32 runs at half the bf16 rate.
+TENSOR_FLOP_PER_CLK_SM = {"bf16": 8192, "tf32": 4096}
 FP32_LANES_PER_SM = 128
 L2_FLUSH_BYTES = 256 << 20
 
@@ -484,6 +487,7 @@ def main():
         extra[ENTRY[also]] = {
             "value": world * flop / (simt_ms * 1e-3) / 1e12, "unit": "TFLOPS", "ms_per_step": simt_ms,
             "roofline": {"bound": "alu", "achieved": flop / (simt_k * 1e-3) / 1e12,
+                         "traffic": stored_traffic("simt_f32_kernel", args.workload),
                          "peak": fp32_peak, "unit": "TFLOP/s",
                          "frac": flop / (simt_k * 1e-3) / 1e12 / fp32_peak,
                          "peak_note": f"{sms} SMs x {FP32_LANES_PER_SM} fp32 lanes x 2 x "
@@ -514,6 +518,17 @@ def main():
                 "peak_source": f"{pk['source']} ({peak_note})"}
     if path in ("3xtf32", "bf16"):
         roofline["cublas_same_run"] = cublas_reference(path, M, N, K, dev, stream, achieved)
+        # The nominal tf32 rate corresponds to a lower clock than this kernel
+        # sustains, so also give the dense rate per SM per clock at the SM
+        # clock sampled during the timed region.
+        per_clk = TENSOR_FLOP_PER_CLK_SM["bf16" if path == "bf16" else "tf32"]
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        mhz = (clocks or {}).get("sm_mhz") or pk["sm_max_mhz"]
+        pclk = per_clk * sms * mhz * 1e6 / 1e12
+        roofline["peak_at_sm_clock"] = {
+            "peak": pclk, "frac": achieved / pclk, "unit": "TFLOP/s",
+            "note": f"{per_clk} dense FLOP/clk/SM x {sms} SMs x {mhz:.0f} MHz (median SM clock "
+                    "in the timed region)"}
 
     # ---------------------------------------------------------------- CPU baseline
     cpu = None
