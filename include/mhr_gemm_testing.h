@@ -48,6 +48,14 @@ int64_t gemm_testing_peek_status(void* stream);
 int gemm_testing_set_cta_pair_mode(int mode);
 
 /*
+ * Tuning hook: the number of tile rows per raster group of the tensor-core
+ * kernels' tile schedule (consecutive work units sweep that many tile rows
+ * column by column, so co-resident CTAs share A and B panels in L2).  0
+ * restores the default (16).  Returns the previous setting.
+ */
+int gemm_testing_set_raster_group(int tile_rows);
+
+/*
  * Name, grid size and tile count of the main kernel that the most recent
  * gemm_* call launched, e.g. "tc_gemm_pair_kernel<3xtf32> grid=148
  * tiles=256" ("none" before the first launch).  Static storage, overwritten

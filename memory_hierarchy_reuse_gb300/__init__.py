@@ -45,7 +45,8 @@ EXPORTS = ("gemm_f32", "gemm_f32_3xtf32", "gemm_bf16_f32acc", "gemm_f32_3xtf32_n
            "gemm_status_string", "gemm_release", "gemm_version",
            "gemm_testing_set_wait_limit_ns", "gemm_testing_set_inject_stall",
            "gemm_testing_peek_status", "gemm_testing_set_main_kernel_events",
-           "gemm_testing_set_cta_pair_mode", "gemm_testing_last_main_kernel")
+           "gemm_testing_set_cta_pair_mode", "gemm_testing_last_main_kernel",
+           "gemm_testing_set_raster_group")
 
 _lib = None
 
@@ -88,6 +89,8 @@ def load(path: str | None = None):
     lib.gemm_testing_set_inject_stall.restype = ctypes.c_int
     lib.gemm_testing_peek_status.argtypes = [vp]
     lib.gemm_testing_peek_status.restype = ctypes.c_int64
+    lib.gemm_testing_set_raster_group.argtypes = [ctypes.c_int]
+    lib.gemm_testing_set_raster_group.restype = ctypes.c_int
     lib.gemm_testing_last_main_kernel.argtypes = []
     lib.gemm_testing_last_main_kernel.restype = ctypes.c_char_p
     lib.gemm_testing_set_cta_pair_mode.argtypes = [ctypes.c_int]
@@ -147,6 +150,10 @@ def gemm_testing_set_inject_stall(enable: int) -> int:
 
 def gemm_testing_peek_status(stream=None) -> int:
     return load().gemm_testing_peek_status(stream)
+
+
+def gemm_testing_set_raster_group(tile_rows: int) -> int:
+    return load().gemm_testing_set_raster_group(int(tile_rows))
 
 
 def gemm_testing_last_main_kernel() -> str:

@@ -44,6 +44,7 @@ std::map<std::pair<int, cudaStream_t>, Workspace> g_workspaces;
 uint64_t g_wait_limit_ns = 2000000000ull;
 int g_inject_stall = 0;
 int g_pair_mode = 0;
+int g_raster_group = 0;
 cudaEvent_t g_main_start = nullptr, g_main_stop = nullptr;
 
 // Brackets the main kernel launch with the caller's profiling events, if set.
@@ -170,6 +171,7 @@ DeviceCtl make_ctl(const DeviceState& st) {
   c.inject_stall = g_inject_stall;
   c.sm_count = st.sm_count;
   c.pair_mode = g_pair_mode;
+  c.raster_group = g_raster_group;
   return c;
 }
 
@@ -389,6 +391,13 @@ MHR_API int gemm_testing_set_inject_stall(int enable) {
 MHR_API const char* gemm_testing_last_main_kernel(void) {
   std::lock_guard<std::mutex> g(g_last_kernel_mu);
   return last_main_kernel();
+}
+
+MHR_API int gemm_testing_set_raster_group(int tile_rows) {
+  std::lock_guard<std::mutex> g(g_mu);
+  const int old = g_raster_group;
+  g_raster_group = tile_rows > 0 ? tile_rows : 0;
+  return old;
 }
 
 MHR_API int gemm_testing_set_cta_pair_mode(int mode) {

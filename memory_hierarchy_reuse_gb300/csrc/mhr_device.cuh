@@ -71,12 +71,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // most `limit_ns` nanoseconds, and give up early if `*abort` becomes nonzero
 // (another role of this CTA gave up).  Returns true on completion.  On a
 // timeout the caller records its error bit and unwinds; nothing traps.
+// With sleep_ns > 0 the thread sleeps that long between polls after the
+// first few (for waits that are expected to last many microseconds).
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns,
-                                                  volatile int* abort) {
+                                                  volatile int* abort, uint32_t sleep_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (sleep_ns && n > 8) __nanosleep(sleep_ns);
     if ((n & 63u) == 0) {
       if (*abort) return false;
       if (global_timer_ns() - t0 > limit_ns) return false;

@@ -16,6 +16,7 @@ struct DeviceCtl {
   int inject_stall = 0;                // test hook: block 0 arms one TMA stage and never loads it
   int sm_count = 0;
   int pair_mode = 0;                   // 0 auto, 1 single-CTA kernel, 2 CTA-pair kernel (test hook)
+  int raster_group = 0;                // tile rows per raster group, 0 = default (tuning hook)
 };
 
 cudaError_t launch_simt_f32(const float* A, const float* B, float* C, int64_t M, int64_t N,

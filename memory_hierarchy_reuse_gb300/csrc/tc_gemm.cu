@@ -81,7 +81,7 @@ constexpr int EPI_WARPS = 4;
 constexpr int EPI_BUF_BYTES = 32 * 32 * 4;                 // 32 rows x 32 fp32
 constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;   // 32 KB
 constexpr int NUM_THREADS = 192;
-constexpr int GROUP_M = 16;                                // tile rows per raster group
+constexpr int GROUP_M = 16;  // default tile rows per raster group
 
 template <int KIND>
 struct Layout {
@@ -101,6 +101,7 @@ struct TcParams {
   // [full_units, num_tiles) split into two K halves, [0, kb_mid) and
   // [kb_mid, num_kb), whose results are reduce-added into a zeroed C.
   int32_t full_units, num_units, kb_mid;
+  int32_t group_m;  // tile rows per raster group
   float* C;
   int64_t ldc;
   uint32_t* status;
@@ -113,10 +114,10 @@ struct TcParams {
 // strips in L2 (a second level of the pages' reuse argument, one level up
 // from shared memory).
 __device__ __forceinline__ void tile_coords(int t, const TcParams& p, int& tm, int& tn) {
-  const int group_size = GROUP_M * p.tiles_n;
+  const int group_size = p.group_m * p.tiles_n;
   const int g = t / group_size;
-  const int first_m = g * GROUP_M;
-  const int gm = min(p.tiles_m - first_m, GROUP_M);
+  const int first_m = g * p.group_m;
+  const int gm = min(p.tiles_m - first_m, p.group_m);
   const int r = t - g * group_size;
   tm = first_m + r % gm;
   tn = r / gm;
@@ -147,8 +148,8 @@ __device__ __forceinline__ Unit unit_of(int u, const TcParams& p) {
 
 // Warp-uniform bounded wait: every lane polls; the warp agrees on the outcome.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_t limit,
-                                          volatile int* abort_flag) {
-  const bool ok = mbar_wait_bounded(bar, parity, limit, abort_flag);
+                                          volatile int* abort_flag, uint32_t sleep_ns = 0) {
+  const bool ok = mbar_wait_bounded(bar, parity, limit, abort_flag, sleep_ns);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -527,33 +528,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint64_t limit = p.wait_limit_ns;
 
   // Give up: record why (first role only), raise the abort flag in both CTAs.
-  auto give_up_pair = [&](uint32_t bit) {
-    if (lane == 0) {
-      if (!*abort_flag) atomicOr(p.status, bit);
-      *abort_flag = 1;
-      st_shared_cluster_u32(peer_abort, 1u);
-    }
+  auto give_up_one = [&](uint32_t bit) {  // called by a single thread
+    if (!*abort_flag) atomicOr(p.status, bit);
+    *abort_flag = 1;
+    st_shared_cluster_u32(peer_abort, 1u);
+  };
+  auto give_up_pair = [&](uint32_t bit) {  // called by a whole warp
+    if (lane == 0) give_up_one(bit);
     __syncwarp();
   };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producers (both CTAs)
-    uint32_t it = 0, inflight = 0;
-    bool ok = true;
-    for (int u = cluster; ok && u < p.num_units; u += num_clusters) {
-      const Unit w = unit_of(u, p);
-      int tm, tn;
-      tile_coords(w.tile, p, tm, tn);
-      const int m0 = tm * 2 * Cf::BM + static_cast<int>(rank) * Cf::BM;
-      const int nb0 = tn * Cf::BN + static_cast<int>(rank) * Cf::BN_HALF;
-      for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-        const uint32_t s = it % Cf::STAGES, ph = (it / Cf::STAGES) & 1u;
-        if (!warp_wait(empty_bar(s), ph ^ 1u, limit, abort_flag)) {
-          give_up_pair(kErrTimeoutProducer);
-          ok = false;
-          break;
-        }
-        if (lane == 0) {
+    // One thread waits, arms and issues; the rest of the warp idles.
+    if (lane == 0) {
+      uint32_t it = 0, inflight = 0;
+      bool ok = true;
+      for (int u = cluster; ok && u < p.num_units; u += num_clusters) {
+        const Unit w = unit_of(u, p);
+        int tm, tn;
+        tile_coords(w.tile, p, tm, tn);
+        const int m0 = tm * 2 * Cf::BM + static_cast<int>(rank) * Cf::BM;
+        const int nb0 = tn * Cf::BN + static_cast<int>(rank) * Cf::BN_HALF;
+        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+          const uint32_t s = it % Cf::STAGES, ph = (it / Cf::STAGES) & 1u;
+          if (!mbar_wait_bounded(empty_bar(s), ph ^ 1u, limit, abort_flag)) {
+            give_up_one(kErrTimeoutProducer);
+            ok = false;
+            break;
+          }
           const uint32_t st = sbase + s * Cf::STAGE_BYTES;
           const uint32_t fb = mapa_shared(full_bar(s), 0);  // rank 0's full[s]
           const int k0 = kb * Cf::BK;
@@ -576,10 +579,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             inflight &= ~(1u << s);
           }
         }
-        __syncwarp();
       }
-    }
-    if (lane == 0) {
       if (leader) {
         // Rank 0 can see its full barriers: wait for every fill it armed and loaded.
         for (uint32_t s = 0; s < static_cast<uint32_t>(Cf::STAGES) && s < it; ++s) {
@@ -598,69 +598,63 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (rank 0)
-    if (leader) {
+    // One thread of rank 0 waits and issues every MMA of the pair.
+    if (leader && lane == 0) {
       uint32_t it = 0, tcount = 0;
       bool ok = true;
       for (int u = cluster; ok && u < p.num_units; u += num_clusters, ++tcount) {
         const Unit w = unit_of(u, p);
         const uint32_t buf = tcount & 1u, aph = (tcount >> 1) & 1u;
-        if (!warp_wait(acce_bar(buf), aph ^ 1u, limit, abort_flag)) {
-          give_up_pair(kErrTimeoutMma);
-          ok = false;
+        if (!mbar_wait_bounded(acce_bar(buf), aph ^ 1u, limit, abort_flag)) {
+          give_up_one(kErrTimeoutMma);
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * Cf::BN;
         for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
           const uint32_t s = it % Cf::STAGES, ph = (it / Cf::STAGES) & 1u;
-          if (!warp_wait(full_bar(s), ph, limit, abort_flag)) {
-            give_up_pair(kErrTimeoutMma);
+          if (!mbar_wait_bounded(full_bar(s), ph, limit, abort_flag)) {
+            give_up_one(kErrTimeoutMma);
             ok = false;
             break;
           }
           tc_fence_after();
-          if (lane == 0) {
-            const uint32_t st = sbase + s * Cf::STAGE_BYTES;
-            if constexpr (KIND == KIND_BF16) {
-              // A: 128 rows x 128 B per CTA, K-major.  B: this CTA's two
-              // 64-column boxes (8 KB apart), MN-major.
+          const uint32_t st = sbase + s * Cf::STAGE_BYTES;
+          if constexpr (KIND == KIND_BF16) {
+            // A: 128 rows x 128 B per CTA, K-major.  B: this CTA's two
+            // 64-column boxes (8 KB apart), MN-major.
 #pragma unroll
-              for (int kk = 0; kk < Cf::BK / Cf::INSTR_K; ++kk) {
-                const uint64_t ad = smem_desc_sw128(st + kk * 32, 16, 1024);
-                const uint64_t bd =
-                    smem_desc_sw128(st + Cf::A_BYTES + kk * 2048, Cf::B_BOX_BYTES, 1024);
-                mma_f16_pair(d_tmem, ad, bd, Cf::IDESC, (kb > w.kb0 || kk > 0) ? 1u : 0u);
-              }
-            } else {
-              const uint32_t a_big = st, a_small = st + Cf::A_BYTES;
-              const uint32_t b_big = st + 2 * Cf::A_BYTES, b_small = b_big + Cf::B_BYTES;
-#pragma unroll
-              for (int kk = 0; kk < Cf::BK / Cf::INSTR_K; ++kk) {
-                const uint32_t off = kk * 32;
-                const uint64_t abd = smem_desc_sw128(a_big + off, 16, 1024);
-                const uint64_t asd = smem_desc_sw128(a_small + off, 16, 1024);
-                const uint64_t bbd = smem_desc_sw128(b_big + off, 16, 1024);
-                const uint64_t bsd = smem_desc_sw128(b_small + off, 16, 1024);
-                mma_tf32_pair(d_tmem, asd, bbd, Cf::IDESC, (kb > w.kb0 || kk > 0) ? 1u : 0u);
-                mma_tf32_pair(d_tmem, abd, bsd, Cf::IDESC, 1u);
-                mma_tf32_pair(d_tmem, abd, bbd, Cf::IDESC, 1u);
-              }
+            for (int kk = 0; kk < Cf::BK / Cf::INSTR_K; ++kk) {
+              const uint64_t ad = smem_desc_sw128(st + kk * 32, 16, 1024);
+              const uint64_t bd =
+                  smem_desc_sw128(st + Cf::A_BYTES + kk * 2048, Cf::B_BOX_BYTES, 1024);
+              mma_f16_pair(d_tmem, ad, bd, Cf::IDESC, (kb > w.kb0 || kk > 0) ? 1u : 0u);
             }
-            mma_commit_pair_multicast(empty_bar(s), 0x3);  // stage s free in both CTAs
+          } else {
+            const uint32_t a_big = st, a_small = st + Cf::A_BYTES;
+            const uint32_t b_big = st + 2 * Cf::A_BYTES, b_small = b_big + Cf::B_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < Cf::BK / Cf::INSTR_K; ++kk) {
+              const uint32_t off = kk * 32;
+              const uint64_t abd = smem_desc_sw128(a_big + off, 16, 1024);
+              const uint64_t asd = smem_desc_sw128(a_small + off, 16, 1024);
+              const uint64_t bbd = smem_desc_sw128(b_big + off, 16, 1024);
+              const uint64_t bsd = smem_desc_sw128(b_small + off, 16, 1024);
+              mma_tf32_pair(d_tmem, asd, bbd, Cf::IDESC, (kb > w.kb0 || kk > 0) ? 1u : 0u);
+              mma_tf32_pair(d_tmem, abd, bsd, Cf::IDESC, 1u);
+              mma_tf32_pair(d_tmem, abd, bbd, Cf::IDESC, 1u);
+            }
           }
-          __syncwarp();
+          mma_commit_pair_multicast(empty_bar(s), 0x3);  // stage s free in both CTAs
         }
         if (!ok) break;
-        if (lane == 0) mma_commit_pair_multicast(accf_bar(buf), 0x3);
-        __syncwarp();
+        mma_commit_pair_multicast(accf_bar(buf), 0x3);  // accumulator `buf` complete
       }
-      if (lane == 0) {
-        mma_commit_pair(drain_bar);
-        volatile int never = 0;
-        if (!mbar_wait_bounded(drain_bar, 0, limit, &never)) atomicOr(p.status, kErrTimeoutDrain);
-      }
-      __syncwarp();
+      mma_commit_pair(drain_bar);
+      volatile int never = 0;
+      if (!mbar_wait_bounded(drain_bar, 0, limit, &never)) atomicOr(p.status, kErrTimeoutDrain);
     }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;
@@ -669,7 +663,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int u = cluster; u < p.num_units; u += num_clusters, ++tcount) {
       const Unit w = unit_of(u, p);
       const uint32_t buf = tcount & 1u, aph = (tcount >> 1) & 1u;
-      if (!warp_wait(accf_bar(buf), aph, limit, abort_flag)) {
+      // The accumulator takes a whole tile's main loop to fill: back off
+      // between polls instead of spinning at full issue rate.
+      if (!warp_wait(accf_bar(buf), aph, limit, abort_flag, 128)) {
         give_up_pair(kErrTimeoutEpilogue);
         break;
       }
@@ -945,6 +941,7 @@ cudaError_t launch_tc(const CUtensorMap& a0, const CUtensorMap& a1, const CUtens
   p.full_units = p.num_tiles;
   p.num_units = p.num_tiles;
   p.kb_mid = p.num_kb;
+  p.group_m = ctl.raster_group > 0 ? ctl.raster_group : GROUP_M;
   p.C = C;
   p.ldc = ldc;
   p.status = ctl.status;
@@ -1038,6 +1035,7 @@ cudaError_t launch_tc_any(const CUtensorMap& a0, const CUtensorMap& a1, const CU
   p.full_units = p.num_tiles;
   p.num_units = p.num_tiles;
   p.kb_mid = p.num_kb;
+  p.group_m = ctl.raster_group > 0 ? ctl.raster_group : GROUP_M;
   p.C = C;
   p.ldc = ldc;
   p.status = ctl.status;
