@@ -425,14 +425,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 template <int KIND>
 struct PairCfg;
 
+#ifndef MHR_PAIR_BF16_BK
+#define MHR_PAIR_BF16_BK 64
+#endif
 template <>
 struct PairCfg<KIND_BF16> {
   static constexpr int BM = 128;                            // rows per CTA (pair: 256)
-  static constexpr int BN = 256, BN_HALF = 128, BK = 64, STAGES = 6;
-  static constexpr int A_BYTES = BM * BK * 2;               // 16 KB
-  static constexpr int B_BOX_BYTES = 64 * BK * 2;           // 8 KB
-  static constexpr int B_BYTES = BN_HALF * BK * 2;          // 16 KB (this CTA's half)
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;     // 32 KB per CTA
+  static constexpr int BN = 256, BN_HALF = 128, BK = MHR_PAIR_BF16_BK;
+  static constexpr int STAGES = BK == 64 ? 6 : 3;
+  static constexpr int A_BOX_BYTES = BM * 64 * 2;           // 128 rows x 64 k = 16 KB
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BOX_BYTES = 64 * BK * 2;           // 64 columns x BK k-rows
+  static constexpr int B_BYTES = BN_HALF * BK * 2;          // this CTA's half
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;     // 32 or 64 KB per CTA
   static constexpr int INSTR_K = 16;
   static constexpr uint32_t IDESC = make_idesc(1, false, true, 2 * BM, BN);
   static constexpr uint32_t TMEM_COLS = 2 * BN;             // 512
@@ -564,10 +569,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const bool stall = p.inject_stall && blockIdx.x == 0 && it == 0;
           if (!stall) {
             if constexpr (KIND == KIND_BF16) {
-              tma_load_2d_pair(st, &tmA0, fb, k0, m0);
+#pragma unroll
+              for (int i = 0; i < Cf::BK / 64; ++i)
+                tma_load_2d_pair(st + i * Cf::A_BOX_BYTES, &tmA0, fb, k0 + 64 * i, m0);
 #pragma unroll
               for (int j = 0; j < Cf::BN_HALF / 64; ++j)
-                tma_load_2d_pair(st + Cf::A_BYTES + j * Cf::B_BOX_BYTES, &tmB0, fb, nb0 + 64 * j, k0);
+#pragma unroll
+                for (int i = 0; i < Cf::BK / 64; ++i)  // 64 k-rows per box, stacked
+                  tma_load_2d_pair(st + Cf::A_BYTES + j * Cf::B_BOX_BYTES + i * 8192, &tmB0, fb,
+                                   nb0 + 64 * j, k0 + 64 * i);
             } else {
               tma_load_2d_pair(st, &tmA0, fb, k0, m0);
               tma_load_2d_pair(st + Cf::A_BYTES, &tmA1, fb, k0, m0);
@@ -625,7 +635,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // 64-column boxes (8 KB apart), MN-major.
 #pragma unroll
             for (int kk = 0; kk < Cf::BK / Cf::INSTR_K; ++kk) {
-              const uint64_t ad = smem_desc_sw128(st + kk * 32, 16, 1024);
+              const uint64_t ad =
+                  smem_desc_sw128(st + (kk / 4) * Cf::A_BOX_BYTES + (kk % 4) * 32, 16, 1024);
               const uint64_t bd =
                   smem_desc_sw128(st + Cf::A_BYTES + kk * 2048, Cf::B_BOX_BYTES, 1024);
               mma_f16_pair(d_tmem, ad, bd, Cf::IDESC, (kb > w.kb0 || kk > 0) ? 1u : 0u);
