@@ -173,6 +173,51 @@ def dist_setup():
     return world, rank, local
 
 
+class Ranks:
+    """The bench's multi-process plumbing: one process per GPU, no collective
+    on the data path -- only a barrier around the timed region and a max of
+    each rank's time (NCCL on GPUs; gloo in the CPU tests)."""
+
+    def __init__(self, world: int, device=None, backend: str = "nccl"):
+        import torch
+
+        self.world = world
+        self.device = device if device is not None else torch.device("cpu")
+        self.dist = None
+        if world > 1:
+            import torch.distributed as dist
+
+            if not dist.is_initialized():
+                if backend == "nccl":
+                    dist.init_process_group("nccl", device_id=self.device)
+                else:
+                    dist.init_process_group(backend)
+            self.dist = dist
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def max(self, x: float) -> float:
+        """Max of x over ranks (every rank gets it)."""
+        if self.dist is None:
+            return x
+        import torch
+
+        t = torch.tensor([x], device=self.device, dtype=torch.float64)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.dist is not None:
+            self.dist.destroy_process_group()
+
+
+def aggregate_tflops(world: int, flop_per_rank: float, max_ms: float) -> float:
+    """Whole-job throughput: every rank did flop_per_rank in at most max_ms."""
+    return world * flop_per_rank / (max_ms * 1e-3) / 1e12
+
+
 def oracle_rows(A, B, rows, nthreads=0):
     """CPU oracle on the first `rows` rows of C (the bounded CPU sample)."""
     import oracle
@@ -358,10 +403,7 @@ def main():
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.init_process_group("nccl", device_id=dev)
+    ranks = Ranks(world, dev, "nccl")
     from memory_hierarchy_reuse_gb300 import build as mbuild
 
     mbuild.build()
@@ -419,16 +461,8 @@ def main():
         kern_ms = [k0.elapsed_time(k1) for _, _, k0, k1 in ev]
         return step_ms, kern_ms
 
-    def barrier():
-        if world > 1:
-            torch.distributed.barrier()
-
-    def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        t = torch.tensor([x], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
+    barrier = ranks.barrier
+    max_over_ranks = ranks.max
 
     sampler = ClockSampler(local) if rank == 0 else None
     # ---------------------------------------------------------------- warm-up
@@ -454,7 +488,7 @@ def main():
     ms_step = max_over_ranks(sum(step_ms) / len(step_ms))
     ms_kern = max_over_ranks(sum(kern_ms) / len(kern_ms))
     flop = model.flops(M, N, K)
-    value = world * flop / (ms_step * 1e-3) / 1e12
+    value = aggregate_tflops(world, flop, ms_step)
 
     # ------------------------------------------------- end to end (host buffers)
     # Every step copies its inputs from pinned host memory, calls the C ABI and
@@ -531,7 +565,7 @@ def main():
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         fp32_peak = sms * FP32_LANES_PER_SM * 2 * clock_mhz * 1e6 / 1e12
         extra[ENTRY[also]] = {
-            "value": world * flop / (simt_ms * 1e-3) / 1e12, "unit": "TFLOPS", "ms_per_step": simt_ms,
+            "value": aggregate_tflops(world, flop, simt_ms), "unit": "TFLOPS", "ms_per_step": simt_ms,
             "roofline": {"bound": "alu", "achieved": flop / (simt_k * 1e-3) / 1e12,
                          "traffic": stored_traffic("simt_f32_kernel", args.workload),
                          "peak": fp32_peak, "unit": "TFLOP/s",
@@ -623,9 +657,9 @@ def main():
             "roofline": roofline,
             "cpu_baseline": cpu,
             "cpu_tiled": cpu_tiled_line,
-            "e2e": {"value": world * flop / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+            "e2e": {"value": aggregate_tflops(world, flop, e2e_ms), "unit": "TFLOPS",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "serial_value": world * flop / (e2e_serial_ms * 1e-3) / 1e12,
+                    "serial_value": aggregate_tflops(world, flop, e2e_serial_ms),
                     "note": "per step: pinned host A, B -> device, C API call, C -> pinned host; "
                             "value pipelines consecutive steps over three streams, serial_value "
                             "runs them one after another on one stream"},
@@ -635,8 +669,7 @@ def main():
             "source_digest": source_digest(),
         }
         print(json.dumps(out), flush=True)
-    if world > 1:
-        torch.distributed.destroy_process_group()
+    ranks.close()
 
 
 if __name__ == "__main__":
