@@ -162,6 +162,63 @@ __device__ __forceinline__ void give_up(const TcParams& p, volatile int* abort_f
   __syncwarp();
 }
 
+// Epilogue of one 32 x 32 fp32 chunk held by a warp (lane = row, r[j] =
+// column j): write it into the warp's staging box in shared memory (128-byte
+// swizzle: 16-byte piece j of row r sits at position j ^ (r % 8), so both the
+// row-wise writes here and the column-wise reads below are conflict-free),
+// then either hand the box to one TMA store / reduce-add, or -- when C is not
+// TMA-aligned -- store it row by row so each warp instruction writes 32
+// consecutive floats of one row of C (masked at the edges; atomic adds for
+// split-K units).
+template <bool TMA_STORE>
+__device__ __forceinline__ void stage_and_store_chunk(const uint32_t (&r)[32], uint32_t epi_base,
+                                                      int ew, uint32_t chunk, int lane,
+                                                      const CUtensorMap* tmC, const TcParams& p,
+                                                      int row0, int col0, bool reduce) {
+  const uint32_t stg = epi_base + (ew * 2 + (chunk & 1u)) * EPI_BUF_BYTES;
+  if (TMA_STORE) {
+    if (lane == 0) bulk_wait_group_read<1>();  // the store that last used this buffer has read it
+  }
+  __syncwarp();
+  const uint32_t row_addr = stg + lane * 128;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t a = row_addr + ((j ^ (lane & 7)) << 4);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(r[4 * j]),
+                 "r"(r[4 * j + 1]), "r"(r[4 * j + 2]), "r"(r[4 * j + 3])
+                 : "memory");
+  }
+  if (TMA_STORE) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if (reduce)
+        tma_reduce_add_2d(tmC, stg, col0, row0);
+      else
+        tma_store_2d(tmC, stg, col0, row0);
+      bulk_commit_group();
+    }
+  } else {
+    __syncwarp();
+    const int col = col0 + lane;
+#pragma unroll 4
+    for (int i = 0; i < 32; ++i) {
+      const int row = row0 + i;
+      const uint32_t a = stg + i * 128 + ((((lane >> 2) ^ i) & 7) << 4) + (lane & 3) * 4;
+      float v;
+      asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+      if (row < p.M && col < p.N) {
+        float* dst = p.C + static_cast<int64_t>(row) * p.ldc + col;
+        if (reduce)
+          atomicAdd(dst, v);
+        else
+          *dst = v;
+      }
+    }
+    __syncwarp();  // the box is free for the next chunk
+  }
+}
+
 template <int KIND, bool TMA_STORE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
@@ -354,37 +411,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t r[32];
         tmem_ld_32cols(taddr + c * 32, r);
         tmem_ld_wait();
-        if constexpr (TMA_STORE) {
-          const uint32_t stg = sbase + L::EPI_OFF + (ew * 2 + (chunk & 1u)) * EPI_BUF_BYTES;
-          if (lane == 0) bulk_wait_group_read<1>();  // the store that last used this buffer has read it
-          __syncwarp();
-          // Row `lane` of the 32 x 32 box, 128-byte swizzle: 16-byte chunk j
-          // of row r sits at chunk position j ^ (r % 8).
-          const uint32_t row_addr = stg + lane * 128;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t a = row_addr + ((j ^ (lane & 7)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(r[4 * j]),
-                         "r"(r[4 * j + 1]), "r"(r[4 * j + 2]), "r"(r[4 * j + 3])
-                         : "memory");
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tmC, stg, n0 + c * 32, m0 + q * 32);
-            bulk_commit_group();
-          }
-          ++chunk;
-        } else {
-          const int row = m0 + q * 32 + lane;
-          if (row < p.M) {
-            float* crow = p.C + static_cast<int64_t>(row) * p.ldc;
-            const int col0 = n0 + c * 32;
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (col0 + j < p.N) crow[col0 + j] = __uint_as_float(r[j]);
-          }
-        }
+        stage_and_store_chunk<TMA_STORE>(r, sbase + L::EPI_OFF, ew, chunk, lane, &tmC, p,
+                                         m0 + q * 32, n0 + c * 32, false);
+        ++chunk;
       }
       tc_fence_before();
       __syncwarp();
@@ -691,44 +720,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t r[32];
         tmem_ld_32cols(taddr + c * 32, r);
         tmem_ld_wait();
-        if constexpr (TMA_STORE) {
-          const uint32_t stg = sbase + L::EPI_OFF + (ew * 2 + (chunk & 1u)) * EPI_BUF_BYTES;
-          if (lane == 0) bulk_wait_group_read<1>();
-          __syncwarp();
-          const uint32_t row_addr = stg + lane * 128;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t a = row_addr + ((j ^ (lane & 7)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(r[4 * j]),
-                         "r"(r[4 * j + 1]), "r"(r[4 * j + 2]), "r"(r[4 * j + 3])
-                         : "memory");
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            if (w.reduce)
-              tma_reduce_add_2d(&tmC, stg, n0 + c * 32, m0 + q * 32);
-            else
-              tma_store_2d(&tmC, stg, n0 + c * 32, m0 + q * 32);
-            bulk_commit_group();
-          }
-          ++chunk;
-        } else {
-          const int row = m0 + q * 32 + lane;
-          if (row < p.M) {
-            float* crow = p.C + static_cast<int64_t>(row) * p.ldc;
-            const int col0 = n0 + c * 32;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (col0 + j < p.N) {
-                if (w.reduce)
-                  atomicAdd(crow + col0 + j, __uint_as_float(r[j]));
-                else
-                  crow[col0 + j] = __uint_as_float(r[j]);
-              }
-            }
-          }
-        }
+        stage_and_store_chunk<TMA_STORE>(r, sbase + L::EPI_OFF, ew, chunk, lane, &tmC, p,
+                                         m0 + q * 32, n0 + c * 32, w.reduce);
+        ++chunk;
       }
       tc_fence_before();
       __syncwarp();
@@ -796,54 +790,13 @@ __device__ __forceinline__ void split_tf32(float x, float& big, float& small) {
   small = isfinite(x) ? tf32_rne(rest) : 0.f;
 }
 
-// A: row-major M x K -> big/small M x Kp (same orientation).
-__global__ void split_a_kernel(const float* __restrict__ A, int64_t M, int64_t K, int64_t lda,
-                               int64_t Kp, float* __restrict__ big, float* __restrict__ small) {
-  for (int64_t r = blockIdx.y; r < M; r += gridDim.y) {
-    for (int64_t k = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; k < K;
-         k += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-      float b, s;
-      split_tf32(__ldg(A + r * lda + k), b, s);
-      big[r * Kp + k] = b;
-      small[r * Kp + k] = s;
-    }
-  }
-}
-
-// B: row-major K x N -> big/small N x Kp (transposed, K-contiguous) through a
-// 32 x 33 shared tile so both the read (along n) and the write (along k) are
-// coalesced.
-__global__ void split_bt_kernel(const float* __restrict__ B, int64_t K, int64_t N, int64_t ldb,
-                                int64_t Kp, float* __restrict__ big, float* __restrict__ small) {
-  __shared__ float tb[32][33];
-  __shared__ float ts[32][33];
-  const int64_t tiles_n = (N + 31) / 32, tiles_k = (K + 31) / 32;
-  for (int64_t tile = blockIdx.x; tile < tiles_n * tiles_k; tile += gridDim.x) {
-    const int64_t n0 = (tile % tiles_n) * 32, k0 = (tile / tiles_n) * 32;
-    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-      const int64_t k = k0 + i, n = n0 + threadIdx.x;
-      float b = 0.f, s = 0.f;
-      if (k < K && n < N) split_tf32(__ldg(B + k * ldb + n), b, s);
-      tb[i][threadIdx.x] = b;
-      ts[i][threadIdx.x] = s;
-    }
-    __syncthreads();
-    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-      const int64_t n = n0 + i, k = k0 + threadIdx.x;
-      if (n < N && k < K) {
-        big[n * Kp + k] = tb[threadIdx.x][i];
-        small[n * Kp + k] = ts[threadIdx.x][i];
-      }
-    }
-    __syncthreads();
-  }
-}
-
-// Vectorised split of both operands in one launch (A, B and C pointers
-// 16-byte aligned, K, N, lda, ldb multiples of 4, so Kp == K).  Blocks
-// [0, a_blocks) split rows of A in place-order; the remaining blocks split
-// 64 x 64 tiles of B and write them transposed.  Each thread keeps four
-// 16-byte loads in flight.
+// Split of both operands in one launch.  Blocks [0, a_blocks) split rows of
+// A in place order; the remaining blocks split 64 x 64 tiles of B and write
+// them transposed.  VA / VB select 16-byte loads when the operand's address,
+// leading dimension (and, for A, K) allow them, else 4-byte loads; the
+// outputs (pitch Kp, a multiple of 4, in the 16-byte-aligned workspace) are
+// always written with 16-byte stores.  Each thread keeps several loads in
+// flight.
 constexpr int SPLIT_THREADS = 256;
 constexpr int SPLIT_TILE = 64;
 
@@ -854,26 +807,36 @@ __device__ __forceinline__ void split4(const float4 v, float4& b, float4& s) {
   split_tf32(v.w, b.w, s.w);
 }
 
+template <bool VA, bool VB>
 __global__ void __launch_bounds__(SPLIT_THREADS)
     split_vec_kernel(const float* __restrict__ A, const float* __restrict__ B, int64_t M,
-                     int64_t N, int64_t K, int64_t lda, int64_t ldb, int a_blocks,
+                     int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t Kp, int a_blocks,
                      float* __restrict__ a_big, float* __restrict__ a_small,
                      float* __restrict__ bt_big, float* __restrict__ bt_small) {
   __shared__ float tb[SPLIT_TILE][SPLIT_TILE + 1];
   __shared__ float ts[SPLIT_TILE][SPLIT_TILE + 1];
   const int t = threadIdx.x;
   if (static_cast<int>(blockIdx.x) < a_blocks) {
-    const int64_t k4 = K / 4;
+    const int64_t k4 = Kp / 4;  // 16-byte chunks of an output row (pad columns get zeros)
     for (int64_t r = blockIdx.x; r < M; r += a_blocks) {
-      const float4* src = reinterpret_cast<const float4*>(A + r * lda);
-      float4* db = reinterpret_cast<float4*>(a_big + r * K);
-      float4* ds = reinterpret_cast<float4*>(a_small + r * K);
+      const float* src = A + r * lda;
+      float4* db = reinterpret_cast<float4*>(a_big + r * Kp);
+      float4* ds = reinterpret_cast<float4*>(a_small + r * Kp);
       for (int64_t c0 = t; c0 < k4; c0 += 4 * SPLIT_THREADS) {
         float4 v[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int64_t c = c0 + j * SPLIT_THREADS;
-          if (c < k4) v[j] = __ldg(src + c);
+          if (c >= k4) continue;
+          if (VA) {
+            v[j] = __ldg(reinterpret_cast<const float4*>(src) + c);
+          } else {
+            const int64_t k = 4 * c;
+            v[j].x = k < K ? __ldg(src + k) : 0.f;
+            v[j].y = k + 1 < K ? __ldg(src + k + 1) : 0.f;
+            v[j].z = k + 2 < K ? __ldg(src + k + 2) : 0.f;
+            v[j].w = k + 3 < K ? __ldg(src + k + 3) : 0.f;
+          }
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -889,39 +852,57 @@ __global__ void __launch_bounds__(SPLIT_THREADS)
     }
     return;
   }
-  // B role: tile (k0, n0) of 64 x 64.
+  // B role: tile (k0, n0) of 64 x 64, transposed.
   const int64_t tiles_n = (N + SPLIT_TILE - 1) / SPLIT_TILE;
   const int64_t tiles = tiles_n * ((K + SPLIT_TILE - 1) / SPLIT_TILE);
   const int64_t nb = gridDim.x - a_blocks;
   for (int64_t tile = blockIdx.x - a_blocks; tile < tiles; tile += nb) {
     const int64_t n0 = (tile % tiles_n) * SPLIT_TILE, k0 = (tile / tiles_n) * SPLIT_TILE;
-    float4 v[4];
+    if (VB) {
+      float4 v[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {  // read: 64 k-rows x 16 float4 along n
-      const int idx = t + j * SPLIT_THREADS;
-      const int64_t k = k0 + (idx >> 4), n = n0 + (idx & 15) * 4;
-      v[j] = (k < K && n < N) ? __ldg(reinterpret_cast<const float4*>(B + k * ldb + n))
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+      for (int j = 0; j < 4; ++j) {  // read: 64 k-rows x 16 float4 along n
+        const int idx = t + j * SPLIT_THREADS;
+        const int64_t k = k0 + (idx >> 4), n = n0 + (idx & 15) * 4;
+        v[j] = (k < K && n < N) ? __ldg(reinterpret_cast<const float4*>(B + k * ldb + n))
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int idx = t + j * SPLIT_THREADS;
-      const int kr = idx >> 4, nc = (idx & 15) * 4;
-      float4 b, s;
-      split4(v[j], b, s);
-      tb[kr][nc] = b.x; tb[kr][nc + 1] = b.y; tb[kr][nc + 2] = b.z; tb[kr][nc + 3] = b.w;
-      ts[kr][nc] = s.x; ts[kr][nc + 1] = s.y; ts[kr][nc + 2] = s.z; ts[kr][nc + 3] = s.w;
+      for (int j = 0; j < 4; ++j) {
+        const int idx = t + j * SPLIT_THREADS;
+        const int kr = idx >> 4, nc = (idx & 15) * 4;
+        float4 b, s;
+        split4(v[j], b, s);
+        tb[kr][nc] = b.x; tb[kr][nc + 1] = b.y; tb[kr][nc + 2] = b.z; tb[kr][nc + 3] = b.w;
+        ts[kr][nc] = s.x; ts[kr][nc + 1] = s.y; ts[kr][nc + 2] = s.z; ts[kr][nc + 3] = s.w;
+      }
+    } else {
+      float v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {  // read: 64 k-rows x 64 n, one float per load
+        const int idx = t + j * SPLIT_THREADS;
+        const int64_t k = k0 + (idx >> 6), n = n0 + (idx & 63);
+        v[j] = (k < K && n < N) ? __ldg(B + k * ldb + n) : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int idx = t + j * SPLIT_THREADS;
+        float b, sm;
+        split_tf32(v[j], b, sm);
+        tb[idx >> 6][idx & 63] = b;
+        ts[idx >> 6][idx & 63] = sm;
+      }
     }
     __syncthreads();
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {  // write: 64 n-rows x 16 float4 along k
+    for (int j = 0; j < 4; ++j) {  // write: 64 n-rows x 16 float4 along k (zeros past K)
       const int idx = t + j * SPLIT_THREADS;
       const int nr = idx >> 4, kc = (idx & 15) * 4;
       const int64_t n = n0 + nr, k = k0 + kc;
-      if (n < N && k < K) {
-        *reinterpret_cast<float4*>(bt_big + n * K + k) =
+      if (n < N && k < Kp) {
+        *reinterpret_cast<float4*>(bt_big + n * Kp + k) =
             make_float4(tb[kc][nr], tb[kc + 1][nr], tb[kc + 2][nr], tb[kc + 3][nr]);
-        *reinterpret_cast<float4*>(bt_small + n * K + k) =
+        *reinterpret_cast<float4*>(bt_small + n * Kp + k) =
             make_float4(ts[kc][nr], ts[kc + 1][nr], ts[kc + 2][nr], ts[kc + 3][nr]);
       }
     }
@@ -1086,33 +1067,36 @@ cudaError_t launch_split_tf32(const float* A, const float* B, int64_t M, int64_t
                               int64_t lda, int64_t ldb, int64_t Kp, float* a_big, float* a_small,
                               float* bt_big, float* bt_small, cudaStream_t s) {
   auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-  const bool vec = Kp == K && K % 4 == 0 && N % 4 == 0 && lda % 4 == 0 && ldb % 4 == 0 &&
-                   al16(A) && al16(B) && al16(a_big) && al16(a_small) && al16(bt_big) &&
-                   al16(bt_small);
-  if (vec) {
-    // One wave of resident blocks (6 per SM fit), shared between the operands
-    // in proportion to their sizes.
-    int dev = 0, sms = 148;
-    if (cudaGetDevice(&dev) == cudaSuccess)
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int64_t total = static_cast<int64_t>(sms) * 6;
-    const int64_t b_tiles = ((N + SPLIT_TILE - 1) / SPLIT_TILE) * ((K + SPLIT_TILE - 1) / SPLIT_TILE);
-    const double a_share = static_cast<double>(M) / static_cast<double>(M + N);
-    int64_t a_blocks = static_cast<int64_t>(a_share * total);
-    a_blocks = a_blocks < 1 ? 1 : (a_blocks > M ? M : a_blocks);
-    int64_t b_blocks = total - a_blocks;
-    b_blocks = b_blocks < 1 ? 1 : (b_blocks > b_tiles ? b_tiles : b_blocks);
-    split_vec_kernel<<<static_cast<unsigned>(a_blocks + b_blocks), SPLIT_THREADS, 0, s>>>(
-        A, B, M, N, K, lda, ldb, static_cast<int>(a_blocks), a_big, a_small, bt_big, bt_small);
-    return cudaGetLastError();
-  }
-  const unsigned gx = static_cast<unsigned>((K + 255) / 256 < 64 ? (K + 255) / 256 : 64);
-  split_a_kernel<<<dim3(gx, grid_rows(M)), 256, 0, s>>>(A, M, K, lda, Kp, a_big, a_small);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const int64_t tiles = ((N + 31) / 32) * ((K + 31) / 32);
-  const unsigned gb = static_cast<unsigned>(tiles < (1 << 20) ? tiles : (1 << 20));
-  split_bt_kernel<<<gb, dim3(32, 8), 0, s>>>(B, K, N, ldb, Kp, bt_big, bt_small);
+  if (Kp % 4 != 0 || !al16(a_big) || !al16(a_small) || !al16(bt_big) || !al16(bt_small))
+    return cudaErrorInvalidValue;  // the workspace layout guarantees these
+  const bool va = al16(A) && lda % 4 == 0 && K % 4 == 0;
+  const bool vb = al16(B) && ldb % 4 == 0 && N % 4 == 0;
+  // One wave of resident blocks (6 per SM fit), shared between the operands
+  // in proportion to their sizes.
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t total = static_cast<int64_t>(sms) * 6;
+  const int64_t b_tiles = ((N + SPLIT_TILE - 1) / SPLIT_TILE) * ((K + SPLIT_TILE - 1) / SPLIT_TILE);
+  const double a_share = static_cast<double>(M) / static_cast<double>(M + N);
+  int64_t a_blocks = static_cast<int64_t>(a_share * total);
+  a_blocks = a_blocks < 1 ? 1 : (a_blocks > M ? M : a_blocks);
+  int64_t b_blocks = total - a_blocks;
+  b_blocks = b_blocks < 1 ? 1 : (b_blocks > b_tiles ? b_tiles : b_blocks);
+  const unsigned grid = static_cast<unsigned>(a_blocks + b_blocks);
+  const int ab = static_cast<int>(a_blocks);
+  if (va && vb)
+    split_vec_kernel<true, true><<<grid, SPLIT_THREADS, 0, s>>>(A, B, M, N, K, lda, ldb, Kp, ab,
+                                                                a_big, a_small, bt_big, bt_small);
+  else if (va)
+    split_vec_kernel<true, false><<<grid, SPLIT_THREADS, 0, s>>>(A, B, M, N, K, lda, ldb, Kp, ab,
+                                                                 a_big, a_small, bt_big, bt_small);
+  else if (vb)
+    split_vec_kernel<false, true><<<grid, SPLIT_THREADS, 0, s>>>(A, B, M, N, K, lda, ldb, Kp, ab,
+                                                                 a_big, a_small, bt_big, bt_small);
+  else
+    split_vec_kernel<false, false><<<grid, SPLIT_THREADS, 0, s>>>(A, B, M, N, K, lda, ldb, Kp, ab,
+                                                                  a_big, a_small, bt_big, bt_small);
   return cudaGetLastError();
 }
 
