@@ -18,7 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmhr_gemm.so")
-SOURCES = ["api.cu", "simt_f32.cu", "tc_gemm.cu", "noalloc.cu", "ladder.cu"]
+SOURCES = ["api.cu", "simt_f32.cu", "tc_gemm.cu", "tc_gemm_1cta.cu", "tc_gemm_pair.cu",
+           "tc_prepass.cu", "noalloc.cu", "ladder.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -41,10 +41,6 @@ cudaError_t launch_split_tf32(const float* A, const float* B, int64_t M, int64_t
                               int64_t lda, int64_t ldb, int64_t Kp, float* a_big, float* a_small,
                               float* bt_big, float* bt_small, cudaStream_t s);
 
-// Shared-memory bytes the tensor-core kernels request (for cudaFuncSetAttribute).
-size_t tc_bf16_smem_bytes();
-size_t tc_3xtf32_smem_bytes();
-
 // bf16 x bf16 -> fp32 on tcgen05.  A: M x K bf16 (row pitch lda, 16-byte
 // aligned rows), B: K x N bf16 (pitch ldb, aligned).  C via TMA store when
 // c_tma is true (C 16-byte aligned, ldc % 4 == 0), else direct stores.

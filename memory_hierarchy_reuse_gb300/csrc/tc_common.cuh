@@ -1,0 +1,242 @@
+// Shared pieces of the tensor-core GEMM kernels for sm_103a (TMA -> mbarrier
+// shared-memory ring -> tcgen05.mma with a TMEM accumulator -> TMA-store
+// epilogue): kinds, the parameter block, the tile schedule, bounded waits and
+// the epilogue's chunk store.  The single-CTA kernel is in tc_gemm_1cta.cu,
+// the CTA-pair kernel in tc_gemm_pair.cu.
+//
+// The method is the pages' tiling ("矩阵乘法 tiling", sections 二-四;
+// "CUDA 深入浅出（二）", sections "分块之后怎么读" and "推广到整个 N×N 矩阵"):
+// one output tile per work unit, K walked in BK-wide steps, each step staging
+// an A box (BM x BK) and a B box (BK x BN) on chip and reusing every staged
+// element across the whole tile.  What differs from the pages' 2016-era SIMT
+// kernel is how each step is executed on Blackwell:
+//
+//   step                    pages                         here
+//   ----------------------  ----------------------------  ------------------------------
+//   global -> shared        each thread loads 1 element   one TMA box copy per operand,
+//                                                          128-byte swizzle (no bank
+//                                                          conflicts), OOB zero-fill
+//   barrier one / two       __syncthreads() x 2           full[s] / empty[s] mbarriers
+//                                                          of a STAGES-deep ring
+//   multiply-accumulate     scalar FMA, acc in a register tcgen05.mma 128 x BN x K_instr,
+//                                                          accumulator in TMEM
+//   write C                 one store per thread          TMEM -> registers -> swizzled
+//                                                          smem -> TMA store
+//
+// Warp roles (192 threads, one CTA per SM, persistent over tiles):
+//   warp 0     TMA producer (lane 0 issues)
+//   warp 1     TMEM allocator + MMA issuer (lane 0 issues)
+//   warps 2-5  epilogue; warp w reads TMEM lanes 32*(w%4) .. 32*(w%4)+31
+// The accumulator is double-buffered in TMEM so the epilogue of tile i runs
+// while the MMAs of tile i+1 are issued.
+//
+// Two kinds:
+//   KIND_BF16:   A bf16 K-major (row-major M x K), B bf16 MN-major (row-major
+//                K x N), kind::f16.
+//   KIND_3XTF32: A_big, A_small K-major; B_big^T, B_small^T K-major (N x K),
+//                kind::tf32, three MMAs per instruction-K step (small*big,
+//                big*small, big*big).
+//
+// Every wait is bounded (DeviceCtl::wait_limit_ns).  A role that runs out of
+// time sets its bit in the device status word and an abort flag in shared
+// memory; the other roles see the flag and unwind; the CTA then waits
+// (bounded) for its own copies and MMAs in flight, frees its TMEM and exits.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "mhr_device.cuh"
+#include "mhr_internal.h"
+
+namespace mhr {
+namespace tc {
+
+constexpr int KIND_BF16 = 0;
+constexpr int KIND_3XTF32 = 1;
+
+constexpr int EPI_WARPS = 4;
+constexpr int EPI_BUF_BYTES = 32 * 32 * 4;                 // 32 rows x 32 fp32
+constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;   // 32 KB
+constexpr int NUM_THREADS = 192;
+constexpr int GROUP_M = 16;  // default tile rows per raster group
+
+struct TcParams {
+  int32_t M, N, K;
+  int32_t tiles_m, tiles_n, num_tiles, num_kb;
+  // Work units of the pair kernel: tiles [0, full_units) whole; tiles
+  // [full_units, num_tiles) split into two K halves, [0, kb_mid) and
+  // [kb_mid, num_kb), whose results are reduce-added into a zeroed C.
+  int32_t full_units, num_units, kb_mid;
+  int32_t group_m;  // tile rows per raster group
+  float* C;
+  int64_t ldc;
+  uint32_t* status;
+  uint64_t wait_limit_ns;
+  int32_t inject_stall;
+};
+
+// Grouped raster: consecutive work units sweep GROUP_M tile rows column by
+// column, so the CTAs resident at one time share A row strips and B column
+// strips in L2 (a second level of the pages' reuse argument, one level up
+// from shared memory).
+__device__ __forceinline__ void tile_coords(int t, const TcParams& p, int& tm, int& tn) {
+  const int group_size = p.group_m * p.tiles_n;
+  const int g = t / group_size;
+  const int first_m = g * p.group_m;
+  const int gm = min(p.tiles_m - first_m, p.group_m);
+  const int r = t - g * group_size;
+  tm = first_m + r % gm;
+  tn = r / gm;
+}
+
+// Work unit u of the pair kernel -> tile, K-block range, and whether its
+// result is added into C (split unit) rather than stored.
+struct Unit {
+  int tile, kb0, kb1;
+  bool reduce;
+};
+__device__ __forceinline__ Unit unit_of(int u, const TcParams& p) {
+  Unit w;
+  if (u < p.full_units) {
+    w.tile = u;
+    w.kb0 = 0;
+    w.kb1 = p.num_kb;
+    w.reduce = false;
+  } else {
+    const int v = u - p.full_units;
+    w.tile = p.full_units + (v >> 1);
+    w.kb0 = (v & 1) ? p.kb_mid : 0;
+    w.kb1 = (v & 1) ? p.num_kb : p.kb_mid;
+    w.reduce = true;
+  }
+  return w;
+}
+
+// Warp-uniform bounded wait: every lane polls; the warp agrees on the outcome.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_t limit,
+                                          volatile int* abort_flag, uint32_t sleep_ns = 0) {
+  const bool ok = mbar_wait_bounded(bar, parity, limit, abort_flag, sleep_ns);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Called by a single thread: record why (first role to give up only) and
+// raise the CTA's abort flag.
+__device__ __forceinline__ void give_up_one(const TcParams& p, volatile int* abort_flag,
+                                            uint32_t bit) {
+  if (!*abort_flag) atomicOr(p.status, bit);
+  *abort_flag = 1;
+}
+
+__device__ __forceinline__ void give_up(const TcParams& p, volatile int* abort_flag, uint32_t bit,
+                                        int lane) {
+  if (lane == 0) {
+    if (!*abort_flag) atomicOr(p.status, bit);  // the first role to give up records why
+    *abort_flag = 1;
+  }
+  __syncwarp();
+}
+
+// Epilogue of one 32 x 32 fp32 chunk held by a warp (lane = row, r[j] =
+// column j): write it into the warp's staging box in shared memory (128-byte
+// swizzle: 16-byte piece j of row r sits at position j ^ (r % 8), so both the
+// row-wise writes here and the column-wise reads below are conflict-free),
+// then either hand the box to one TMA store / reduce-add, or -- when C is not
+// TMA-aligned -- store it row by row so each warp instruction writes 32
+// consecutive floats of one row of C (masked at the edges; atomic adds for
+// split-K units).
+template <bool TMA_STORE>
+__device__ __forceinline__ void stage_and_store_chunk(const uint32_t (&r)[32], uint32_t epi_base,
+                                                      int ew, uint32_t chunk, int lane,
+                                                      const CUtensorMap* tmC, const TcParams& p,
+                                                      int row0, int col0, bool reduce) {
+  const uint32_t stg = epi_base + (ew * 2 + (chunk & 1u)) * EPI_BUF_BYTES;
+  if (TMA_STORE) {
+    if (lane == 0) bulk_wait_group_read<1>();  // the store that last used this buffer has read it
+  }
+  __syncwarp();
+  const uint32_t row_addr = stg + lane * 128;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t a = row_addr + ((j ^ (lane & 7)) << 4);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(r[4 * j]),
+                 "r"(r[4 * j + 1]), "r"(r[4 * j + 2]), "r"(r[4 * j + 3])
+                 : "memory");
+  }
+  if (TMA_STORE) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if (reduce)
+        tma_reduce_add_2d(tmC, stg, col0, row0);
+      else
+        tma_store_2d(tmC, stg, col0, row0);
+      bulk_commit_group();
+    }
+  } else {
+    __syncwarp();
+    const int col = col0 + lane;
+#pragma unroll 4
+    for (int i = 0; i < 32; ++i) {
+      const int row = row0 + i;
+      const uint32_t a = stg + i * 128 + ((((lane >> 2) ^ i) & 7) << 4) + (lane & 3) * 4;
+      float v;
+      asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+      if (row < p.M && col < p.N) {
+        float* dst = p.C + static_cast<int64_t>(row) * p.ldc + col;
+        if (reduce)
+          atomicAdd(dst, v);
+        else
+          *dst = v;
+      }
+    }
+    __syncwarp();  // the box is free for the next chunk
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+// Parameter block for a grid of tile_m x tile_n tiles walking K in bk steps.
+inline TcParams make_params(int64_t M, int64_t N, int64_t K, int tile_m, int tile_n, int bk,
+                            float* C, int64_t ldc, const DeviceCtl& ctl) {
+  TcParams p;
+  p.M = static_cast<int32_t>(M);
+  p.N = static_cast<int32_t>(N);
+  p.K = static_cast<int32_t>(K);
+  p.tiles_m = static_cast<int32_t>((M + tile_m - 1) / tile_m);
+  p.tiles_n = static_cast<int32_t>((N + tile_n - 1) / tile_n);
+  p.num_tiles = p.tiles_m * p.tiles_n;
+  p.num_kb = static_cast<int32_t>((K + bk - 1) / bk);
+  p.full_units = p.num_tiles;
+  p.num_units = p.num_tiles;
+  p.kb_mid = p.num_kb;
+  p.group_m = ctl.raster_group > 0 ? ctl.raster_group : GROUP_M;
+  p.C = C;
+  p.ldc = ldc;
+  p.status = ctl.status;
+  p.wait_limit_ns = ctl.wait_limit_ns;
+  p.inject_stall = ctl.inject_stall;
+  return p;
+}
+
+// The CTA pair's output tile (both kinds).
+constexpr int PAIR_TILE_M = 256, PAIR_TILE_N = 256;
+
+// Tensor maps of one launch: A parts, B parts (the bf16 kind uses a0 / b0
+// only) and C (unused without TMA stores).
+struct TcMaps {
+  CUtensorMap a0, a1, b0, b1, c;
+};
+
+// tc_gemm_1cta.cu
+cudaError_t launch_single_cta(int kind, const TcMaps& maps, float* C, int64_t M, int64_t N,
+                              int64_t K, int64_t ldc, bool c_tma, const DeviceCtl& ctl,
+                              cudaStream_t s);
+// tc_gemm_pair.cu
+cudaError_t launch_cta_pair(int kind, const TcMaps& maps, float* C, int64_t M, int64_t N,
+                            int64_t K, int64_t ldc, bool c_tma, const DeviceCtl& ctl,
+                            cudaStream_t s);
+
+}  // namespace tc
+}  // namespace mhr

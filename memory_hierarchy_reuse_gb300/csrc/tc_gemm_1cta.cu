@@ -1,0 +1,294 @@
+// Single-CTA tensor-core GEMM kernel (one SM per output tile, persistent):
+//   bf16:   128 x 256 x 64 tiles, 4 stages of 48 KB, kind::f16 M128 N256 K16;
+//   3xTF32: 128 x 128 x 32 tiles, 3 stages of 64 KB, kind::tf32 M128 N128 K8.
+// Used for problems whose 256-row CTA-pair tiles would not keep the GPU busy.
+// The method and the warp roles are described in tc_common.cuh.
+#include "tc_common.cuh"
+
+namespace mhr {
+namespace tc {
+namespace {
+
+template <int KIND>
+struct Cfg;
+
+template <>
+struct Cfg<KIND_BF16> {
+  static constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+  static constexpr int A_BYTES = BM * BK * 2;              // 16 KB
+  static constexpr int B_BOX_BYTES = 64 * BK * 2;          // 64 cols x 64 k = 8 KB
+  static constexpr int B_BYTES = BK * BN * 2;              // 32 KB
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;    // 48 KB
+  static constexpr int INSTR_K = 16;
+  static constexpr uint32_t IDESC = make_idesc(1, false, true, BM, BN);
+  static constexpr uint32_t TMEM_COLS = 2 * BN;            // 512
+};
+
+template <>
+struct Cfg<KIND_3XTF32> {
+  static constexpr int BM = 128, BN = 128, BK = 32, STAGES = 3;
+  static constexpr int A_BYTES = BM * BK * 4;              // 16 KB each (big, small)
+  static constexpr int B_BYTES = BN * BK * 4;              // 16 KB each (big, small)
+  static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;  // 64 KB
+  static constexpr int INSTR_K = 8;
+  static constexpr uint32_t IDESC = make_idesc(2, false, false, BM, BN);
+  static constexpr uint32_t TMEM_COLS = 2 * BN;            // 256
+};
+
+template <int KIND>
+struct Layout {
+  using C = Cfg<KIND>;
+  static constexpr int EPI_OFF = C::STAGES * C::STAGE_BYTES;
+  static constexpr int BAR_OFF = EPI_OFF + EPI_BYTES;
+  static constexpr int NUM_BARS = 2 * C::STAGES + 5;        // full, empty, acc_full x2, acc_empty x2, drain
+  static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;   // tmem slot, abort flag
+  static constexpr int USED = MISC_OFF + 16;
+  static constexpr int ALLOC = USED + 1024;                 // slack for 1024-byte alignment
+};
+
+template <int KIND, bool TMA_STORE>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+                   const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
+                   const __grid_constant__ CUtensorMap tmC, const TcParams p) {
+  using Cf = Cfg<KIND>;
+  using L = Layout<KIND>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + L::BAR_OFF;
+  auto full_bar = [&](uint32_t s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (Cf::STAGES + s); };
+  auto accf_bar = [&](uint32_t b) { return bar0 + 8u * (2 * Cf::STAGES + b); };
+  auto acce_bar = [&](uint32_t b) { return bar0 + 8u * (2 * Cf::STAGES + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * Cf::STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Cf::STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf_bar(b), 1);
+      mbar_init(acce_bar(b), EPI_WARPS);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA0);
+    tma_prefetch_desc(&tmB0);
+    if constexpr (KIND == KIND_3XTF32) {
+      tma_prefetch_desc(&tmA1);
+      tma_prefetch_desc(&tmB1);
+    }
+    if (TMA_STORE) tma_prefetch_desc(&tmC);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), Cf::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint64_t limit = p.wait_limit_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    // One thread waits, arms and issues; the rest of the warp idles.
+    if (lane == 0) {
+      uint32_t it = 0;
+      uint32_t inflight = 0;  // bit s: the latest fill of stage s had a TMA issued
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        int tm, tn;
+        tile_coords(t, p, tm, tn);
+        const int m0 = tm * Cf::BM, n0 = tn * Cf::BN;
+        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+          const uint32_t s = it % Cf::STAGES, ph = (it / Cf::STAGES) & 1u;
+          if (!mbar_wait_bounded(empty_bar(s), ph ^ 1u, limit, abort_flag)) {
+            give_up_one(p, abort_flag, kErrTimeoutProducer);
+            ok = false;
+            break;
+          }
+          const uint32_t st = sbase + s * Cf::STAGE_BYTES;
+          const int k0 = kb * Cf::BK;
+          mbar_arrive_expect_tx(full_bar(s), Cf::STAGE_BYTES);
+          const bool stall = p.inject_stall && blockIdx.x == 0 && it == 0;
+          if (!stall) {
+            if constexpr (KIND == KIND_BF16) {
+              tma_load_2d(st, &tmA0, full_bar(s), k0, m0);
+#pragma unroll
+              for (int j = 0; j < Cf::BN / 64; ++j)
+                tma_load_2d(st + Cf::A_BYTES + j * Cf::B_BOX_BYTES, &tmB0, full_bar(s), n0 + 64 * j,
+                            k0);
+            } else {
+              tma_load_2d(st, &tmA0, full_bar(s), k0, m0);
+              tma_load_2d(st + Cf::A_BYTES, &tmA1, full_bar(s), k0, m0);
+              tma_load_2d(st + 2 * Cf::A_BYTES, &tmB0, full_bar(s), k0, n0);
+              tma_load_2d(st + 2 * Cf::A_BYTES + Cf::B_BYTES, &tmB1, full_bar(s), k0, n0);
+            }
+            inflight |= 1u << s;
+          } else {
+            inflight &= ~(1u << s);
+          }
+        }
+      }
+      // Drain: every TMA this CTA issued must have landed before it exits.
+      for (uint32_t s = 0; s < static_cast<uint32_t>(Cf::STAGES) && s < it; ++s) {
+        if (!(inflight & (1u << s))) continue;
+        const uint32_t last = it - 1 - ((it - 1 - s) % Cf::STAGES);  // latest fill of stage s
+        volatile int never = 0;
+        if (!mbar_wait_bounded(full_bar(s), (last / Cf::STAGES) & 1u, limit, &never))
+          atomicOr(p.status, kErrTimeoutDrain);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    // One thread waits and issues every MMA.
+    if (lane == 0) {
+      uint32_t it = 0, tcount = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++tcount) {
+        const uint32_t buf = tcount & 1u, aph = (tcount >> 1) & 1u;
+        if (!mbar_wait_bounded(acce_bar(buf), aph ^ 1u, limit, abort_flag)) {
+          give_up_one(p, abort_flag, kErrTimeoutMma);
+          break;
+        }
+        tc_fence_after();  // the epilogue's TMEM reads precede these MMAs' writes
+        const uint32_t d_tmem = tmem_base + buf * Cf::BN;
+        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+          const uint32_t s = it % Cf::STAGES, ph = (it / Cf::STAGES) & 1u;
+          if (!mbar_wait_bounded(full_bar(s), ph, limit, abort_flag)) {
+            give_up_one(p, abort_flag, kErrTimeoutMma);
+            ok = false;
+            break;
+          }
+          const uint32_t st = sbase + s * Cf::STAGE_BYTES;
+          if constexpr (KIND == KIND_BF16) {
+            // A: 128 rows x 128 B, K-major, 8-row groups 1024 B apart.
+            // B: four 64-column boxes (8 KB apart) of 64 k-rows x 128 B,
+            //    MN-major: LBO = next 64 columns, SBO = next 8 k-rows.
+#pragma unroll
+            for (int kk = 0; kk < Cf::BK / Cf::INSTR_K; ++kk) {
+              const uint64_t ad = smem_desc_sw128(st + kk * 32, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(st + Cf::A_BYTES + kk * 2048, Cf::B_BOX_BYTES, 1024);
+              mma_f16(d_tmem, ad, bd, Cf::IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+            }
+          } else {
+            // All four operands K-major, 128 B rows (32 floats), 8-row groups
+            // 1024 B apart; one instruction-K step (8 tf32) = 32 B.
+            const uint32_t a_big = st, a_small = st + Cf::A_BYTES;
+            const uint32_t b_big = st + 2 * Cf::A_BYTES, b_small = b_big + Cf::B_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < Cf::BK / Cf::INSTR_K; ++kk) {
+              const uint32_t off = kk * 32;
+              const uint64_t abd = smem_desc_sw128(a_big + off, 16, 1024);
+              const uint64_t asd = smem_desc_sw128(a_small + off, 16, 1024);
+              const uint64_t bbd = smem_desc_sw128(b_big + off, 16, 1024);
+              const uint64_t bsd = smem_desc_sw128(b_small + off, 16, 1024);
+              mma_tf32(d_tmem, asd, bbd, Cf::IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+              mma_tf32(d_tmem, abd, bsd, Cf::IDESC, 1u);
+              mma_tf32(d_tmem, abd, bbd, Cf::IDESC, 1u);
+            }
+          }
+          mma_commit(empty_bar(s));  // stage s may be refilled once these MMAs finish
+        }
+        if (!ok) break;
+        mma_commit(accf_bar(buf));  // accumulator `buf` complete
+      }
+      // Drain: all MMAs issued by this thread complete before TMEM is freed.
+      mma_commit(drain_bar);
+      volatile int never = 0;
+      if (!mbar_wait_bounded(drain_bar, 0, limit, &never)) atomicOr(p.status, kErrTimeoutDrain);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;           // TMEM lane quarter this warp may access
+    const int ew = warp - 2;          // epilogue warp index 0..3
+    uint32_t tcount = 0, chunk = 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++tcount) {
+      const uint32_t buf = tcount & 1u, aph = (tcount >> 1) & 1u;
+      if (!warp_wait(accf_bar(buf), aph, limit, abort_flag, 128)) {
+        give_up(p, abort_flag, kErrTimeoutEpilogue, lane);
+        break;
+      }
+      tc_fence_after();
+      int tm, tn;
+      tile_coords(t, p, tm, tn);
+      const int m0 = tm * Cf::BM, n0 = tn * Cf::BN;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * Cf::BN;
+#pragma unroll 1
+      for (int c = 0; c < Cf::BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32cols(taddr + c * 32, r);
+        tmem_ld_wait();
+        stage_and_store_chunk<TMA_STORE>(r, sbase + L::EPI_OFF, ew, chunk, lane, &tmC, p,
+                                         m0 + q * 32, n0 + c * 32, false);
+        ++chunk;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce_bar(buf));  // TMEM buffer `buf` may be overwritten
+    }
+    if constexpr (TMA_STORE) {
+      if (lane == 0) bulk_wait_group<0>();
+      __syncwarp();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cf::TMEM_COLS);
+  }
+}
+
+template <int KIND, bool TMA_STORE>
+cudaError_t prepare_kernel() {
+  // cudaFuncSetAttribute is per device; callers run it on every launch (cheap).
+  return cudaFuncSetAttribute(tc_gemm_kernel<KIND, TMA_STORE>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<KIND>::ALLOC);
+}
+
+template <int KIND>
+cudaError_t launch_t(const TcMaps& mp, float* C, int64_t M, int64_t N, int64_t K, int64_t ldc,
+                     bool c_tma, const DeviceCtl& ctl, cudaStream_t s) {
+  using Cf = Cfg<KIND>;
+  const TcParams p = make_params(M, N, K, Cf::BM, Cf::BN, Cf::BK, C, ldc, ctl);
+  const int grid = p.num_tiles < ctl.sm_count ? p.num_tiles : ctl.sm_count;
+  note_main_kernel(KIND == KIND_BF16 ? "tc_gemm_kernel<bf16>" : "tc_gemm_kernel<3xtf32>", grid,
+                   p.num_tiles);
+  cudaError_t e;
+  if (c_tma) {
+    if ((e = prepare_kernel<KIND, true>()) != cudaSuccess) return e;
+    tc_gemm_kernel<KIND, true><<<grid, NUM_THREADS, Layout<KIND>::ALLOC, s>>>(mp.a0, mp.a1, mp.b0,
+                                                                               mp.b1, mp.c, p);
+  } else {
+    if ((e = prepare_kernel<KIND, false>()) != cudaSuccess) return e;
+    tc_gemm_kernel<KIND, false><<<grid, NUM_THREADS, Layout<KIND>::ALLOC, s>>>(mp.a0, mp.a1, mp.b0,
+                                                                                mp.b1, mp.c, p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_single_cta(int kind, const TcMaps& maps, float* C, int64_t M, int64_t N,
+                              int64_t K, int64_t ldc, bool c_tma, const DeviceCtl& ctl,
+                              cudaStream_t s) {
+  return kind == KIND_BF16 ? launch_t<KIND_BF16>(maps, C, M, N, K, ldc, c_tma, ctl, s)
+                           : launch_t<KIND_3XTF32>(maps, C, M, N, K, ldc, c_tma, ctl, s);
+}
+
+}  // namespace tc
+}  // namespace mhr

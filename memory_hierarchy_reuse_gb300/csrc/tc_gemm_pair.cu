@@ -1,0 +1,402 @@
+// CTA-pair tensor-core GEMM kernel (tcgen05.mma.cta_group::2): two CTAs on
+// two SMs share one 256 x 256 output tile; persistent over tiles, with the
+// sparse last round split along K.  Used for large problems.  The method and
+// the warp roles are described in tc_common.cuh.
+#include "tc_common.cuh"
+
+namespace mhr {
+namespace tc {
+namespace {
+
+// ------------------------------------------------------------------ CTA pairs
+//
+// The same method one level up: two CTAs on two SMs (a cluster of 2) share
+// one 256 x BN output tile.  Each CTA stages its own 128 rows of A and its own
+// half of B's columns; one tcgen05.mma.cta_group::2 instruction (M = 256)
+// reads both CTAs' shared memory and writes each CTA's 128 accumulator rows
+// into that CTA's TMEM.  Every staged B element now feeds 256 output rows
+// instead of 128, so each SM reads half as many B bytes from shared memory
+// per FLOP -- the shared-memory bandwidth that binds the 1-CTA kernel.
+//
+// Synchronisation across the pair:
+//   full[s]      (rank 0 only) both CTAs' TMA bytes complete on it; rank 0's
+//                producer arms it for the pair's bytes
+//   empty[s]     (both) rank 0's MMA thread commits to both CTAs' copy
+//   acc_full[b]  (both) likewise, when accumulator b is complete
+//   acc_empty[b] (rank 0 only) all 8 epilogue warps of the pair arrive
+// On a timeout, the role that gave up raises the abort flag in both CTAs.
+
+template <int KIND>
+struct PairCfg;
+
+#ifndef MHR_PAIR_BF16_BK
+#define MHR_PAIR_BF16_BK 64
+#endif
+template <>
+struct PairCfg<KIND_BF16> {
+  static constexpr int BM = 128;                            // rows per CTA (pair: 256)
+  static constexpr int BN = 256, BN_HALF = 128, BK = MHR_PAIR_BF16_BK;
+  static constexpr int STAGES = BK == 64 ? 6 : 3;
+  static constexpr int A_BOX_BYTES = BM * 64 * 2;           // 128 rows x 64 k = 16 KB
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BOX_BYTES = 64 * BK * 2;           // 64 columns x BK k-rows
+  static constexpr int B_BYTES = BN_HALF * BK * 2;          // this CTA's half
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;     // 32 or 64 KB per CTA
+  static constexpr int INSTR_K = 16;
+  static constexpr uint32_t IDESC = make_idesc(1, false, true, 2 * BM, BN);
+  static constexpr uint32_t TMEM_COLS = 2 * BN;             // 512
+};
+
+template <>
+struct PairCfg<KIND_3XTF32> {
+  static constexpr int BM = 128;
+  static constexpr int BN = 256, BN_HALF = 128, BK = 32, STAGES = 3;
+  static constexpr int A_BYTES = BM * BK * 4;               // 16 KB each (big, small)
+  static constexpr int B_BYTES = BN_HALF * BK * 4;          // 16 KB each (big, small)
+  static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;  // 64 KB per CTA
+  static constexpr int INSTR_K = 8;
+  static constexpr uint32_t IDESC = make_idesc(2, false, false, 2 * BM, BN);
+  static constexpr uint32_t TMEM_COLS = 2 * BN;             // 512
+};
+
+template <int KIND>
+struct PairLayout {
+  using C = PairCfg<KIND>;
+  static constexpr int EPI_OFF = C::STAGES * C::STAGE_BYTES;
+  static constexpr int BAR_OFF = EPI_OFF + EPI_BYTES;
+  static constexpr int NUM_BARS = 2 * C::STAGES + 5;
+  static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
+  static constexpr int USED = MISC_OFF + 16;
+  static constexpr int ALLOC = USED + 1024;
+};
+
+// Pause for `ns` nanoseconds (bounded).
+__device__ __forceinline__ void pause_ns(uint64_t ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (global_timer_ns() - t0 < ns) {
+  }
+}
+
+template <int KIND, bool TMA_STORE>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA0,
+                        const __grid_constant__ CUtensorMap tmA1,
+                        const __grid_constant__ CUtensorMap tmB0,
+                        const __grid_constant__ CUtensorMap tmB1,
+                        const __grid_constant__ CUtensorMap tmC, const TcParams p) {
+  using Cf = PairCfg<KIND>;
+  using L = PairLayout<KIND>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + L::BAR_OFF;
+  auto full_bar = [&](uint32_t s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (Cf::STAGES + s); };
+  auto accf_bar = [&](uint32_t b) { return bar0 + 8u * (2 * Cf::STAGES + b); };
+  auto acce_bar = [&](uint32_t b) { return bar0 + 8u * (2 * Cf::STAGES + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * Cf::STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int cluster = blockIdx.x >> 1, num_clusters = gridDim.x >> 1;
+  const uint32_t peer_abort = mapa_shared(smem_u32(const_cast<int*>(abort_flag)), rank ^ 1u);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Cf::STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf_bar(b), 1);
+      mbar_init(acce_bar(b), 2 * EPI_WARPS);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA0);
+    tma_prefetch_desc(&tmB0);
+    if constexpr (KIND == KIND_3XTF32) {
+      tma_prefetch_desc(&tmA1);
+      tma_prefetch_desc(&tmB1);
+    }
+    if (TMA_STORE) tma_prefetch_desc(&tmC);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), Cf::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync_all();  // both CTAs' barriers initialised, TMEM allocated in both
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint64_t limit = p.wait_limit_ns;
+
+  // Give up: record why (first role only), raise the abort flag in both CTAs.
+  auto give_up_one = [&](uint32_t bit) {  // called by a single thread
+    if (!*abort_flag) atomicOr(p.status, bit);
+    *abort_flag = 1;
+    st_shared_cluster_u32(peer_abort, 1u);
+  };
+  auto give_up_pair = [&](uint32_t bit) {  // called by a whole warp
+    if (lane == 0) give_up_one(bit);
+    __syncwarp();
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producers (both CTAs)
+    // One thread waits, arms and issues; the rest of the warp idles.
+    if (lane == 0) {
+      uint32_t it = 0, inflight = 0;
+      bool ok = true;
+      for (int u = cluster; ok && u < p.num_units; u += num_clusters) {
+        const Unit w = unit_of(u, p);
+        int tm, tn;
+        tile_coords(w.tile, p, tm, tn);
+        const int m0 = tm * 2 * Cf::BM + static_cast<int>(rank) * Cf::BM;
+        const int nb0 = tn * Cf::BN + static_cast<int>(rank) * Cf::BN_HALF;
+        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+          const uint32_t s = it % Cf::STAGES, ph = (it / Cf::STAGES) & 1u;
+          if (!mbar_wait_bounded(empty_bar(s), ph ^ 1u, limit, abort_flag)) {
+            give_up_one(kErrTimeoutProducer);
+            ok = false;
+            break;
+          }
+          const uint32_t st = sbase + s * Cf::STAGE_BYTES;
+          const uint32_t fb = mapa_shared(full_bar(s), 0);  // rank 0's full[s]
+          const int k0 = kb * Cf::BK;
+          if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * Cf::STAGE_BYTES);
+          const bool stall = p.inject_stall && blockIdx.x == 0 && it == 0;
+          if (!stall) {
+            if constexpr (KIND == KIND_BF16) {
+#pragma unroll
+              for (int i = 0; i < Cf::BK / 64; ++i)
+                tma_load_2d_pair(st + i * Cf::A_BOX_BYTES, &tmA0, fb, k0 + 64 * i, m0);
+#pragma unroll
+              for (int j = 0; j < Cf::BN_HALF / 64; ++j)
+#pragma unroll
+                for (int i = 0; i < Cf::BK / 64; ++i)  // 64 k-rows per box, stacked
+                  tma_load_2d_pair(st + Cf::A_BYTES + j * Cf::B_BOX_BYTES + i * 8192, &tmB0, fb,
+                                   nb0 + 64 * j, k0 + 64 * i);
+            } else {
+              tma_load_2d_pair(st, &tmA0, fb, k0, m0);
+              tma_load_2d_pair(st + Cf::A_BYTES, &tmA1, fb, k0, m0);
+              tma_load_2d_pair(st + 2 * Cf::A_BYTES, &tmB0, fb, k0, nb0);
+              tma_load_2d_pair(st + 2 * Cf::A_BYTES + Cf::B_BYTES, &tmB1, fb, k0, nb0);
+            }
+            inflight |= 1u << s;
+          } else {
+            inflight &= ~(1u << s);
+          }
+        }
+      }
+      if (leader) {
+        // Rank 0 can see its full barriers: wait for every fill it armed and loaded.
+        for (uint32_t s = 0; s < static_cast<uint32_t>(Cf::STAGES) && s < it; ++s) {
+          if (!(inflight & (1u << s))) continue;
+          const uint32_t last = it - 1 - ((it - 1 - s) % Cf::STAGES);
+          volatile int never = 0;
+          if (!mbar_wait_bounded(full_bar(s), (last / Cf::STAGES) & 1u, limit, &never))
+            atomicOr(p.status, kErrTimeoutDrain);
+        }
+      }
+      // After an abort, the loads this CTA issued signal rank 0's barriers,
+      // which rank 1 cannot poll: give them time to land (a TMA load takes
+      // microseconds) before the CTA may leave.
+      if (*abort_flag) pause_ns(100000);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (rank 0)
+    // One thread of rank 0 waits and issues every MMA of the pair.
+    if (leader && lane == 0) {
+      uint32_t it = 0, tcount = 0;
+      bool ok = true;
+      for (int u = cluster; ok && u < p.num_units; u += num_clusters, ++tcount) {
+        const Unit w = unit_of(u, p);
+        const uint32_t buf = tcount & 1u, aph = (tcount >> 1) & 1u;
+        if (!mbar_wait_bounded(acce_bar(buf), aph ^ 1u, limit, abort_flag)) {
+          give_up_one(kErrTimeoutMma);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * Cf::BN;
+        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+          const uint32_t s = it % Cf::STAGES, ph = (it / Cf::STAGES) & 1u;
+          if (!mbar_wait_bounded(full_bar(s), ph, limit, abort_flag)) {
+            give_up_one(kErrTimeoutMma);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = sbase + s * Cf::STAGE_BYTES;
+          if constexpr (KIND == KIND_BF16) {
+            // A: 128 rows x 128 B per CTA, K-major.  B: this CTA's two
+            // 64-column boxes (8 KB apart), MN-major.
+#pragma unroll
+            for (int kk = 0; kk < Cf::BK / Cf::INSTR_K; ++kk) {
+              const uint64_t ad =
+                  smem_desc_sw128(st + (kk / 4) * Cf::A_BOX_BYTES + (kk % 4) * 32, 16, 1024);
+              const uint64_t bd =
+                  smem_desc_sw128(st + Cf::A_BYTES + kk * 2048, Cf::B_BOX_BYTES, 1024);
+              mma_f16_pair(d_tmem, ad, bd, Cf::IDESC, (kb > w.kb0 || kk > 0) ? 1u : 0u);
+            }
+          } else {
+            const uint32_t a_big = st, a_small = st + Cf::A_BYTES;
+            const uint32_t b_big = st + 2 * Cf::A_BYTES, b_small = b_big + Cf::B_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < Cf::BK / Cf::INSTR_K; ++kk) {
+              const uint32_t off = kk * 32;
+              const uint64_t abd = smem_desc_sw128(a_big + off, 16, 1024);
+              const uint64_t asd = smem_desc_sw128(a_small + off, 16, 1024);
+              const uint64_t bbd = smem_desc_sw128(b_big + off, 16, 1024);
+              const uint64_t bsd = smem_desc_sw128(b_small + off, 16, 1024);
+              mma_tf32_pair(d_tmem, asd, bbd, Cf::IDESC, (kb > w.kb0 || kk > 0) ? 1u : 0u);
+              mma_tf32_pair(d_tmem, abd, bsd, Cf::IDESC, 1u);
+              mma_tf32_pair(d_tmem, abd, bbd, Cf::IDESC, 1u);
+            }
+          }
+          mma_commit_pair_multicast(empty_bar(s), 0x3);  // stage s free in both CTAs
+        }
+        if (!ok) break;
+        mma_commit_pair_multicast(accf_bar(buf), 0x3);  // accumulator `buf` complete
+      }
+      mma_commit_pair(drain_bar);
+      volatile int never = 0;
+      if (!mbar_wait_bounded(drain_bar, 0, limit, &never)) atomicOr(p.status, kErrTimeoutDrain);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    const int ew = warp - 2;
+    uint32_t tcount = 0, chunk = 0;
+    for (int u = cluster; u < p.num_units; u += num_clusters, ++tcount) {
+      const Unit w = unit_of(u, p);
+      const uint32_t buf = tcount & 1u, aph = (tcount >> 1) & 1u;
+      // The accumulator takes a whole tile's main loop to fill: back off
+      // between polls instead of spinning at full issue rate.
+      if (!warp_wait(accf_bar(buf), aph, limit, abort_flag, 128)) {
+        give_up_pair(kErrTimeoutEpilogue);
+        break;
+      }
+      tc_fence_after();
+      int tm, tn;
+      tile_coords(w.tile, p, tm, tn);
+      const int m0 = tm * 2 * Cf::BM + static_cast<int>(rank) * Cf::BM;
+      const int n0 = tn * Cf::BN;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * Cf::BN;
+#pragma unroll 1
+      for (int c = 0; c < Cf::BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32cols(taddr + c * 32, r);
+        tmem_ld_wait();
+        stage_and_store_chunk<TMA_STORE>(r, sbase + L::EPI_OFF, ew, chunk, lane, &tmC, p,
+                                         m0 + q * 32, n0 + c * 32, w.reduce);
+        ++chunk;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(buf), 0));
+    }
+    if constexpr (TMA_STORE) {
+      if (lane == 0) bulk_wait_group<0>();
+      __syncwarp();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // neither CTA leaves while the pair's MMAs or arrivals may touch it
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, Cf::TMEM_COLS);
+  }
+}
+
+// Zero the C tiles of the split work units (pair tiles [full_units,
+// num_tiles)), which both K halves then add into.  Block (x, y) clears rows
+// [8y, 8y + 8) of split tile x.
+__global__ void zero_split_tiles_kernel(TcParams p, int tile_cols) {
+  const int tile = p.full_units + blockIdx.x;
+  int tm, tn;
+  tile_coords(tile, p, tm, tn);
+  const int64_t row = static_cast<int64_t>(tm) * (8 * gridDim.y) + 8 * blockIdx.y + threadIdx.y;
+  if (row >= p.M) return;
+  const int64_t c0 = static_cast<int64_t>(tn) * tile_cols;
+  float* crow = p.C + row * p.ldc;
+  for (int c = threadIdx.x; c < tile_cols; c += blockDim.x)
+    if (c0 + c < p.N) crow[c0 + c] = 0.f;
+}
+
+// Pair kernel launch: clusters of 2 CTAs, persistent over 256 x BN pair
+// tiles, as many clusters as can be co-resident (at most one per pair tile).
+template <int KIND, bool TMA_STORE>
+cudaError_t launch_pair_t(const TcMaps& mp, const TcParams& p, const DeviceCtl& ctl,
+                          cudaStream_t s) {
+  auto kern = tc_gemm_pair_kernel<KIND, TMA_STORE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       PairLayout<KIND>::ALLOC);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = PairLayout<KIND>::ALLOC;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(2 * (ctl.sm_count / 2));
+  int max_clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
+  if (e != cudaSuccess) return e;
+  if (max_clusters < 1) return cudaErrorInvalidConfiguration;
+  const int clusters = p.num_tiles < max_clusters ? p.num_tiles : max_clusters;
+  // A last round that would leave more than half of the clusters idle is
+  // split along K: its tiles become two half-K units each, reduce-added into
+  // C (zeroed first).  Two addends onto zero give the same sum in either
+  // order, so results stay bit-reproducible.
+  TcParams q = p;
+  const int rem = p.num_tiles % clusters;
+  if (p.num_tiles > clusters && rem > 0 && 2 * rem <= clusters && p.num_kb >= 2) {
+    q.full_units = p.num_tiles - rem;
+    q.num_units = q.full_units + 2 * rem;
+    q.kb_mid = p.num_kb / 2;
+    zero_split_tiles_kernel<<<dim3(rem, 2 * PairCfg<KIND>::BM / 8), dim3(128, 8), 0, s>>>(
+        q, PairCfg<KIND>::BN);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  cfg.gridDim = dim3(2 * clusters);
+  note_main_kernel(KIND == KIND_BF16 ? "tc_gemm_pair_kernel<bf16>" : "tc_gemm_pair_kernel<3xtf32>",
+                   2 * clusters, p.num_tiles);
+  e = cudaLaunchKernelEx(&cfg, kern, mp.a0, mp.a1, mp.b0, mp.b1, mp.c, q);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_cta_pair(int kind, const TcMaps& maps, float* C, int64_t M, int64_t N,
+                            int64_t K, int64_t ldc, bool c_tma, const DeviceCtl& ctl,
+                            cudaStream_t s) {
+  if (kind == KIND_BF16) {
+    const TcParams p = make_params(M, N, K, PAIR_TILE_M, PAIR_TILE_N, PairCfg<KIND_BF16>::BK, C,
+                                   ldc, ctl);
+    return c_tma ? launch_pair_t<KIND_BF16, true>(maps, p, ctl, s)
+                 : launch_pair_t<KIND_BF16, false>(maps, p, ctl, s);
+  }
+  const TcParams p = make_params(M, N, K, PAIR_TILE_M, PAIR_TILE_N, PairCfg<KIND_3XTF32>::BK, C,
+                                 ldc, ctl);
+  return c_tma ? launch_pair_t<KIND_3XTF32, true>(maps, p, ctl, s)
+               : launch_pair_t<KIND_3XTF32, false>(maps, p, ctl, s);
+}
+
+}  // namespace tc
+}  // namespace mhr
