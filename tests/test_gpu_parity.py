@@ -32,7 +32,8 @@ def path(request, mhr):
 
 # (M, N, K): single elements, thin shapes, several tiles with ragged tails in
 # every dimension, and K long enough to wrap every ring several times
-# (bf16: 64-wide K steps x 4 or 6 stages; tf32: 32-wide x 3; SIMT: 8-wide x 2).
+# (bf16: 64-wide K steps x 4 stages, 1-CTA, or 128-wide x 3, pair; tf32: 32-wide x 3;
+# SIMT: 8-wide x 2).
 SMALL_SHAPES = [
     (1, 1, 1), (1, 300, 7), (7, 1, 300), (2, 3, 5), (127, 129, 65), (129, 257, 127),
     (256, 256, 256), (300, 520, 200), (255, 513, 1000), (130, 260, 769), (200, 200, 289),
