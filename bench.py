@@ -50,9 +50,6 @@ WORKLOADS = {
 }
 ENTRY = {"f32": "gemm_f32", "3xtf32": "gemm_f32_3xtf32", "bf16": "gemm_bf16_f32acc"}
 DTYPE = {"f32": "f32", "3xtf32": "tf32x3", "bf16": "bf16"}
-# our kernel launches per call (split A, split B^T, main; pack kernels only for
-# unaligned bf16 operands, never in these workloads)
-LAUNCHES = {"f32": 1, "3xtf32": 3, "bf16": 1}
 TF32_OVER_BF16 = 1.1 / 2.25   # nominal dense tensor rates (PFLOP/s) of GB300
 # Dense tensor-core rate of one Blackwell SM per clock: 2.25 PFLOP/s bf16 over
 # 152 SMs is 8192 FLOP/clk at ~1.8 GHz; tf32 runs at half the bf16 rate.
@@ -73,10 +70,10 @@ def peaks():
 
 
 KERNEL_SOURCES = {  # the files whose text determines each kernel
-    "tc_gemm_pair_kernel": ["tc_gemm_pair.cu", "tc_common.cuh", "mhr_device.cuh"],
+    "tc_gemm_pair_kernel": ["tc_gemm_pair.cu", "tc_common.cuh", "mhr_device.cuh", "tf32_split.cuh"],
     "tc_gemm_kernel": ["tc_gemm_1cta.cu", "tc_common.cuh", "mhr_device.cuh"],
     "simt_f32_kernel": ["simt_f32.cu"],
-    "split_vec_kernel": ["tc_prepass.cu"],
+    "split_vec_kernel": ["tc_prepass.cu", "tf32_split.cuh"],
 }
 
 
@@ -473,6 +470,9 @@ def main():
     if rc != mhr.MHR_OK:
         raise mhr.GemmError(rc, "warm-up")
     main_kernel = lib.gemm_testing_last_main_kernel().decode()
+    # our kernels per call, as counted by the library (pre-passes, zero fills
+    # of split tiles, the main kernel)
+    launches_per_call = lib.gemm_testing_last_launches()
 
     # ---------------------------------------------------------------- timed
     time.sleep(0.5)  # let the clock sampler start
@@ -664,7 +664,7 @@ def main():
                     "note": "per step: pinned host A, B -> device, C API call, C -> pinned host; "
                             "value pipelines consecutive steps over three streams, serial_value "
                             "runs them one after another on one stream"},
-            "gpu_launches": LAUNCHES[path] * args.steps,
+            "gpu_launches": launches_per_call * args.steps,
             "clocks": clocks,
             "paths": extra,
             "source_digest": source_digest(),

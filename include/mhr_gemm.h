@@ -33,10 +33,12 @@
  * (a bounded wait that ran out) is recorded in a per-device status word that
  * gemm_check() reads.
  *
- * Scratch: gemm_f32_3xtf32 (always) and gemm_bf16_f32acc (only when an
+ * Scratch: gemm_f32_3xtf32 (normally) and gemm_bf16_f32acc (only when an
  * operand's address or leading dimension is not 16-byte aligned) need a
  * device workspace.  The library owns it: one buffer per (device, stream),
- * grown with cudaMalloc on demand and kept until gemm_release().
+ * grown with cudaMalloc on demand and kept until gemm_release().  When the
+ * 3xTF32 workspace cannot be allocated, gemm_f32_3xtf32 splits its operands
+ * inside the kernel instead (same result bit for bit, slower, no workspace).
  *
  * Errors: every entry point returns an int status (mhr_status below); none
  * throws, none traps on the device.  Thread safety: calls from several host
@@ -79,8 +81,12 @@ int gemm_f32(const float* A, const float* B, float* C, int64_t M, int64_t N, int
  * nearest even), and C accumulates small*big + big*small + big*big with
  * tcgen05.mma kind::tf32 into a TMEM accumulator (the small*small term is
  * dropped).  A split pre-pass writes the four tf32 operands into the
- * library's workspace (B transposed to K-major), then a TMA + mbarrier ring
- * feeds the tensor cores.  Any alignment and leading dimension are accepted.
+ * library's workspace (B transposed to K-major, 8 (M + N) K bytes in all),
+ * then a TMA + mbarrier ring feeds the tensor cores.  If that workspace cannot
+ * be allocated, converter warps of the CTA-pair kernel load A and B directly
+ * and split them on chip instead: the same MMAs in the same order, so the
+ * same C bit for bit, at about 60 % of the speed on GB300.  Any alignment and
+ * leading dimension are accepted.
  */
 int gemm_f32_3xtf32(const float* A, const float* B, float* C, int64_t M, int64_t N,
                     int64_t K, int64_t lda, int64_t ldb, int64_t ldc, void* stream);

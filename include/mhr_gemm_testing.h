@@ -48,12 +48,36 @@ int64_t gemm_testing_peek_status(void* stream);
 int gemm_testing_set_cta_pair_mode(int mode);
 
 /*
+ * Chooses where gemm_f32_3xtf32 splits its operands into tf32 big and small
+ * parts (process-wide): 0 = automatic (a pre-pass into the workspace, or
+ * inside the CTA-pair kernel when the workspace cannot be allocated), 1 =
+ * always a pre-pass, 2 = always inside the CTA-pair kernel (which is then
+ * used whatever the CTA-pair mode says).  Other values mean 0.  Both give
+ * bit-identical results for the same kernel.  Returns the previous mode.
+ */
+int gemm_testing_set_split_mode(int mode);
+
+/*
+ * Caps the bytes the library's workspace may grow to (process-wide), so that
+ * a larger request fails as an allocation failure would.  UINT64_MAX (the
+ * initial value) removes the cap.  Returns the previous cap.
+ */
+uint64_t gemm_testing_set_workspace_limit(uint64_t bytes);
+
+/*
  * Tuning hook: the number of tile rows per raster group of the tensor-core
  * kernels' tile schedule (consecutive work units sweep that many tile rows
  * column by column, so co-resident CTAs share A and B panels in L2).  0
  * restores the default (16).  Returns the previous setting.
  */
 int gemm_testing_set_raster_group(int tile_rows);
+
+/*
+ * Number of kernels the most recent gemm_* call launched: its pre-passes
+ * (split, repack, zero fills) and its main kernel.  Meaningful when calls do
+ * not overlap in time from several host threads.
+ */
+int gemm_testing_last_launches(void);
 
 /*
  * Name, grid size and tile count of the main kernel that the most recent

@@ -46,7 +46,8 @@ EXPORTS = ("gemm_f32", "gemm_f32_3xtf32", "gemm_bf16_f32acc", "gemm_f32_3xtf32_n
            "gemm_testing_set_wait_limit_ns", "gemm_testing_set_inject_stall",
            "gemm_testing_peek_status", "gemm_testing_set_main_kernel_events",
            "gemm_testing_set_cta_pair_mode", "gemm_testing_last_main_kernel",
-           "gemm_testing_set_raster_group")
+           "gemm_testing_set_raster_group", "gemm_testing_set_split_mode",
+           "gemm_testing_last_launches", "gemm_testing_set_workspace_limit")
 
 _lib = None
 
@@ -95,6 +96,12 @@ def load(path: str | None = None):
     lib.gemm_testing_last_main_kernel.restype = ctypes.c_char_p
     lib.gemm_testing_set_cta_pair_mode.argtypes = [ctypes.c_int]
     lib.gemm_testing_set_cta_pair_mode.restype = ctypes.c_int
+    lib.gemm_testing_set_split_mode.argtypes = [ctypes.c_int]
+    lib.gemm_testing_set_split_mode.restype = ctypes.c_int
+    lib.gemm_testing_set_workspace_limit.argtypes = [ctypes.c_uint64]
+    lib.gemm_testing_set_workspace_limit.restype = ctypes.c_uint64
+    lib.gemm_testing_last_launches.argtypes = []
+    lib.gemm_testing_last_launches.restype = ctypes.c_int
     lib.gemm_testing_set_main_kernel_events.argtypes = [vp, vp]
     lib.gemm_testing_set_main_kernel_events.restype = None
     _lib = lib
@@ -163,6 +170,22 @@ def gemm_testing_last_main_kernel() -> str:
 def gemm_testing_set_cta_pair_mode(mode: int) -> int:
     """0 = automatic, 1 = single-CTA tensor-core kernel, 2 = CTA-pair kernel."""
     return load().gemm_testing_set_cta_pair_mode(int(mode))
+
+
+def gemm_testing_last_launches() -> int:
+    """Kernels launched by the most recent gemm_* call."""
+    return load().gemm_testing_last_launches()
+
+
+def gemm_testing_set_workspace_limit(nbytes: int) -> int:
+    """Cap the workspace (2**64 - 1 = no cap); a larger request fails like an allocation."""
+    return load().gemm_testing_set_workspace_limit(int(nbytes))
+
+
+def gemm_testing_set_split_mode(mode: int) -> int:
+    """3xTF32 split: 0 = automatic (pre-pass; on chip without workspace), 1 = pre-pass,
+    2 = inside the CTA-pair kernel."""
+    return load().gemm_testing_set_split_mode(int(mode))
 
 
 def gemm_testing_set_main_kernel_events(start=None, stop=None) -> None:

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <climits>
 #include <cstdint>
 #include <cstdio>
@@ -45,6 +46,8 @@ uint64_t g_wait_limit_ns = 2000000000ull;
 int g_inject_stall = 0;
 int g_pair_mode = 0;
 int g_raster_group = 0;
+int g_split_mode = 0;
+uint64_t g_workspace_limit = UINT64_MAX;
 cudaEvent_t g_main_start = nullptr, g_main_stop = nullptr;
 
 // Brackets the main kernel launch with the caller's profiling events, if set.
@@ -145,6 +148,9 @@ int validate(const void* A, const void* B, const void* C, int64_t M, int64_t N, 
 // buffer first (cudaFree waits for the device), so earlier calls on the same
 // stream that still read it have finished.
 int workspace(int dev, cudaStream_t s, size_t bytes, void** out) {
+  constexpr size_t kGrain = size_t{2} << 20;
+  if (bytes > SIZE_MAX - kGrain) return MHR_ERR_CUDA;  // no such allocation exists
+  if (bytes > g_workspace_limit) return MHR_ERR_CUDA;  // test hook: as if cudaMalloc failed
   Workspace& w = g_workspaces[{dev, s}];
   if (w.bytes < bytes) {
     if (w.ptr) {
@@ -152,7 +158,7 @@ int workspace(int dev, cudaStream_t s, size_t bytes, void** out) {
       w.ptr = nullptr;
       w.bytes = 0;
     }
-    const size_t rounded = (bytes + (size_t{2} << 20) - 1) & ~((size_t{2} << 20) - 1);
+    const size_t rounded = (bytes + kGrain - 1) & ~(kGrain - 1);
     if (cudaMalloc(&w.ptr, rounded) != cudaSuccess) {
       cudaGetLastError();
       w.ptr = nullptr;
@@ -172,6 +178,7 @@ DeviceCtl make_ctl(const DeviceState& st) {
   c.sm_count = st.sm_count;
   c.pair_mode = g_pair_mode;
   c.raster_group = g_raster_group;
+  c.split_mode = g_split_mode;
   return c;
 }
 
@@ -203,9 +210,15 @@ CUresult encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void*
 namespace {
 char g_last_kernel[160] = "none";
 std::mutex g_last_kernel_mu;
+std::atomic<int> g_call_launches{0};
 }  // namespace
 
+void begin_call() { g_call_launches.store(0); }
+
+void note_launch() { g_call_launches.fetch_add(1); }
+
 void note_main_kernel(const char* name, int grid, int tiles) {
+  note_launch();
   std::lock_guard<std::mutex> g(g_last_kernel_mu);
   snprintf(g_last_kernel, sizeof(g_last_kernel), "%s grid=%d tiles=%d", name, grid, tiles);
 }
@@ -234,6 +247,7 @@ MHR_API int gemm_f32(const float* A, const float* B, float* C, int64_t M, int64_
   bool noop;
   int rc = validate(A, B, C, M, N, K, lda, ldb, ldc, 4, &noop);
   if (rc != MHR_OK || noop) return rc;
+  begin_call();
   std::lock_guard<std::mutex> g(g_mu);
   DeviceState* st;
   if ((rc = device_state(&st, nullptr)) != MHR_OK) return rc;
@@ -250,6 +264,7 @@ MHR_API int gemm_f32_ladder(int rung, const float* A, const float* B, float* C, 
   bool noop;
   int rc = validate(A, B, C, M, N, K, lda, ldb, ldc, 4, &noop);
   if (rc != MHR_OK || noop) return rc;
+  begin_call();
   const int64_t T = rung == 2 ? 32 : 16;
   if ((M + T - 1) / T > 65535) return MHR_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> g(g_mu);
@@ -266,27 +281,43 @@ MHR_API int gemm_f32_3xtf32(const float* A, const float* B, float* C, int64_t M,
   bool noop;
   int rc = validate(A, B, C, M, N, K, lda, ldb, ldc, 4, &noop);
   if (rc != MHR_OK || noop) return rc;
+  begin_call();
   std::lock_guard<std::mutex> g(g_mu);
   DeviceState* st;
   int dev;
   if ((rc = device_state(&st, &dev)) != MHR_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (K == 0) return from_cuda(launch_zero_fill(C, M, N, ldc, s));
-  // Split operands: a_big, a_small (M x Kp), bt_big, bt_small (N x Kp).
+  const bool c_tma = aligned16(C) && (ldc % 4) == 0;
+  const DeviceCtl ctl = make_ctl(*st);
+  // Split operands: a_big, a_small (M x Kp), bt_big, bt_small (N x Kp), in
+  // the workspace.  Without one (split mode 2, or no memory for it) the
+  // CTA-pair kernel splits on chip.
   const int64_t Kp = round_up(K, 4);
-  const size_t a_bytes = static_cast<size_t>(M) * Kp * 4, b_bytes = static_cast<size_t>(N) * Kp * 4;
-  void* ws;
-  if ((rc = workspace(dev, s, 2 * (a_bytes + b_bytes), &ws)) != MHR_OK) return rc;
+  size_t a_bytes, b_bytes, ws_bytes;
+  const bool fits = !__builtin_mul_overflow(static_cast<size_t>(M), static_cast<size_t>(Kp) * 4,
+                                            &a_bytes) &&
+                    !__builtin_mul_overflow(static_cast<size_t>(N), static_cast<size_t>(Kp) * 4,
+                                            &b_bytes) &&
+                    !__builtin_add_overflow(a_bytes, b_bytes, &ws_bytes) &&
+                    !__builtin_mul_overflow(ws_bytes, size_t{2}, &ws_bytes);
+  void* ws = nullptr;
+  if (ctl.split_mode == 2 ||
+      (ctl.split_mode == 0 && (!fits || workspace(dev, s, ws_bytes, &ws) != MHR_OK))) {
+    MainKernelEvents ev(s);
+    return from_cuda(launch_tc_3xtf32_split(A, B, C, M, N, K, lda, ldb, ldc, c_tma, ctl, s));
+  }
+  if (!fits) return MHR_ERR_CUDA;
+  if (!ws && (rc = workspace(dev, s, ws_bytes, &ws)) != MHR_OK) return rc;
   float* a_big = static_cast<float*>(ws);
   float* a_small = a_big + M * Kp;
   float* bt_big = a_small + M * Kp;
   float* bt_small = bt_big + N * Kp;
   cudaError_t e = launch_split_tf32(A, B, M, N, K, lda, ldb, Kp, a_big, a_small, bt_big, bt_small, s);
   if (e != cudaSuccess) return from_cuda(e);
-  const bool c_tma = aligned16(C) && (ldc % 4) == 0;
   MainKernelEvents ev(s);
   return from_cuda(launch_tc_3xtf32(a_big, a_small, bt_big, bt_small, C, M, N, K, Kp, ldc, c_tma,
-                                    make_ctl(*st), s));
+                                    ctl, s));
 }
 
 MHR_API int gemm_bf16_f32acc(const uint16_t* A, const uint16_t* B, float* C, int64_t M, int64_t N,
@@ -294,6 +325,7 @@ MHR_API int gemm_bf16_f32acc(const uint16_t* A, const uint16_t* B, float* C, int
   bool noop;
   int rc = validate(A, B, C, M, N, K, lda, ldb, ldc, 2, &noop);
   if (rc != MHR_OK || noop) return rc;
+  begin_call();
   std::lock_guard<std::mutex> g(g_mu);
   DeviceState* st;
   int dev;
@@ -307,8 +339,11 @@ MHR_API int gemm_bf16_f32acc(const uint16_t* A, const uint16_t* B, float* C, int
     const int64_t lda_p = round_up(K, 8), ldb_p = round_up(N, 8);
     const size_t a_bytes = a_ok ? 0 : static_cast<size_t>(M) * lda_p * 2;
     const size_t b_bytes = b_ok ? 0 : static_cast<size_t>(K) * ldb_p * 2;
+    size_t ws_bytes;  // each part is below 2^63 (validated extents); their sum may not be
+    if (__builtin_add_overflow(static_cast<size_t>(round_up(a_bytes, 256)), b_bytes, &ws_bytes))
+      return MHR_ERR_CUDA;
     void* ws;
-    if ((rc = workspace(dev, s, round_up(a_bytes, 256) + b_bytes, &ws)) != MHR_OK) return rc;
+    if ((rc = workspace(dev, s, ws_bytes, &ws)) != MHR_OK) return rc;
     uint16_t* pa = static_cast<uint16_t*>(ws);
     uint16_t* pb = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + round_up(a_bytes, 256));
     cudaError_t e;
@@ -404,6 +439,22 @@ MHR_API int gemm_testing_set_cta_pair_mode(int mode) {
   std::lock_guard<std::mutex> g(g_mu);
   const int old = g_pair_mode;
   g_pair_mode = (mode == 1 || mode == 2) ? mode : 0;
+  return old;
+}
+
+MHR_API int gemm_testing_last_launches(void) { return g_call_launches.load(); }
+
+MHR_API uint64_t gemm_testing_set_workspace_limit(uint64_t bytes) {
+  std::lock_guard<std::mutex> g(g_mu);
+  const uint64_t old = g_workspace_limit;
+  g_workspace_limit = bytes;
+  return old;
+}
+
+MHR_API int gemm_testing_set_split_mode(int mode) {
+  std::lock_guard<std::mutex> g(g_mu);
+  const int old = g_split_mode;
+  g_split_mode = (mode == 1 || mode == 2) ? mode : 0;
   return old;
 }
 

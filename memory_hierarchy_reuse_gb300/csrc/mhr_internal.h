@@ -17,6 +17,7 @@ struct DeviceCtl {
   int sm_count = 0;
   int pair_mode = 0;                   // 0 auto, 1 single-CTA kernel, 2 CTA-pair kernel (test hook)
   int raster_group = 0;                // tile rows per raster group, 0 = default (tuning hook)
+  int split_mode = 0;                  // 3xTF32: 0 auto, 1 split pre-pass, 2 in-kernel split (test hook)
 };
 
 cudaError_t launch_simt_f32(const float* A, const float* B, float* C, int64_t M, int64_t N,
@@ -54,14 +55,28 @@ cudaError_t launch_tc_3xtf32(const float* a_big, const float* a_small, const flo
                              int64_t Kp, int64_t ldc, bool c_tma, const DeviceCtl& ctl,
                              cudaStream_t s);
 
+// 3xTF32 with the split done inside the CTA-pair kernel: A (M x K, lda) and
+// B (K x N, ldb) row-major fp32, read directly; no workspace.
+cudaError_t launch_tc_3xtf32_split(const float* A, const float* B, float* C, int64_t M,
+                                   int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                                   bool c_tma, const DeviceCtl& ctl, cudaStream_t s);
+
+// Whether the tensor-core paths run the CTA-pair kernel for this shape (else
+// the single-CTA kernel).
+bool tc_pair_chosen(int64_t M, int64_t N, int64_t K, const DeviceCtl& ctl);
+
 // Tensor-map encoding through the driver entry point (no libcuda link).
 CUresult encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                         uint64_t inner, uint64_t outer, uint64_t row_pitch_bytes,
                         uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
 
 // Name of the main kernel the last tensor-core or SIMT launch used, with its
-// grid (for profiling labels; static storage).
+// grid (for profiling labels; static storage).  Also counts as a launch.
 void note_main_kernel(const char* name, int grid, int tiles);
+// Kernel-launch count of the current gemm_* call: reset by begin_call() at
+// the start of every entry point, incremented by each launcher.
+void begin_call();
+void note_launch();
 const char* last_main_kernel();
 
 // The C-ABI front end's argument checks (api.cu), for entry points defined in

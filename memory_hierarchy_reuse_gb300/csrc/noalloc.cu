@@ -78,6 +78,7 @@ MHR_API int gemm_f32_3xtf32_noalloc(const float* A, const float* B, float* C, in
   bool noop;
   int rc = check_gemm_args(A, B, C, M, N, K, lda, ldb, ldc, 4, &noop);
   if (rc != MHR_OK || noop) return rc;
+  begin_call();
   const int64_t Kp = (K + 3) / 4 * 4;
   // 8 * Kp * (M + N) bytes must fit; M, N, K are below 2^31, so no overflow.
   if (K > 0 && static_cast<uint64_t>(Kp) * static_cast<uint64_t>(M + N) * 8u > kScratchBytes)

@@ -30,12 +30,16 @@
 // The accumulator is double-buffered in TMEM so the epilogue of tile i runs
 // while the MMAs of tile i+1 are issued.
 //
-// Two kinds:
+// Three kinds:
 //   KIND_BF16:   A bf16 K-major (row-major M x K), B bf16 MN-major (row-major
 //                K x N), kind::f16.
 //   KIND_3XTF32: A_big, A_small K-major; B_big^T, B_small^T K-major (N x K),
 //                kind::tf32, three MMAs per instruction-K step (small*big,
-//                big*small, big*big).
+//                big*small, big*big).  The operands come from a split pre-pass.
+//   KIND_3XTF32_SPLIT (CTA-pair kernel only): the same MMAs, but the split is
+//                done in the kernel: converter warps load the fp32 operands
+//                from global memory, split them and write the four tf32 parts
+//                into the shared-memory ring in the layout TMA would produce.
 //
 // Every wait is bounded (DeviceCtl::wait_limit_ns).  A role that runs out of
 // time sets its bit in the device status word and an abort flag in shared
@@ -55,6 +59,7 @@ namespace tc {
 
 constexpr int KIND_BF16 = 0;
 constexpr int KIND_3XTF32 = 1;
+constexpr int KIND_3XTF32_SPLIT = 2;
 
 constexpr int EPI_WARPS = 4;
 constexpr int EPI_BUF_BYTES = 32 * 32 * 4;                 // 32 rows x 32 fp32
@@ -75,6 +80,12 @@ struct TcParams {
   uint32_t* status;
   uint64_t wait_limit_ns;
   int32_t inject_stall;
+  // KIND_3XTF32_SPLIT only: the fp32 operands, row-major, and whether A rows
+  // may be read with 16-byte loads (A 16-byte aligned, lda % 4 == 0).
+  const float* A;
+  const float* B;
+  int64_t lda, ldb;
+  int32_t vec_a;
 };
 
 // Grouped raster: consecutive work units sweep GROUP_M tile rows column by
@@ -217,6 +228,10 @@ inline TcParams make_params(int64_t M, int64_t N, int64_t K, int tile_m, int til
   p.status = ctl.status;
   p.wait_limit_ns = ctl.wait_limit_ns;
   p.inject_stall = ctl.inject_stall;
+  p.A = nullptr;
+  p.B = nullptr;
+  p.lda = p.ldb = 0;
+  p.vec_a = 0;
   return p;
 }
 
@@ -237,6 +252,12 @@ cudaError_t launch_single_cta(int kind, const TcMaps& maps, float* C, int64_t M,
 cudaError_t launch_cta_pair(int kind, const TcMaps& maps, float* C, int64_t M, int64_t N,
                             int64_t K, int64_t ldc, bool c_tma, const DeviceCtl& ctl,
                             cudaStream_t s);
+// The CTA-pair kernel with the 3xTF32 split done in the kernel (no workspace):
+// A (M x K, pitch lda) and B (K x N, pitch ldb) row-major fp32.
+cudaError_t launch_cta_pair_split(const float* A, const float* B, const CUtensorMap& c_map,
+                                  float* C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                                  int64_t ldb, int64_t ldc, bool c_tma, const DeviceCtl& ctl,
+                                  cudaStream_t s);
 
 }  // namespace tc
 }  // namespace mhr

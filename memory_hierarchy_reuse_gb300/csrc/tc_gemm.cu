@@ -4,6 +4,16 @@
 #include "tc_common.cuh"
 
 namespace mhr {
+
+bool tc_pair_chosen(int64_t M, int64_t N, int64_t K, const DeviceCtl& ctl) {
+  if (ctl.pair_mode == 1) return false;
+  if (ctl.pair_mode == 2) return true;
+  const int64_t pair_tiles = ((M + tc::PAIR_TILE_M - 1) / tc::PAIR_TILE_M) *
+                             ((N + tc::PAIR_TILE_N - 1) / tc::PAIR_TILE_N);
+  const int64_t clusters = ctl.sm_count / 2;
+  return 2 * pair_tiles >= clusters && (K >= 2048 || pair_tiles >= 2 * clusters);
+}
+
 namespace {
 
 using namespace tc;
@@ -14,17 +24,12 @@ using namespace tc;
 // epilogue (K >= 2048, or at least two rounds of tiles); otherwise the 1-CTA
 // kernel's smaller tiles spread the work better (GB300 measurements:
 // 2048^3 pair 1.2x faster; 3000x2050x1000 and 1024x1024x4096 1-CTA faster).
-// DeviceCtl::pair_mode forces one of them (tests).
+// DeviceCtl::pair_mode forces one of them (tests); tc_pair_chosen() above.
 cudaError_t launch_tc_any(int kind, const TcMaps& maps, float* C, int64_t M, int64_t N, int64_t K,
                           int64_t ldc, bool c_tma, const DeviceCtl& ctl, cudaStream_t s) {
-  const int64_t pair_tiles =
-      ((M + PAIR_TILE_M - 1) / PAIR_TILE_M) * ((N + PAIR_TILE_N - 1) / PAIR_TILE_N);
-  const int64_t clusters = ctl.sm_count / 2;
-  bool pair = 2 * pair_tiles >= clusters && (K >= 2048 || pair_tiles >= 2 * clusters);
-  if (ctl.pair_mode == 1) pair = false;
-  if (ctl.pair_mode == 2) pair = true;
-  return pair ? launch_cta_pair(kind, maps, C, M, N, K, ldc, c_tma, ctl, s)
-              : launch_single_cta(kind, maps, C, M, N, K, ldc, c_tma, ctl, s);
+  return tc_pair_chosen(M, N, K, ctl)
+             ? launch_cta_pair(kind, maps, C, M, N, K, ldc, c_tma, ctl, s)
+             : launch_single_cta(kind, maps, C, M, N, K, ldc, c_tma, ctl, s);
 }
 
 CUresult encode_c_map(CUtensorMap* cm, float* C, int64_t M, int64_t N, int64_t ldc, bool c_tma) {
@@ -66,6 +71,14 @@ cudaError_t launch_tc_3xtf32(const float* a_big, const float* a_small, const flo
     return cudaErrorInvalidValue;
   if (!c_tma) mp.c = mp.a0;  // unused without TMA stores
   return launch_tc_any(KIND_3XTF32, mp, C, M, N, K, ldc, c_tma, ctl, s);
+}
+
+cudaError_t launch_tc_3xtf32_split(const float* A, const float* B, float* C, int64_t M,
+                                   int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                                   bool c_tma, const DeviceCtl& ctl, cudaStream_t s) {
+  CUtensorMap cm = {};
+  if (encode_c_map(&cm, C, M, N, ldc, c_tma) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  return launch_cta_pair_split(A, B, cm, C, M, N, K, lda, ldb, ldc, c_tma, ctl, s);
 }
 
 }  // namespace mhr

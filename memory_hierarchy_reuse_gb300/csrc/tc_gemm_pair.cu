@@ -2,7 +2,10 @@
 // two SMs share one 256 x 256 output tile; persistent over tiles, with the
 // sparse last round split along K.  Used for large problems.  The method and
 // the warp roles are described in tc_common.cuh.
+#include <type_traits>
+
 #include "tc_common.cuh"
+#include "tf32_split.cuh"
 
 namespace mhr {
 namespace tc {
@@ -66,6 +69,213 @@ struct PairCfg<KIND_3XTF32> {
   static constexpr uint32_t TMEM_COLS = 2 * BN;             // 512
 };
 
+// The in-kernel split runs the 3xTF32 main loop unchanged; only the producer
+// differs (converter warps instead of TMA).
+template <>
+struct PairCfg<KIND_3XTF32_SPLIT> : PairCfg<KIND_3XTF32> {};
+
+// ------------------------------------------------------------------ in-kernel split
+//
+// KIND_3XTF32_SPLIT replaces the TMA producer by SPLIT_WARPS converter warps
+// per CTA.  They read the fp32 operands straight from global memory, split
+// each value into tf32 big + small in registers, and store the four parts
+// into the ring stage in exactly the layout the TMA loads of the pre-split
+// operands produce: 128-row x 128-byte K-major boxes with the 128-byte swizzle,
+// 16-byte chunk c of row r at r * 128 + ((c ^ (r % 8)) * 16).  Compared with
+// the split pre-pass, the split operands never exist in HBM, and the kernel
+// needs no workspace.  On GB300 it runs at about 60 % of the speed of the
+// pre-pass path, though: the converter warps are issue-bound (some 16
+// instructions per element at about 1.2 instructions per SM cycle), so the
+// C ABI uses it only when the pre-pass's workspace cannot be allocated.
+//
+// Thread ct (0..255) of the converter warps owns four chunks of each box per
+// K-block:
+//   A (this CTA's 128 rows x 32 k): chunk (row ct/8 + 32j, k-chunk ct%8) -- one
+//     16-byte load when A allows it; a warp reads 4 rows x 128 contiguous bytes;
+//   B (32 k x this CTA's 128 columns): chunk (column ct%128, k-chunk ct/128 + 2j)
+//     -- four 4-byte loads, one per k, each coalesced across the warp along a
+//     row of B -- stored as row `column` of the K-major box: B is transposed on
+//     the way in.
+// Both store patterns write 8 distinct 16-byte slots per 8 lanes: no bank
+// conflicts.
+//
+// Latency: a thread keeps two K-blocks of loads in flight in two register
+// sets used in turn, issuing a block's loads after the proxy fence of the
+// block before, so that no fence has the thread's own loads outstanding to
+// order.  A third stream of prefetches pulls the K-block SPLIT_PREFETCH ahead
+// of the loads from HBM into L2, so that the register loads hit there.
+constexpr int SPLIT_WARPS = 8;
+constexpr int SPLIT_THREADS = 32 * SPLIT_WARPS;
+constexpr int SPLIT_CHUNKS = 4;    // per thread, per operand, per K-block
+constexpr int SPLIT_PREFETCH = 4;  // K-blocks between the L2 prefetches and the loads
+
+template <int KIND>
+constexpr int pair_threads() {
+  return KIND == KIND_3XTF32_SPLIT ? NUM_THREADS + SPLIT_THREADS : NUM_THREADS;
+}
+
+struct SplitRegs {
+  float4 a[SPLIT_CHUNKS], b[SPLIT_CHUNKS];
+};
+
+// This CTA's boxes of work unit u, and the unit's K-block range.
+__device__ __forceinline__ bool unit_boxes(const TcParams& p, int u, uint32_t rank, int& m0,
+                                           int& nb0, int& kb0, int& kb1) {
+  if (u >= p.num_units) return false;
+  const Unit w = unit_of(u, p);
+  int tm, tn;
+  tile_coords(w.tile, p, tm, tn);
+  m0 = tm * PAIR_TILE_M + static_cast<int>(rank) * (PAIR_TILE_M / 2);
+  nb0 = tn * PAIR_TILE_N + static_cast<int>(rank) * (PAIR_TILE_N / 2);
+  kb0 = w.kb0;
+  kb1 = w.kb1;
+  return true;
+}
+
+// The next K-block whose loads a converter thread issues: its chunk-0
+// addresses at k = 0, the row of its A chunk 0 and the column of its B chunks.
+struct LoadCursor {
+  const float* a;
+  const float* b;
+  int arow, bcol, u, kb, kb1;
+  bool valid;
+
+  __device__ __forceinline__ void seek(const TcParams& p, int unit, uint32_t rank, int ct) {
+    int m0, nb0;
+    valid = unit_boxes(p, unit, rank, m0, nb0, kb, kb1);
+    if (!valid) return;
+    u = unit;
+    arow = m0 + (ct >> 3);
+    bcol = nb0 + (ct & 127);
+    a = p.A + static_cast<int64_t>(arow) * p.lda + 4 * (ct & 7);
+    b = p.B + static_cast<int64_t>(4 * (ct >> 7)) * p.ldb + bcol;
+  }
+  __device__ __forceinline__ void advance(const TcParams& p, int stride, uint32_t rank, int ct) {
+    if (valid && ++kb == kb1) seek(p, u + stride, rank, ct);
+  }
+};
+
+struct PrefetchCursor {
+  int m0, nb0, u, kb, kb1;
+  bool valid;
+
+  __device__ __forceinline__ void seek(const TcParams& p, int unit, uint32_t rank) {
+    valid = unit_boxes(p, unit, rank, m0, nb0, kb, kb1);
+    u = unit;
+  }
+  __device__ __forceinline__ void advance(const TcParams& p, int stride, uint32_t rank) {
+    if (valid && ++kb == kb1) seek(p, u + stride, rank);
+  }
+};
+
+// Loads of K-block c.kb into r.  Blocks wholly inside K (all but a ragged
+// last one) skip the per-element K checks.
+template <bool VA>
+__device__ __forceinline__ void split_load(SplitRegs& r, const TcParams& p, const LoadCursor& c,
+                                           int ct) {
+  const int k0 = c.kb * 32;
+  const bool full_k = k0 + 32 <= p.K;
+  const int ka = k0 + 4 * (ct & 7);  // first k of the thread's A chunks
+#pragma unroll
+  for (int j = 0; j < SPLIT_CHUNKS; ++j) {
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (c.arow + 32 * j < p.M) {
+      const float* src = c.a + static_cast<int64_t>(32 * j) * p.lda + k0;
+      if (full_k) {
+        if (VA) {
+          v = __ldg(reinterpret_cast<const float4*>(src));
+        } else {
+          v.x = __ldg(src);
+          v.y = __ldg(src + 1);
+          v.z = __ldg(src + 2);
+          v.w = __ldg(src + 3);
+        }
+      } else if (ka < p.K) {
+        v.x = __ldg(src);
+        if (ka + 1 < p.K) v.y = __ldg(src + 1);
+        if (ka + 2 < p.K) v.z = __ldg(src + 2);
+        if (ka + 3 < p.K) v.w = __ldg(src + 3);
+      }
+    }
+    r.a[j] = v;
+  }
+  const int kb_first = k0 + 4 * (ct >> 7);  // first k of the thread's B chunk 0
+#pragma unroll
+  for (int j = 0; j < SPLIT_CHUNKS; ++j) {
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int k = kb_first + 8 * j;
+    if (c.bcol < p.N) {
+      const float* src = c.b + static_cast<int64_t>(k0 + 8 * j) * p.ldb;
+      if (full_k) {
+        v.x = __ldg(src);
+        v.y = __ldg(src + p.ldb);
+        v.z = __ldg(src + 2 * p.ldb);
+        v.w = __ldg(src + 3 * p.ldb);
+      } else if (k < p.K) {
+        v.x = __ldg(src);
+        if (k + 1 < p.K) v.y = __ldg(src + p.ldb);
+        if (k + 2 < p.K) v.z = __ldg(src + 2 * p.ldb);
+        if (k + 3 < p.K) v.w = __ldg(src + 3 * p.ldb);
+      }
+    }
+    r.b[j] = v;
+  }
+}
+
+// Pull one future K-block of this CTA's boxes into L2: each of the first 128
+// converter threads takes one row of the A box (128 bytes), each of the others
+// one 128-byte quarter of a row of the B box (32 rows x 512 bytes).  Both ends
+// of each piece are touched, in case it straddles two lines.  Addresses
+// outside the matrices are skipped.
+__device__ __forceinline__ void prefetch_l2(const float* a) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+}
+
+__device__ __forceinline__ void split_prefetch_l2(const TcParams& p, int ct,
+                                                  const PrefetchCursor& c) {
+  if (!c.valid) return;
+  const int k0 = c.kb * 32;
+  if (ct < 128) {
+    const int row = c.m0 + ct;
+    if (row >= p.M || k0 >= p.K) return;
+    const float* a = p.A + static_cast<int64_t>(row) * p.lda + k0;
+    prefetch_l2(a);
+    prefetch_l2(a + (min(k0 + 31, p.K - 1) - k0));
+  } else {
+    const int q = ct - 128, k = k0 + (q >> 2), col = c.nb0 + 32 * (q & 3);
+    if (k >= p.K || col >= p.N) return;
+    const float* b = p.B + static_cast<int64_t>(k) * p.ldb + col;
+    prefetch_l2(b);
+    prefetch_l2(b + (min(col + 31, p.N - 1) - col));
+  }
+}
+
+// Split the registers of one K-block into ring stage `st`: A_big, A_small,
+// B_big^T, B_small^T boxes of 16 KB each, in that order.
+__device__ __forceinline__ void split_store(const SplitRegs& r, uint32_t st, int ct) {
+  using Cf = PairCfg<KIND_3XTF32>;
+#pragma unroll
+  for (int j = 0; j < SPLIT_CHUNKS; ++j) {
+    const int idx = ct + SPLIT_THREADS * j;
+    const int row = idx >> 3, c = idx & 7;
+    const uint32_t off = row * 128 + ((c ^ (row & 7)) << 4);
+    float4 big, small;
+    split4(r.a[j], big, small);
+    st_shared_v4(st + off, big);
+    st_shared_v4(st + Cf::A_BYTES + off, small);
+  }
+#pragma unroll
+  for (int j = 0; j < SPLIT_CHUNKS; ++j) {
+    const int idx = ct + SPLIT_THREADS * j;
+    const int row = idx & 127, c = idx >> 7;
+    const uint32_t off = row * 128 + ((c ^ (row & 7)) << 4);
+    float4 big, small;
+    split4(r.b[j], big, small);
+    st_shared_v4(st + 2 * Cf::A_BYTES + off, big);
+    st_shared_v4(st + 2 * Cf::A_BYTES + Cf::B_BYTES + off, small);
+  }
+}
+
 template <int KIND>
 struct PairLayout {
   using C = PairCfg<KIND>;
@@ -85,7 +295,7 @@ __device__ __forceinline__ void pause_ns(uint64_t ns) {
 }
 
 template <int KIND, bool TMA_STORE>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(pair_threads<KIND>(), 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA0,
                         const __grid_constant__ CUtensorMap tmA1,
                         const __grid_constant__ CUtensorMap tmB0,
@@ -114,8 +324,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t peer_abort = mapa_shared(smem_u32(const_cast<int*>(abort_flag)), rank ^ 1u);
 
   if (threadIdx.x == 0) {
+    // full[s]: one arrive.expect_tx by the TMA producer, or one arrive per
+    // converter warp of both CTAs (split kind)
+    constexpr uint32_t full_count = KIND == KIND_3XTF32_SPLIT ? 2 * SPLIT_WARPS : 1;
     for (int s = 0; s < Cf::STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
+      mbar_init(full_bar(s), full_count);
       mbar_init(empty_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -125,8 +338,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
-    tma_prefetch_desc(&tmA0);
-    tma_prefetch_desc(&tmB0);
+    if constexpr (KIND != KIND_3XTF32_SPLIT) {
+      tma_prefetch_desc(&tmA0);
+      tma_prefetch_desc(&tmB0);
+    }
     if constexpr (KIND == KIND_3XTF32) {
       tma_prefetch_desc(&tmA1);
       tma_prefetch_desc(&tmB1);
@@ -156,8 +371,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producers (both CTAs)
-    // One thread waits, arms and issues; the rest of the warp idles.
-    if (lane == 0) {
+    // One thread waits, arms and issues; the rest of the warp idles.  (The
+    // split kind has converter warps instead; its warp 0 only idles.)
+    if (KIND != KIND_3XTF32_SPLIT && lane == 0) {
       uint32_t it = 0, inflight = 0;
       bool ok = true;
       for (int u = cluster; ok && u < p.num_units; u += num_clusters) {
@@ -234,7 +450,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t d_tmem = tmem_base + buf * Cf::BN;
         for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
           const uint32_t s = it % Cf::STAGES, ph = (it / Cf::STAGES) & 1u;
-          if (!mbar_wait_bounded(full_bar(s), ph, limit, abort_flag)) {
+          // the split kind's stages are completed by plain stores from both
+          // CTAs, released at cluster scope
+          if (!mbar_wait_bounded<KIND == KIND_3XTF32_SPLIT>(full_bar(s), ph, limit, abort_flag)) {
             give_up_one(kErrTimeoutMma);
             ok = false;
             break;
@@ -278,7 +496,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!mbar_wait_bounded(drain_bar, 0, limit, &never)) atomicOr(p.status, kErrTimeoutDrain);
     }
     __syncwarp();
-  } else {
+  } else if (warp < NUM_THREADS / 32) {
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;
     const int ew = warp - 2;
@@ -315,6 +533,60 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (lane == 0) bulk_wait_group<0>();
       __syncwarp();
     }
+  } else if constexpr (KIND == KIND_3XTF32_SPLIT) {
+    // ------------------------------------------------------------ converters (both CTAs)
+    const int ct = threadIdx.x - NUM_THREADS;
+    auto convert = [&](auto vec_a) {
+      constexpr bool VA = decltype(vec_a)::value;
+      // how many K-blocks this cluster stores
+      int left = 0;
+      for (int u = cluster; u < p.num_units; u += num_clusters) {
+        const Unit w = unit_of(u, p);
+        left += w.kb1 - w.kb0;
+      }
+      if (left == 0) return;
+      LoadCursor ld;
+      ld.seek(p, cluster, rank, ct);
+      PrefetchCursor pf;
+      pf.seek(p, cluster, rank);
+      for (int d = 0; d < 2 + SPLIT_PREFETCH; ++d) {
+        if (d >= 2) split_prefetch_l2(p, ct, pf);
+        pf.advance(p, num_clusters, rank);
+      }
+      SplitRegs r0, r1;
+      split_load<VA>(r0, p, ld, ct);
+      ld.advance(p, num_clusters, rank, ct);
+      if (ld.valid) split_load<VA>(r1, p, ld, ct);
+      ld.advance(p, num_clusters, rank, ct);
+      uint32_t it = 0;
+      // Store the K-block held in r, then reuse r for the loads two blocks on.
+      auto step = [&](SplitRegs& r) -> bool {
+        const uint32_t s = it % Cf::STAGES, ph = (it / Cf::STAGES) & 1u;
+        if (!warp_wait(empty_bar(s), ph ^ 1u, limit, abort_flag)) {
+          give_up_pair(kErrTimeoutProducer);
+          return false;
+        }
+        split_store(r, sbase + s * Cf::STAGE_BYTES, ct);
+        fence_proxy_async_smem();  // the stores, visible to the pair's MMA reads
+        __syncwarp();
+        // test hook: block 0 never completes its first stage
+        const bool stall = p.inject_stall && blockIdx.x == 0 && it == 0;
+        if (lane == 0 && !stall) mbar_arrive_cluster(mapa_shared(full_bar(s), 0));
+        ++it;
+        if (--left == 0) return false;
+        if (ld.valid) split_load<VA>(r, p, ld, ct);
+        ld.advance(p, num_clusters, rank, ct);
+        split_prefetch_l2(p, ct, pf);
+        pf.advance(p, num_clusters, rank);
+        return true;
+      };
+      while (step(r0) && step(r1)) {
+      }
+    };
+    if (p.vec_a)
+      convert(std::true_type{});
+    else
+      convert(std::false_type{});
   }
 
   tc_fence_before();
@@ -356,7 +628,7 @@ cudaError_t launch_pair_t(const TcMaps& mp, const TcParams& p, const DeviceCtl& 
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.blockDim = dim3(pair_threads<KIND>());
   cfg.dynamicSmemBytes = PairLayout<KIND>::ALLOC;
   cfg.stream = s;
   cfg.attrs = attr;
@@ -377,12 +649,15 @@ cudaError_t launch_pair_t(const TcMaps& mp, const TcParams& p, const DeviceCtl& 
     q.full_units = p.num_tiles - rem;
     q.num_units = q.full_units + 2 * rem;
     q.kb_mid = p.num_kb / 2;
+    note_launch();
     zero_split_tiles_kernel<<<dim3(rem, 2 * PairCfg<KIND>::BM / 8), dim3(128, 8), 0, s>>>(
         q, PairCfg<KIND>::BN);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   cfg.gridDim = dim3(2 * clusters);
-  note_main_kernel(KIND == KIND_BF16 ? "tc_gemm_pair_kernel<bf16>" : "tc_gemm_pair_kernel<3xtf32>",
+  note_main_kernel(KIND == KIND_BF16     ? "tc_gemm_pair_kernel<bf16>"
+                   : KIND == KIND_3XTF32 ? "tc_gemm_pair_kernel<3xtf32>"
+                                         : "tc_gemm_pair_kernel<3xtf32,split>",
                    2 * clusters, p.num_tiles);
   e = cudaLaunchKernelEx(&cfg, kern, mp.a0, mp.a1, mp.b0, mp.b1, mp.c, q);
   if (e != cudaSuccess) return e;
@@ -390,6 +665,23 @@ cudaError_t launch_pair_t(const TcMaps& mp, const TcParams& p, const DeviceCtl& 
 }
 
 }  // namespace
+
+cudaError_t launch_cta_pair_split(const float* A, const float* B, const CUtensorMap& c_map,
+                                  float* C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                                  int64_t ldb, int64_t ldc, bool c_tma, const DeviceCtl& ctl,
+                                  cudaStream_t s) {
+  TcParams p = make_params(M, N, K, PAIR_TILE_M, PAIR_TILE_N, PairCfg<KIND_3XTF32_SPLIT>::BK, C,
+                           ldc, ctl);
+  p.A = A;
+  p.B = B;
+  p.lda = lda;
+  p.ldb = ldb;
+  p.vec_a = (reinterpret_cast<uintptr_t>(A) % 16 == 0) && (lda % 4 == 0);
+  TcMaps mp;  // only the C map is read (TMA stores); the operand maps are unused
+  mp.a0 = mp.a1 = mp.b0 = mp.b1 = mp.c = c_map;
+  return c_tma ? launch_pair_t<KIND_3XTF32_SPLIT, true>(mp, p, ctl, s)
+               : launch_pair_t<KIND_3XTF32_SPLIT, false>(mp, p, ctl, s);
+}
 
 cudaError_t launch_cta_pair(int kind, const TcMaps& maps, float* C, int64_t M, int64_t N,
                             int64_t K, int64_t ldc, bool c_tma, const DeviceCtl& ctl,

@@ -5,6 +5,7 @@
 #include <cstdint>
 
 #include "mhr_internal.h"
+#include "tf32_split.cuh"
 
 namespace mhr {
 namespace {
@@ -24,21 +25,6 @@ __global__ void pack_u16_kernel(const uint16_t* __restrict__ src, int64_t rows, 
       dst[r * dst_ld + c] = src[r * src_ld + c];
 }
 
-// Round an fp32 value to tf32 (10 explicit mantissa bits) to nearest, ties to
-// even, by integer arithmetic on the bit pattern; Inf and NaN pass unchanged.
-__device__ __forceinline__ float tf32_rne(float x) {
-  uint32_t u = __float_as_uint(x);
-  if ((u & 0x7F800000u) == 0x7F800000u) return x;
-  u += 0x0FFFu + ((u >> 13) & 1u);
-  return __uint_as_float(u & 0xFFFFE000u);
-}
-
-__device__ __forceinline__ void split_tf32(float x, float& big, float& small) {
-  big = tf32_rne(x);
-  const float rest = x - big;  // exact: the discarded low bits
-  small = isfinite(x) ? tf32_rne(rest) : 0.f;
-}
-
 // Split of both operands in one launch.  Blocks [0, a_blocks) split rows of
 // A in place order; the remaining blocks split 64 x 64 tiles of B and write
 // them transposed.  VA / VB select 16-byte loads when the operand's address,
@@ -48,13 +34,6 @@ __device__ __forceinline__ void split_tf32(float x, float& big, float& small) {
 // flight.
 constexpr int SPLIT_THREADS = 256;
 constexpr int SPLIT_TILE = 64;
-
-__device__ __forceinline__ void split4(const float4 v, float4& b, float4& s) {
-  split_tf32(v.x, b.x, s.x);
-  split_tf32(v.y, b.y, s.y);
-  split_tf32(v.z, b.z, s.z);
-  split_tf32(v.w, b.w, s.w);
-}
 
 template <bool VA, bool VB>
 __global__ void __launch_bounds__(SPLIT_THREADS)
@@ -166,6 +145,7 @@ unsigned grid_rows(int64_t rows) { return static_cast<unsigned>(rows < 65535 ? r
 
 cudaError_t launch_zero_fill(float* C, int64_t M, int64_t N, int64_t ldc, cudaStream_t s) {
   const unsigned gx = static_cast<unsigned>((N + 255) / 256 < 64 ? (N + 255) / 256 : 64);
+  note_launch();
   zero_fill_kernel<<<dim3(gx, grid_rows(M)), 256, 0, s>>>(C, M, N, ldc);
   return cudaGetLastError();
 }
@@ -173,6 +153,7 @@ cudaError_t launch_zero_fill(float* C, int64_t M, int64_t N, int64_t ldc, cudaSt
 cudaError_t launch_pack_u16(const uint16_t* src, int64_t rows, int64_t cols, int64_t src_ld,
                             uint16_t* dst, int64_t dst_ld, cudaStream_t s) {
   const unsigned gx = static_cast<unsigned>((cols + 255) / 256 < 64 ? (cols + 255) / 256 : 64);
+  note_launch();
   pack_u16_kernel<<<dim3(gx, grid_rows(rows)), 256, 0, s>>>(src, rows, cols, src_ld, dst, dst_ld);
   return cudaGetLastError();
 }
@@ -199,6 +180,7 @@ cudaError_t launch_split_tf32(const float* A, const float* B, int64_t M, int64_t
   b_blocks = b_blocks < 1 ? 1 : (b_blocks > b_tiles ? b_tiles : b_blocks);
   const unsigned grid = static_cast<unsigned>(a_blocks + b_blocks);
   const int ab = static_cast<int>(a_blocks);
+  note_launch();
   if (va && vb)
     split_vec_kernel<true, true><<<grid, SPLIT_THREADS, 0, s>>>(A, B, M, N, K, lda, ldb, Kp, ab,
                                                                 a_big, a_small, bt_big, bt_small);

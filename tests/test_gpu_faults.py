@@ -1,7 +1,9 @@
 """Failure detection on the GPU without a fault (GB300 only).
 
-A test hook makes block 0 of a tensor-core kernel arm one ring stage without
-loading it, so its consumers' bounded waits run out. The kernel must record
+A test hook makes block 0 of a tensor-core kernel leave its first ring stage
+incomplete (the TMA producer arms it without loading it; the in-kernel split's
+converter warps fill it without arriving), so its consumers' bounded waits run
+out. The kernel must record
 the timeout, free its TMEM and exit; gemm_check() must report
 MHR_ERR_TIMEOUT; and the context must stay usable (a following call is
 correct). Nothing traps, faults or hangs.
@@ -15,11 +17,18 @@ from parity_util import TOL, DeviceCall, normalised_error, operands
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("mode", [1, 2], ids=["1cta", "pair"])
-@pytest.mark.parametrize("path", ["3xtf32", "bf16"])
-def test_injected_stall_reports_timeout(mhr, path, mode):
+# (path, CTA-pair mode, 3xTF32 split mode): every producer kind -- TMA loads
+# in both kernels, and the converter warps of the in-kernel split
+VARIANTS = [("3xtf32", 1, 1), ("3xtf32", 2, 1), ("3xtf32", 2, 2), ("bf16", 1, 0), ("bf16", 2, 0)]
+IDS = ["3xtf32-1cta", "3xtf32-pair-prepass", "3xtf32-pair-insplit", "bf16-1cta", "bf16-pair"]
+
+
+@pytest.mark.parametrize("variant", VARIANTS, ids=IDS)
+def test_injected_stall_reports_timeout(mhr, variant):
+    path, mode, split = variant
     A, B, Ab, Bb = operands(300, 520, 700, 6001, "normal", path)
     call = DeviceCall(path, A, B, Ab, Bb)
+    old_split = mhr.gemm_testing_set_split_mode(split)
     old_mode = mhr.gemm_testing_set_cta_pair_mode(mode)
     old_limit = mhr.gemm_testing_set_wait_limit_ns(50_000_000)  # 50 ms
     mhr.gemm_testing_set_inject_stall(1)
@@ -37,6 +46,7 @@ def test_injected_stall_reports_timeout(mhr, path, mode):
         C = call.run(mhr).result()
     finally:
         mhr.gemm_testing_set_cta_pair_mode(old_mode)
+        mhr.gemm_testing_set_split_mode(old_split)
     Cref, S = oracle.gemm(A, B, with_abs=True)
     assert normalised_error(C, Cref, S) <= TOL[path]
 

@@ -16,18 +16,24 @@ pytestmark = pytest.mark.gpu
 
 PATHS = ["f32", "3xtf32", "bf16"]
 # Each tensor-core path has two kernels: the single-CTA kernel (128-row tiles)
-# and the CTA-pair kernel (256-row tiles over a cluster of 2). Both are forced
-# in turn on every small shape; full-size checks use the automatic choice, as
-# the benchmark does.
-VARIANTS = [("f32", 0), ("3xtf32", 1), ("3xtf32", 2), ("bf16", 1), ("bf16", 2)]
-VARIANT_IDS = ["f32", "3xtf32-1cta", "3xtf32-pair", "bf16-1cta", "bf16-pair"]
+# and the CTA-pair kernel (256-row tiles over a cluster of 2); 3xTF32 on the
+# CTA-pair kernel splits its operands either in a pre-pass or inside the
+# kernel. Every combination is forced in turn on every small shape; full-size
+# checks use the automatic choice, as the benchmark does.
+# (path, CTA-pair mode, split mode)
+VARIANTS = [("f32", 0, 0), ("3xtf32", 1, 1), ("3xtf32", 2, 1), ("3xtf32", 2, 2), ("bf16", 1, 0),
+            ("bf16", 2, 0)]
+VARIANT_IDS = ["f32", "3xtf32-1cta", "3xtf32-pair-prepass", "3xtf32-pair-insplit", "bf16-1cta",
+               "bf16-pair"]
 
 
 @pytest.fixture(params=VARIANTS, ids=VARIANT_IDS)
 def path(request, mhr):
-    name, mode = request.param
+    name, mode, split = request.param
     old = mhr.gemm_testing_set_cta_pair_mode(mode)
+    old_split = mhr.gemm_testing_set_split_mode(split)
     yield name
+    mhr.gemm_testing_set_split_mode(old_split)
     mhr.gemm_testing_set_cta_pair_mode(old)
 
 # (M, N, K): single elements, thin shapes, several tiles with ragged tails in
@@ -221,3 +227,56 @@ def test_pair_kernel_split_last_round(mhr, path):
         assert np.array_equal(DeviceCall(path, A, B, Ab, Bb).run(mhr).result(), oracle.gemm(A, B))
     finally:
         mhr.gemm_testing_set_cta_pair_mode(old)
+
+
+@pytest.mark.parametrize("shape", [(300, 520, 1000), (255, 513, 1001), (130, 260, 37),
+                                   (512, 512, 4096)], ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("offset", [0, 1], ids=["aligned", "offset1"])
+def test_in_kernel_split_matches_prepass_bitwise(mhr, shape, offset):
+    """The CTA-pair kernel with the split inside the kernel computes exactly
+    what it computes on pre-split operands: the same tf32 parts, the same
+    MMAs in the same order. Ragged K (not a multiple of 4, of the 32-wide K
+    step), and operands one element off 16-byte alignment (A read with 4-byte
+    loads) included."""
+    M, N, K = shape
+    A, B, _, _ = operands(M, N, K, 3201 + K, "normal", "3xtf32")
+    old = mhr.gemm_testing_set_cta_pair_mode(2)
+    try:
+        outs = []
+        for split in (1, 2):
+            old_split = mhr.gemm_testing_set_split_mode(split)
+            try:
+                outs.append(DeviceCall("3xtf32", A, B, offset=offset).run(mhr).result())
+                label = mhr.gemm_testing_last_main_kernel()
+                assert label.startswith("tc_gemm_pair_kernel<3xtf32" +
+                                        (",split>" if split == 2 else ">")), label
+            finally:
+                mhr.gemm_testing_set_split_mode(old_split)
+    finally:
+        mhr.gemm_testing_set_cta_pair_mode(old)
+    assert np.array_equal(outs[0], outs[1])
+    Cref, S = oracle.gemm(A, B, with_abs=True)
+    assert normalised_error(outs[1], Cref, S) <= TOL["3xtf32"]
+
+
+def test_workspace_fallback_splits_in_kernel(mhr):
+    """When the split operands' workspace cannot be allocated (a cap set by a
+    test hook stands in for an allocation failure), gemm_f32_3xtf32 splits
+    inside the CTA-pair kernel instead and returns the same C bit for bit."""
+    A, B, _, _ = operands(300, 520, 1000, 3301, "normal", "3xtf32")
+    old = mhr.gemm_testing_set_cta_pair_mode(2)
+    try:
+        ref = DeviceCall("3xtf32", A, B).run(mhr).result()
+        assert mhr.gemm_testing_last_main_kernel().startswith("tc_gemm_pair_kernel<3xtf32> ")
+        assert mhr.gemm_testing_last_launches() == 2  # split pre-pass + main kernel
+        old_limit = mhr.gemm_testing_set_workspace_limit(0)
+        try:
+            C = DeviceCall("3xtf32", A, B).run(mhr).result()
+            assert mhr.gemm_testing_last_main_kernel().startswith(
+                "tc_gemm_pair_kernel<3xtf32,split> ")
+            assert mhr.gemm_testing_last_launches() == 1
+        finally:
+            mhr.gemm_testing_set_workspace_limit(old_limit)
+    finally:
+        mhr.gemm_testing_set_cta_pair_mode(old)
+    assert np.array_equal(C, ref)
