@@ -383,6 +383,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ladder", action="store_true",
                     help="time the pages' naive/tiled kernels beside the build's paths at 4096^3")
+    ap.add_argument("--split", default="auto", choices=["auto", "onchip"],
+                    help="3xTF32 workloads: where the operands are split into tf32 parts "
+                         "(auto: the library's choice, a pre-pass; onchip: inside the CTA-pair "
+                         "kernel)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -409,6 +413,8 @@ def main():
     from memory_hierarchy_reuse_gb300 import model
 
     lib = mhr.load()
+    if args.split == "onchip":
+        lib.gemm_testing_set_split_mode(2)
     M, N, K = w["M"], w["N"], w["K"]
     A_h, B_h, Ab_h, Bb_h = host_operands(w)
     path = w["path"]
@@ -654,7 +660,9 @@ def main():
             "config": {"workload": w["desc"], "M": M, "N": N, "K": K, "entry": ENTRY[path],
                        "dist": w["dist"], "seeds": list(w["seeds"]),
                        "l2": "flushed before every timed step (256 MiB write, outside the step events)",
-                       "parallelism": "replicas" if world > 1 else "single GPU"},
+                       "parallelism": "replicas" if world > 1 else "single GPU",
+                       **({"split": "on chip (CTA-pair kernel)" if args.split == "onchip"
+                           else "pre-pass"} if path == "3xtf32" else {})},
             "roofline": roofline,
             "cpu_baseline": cpu,
             "cpu_tiled": cpu_tiled_line,

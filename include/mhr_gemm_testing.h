@@ -68,7 +68,7 @@ uint64_t gemm_testing_set_workspace_limit(uint64_t bytes);
  * Tuning hook: the number of tile rows per raster group of the tensor-core
  * kernels' tile schedule (consecutive work units sweep that many tile rows
  * column by column, so co-resident CTAs share A and B panels in L2).  0
- * restores the default (16).  Returns the previous setting.
+ * restores the default (8).  Returns the previous setting.
  */
 int gemm_testing_set_raster_group(int tile_rows);
 

@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS)
           const int64_t c = c0 + j * SPLIT_THREADS;
           if (c < k4) {
             float4 b, s;
-            split4(v[j], b, s);
+            split4<VA>(v[j], b, s);  // conversion where 16-byte loads keep this memory-bound
             db[c] = b;
             ds[c] = s;
           }
@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS)
         const int idx = t + j * SPLIT_THREADS;
         const int kr = idx >> 4, nc = (idx & 15) * 4;
         float4 b, s;
-        split4(v[j], b, s);
+        split4<true>(v[j], b, s);
         tb[kr][nc] = b.x; tb[kr][nc + 1] = b.y; tb[kr][nc + 2] = b.z; tb[kr][nc + 3] = b.w;
         ts[kr][nc] = s.x; ts[kr][nc + 1] = s.y; ts[kr][nc + 2] = s.z; ts[kr][nc + 3] = s.w;
       }
@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS)
       for (int j = 0; j < 16; ++j) {
         const int idx = t + j * SPLIT_THREADS;
         float b, sm;
-        split_tf32(v[j], b, sm);
+        split_tf32<false>(v[j], b, sm);  // integer rounding: this 4-byte-load branch is latency-bound
         tb[idx >> 6][idx & 63] = b;
         ts[idx >> 6][idx & 63] = sm;
       }
