@@ -98,6 +98,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const uint64_t limit = p.wait_limit_ns;
+  // The set-up above may overlap the pre-pass kernel before this one; its
+  // outputs (split or repacked operands, zeroed C tiles) are read from here on.
+  grid_dependency_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -268,16 +271,25 @@ cudaError_t launch_t(const TcMaps& mp, float* C, int64_t M, int64_t N, int64_t K
   const int grid = p.num_tiles < ctl.sm_count ? p.num_tiles : ctl.sm_count;
   note_main_kernel(KIND == KIND_BF16 ? "tc_gemm_kernel<bf16>" : "tc_gemm_kernel<3xtf32>", grid,
                    p.num_tiles);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = Layout<KIND>::ALLOC;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   cudaError_t e;
   if (c_tma) {
     if ((e = prepare_kernel<KIND, true>()) != cudaSuccess) return e;
-    tc_gemm_kernel<KIND, true><<<grid, NUM_THREADS, Layout<KIND>::ALLOC, s>>>(mp.a0, mp.a1, mp.b0,
-                                                                               mp.b1, mp.c, p);
+    e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<KIND, true>, mp.a0, mp.a1, mp.b0, mp.b1, mp.c, p);
   } else {
     if ((e = prepare_kernel<KIND, false>()) != cudaSuccess) return e;
-    tc_gemm_kernel<KIND, false><<<grid, NUM_THREADS, Layout<KIND>::ALLOC, s>>>(mp.a0, mp.a1, mp.b0,
-                                                                                mp.b1, mp.c, p);
+    e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<KIND, false>, mp.a0, mp.a1, mp.b0, mp.b1, mp.c, p);
   }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -357,6 +357,9 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const uint64_t limit = p.wait_limit_ns;
+  // The set-up above may overlap the pre-pass kernel before this one; its
+  // outputs (split or repacked operands, zeroed C tiles) are read from here on.
+  grid_dependency_wait();
 
   // Give up: record why (first role only), raise the abort flag in both CTAs.
   auto give_up_one = [&](uint32_t bit) {  // called by a single thread
@@ -602,6 +605,11 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
 // num_tiles)), which both K halves then add into.  Block (x, y) clears rows
 // [8y, 8y + 8) of split tile x.
 __global__ void zero_split_tiles_kernel(TcParams p, int tile_cols) {
+  grid_launch_dependents();
+  // Launched as a dependent of the kernel before it (the split pre-pass, or
+  // the previous call's GEMM, which may still read or write C): wait for it,
+  // so that this kernel's completion implies that one's.
+  grid_dependency_wait();
   const int tile = p.full_units + blockIdx.x;
   int tm, tn;
   tile_coords(tile, p, tm, tn);
@@ -622,11 +630,13 @@ cudaError_t launch_pair_t(const TcMaps& mp, const TcParams& p, const DeviceCtl& 
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        PairLayout<KIND>::ALLOC);
   if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(pair_threads<KIND>());
   cfg.dynamicSmemBytes = PairLayout<KIND>::ALLOC;
@@ -650,11 +660,18 @@ cudaError_t launch_pair_t(const TcMaps& mp, const TcParams& p, const DeviceCtl& 
     q.num_units = q.full_units + 2 * rem;
     q.kb_mid = p.num_kb / 2;
     note_launch();
-    zero_split_tiles_kernel<<<dim3(rem, 2 * PairCfg<KIND>::BM / 8), dim3(128, 8), 0, s>>>(
-        q, PairCfg<KIND>::BN);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    cudaLaunchConfig_t zcfg = {};
+    zcfg.gridDim = dim3(rem, 2 * PairCfg<KIND>::BM / 8);
+    zcfg.blockDim = dim3(128, 8);
+    zcfg.stream = s;
+    zcfg.attrs = &attr[1];
+    zcfg.numAttrs = 1;
+    if ((e = cudaLaunchKernelEx(&zcfg, zero_split_tiles_kernel, q,
+                                static_cast<int>(PairCfg<KIND>::BN))) != cudaSuccess)
+      return e;
   }
   cfg.gridDim = dim3(2 * clusters);
+  cfg.numAttrs = 2;  // and programmatic serialisation behind the kernel before
   note_main_kernel(KIND == KIND_BF16     ? "tc_gemm_pair_kernel<bf16>"
                    : KIND == KIND_3XTF32 ? "tc_gemm_pair_kernel<3xtf32>"
                                          : "tc_gemm_pair_kernel<3xtf32,split>",

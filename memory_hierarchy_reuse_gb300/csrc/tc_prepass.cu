@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
+#include "mhr_device.cuh"
 #include "mhr_internal.h"
 #include "tf32_split.cuh"
 
@@ -19,6 +20,7 @@ __global__ void zero_fill_kernel(float* C, int64_t M, int64_t N, int64_t ldc) {
 
 __global__ void pack_u16_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t cols,
                                 int64_t src_ld, uint16_t* __restrict__ dst, int64_t dst_ld) {
+  grid_launch_dependents();  // the GEMM kernel after this one may start its set-up
   for (int64_t r = blockIdx.y; r < rows; r += gridDim.y)
     for (int64_t c = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; c < cols;
          c += static_cast<int64_t>(gridDim.x) * blockDim.x)
@@ -41,6 +43,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS)
                      int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t Kp, int a_blocks,
                      float* __restrict__ a_big, float* __restrict__ a_small,
                      float* __restrict__ bt_big, float* __restrict__ bt_small) {
+  grid_launch_dependents();  // the GEMM kernel after this one may start its set-up
   __shared__ float tb[SPLIT_TILE][SPLIT_TILE + 1];
   __shared__ float ts[SPLIT_TILE][SPLIT_TILE + 1];
   const int t = threadIdx.x;
