@@ -197,6 +197,18 @@ def test_config5_8192_bf16_sampled(mhr):
     sampled_check(mhr, "bf16", 8192, 8192, 8192, 5001, "normal")
 
 
+def pair_clusters(mhr, path):
+    """The number of clusters the CTA-pair kernel runs on this GPU."""
+    import re
+
+    A, B, Ab, Bb = operands(4096, 4096, 64, 3101, "normal", path)
+    DeviceCall(path, A, B, Ab, Bb).run(mhr)
+    label = mhr.gemm_testing_last_main_kernel()
+    clusters = int(re.search(r"grid=(\d+)", label).group(1)) // 2
+    assert clusters >= 8, label
+    return clusters
+
+
 @pytest.mark.parametrize("path", ["3xtf32", "bf16"])
 def test_pair_kernel_split_last_round(mhr, path):
     """The CTA-pair kernel splits a sparse last round of tiles into two K halves
@@ -204,15 +216,9 @@ def test_pair_kernel_split_last_round(mhr, path):
     co-resident clusters, so exactly 3 tiles are split, and compare it in full
     with the oracle, through the TMA reduce path (aligned C) and the atomic
     path (ldc odd), and for bitwise repeatability."""
-    import re
-
     old = mhr.gemm_testing_set_cta_pair_mode(2)
     try:
-        A, B, Ab, Bb = operands(4096, 4096, 64, 3101, "normal", path)
-        DeviceCall(path, A, B, Ab, Bb).run(mhr)
-        label = mhr.gemm_testing_last_main_kernel()
-        clusters = int(re.search(r"grid=(\d+)", label).group(1)) // 2
-        assert clusters >= 8, label
+        clusters = pair_clusters(mhr, path)
         M, N, K = 256 * (clusters + 3), 256, 320
         for ldc in (None, N + 1):
             A, B, Ab, Bb = operands(M, N, K, 3103, "normal", path)
@@ -222,22 +228,43 @@ def test_pair_kernel_split_last_round(mhr, path):
             Cref, S = oracle.gemm(A, B, with_abs=True)
             assert normalised_error(C, Cref, S) <= TOL[path]
             assert np.array_equal(call.run(mhr).result(), C)
-        # integer inputs: the two halves' sum is exact, so still bit-exact
-        A, B, Ab, Bb = operands(M, N, K, 3105, "int", path)
-        assert np.array_equal(DeviceCall(path, A, B, Ab, Bb).run(mhr).result(), oracle.gemm(A, B))
+    finally:
+        mhr.gemm_testing_set_cta_pair_mode(old)
+
+
+@pytest.mark.parametrize("path", ["3xtf32", "bf16"])
+@pytest.mark.parametrize("extra", [1, -1, 5, 28], ids=["c+1", "2c-1", "2c+5", "3c+28"])
+def test_pair_kernel_schedule_bit_exact(mhr, path, extra):
+    """Integer inputs through tile counts around the round boundaries of the
+    persistent schedule: one round plus one tile, two rounds minus one, two
+    plus five, and three plus 28 (the 4096^3 case's 256 tiles on 76
+    clusters). Every K-block of every tile must be computed exactly once,
+    split or not; the sums are exact, so C must match the oracle bit for
+    bit."""
+    old = mhr.gemm_testing_set_cta_pair_mode(2)
+    try:
+        clusters = pair_clusters(mhr, path)
+        tiles = {1: clusters + 1, -1: 2 * clusters - 1, 5: 2 * clusters + 5,
+                 28: 3 * clusters + 28}[extra]
+        M, N, K = 256 * tiles, 256, 320
+        A, B, Ab, Bb = operands(M, N, K, 3105 + extra, "int", path)
+        C = DeviceCall(path, A, B, Ab, Bb).run(mhr).result()
+        assert f"tiles={tiles}" in mhr.gemm_testing_last_main_kernel()
+        assert np.array_equal(C, oracle.gemm(A, B))
     finally:
         mhr.gemm_testing_set_cta_pair_mode(old)
 
 
 @pytest.mark.parametrize("shape", [(300, 520, 1000), (255, 513, 1001), (130, 260, 37),
-                                   (512, 512, 4096)], ids=lambda s: "x".join(map(str, s)))
+                                   (512, 512, 4096), (256 * 79, 256, 320)],
+                         ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("offset", [0, 1], ids=["aligned", "offset1"])
 def test_in_kernel_split_matches_prepass_bitwise(mhr, shape, offset):
     """The CTA-pair kernel with the split inside the kernel computes exactly
     what it computes on pre-split operands: the same tf32 parts, the same
     MMAs in the same order. Ragged K (not a multiple of 4, of the 32-wide K
-    step), and operands one element off 16-byte alignment (A read with 4-byte
-    loads) included."""
+    step), operands one element off 16-byte alignment (A read with 4-byte
+    loads), and 79 tiles (a split last round on 76 clusters) included."""
     M, N, K = shape
     A, B, _, _ = operands(M, N, K, 3201 + K, "normal", "3xtf32")
     old = mhr.gemm_testing_set_cta_pair_mode(2)
