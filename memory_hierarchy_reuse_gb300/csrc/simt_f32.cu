@@ -60,18 +60,27 @@ __device__ __forceinline__ float2 unpack2(uint64_t v) {
   return r;
 }
 
+// k_mid > 0 splits every tile's K range in two at k_mid (a multiple of BK):
+// blocks [0, tiles) take [0, k_mid), blocks [tiles, 2 tiles) take [k_mid, K),
+// and both add their partial sums into C, which the caller has zeroed.  Two
+// addends onto zero give the same fp32 sum in either order, so the result is
+// reproducible bit for bit.
 template <bool VA, bool VB, bool VC>
 __global__ void __launch_bounds__(NT, 2)
     simt_f32_kernel(const float* __restrict__ A, const float* __restrict__ B,
                     float* __restrict__ C, int64_t M, int64_t N, int64_t K, int64_t lda,
-                    int64_t ldb, int64_t ldc, int64_t tiles_m, int64_t tiles_n) {
+                    int64_t ldb, int64_t ldc, int64_t tiles_m, int64_t tiles_n, int64_t k_mid) {
   __shared__ __align__(16) float As[2][BK][BM + APAD];
   __shared__ __align__(16) float Bs[2][BK][BN];
 
   const int tid = threadIdx.x;
+  const int64_t tiles = tiles_m * tiles_n;
+  const bool second_half = k_mid > 0 && static_cast<int64_t>(blockIdx.x) >= tiles;
+  const int64_t k_begin = second_half ? k_mid : 0;
+  const int64_t k_end = k_mid > 0 && !second_half ? k_mid : K;
   // Grouped raster over a 1-D grid: blocks launched together cover GROUP_M
   // tile rows, column by column.
-  const int64_t t = blockIdx.x;
+  const int64_t t = second_half ? blockIdx.x - tiles : blockIdx.x;
   const int64_t group_size = GROUP_M * tiles_n;
   const int64_t first_m = (t / group_size) * GROUP_M;
   const int64_t gm = tiles_m - first_m < GROUP_M ? tiles_m - first_m : GROUP_M;
@@ -125,14 +134,14 @@ __global__ void __launch_bounds__(NT, 2)
     *reinterpret_cast<float4*>(&Bs[buf][b_k][b_col]) = make_float4(rb[0], rb[1], rb[2], rb[3]);
   };
 
-  const int64_t nk = (K + BK - 1) / BK;
-  fetch(0);
+  const int64_t nk = (k_end - k_begin + BK - 1) / BK;
+  fetch(k_begin);
   stash(0);
   __syncthreads();
 
   for (int64_t kt = 0; kt < nk; ++kt) {
     const int cur = static_cast<int>(kt & 1);
-    if (kt + 1 < nk) fetch((kt + 1) * BK);
+    if (kt + 1 < nk) fetch(k_begin + (kt + 1) * BK);
 #pragma unroll
     for (int k = 0; k < BK; ++k) {
       const float4 a0 = *reinterpret_cast<const float4*>(&As[cur][k][ty * 4]);
@@ -169,13 +178,23 @@ __global__ void __launch_bounds__(NT, 2)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int64_t col = n0 + h * 64 + tx * 4;
+      const float4 v =
+          make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2], acc[i][4 * h + 3]);
       if (VC && col + 4 <= N) {
-        *reinterpret_cast<float4*>(crow + col) =
-            make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2], acc[i][4 * h + 3]);
+        if (k_mid > 0)
+          atomicAdd(reinterpret_cast<float4*>(crow + col), v);
+        else
+          *reinterpret_cast<float4*>(crow + col) = v;
       } else {
+        const float w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          if (col + j < N) crow[col + j] = acc[i][4 * h + j];
+          if (col + j < N) {
+            if (k_mid > 0)
+              atomicAdd(crow + col + j, w[j]);
+            else
+              crow[col + j] = w[j];
+          }
       }
     }
   }
@@ -185,10 +204,31 @@ template <bool VA, bool VB, bool VC>
 cudaError_t launch_t(const float* A, const float* B, float* C, int64_t M, int64_t N, int64_t K,
                      int64_t lda, int64_t ldb, int64_t ldc, cudaStream_t s) {
   const int64_t tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
-  note_main_kernel("simt_f32_kernel", static_cast<int>(tiles_m * tiles_n),
-                   static_cast<int>(tiles_m * tiles_n));
-  simt_f32_kernel<VA, VB, VC><<<static_cast<unsigned>(tiles_m * tiles_n), NT, 0, s>>>(
-      A, B, C, M, N, K, lda, ldb, ldc, tiles_m, tiles_n);
+  const int64_t tiles = tiles_m * tiles_n;
+  // Split every tile along K when that shortens the busiest SM's queue.  On
+  // GB300 the time of this kernel follows the largest number of blocks any
+  // SM runs, ceil(tiles / SMs) -- a block alone on its SM finishes no sooner
+  // than one sharing it -- so halves help when the last layer of blocks is
+  // thin: ceil(2 tiles / SMs) / 2 against ceil(tiles / SMs).  Measured at
+  // K = 4096: 320 tiles 40.2 -> 48.1 TFLOPS split (3 against 2.5 block
+  // times); 400, 576 and 1024 tiles equal or 1 % slower split (3/3, 4/4,
+  // 7/7), which is what the zero fill and the second add cost.  Each half
+  // keeps at least 64 K steps.
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t whole = (tiles + sms - 1) / sms;
+  const int64_t halves = (2 * tiles + sms - 1) / sms;  // in half-block times
+  int64_t k_mid = 0;
+  if (K >= 2 * 64 * BK && tiles < (int64_t{1} << 30) && halves < 2 * whole * 0.93)
+    k_mid = (K / 2 + BK - 1) / BK * BK;
+  cudaError_t e;
+  if (k_mid > 0 && (e = launch_zero_fill(C, M, N, ldc, s)) != cudaSuccess) return e;
+  const int64_t blocks = k_mid > 0 ? 2 * tiles : tiles;
+  note_main_kernel(k_mid > 0 ? "simt_f32_kernel<split-K>" : "simt_f32_kernel",
+                   static_cast<int>(blocks), static_cast<int>(tiles));
+  simt_f32_kernel<VA, VB, VC><<<static_cast<unsigned>(blocks), NT, 0, s>>>(
+      A, B, C, M, N, K, lda, ldb, ldc, tiles_m, tiles_n, k_mid);
   return cudaGetLastError();
 }
 

@@ -307,3 +307,23 @@ def test_workspace_fallback_splits_in_kernel(mhr):
     finally:
         mhr.gemm_testing_set_cta_pair_mode(old)
     assert np.array_equal(C, ref)
+
+
+def test_simt_split_k(mhr):
+    """The SIMT kernel splits every tile along K when a partial last round of
+    blocks would waste more than the split costs; both halves add into a
+    zeroed C. 2560 x 2048 is 320 tiles of 128 x 128 (more than two blocks on
+    each of the SMs); K = 1030 is ragged. Integer inputs must match the
+    oracle bit for bit, real ones within tolerance and bitwise repeatably."""
+    M, N, K = 2560, 2048, 1030
+    A, B, _, _ = operands(M, N, K, 3401, "int", "f32")
+    call = DeviceCall("f32", A, B)
+    C = call.run(mhr).result()
+    assert mhr.gemm_testing_last_main_kernel().startswith("simt_f32_kernel<split-K> grid=640 ")
+    assert np.array_equal(C, oracle.gemm(A, B))
+    A, B, _, _ = operands(M, N, K, 3402, "normal", "f32")
+    call = DeviceCall("f32", A, B, ldc=N + 1)  # scalar atomic adds
+    C = call.run(mhr).result()
+    Cref, S = oracle.gemm(A, B, with_abs=True)
+    assert normalised_error(C, Cref, S) <= TOL["f32"]
+    assert np.array_equal(call.run(mhr).result(), C)
