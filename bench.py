@@ -24,6 +24,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -77,16 +78,24 @@ KERNEL_SOURCES = {  # the files whose text determines each kernel
 }
 
 
+def _code_only(text: str) -> str:
+    """C++/CUDA source with comments removed and whitespace collapsed."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def source_digest(kernel: str | None = None) -> str:
-    """Hash of a kernel's source files (all sources if kernel is None), to
-    tell whether stored ncu counters still apply."""
+    """Hash of the code (comments and layout ignored) of a kernel's source
+    files (all sources if kernel is None), to tell whether stored ncu counters
+    still apply."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "memory_hierarchy_reuse_gb300", "csrc")
     base = kernel.split("<")[0] if kernel else None
     files = KERNEL_SOURCES.get(base) if base else None
     for f in sorted(files or os.listdir(csrc)):
         h.update(f.encode())
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        h.update(_code_only(open(os.path.join(csrc, f), encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -23,11 +23,13 @@ uint64_t gemm_testing_set_wait_limit_ns(uint64_t limit_ns);
 
 /*
  * When `enable` is nonzero, the next tensor-core launches run with an
- * injected stall: block 0 arms its first ring stage for a TMA load but never
- * issues the load, so that stage never fills.  Its consumers' waits then run
- * out, the kernel records MHR_ERR_TIMEOUT in the device status word, frees
- * its TMEM and exits; gemm_check() reports the timeout.  No GPU fault occurs
- * and the CUDA context stays usable.  Returns the previous setting.
+ * injected stall: block 0 leaves its first ring stage incomplete (the TMA
+ * producer arms it for a load it never issues; the on-chip split's converter
+ * warps fill it without arriving), so that stage never fills.  Its consumers'
+ * waits then run out, the kernel records MHR_ERR_TIMEOUT in the device status
+ * word, frees its TMEM and exits; gemm_check() reports the timeout.  No GPU
+ * fault occurs and the CUDA context stays usable.  Returns the previous
+ * setting.
  */
 int gemm_testing_set_inject_stall(int enable);
 

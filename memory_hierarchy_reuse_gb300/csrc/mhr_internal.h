@@ -13,7 +13,7 @@ namespace mhr {
 struct DeviceCtl {
   uint32_t* status = nullptr;          // device address of the status word
   uint64_t wait_limit_ns = 2000000000ull;
-  int inject_stall = 0;                // test hook: block 0 arms one TMA stage and never loads it
+  int inject_stall = 0;                // test hook: block 0 leaves its first ring stage incomplete
   int sm_count = 0;
   int pair_mode = 0;                   // 0 auto, 1 single-CTA kernel, 2 CTA-pair kernel (test hook)
   int raster_group = 0;                // tile rows per raster group, 0 = default (tuning hook)

@@ -27,8 +27,11 @@
 //   warp 0     TMA producer (lane 0 issues)
 //   warp 1     TMEM allocator + MMA issuer (lane 0 issues)
 //   warps 2-5  epilogue; warp w reads TMEM lanes 32*(w%4) .. 32*(w%4)+31
+//   (KIND_3XTF32_SPLIT adds warps 6-13 as converters; its warp 0 idles)
 // The accumulator is double-buffered in TMEM so the epilogue of tile i runs
-// while the MMAs of tile i+1 are issued.
+// while the MMAs of tile i+1 are issued.  The kernels are launched with
+// programmatic stream serialisation: their set-up overlaps the kernel before
+// them, and griddepcontrol.wait precedes every access to inputs or C.
 //
 // Three kinds:
 //   KIND_BF16:   A bf16 K-major (row-major M x K), B bf16 MN-major (row-major

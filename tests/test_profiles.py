@@ -33,3 +33,14 @@ def test_summaries_state_their_commands():
 def test_profiles_hold_only_text():
     for f in os.listdir(PROFILES):
         assert f.endswith((".md", ".txt", ".json")), f
+
+
+def test_source_digest_ignores_comments_and_layout():
+    """Stored counters stay valid across comment-only edits of a kernel's
+    sources, and become stale on any change to its code."""
+    import bench
+
+    code = "int f(int x) {\n  return x + 1;  // one more\n}\n/* block\n comment */\n"
+    assert bench._code_only(code) == "int f(int x) { return x + 1; }"
+    assert bench._code_only(code.replace("// one more", "// two more")) == bench._code_only(code)
+    assert bench._code_only(code.replace("x + 1", "x + 2")) != bench._code_only(code)
