@@ -656,6 +656,13 @@ def main():
                "sample": f"rows 0..{rows - 1} of C ({rows} x {N} outputs, K={K}), "
                          f"{t_cpu:.1f} s of CPU work",
                "gpu_vs_sample_normalised_error": nerr}
+        if args.workload in ("c1", "c2"):
+            # the same oracle on one core, on a smaller sample (about 3 s)
+            rows1 = max(1, min(M, int(rows * 3.0 / max(t_cpu * oracle.max_threads(), 1e-6))))
+            _, t1 = oracle_rows(A_h, B_h, rows1, nthreads=1)
+            cpu["single_core"] = {"value": 2.0 * rows1 * N * K / t1 / 1e12, "unit": "TFLOPS",
+                                  "cores": 1,
+                                  "sample": f"rows 0..{rows1 - 1} of C, {t1:.1f} s on one core"}
 
     # the pages' tiling on the host caches: a realistic CPU comparator (full problem)
     cpu_tiled_line = None

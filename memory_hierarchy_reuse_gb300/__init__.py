@@ -240,3 +240,7 @@ def matmul(a, b, path: str = "f32", out=None, stream=None, lda=None, ldb=None, l
     if rc != MHR_OK:
         raise GemmError(rc, _ENTRY[path])
     return out
+
+
+# The same call under the name the C ABI's family uses: gemm(a, b, path).
+gemm = matmul
