@@ -72,3 +72,50 @@ def test_maximum_dimension(mhr, case, dim):
         mhr.gemm_release()
         del c
         torch.cuda.empty_cache()
+
+
+def _int_bf16(torch, n, seed):
+    """The same integers as _int_vector, stored as bf16 (exact)."""
+    out = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    chunk = 1 << 27
+    for s in range(0, n, chunk):
+        i = torch.arange(s, min(s + chunk, n), dtype=torch.int64, device="cuda")
+        out[s:s + i.numel()] = (((i * 2654435761 + seed) >> 7) % 5 - 2).to(torch.bfloat16)
+    return out
+
+
+@pytest.mark.parametrize("dim", ["M", "N"])
+def test_maximum_dimension_bf16(mhr, dim):
+    """bf16 on the tensor cores at the largest M (A: M x 8, 32 GiB) or N
+    (B: 8 x N, 32 GiB), K = 8 so that the long operand's rows are 16-byte
+    aligned for TMA; C in fp32 with a guard band."""
+    import torch
+
+    torch.cuda.empty_cache()
+    n, k = KMAX, 8
+    try:
+        long_mat = _int_bf16(torch, n * k, 13)                  # A (n x 8) or B (8 x n)
+        short = _int_bf16(torch, k, 17)                          # B (8 x 1) or A (1 x 8)
+        c = torch.full((n + GUARD,), float("nan"), device="cuda")
+        if dim == "M":
+            args = (long_mat.data_ptr(), short.data_ptr(), c.data_ptr(), n, 1, k, k, 1, 1)
+        else:
+            args = (short.data_ptr(), long_mat.data_ptr(), c.data_ptr(), 1, n, k, k, n, n)
+        assert mhr.gemm_bf16_f32acc(*args, None) == mhr.MHR_OK
+        assert mhr.gemm_check(None) == mhr.MHR_OK
+        label = mhr.gemm_testing_last_main_kernel()
+        rows = _samples(n)
+        idx = torch.from_numpy(rows).cuda()
+        got = c[idx].cpu().numpy()
+        s = short.float().cpu().numpy()
+        if dim == "M":
+            a = long_mat.view(n, k)[idx].float().cpu().numpy()
+            ref = oracle.gemm(a, s.reshape(k, 1)).reshape(-1)
+        else:
+            b = long_mat.view(k, n)[:, idx].float().cpu().numpy()
+            ref = oracle.gemm(s.reshape(1, k), np.ascontiguousarray(b)).reshape(-1)
+        assert np.array_equal(got, ref), (dim, label)
+        assert torch.isnan(c[n:]).all()
+    finally:
+        mhr.gemm_release()
+        torch.cuda.empty_cache()
