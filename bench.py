@@ -256,20 +256,27 @@ def host_operands(w):
     return A, B, None, None
 
 
-def cublas_reference(path, M, N, K, dev, stream, achieved):
+def cublas_reference(path, M, N, K, dev, stream, achieved, steps, flush, dist):
     """cuBLAS (through torch) on the same shape in the same run, for context:
     tf32 for the 3xTF32 path (one tf32 pass); for the bf16 path bf16 inputs
     with fp32 output, the same operation as ours (torch.mm with
-    out_dtype=float32), or bf16 output where that is not available. Best of 10
-    launches, L2 not flushed. Not a roofline denominator: the recipe's peak is."""
+    out_dtype=float32), or bf16 output where that is not available.  Timed
+    like our main kernel: `steps` calls, the L2 flushed before each, the mean
+    of per-call CUDA events, on inputs drawn like the workload's (the tensor
+    cores' power, and so the clock under the power cap, depends on the
+    values).  Not a roofline denominator: the recipe's peak is."""
     import torch
 
     old = torch.backends.cuda.matmul.allow_tf32
     torch.backends.cuda.matmul.allow_tf32 = True
     try:
         dt = torch.bfloat16 if path == "bf16" else torch.float32
-        a = torch.randn(M, K, device=dev).to(dt)
-        b = torch.randn(K, N, device=dev).to(dt)
+        if dist == "uniform":
+            a = (torch.rand(M, K, device=dev) * 2 - 1).to(dt)
+            b = (torch.rand(K, N, device=dev) * 2 - 1).to(dt)
+        else:
+            a = torch.randn(M, K, device=dev).to(dt)
+            b = torch.randn(K, N, device=dev).to(dt)
         kind = "tf32"
         fn = lambda: torch.matmul(a, b)  # noqa: E731
         if path == "bf16":
@@ -282,16 +289,19 @@ def cublas_reference(path, M, N, K, dev, stream, achieved):
                 pass
         for _ in range(3):
             fn()
-        best = float("inf")
-        for _ in range(10):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        torch.cuda.synchronize(dev)
+        for e0, e1 in ev:
+            flush.zero_()
             e0.record(stream)
             fn()
             e1.record(stream)
-            e1.synchronize()
-            best = min(best, e0.elapsed_time(e1))
-        tflops = 2.0 * M * N * K / (best * 1e-3) / 1e12
-        return {"kind": kind, "tflops": tflops, "frac": achieved / tflops}
+        torch.cuda.synchronize(dev)
+        ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / steps
+        tflops = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+        return {"kind": kind, "tflops": tflops, "frac": achieved / tflops,
+                "timing": f"mean of {steps} calls, L2 flushed before each, {dist} inputs"}
     finally:
         torch.backends.cuda.matmul.allow_tf32 = old
 
@@ -635,7 +645,8 @@ def main():
                                  "a pre-pass and the main kernel would serialise them)",
                 "peak_source": f"{pk['source']} ({peak_note})"}
     if path in ("3xtf32", "bf16"):
-        roofline["cublas_same_run"] = cublas_reference(path, M, N, K, dev, stream, achieved)
+        roofline["cublas_same_run"] = cublas_reference(path, M, N, K, dev, stream, achieved,
+                                                       args.steps, flush, w["dist"])
         # The nominal tf32 rate corresponds to a lower clock than this kernel
         # sustains, so also give the dense rate per SM per clock at the SM
         # clock sampled during the timed region.
