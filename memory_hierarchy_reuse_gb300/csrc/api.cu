@@ -288,7 +288,7 @@ MHR_API int gemm_f32_3xtf32(const float* A, const float* B, float* C, int64_t M,
   if ((rc = device_state(&st, &dev)) != MHR_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (K == 0) return from_cuda(launch_zero_fill(C, M, N, ldc, s));
-  const bool c_tma = aligned16(C) && (ldc % 4) == 0;
+  const bool c_tma = c_tma_eligible(C, N, ldc);
   const DeviceCtl ctl = make_ctl(*st);
   // Split operands: a_big, a_small (M x Kp), bt_big, bt_small (N x Kp), in
   // the workspace.  Without one (split mode 2, or no memory for it) the
@@ -358,7 +358,7 @@ MHR_API int gemm_bf16_f32acc(const uint16_t* A, const uint16_t* B, float* C, int
       ldb = ldb_p;
     }
   }
-  const bool c_tma = aligned16(C) && (ldc % 4) == 0;
+  const bool c_tma = c_tma_eligible(C, N, ldc);
   MainKernelEvents ev(s);
   return from_cuda(launch_tc_bf16(A, B, C, M, N, K, lda, ldb, ldc, c_tma, make_ctl(*st), s));
 }

@@ -65,6 +65,14 @@ cudaError_t launch_tc_3xtf32_split(const float* A, const float* B, float* C, int
 // the single-CTA kernel).
 bool tc_pair_chosen(int64_t M, int64_t N, int64_t K, const DeviceCtl& ctl);
 
+// Whether C can be written with TMA stores: 16-byte aligned base and pitch,
+// and N a multiple of 4.  A TMA store clips a box at the tensor's inner extent
+// only in 16-byte units, so with N % 4 != 0 it would also write the columns
+// of C's padding up to the next multiple of 4 (measured on GB300).
+inline bool c_tma_eligible(const float* C, int64_t N, int64_t ldc) {
+  return (reinterpret_cast<uintptr_t>(C) & 15u) == 0 && ldc % 4 == 0 && N % 4 == 0;
+}
+
 // Tensor-map encoding through the driver entry point (no libcuda link).
 CUresult encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                         uint64_t inner, uint64_t outer, uint64_t row_pitch_bytes,

@@ -99,7 +99,7 @@ MHR_API int gemm_f32_3xtf32_noalloc(const float* A, const float* B, float* C, in
     float* bt_small = bt_big + N * Kp;
     e = launch_split_tf32(A, B, M, N, K, lda, ldb, Kp, a_big, a_small, bt_big, bt_small, s);
     if (e == cudaSuccess) {
-      const bool c_tma = (reinterpret_cast<uintptr_t>(C) & 15u) == 0 && (ldc % 4) == 0;
+      const bool c_tma = c_tma_eligible(C, N, ldc);
       e = launch_tc_3xtf32(a_big, a_small, bt_big, bt_small, C, M, N, K, Kp, ldc, c_tma, ctl, s);
     }
   }

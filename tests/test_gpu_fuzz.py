@@ -1,0 +1,53 @@
+"""Seeded random sweep of every path variant against the oracle (GB300 only).
+
+Sixty cases, each drawing a path variant (SIMT fp32; 3xTF32 on the single-CTA
+kernel, on the CTA-pair kernel with the split pre-pass, and with the split on
+chip; bf16 on either kernel), a shape with each of M, N, K in 1..700, padded
+leading dimensions (0 to 9 extra elements), an element offset that breaks
+16-byte alignment or not, and integer or real inputs. Integer inputs must
+match the oracle bit for bit, real ones within the path's tolerance; the
+padding of C must keep its guard value (checked by DeviceCall.result)."""
+import numpy as np
+import pytest
+
+import oracle
+from parity_util import TOL, DeviceCall, normalised_error, operands
+
+pytestmark = pytest.mark.gpu
+
+# (path, CTA-pair mode, split mode)
+VARIANTS = [("f32", 0, 0), ("3xtf32", 1, 1), ("3xtf32", 2, 1), ("3xtf32", 2, 2), ("bf16", 1, 0),
+            ("bf16", 2, 0)]
+
+
+def cases(n=60, seed=20261202):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        v = VARIANTS[i % len(VARIANTS)]
+        M, N, K = (int(x) for x in rng.integers(1, 701, 3))
+        pads = [int(x) for x in rng.integers(0, 10, 3)]
+        offset = int(rng.integers(0, 2))
+        dist = "int" if rng.random() < 0.4 else ("normal" if rng.random() < 0.5 else "uniform")
+        out.append((v, M, N, K, pads, offset, dist, 9000 + i))
+    return out
+
+
+@pytest.mark.parametrize("case", cases(), ids=lambda c: f"{c[0][0]}-{c[0][1]}{c[0][2]}-"
+                         f"{c[1]}x{c[2]}x{c[3]}-{c[6]}")
+def test_random_case(mhr, case):
+    (path, pair_mode, split_mode), M, N, K, pads, offset, dist, seed = case
+    A, B, Ab, Bb = operands(M, N, K, seed, dist, path)
+    old_pair = mhr.gemm_testing_set_cta_pair_mode(pair_mode)
+    old_split = mhr.gemm_testing_set_split_mode(split_mode)
+    try:
+        C = DeviceCall(path, A, B, Ab, Bb, lda=K + pads[0], ldb=N + pads[1], ldc=N + pads[2],
+                       offset=offset).run(mhr).result()
+    finally:
+        mhr.gemm_testing_set_split_mode(old_split)
+        mhr.gemm_testing_set_cta_pair_mode(old_pair)
+    if dist == "int":
+        assert np.array_equal(C, oracle.gemm(A, B)), case
+    else:
+        Cref, S = oracle.gemm(A, B, with_abs=True)
+        assert normalised_error(C, Cref, S) <= TOL[path], case

@@ -327,3 +327,29 @@ def test_simt_split_k(mhr):
     Cref, S = oracle.gemm(A, B, with_abs=True)
     assert normalised_error(C, Cref, S) <= TOL["f32"]
     assert np.array_equal(call.run(mhr).result(), C)
+
+
+@pytest.mark.parametrize("N", [182, 195, 1], ids=lambda n: f"N{n}")
+def test_ragged_n_with_tma_aligned_c(mhr, path, N):
+    """C 16-byte aligned with ldc % 4 == 0 but N % 4 != 0: C's padding columns
+    must keep their guard values (a TMA store clips only in 16-byte units, so
+    such C must not be written with TMA stores). Found by the random sweep."""
+    ldc = (N + 3) // 4 * 4 + 4
+    check_full(mhr, path, 300, N, 150, seed=3501 + N, ldc=ldc)
+    check_full(mhr, path, 97, N, 1000, seed=3601 + N, dist="int", ldc=ldc)
+
+
+@pytest.mark.parametrize("shape", [(130, 264, 77), (257, 90, 200), (40, 45, 13)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_bf16_tma_operands_with_ragged_extents(mhr, shape):
+    """bf16 operands whose pitches are TMA-aligned (lda, ldb multiples of 8)
+    while K or N is not a multiple of 8, with NaN in every padding element: the
+    TMA loads must stop at the logical extent (a NaN read would poison C)."""
+    M, N, K = shape
+    for mode in (1, 2):
+        old = mhr.gemm_testing_set_cta_pair_mode(mode)
+        try:
+            check_full(mhr, "bf16", M, N, K, seed=3701 + K, lda=(K + 7) // 8 * 8,
+                       ldb=(N + 7) // 8 * 8 + 8)
+        finally:
+            mhr.gemm_testing_set_cta_pair_mode(old)
