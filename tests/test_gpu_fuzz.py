@@ -1,6 +1,7 @@
 """Seeded random sweep of every path variant against the oracle (GB300 only).
 
-Sixty cases, each drawing a path variant (SIMT fp32; 3xTF32 on the single-CTA
+Sixty cases with dimensions anywhere in 1..700, and sixty with every
+dimension at or next to a tile boundary (1, 8, 16, ..., 512, each +-1), each drawing a path variant (SIMT fp32; 3xTF32 on the single-CTA
 kernel, on the CTA-pair kernel with the split pre-pass, and with the split on
 chip; bf16 on either kernel), a shape with each of M, N, K in 1..700, padded
 leading dimensions (0 to 9 extra elements), an element offset that breaks
@@ -33,8 +34,23 @@ def cases(n=60, seed=20261202):
     return out
 
 
-@pytest.mark.parametrize("case", cases(), ids=lambda c: f"{c[0][0]}-{c[0][1]}{c[0][2]}-"
-                         f"{c[1]}x{c[2]}x{c[3]}-{c[6]}")
+EDGES = [1, 2, 3, 7, 8, 9, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 255, 256, 257,
+         511, 512, 513]
+
+
+def edge_cases(n=60, seed=20261203):
+    """Shapes whose every dimension sits at or next to a tile, box or K-step
+    boundary."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for v, M, N, K, pads, offset, dist, s in cases(n, seed):
+        M, N, K = (EDGES[int(x)] for x in rng.integers(0, len(EDGES), 3))
+        out.append((v, M, N, K, pads, offset, dist, s + 1000))
+    return out
+
+
+@pytest.mark.parametrize("case", cases() + edge_cases(),
+                         ids=lambda c: f"{c[0][0]}-{c[0][1]}{c[0][2]}-{c[1]}x{c[2]}x{c[3]}-{c[6]}")
 def test_random_case(mhr, case):
     (path, pair_mode, split_mode), M, N, K, pads, offset, dist, seed = case
     A, B, Ab, Bb = operands(M, N, K, seed, dist, path)
