@@ -92,8 +92,9 @@ const char* gemm_testing_last_main_kernel(void);
 /*
  * Profiling hook.  When `start` and `stop` are both non-NULL cudaEvent_t
  * handles, every following gemm_* call records `start` on its stream just
- * before it launches its main GEMM kernel (after any split or pack pre-pass)
- * and `stop` just after, so the caller can time that kernel alone with
+ * before it launches its main GEMM kernel (after any split or pack pre-pass
+ * and any kernel zeroing C for a K-split schedule) and `stop` just after, so
+ * the caller can time that kernel alone with
  * cudaEventElapsedTime.  Passing NULL for either turns the hook off.  The
  * events stay owned by the caller.
  */

@@ -50,14 +50,22 @@ int g_split_mode = 0;
 uint64_t g_workspace_limit = UINT64_MAX;
 cudaEvent_t g_main_start = nullptr, g_main_stop = nullptr;
 
-// Brackets the main kernel launch with the caller's profiling events, if set.
+// Brackets the main kernel launch with the caller's profiling events, if set:
+// the start event is recorded by note_main_kernel(), right before the launch
+// (after any pre-pass or zeroing kernel), the stop event when the entry point
+// returns.  Entry points hold g_mu meanwhile.
+cudaStream_t g_events_stream = nullptr;
+bool g_events_armed = false;
 struct MainKernelEvents {
-  cudaStream_t s;
-  explicit MainKernelEvents(cudaStream_t st) : s(st) {
-    if (g_main_start && g_main_stop) cudaEventRecord(g_main_start, s);
+  explicit MainKernelEvents(cudaStream_t st) {
+    if (g_main_start && g_main_stop) {
+      g_events_stream = st;
+      g_events_armed = true;
+    }
   }
   ~MainKernelEvents() {
-    if (g_main_start && g_main_stop) cudaEventRecord(g_main_stop, s);
+    if (g_events_armed) cudaEventRecord(g_main_stop, g_events_stream);
+    g_events_armed = false;
   }
 };
 
@@ -219,6 +227,7 @@ void note_launch() { g_call_launches.fetch_add(1); }
 
 void note_main_kernel(const char* name, int grid, int tiles) {
   note_launch();
+  if (g_events_armed) cudaEventRecord(g_main_start, g_events_stream);
   std::lock_guard<std::mutex> g(g_last_kernel_mu);
   snprintf(g_last_kernel, sizeof(g_last_kernel), "%s grid=%d tiles=%d", name, grid, tiles);
 }
@@ -360,7 +369,8 @@ MHR_API int gemm_bf16_f32acc(const uint16_t* A, const uint16_t* B, float* C, int
   }
   const bool c_tma = c_tma_eligible(C, N, ldc);
   MainKernelEvents ev(s);
-  return from_cuda(launch_tc_bf16(A, B, C, M, N, K, lda, ldb, ldc, c_tma, make_ctl(*st), s));
+  return from_cuda(launch_tc_bf16(A, B, C, M, N, K, lda, ldb, ldc, c_tma, !a_ok || !b_ok,
+                                  make_ctl(*st), s));
 }
 
 MHR_API int gemm_check(void* stream) {

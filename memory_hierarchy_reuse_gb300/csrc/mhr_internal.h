@@ -45,11 +45,14 @@ cudaError_t launch_split_tf32(const float* A, const float* B, int64_t M, int64_t
 // bf16 x bf16 -> fp32 on tcgen05.  A: M x K bf16 (row pitch lda, 16-byte
 // aligned rows), B: K x N bf16 (pitch ldb, aligned).  C via TMA store when
 // c_tma is true (C 16-byte aligned, ldc % 4 == 0), else direct stores.
+// after_prepass: this call launched a pre-pass (repack) just before, in plain
+// stream order (see launch_cta_pair).
 cudaError_t launch_tc_bf16(const uint16_t* A, const uint16_t* B, float* C, int64_t M, int64_t N,
                            int64_t K, int64_t lda, int64_t ldb, int64_t ldc, bool c_tma,
-                           const DeviceCtl& ctl, cudaStream_t s);
+                           bool after_prepass, const DeviceCtl& ctl, cudaStream_t s);
 
-// 3xTF32 main loop over the split operands (pitch Kp floats).
+// 3xTF32 main loop over the split operands (pitch Kp floats), launched right
+// after the split pre-pass that writes them.
 cudaError_t launch_tc_3xtf32(const float* a_big, const float* a_small, const float* bt_big,
                              const float* bt_small, float* C, int64_t M, int64_t N, int64_t K,
                              int64_t Kp, int64_t ldc, bool c_tma, const DeviceCtl& ctl,
@@ -61,9 +64,10 @@ cudaError_t launch_tc_3xtf32_split(const float* A, const float* B, float* C, int
                                    int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                                    bool c_tma, const DeviceCtl& ctl, cudaStream_t s);
 
-// Whether the tensor-core paths run the CTA-pair kernel for this shape (else
-// the single-CTA kernel).
-bool tc_pair_chosen(int64_t M, int64_t N, int64_t K, const DeviceCtl& ctl);
+// Whether the tensor-core path of `kind` (KIND_BF16 or KIND_3XTF32, in
+// tc_common.cuh) runs the CTA-pair kernel for this shape (else the
+// single-CTA kernel).
+bool tc_pair_chosen(int kind, int64_t M, int64_t N, int64_t K, const DeviceCtl& ctl);
 
 // Whether C can be written with TMA stores: 16-byte aligned base and pitch,
 // and N a multiple of 4.  A TMA store clips a box at the tensor's inner extent
@@ -79,7 +83,9 @@ CUresult encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void*
                         uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
 
 // Name of the main kernel the last tensor-core or SIMT launch used, with its
-// grid (for profiling labels; static storage).  Also counts as a launch.
+// grid (for profiling labels; static storage).  Called right before that
+// kernel's launch: counts as a launch, and records the caller's main-kernel
+// start event there when one is set.
 void note_main_kernel(const char* name, int grid, int tiles);
 // Kernel-launch count of the current gemm_* call: reset by begin_call() at
 // the start of every entry point, incremented by each launcher.

@@ -603,29 +603,48 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
 
 // Zero the C tiles of the split work units (pair tiles [full_units,
 // num_tiles)), which both K halves then add into.  Block (x, y) clears rows
-// [8y, 8y + 8) of split tile x.
-__global__ void zero_split_tiles_kernel(TcParams p, int tile_cols) {
+// y * blockDim.y + threadIdx.y + k * gridDim.y * blockDim.y of split tile x,
+// with 16-byte stores when `vec` (C 16-byte aligned, ldc % 4 == 0).
+//
+// Launched either in plain stream order (nothing of the call before it) or as
+// a programmatic dependent of the call's pre-pass, which was itself launched
+// in plain stream order, so everything before the call has finished in both
+// cases and C may be written at once: the zeroing runs alongside the
+// pre-pass.  Each block waits for its predecessor only before exiting, so
+// that this kernel's completion, which the GEMM kernel waits for, implies the
+// pre-pass's.
+__global__ void zero_split_tiles_kernel(TcParams p, int tile_rows, int tile_cols, bool vec) {
   grid_launch_dependents();
-  // Launched as a dependent of the kernel before it (the split pre-pass, or
-  // the previous call's GEMM, which may still read or write C): wait for it,
-  // so that this kernel's completion implies that one's.
-  grid_dependency_wait();
   const int tile = p.full_units + blockIdx.x;
   int tm, tn;
   tile_coords(tile, p, tm, tn);
-  const int64_t row = static_cast<int64_t>(tm) * (8 * gridDim.y) + 8 * blockIdx.y + threadIdx.y;
-  if (row >= p.M) return;
+  const int64_t r0 = static_cast<int64_t>(tm) * tile_rows;
+  const int64_t r_end = r0 + tile_rows < p.M ? r0 + tile_rows : p.M;
   const int64_t c0 = static_cast<int64_t>(tn) * tile_cols;
-  float* crow = p.C + row * p.ldc;
-  for (int c = threadIdx.x; c < tile_cols; c += blockDim.x)
-    if (c0 + c < p.N) crow[c0 + c] = 0.f;
+  const int cols = static_cast<int>(c0 + tile_cols < p.N ? tile_cols : p.N - c0);
+  const int64_t r_step = static_cast<int64_t>(gridDim.y) * blockDim.y;
+  for (int64_t r = r0 + blockIdx.y * blockDim.y + threadIdx.y; r < r_end; r += r_step) {
+    float* crow = p.C + r * p.ldc + c0;
+    if (vec) {
+      for (int c = 4 * threadIdx.x; c < cols; c += 4 * blockDim.x) {
+        if (c + 4 <= cols) {
+          *reinterpret_cast<float4*>(crow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+          for (int j = c; j < cols; ++j) crow[j] = 0.f;
+        }
+      }
+    } else {
+      for (int c = threadIdx.x; c < cols; c += blockDim.x) crow[c] = 0.f;
+    }
+  }
+  grid_dependency_wait();
 }
 
 // Pair kernel launch: clusters of 2 CTAs, persistent over 256 x BN pair
 // tiles, as many clusters as can be co-resident (at most one per pair tile).
 template <int KIND, bool TMA_STORE>
-cudaError_t launch_pair_t(const TcMaps& mp, const TcParams& p, const DeviceCtl& ctl,
-                          cudaStream_t s) {
+cudaError_t launch_pair_t(const TcMaps& mp, const TcParams& p, bool after_prepass,
+                          const DeviceCtl& ctl, cudaStream_t s) {
   auto kern = tc_gemm_pair_kernel<KIND, TMA_STORE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        PairLayout<KIND>::ALLOC);
@@ -659,15 +678,16 @@ cudaError_t launch_pair_t(const TcMaps& mp, const TcParams& p, const DeviceCtl& 
     q.full_units = p.num_tiles - rem;
     q.num_units = q.full_units + 2 * rem;
     q.kb_mid = p.num_kb / 2;
+    const bool vec = (reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 && p.ldc % 4 == 0;
     note_launch();
     cudaLaunchConfig_t zcfg = {};
-    zcfg.gridDim = dim3(rem, 2 * PairCfg<KIND>::BM / 8);
-    zcfg.blockDim = dim3(128, 8);
+    zcfg.gridDim = dim3(rem, 8);
+    zcfg.blockDim = dim3(64, 4);
     zcfg.stream = s;
     zcfg.attrs = &attr[1];
-    zcfg.numAttrs = 1;
-    if ((e = cudaLaunchKernelEx(&zcfg, zero_split_tiles_kernel, q,
-                                static_cast<int>(PairCfg<KIND>::BN))) != cudaSuccess)
+    zcfg.numAttrs = after_prepass ? 1 : 0;  // see zero_split_tiles_kernel
+    if ((e = cudaLaunchKernelEx(&zcfg, zero_split_tiles_kernel, q, 2 * PairCfg<KIND>::BM,
+                                static_cast<int>(PairCfg<KIND>::BN), vec)) != cudaSuccess)
       return e;
   }
   cfg.gridDim = dim3(2 * clusters);
@@ -696,23 +716,23 @@ cudaError_t launch_cta_pair_split(const float* A, const float* B, const CUtensor
   p.vec_a = (reinterpret_cast<uintptr_t>(A) % 16 == 0) && (lda % 4 == 0);
   TcMaps mp;  // only the C map is read (TMA stores); the operand maps are unused
   mp.a0 = mp.a1 = mp.b0 = mp.b1 = mp.c = c_map;
-  return c_tma ? launch_pair_t<KIND_3XTF32_SPLIT, true>(mp, p, ctl, s)
-               : launch_pair_t<KIND_3XTF32_SPLIT, false>(mp, p, ctl, s);
+  return c_tma ? launch_pair_t<KIND_3XTF32_SPLIT, true>(mp, p, false, ctl, s)
+               : launch_pair_t<KIND_3XTF32_SPLIT, false>(mp, p, false, ctl, s);
 }
 
 cudaError_t launch_cta_pair(int kind, const TcMaps& maps, float* C, int64_t M, int64_t N,
-                            int64_t K, int64_t ldc, bool c_tma, const DeviceCtl& ctl,
-                            cudaStream_t s) {
+                            int64_t K, int64_t ldc, bool c_tma, bool after_prepass,
+                            const DeviceCtl& ctl, cudaStream_t s) {
   if (kind == KIND_BF16) {
     const TcParams p = make_params(M, N, K, PAIR_TILE_M, PAIR_TILE_N, PairCfg<KIND_BF16>::BK, C,
                                    ldc, ctl);
-    return c_tma ? launch_pair_t<KIND_BF16, true>(maps, p, ctl, s)
-                 : launch_pair_t<KIND_BF16, false>(maps, p, ctl, s);
+    return c_tma ? launch_pair_t<KIND_BF16, true>(maps, p, after_prepass, ctl, s)
+                 : launch_pair_t<KIND_BF16, false>(maps, p, after_prepass, ctl, s);
   }
   const TcParams p = make_params(M, N, K, PAIR_TILE_M, PAIR_TILE_N, PairCfg<KIND_3XTF32>::BK, C,
                                  ldc, ctl);
-  return c_tma ? launch_pair_t<KIND_3XTF32, true>(maps, p, ctl, s)
-               : launch_pair_t<KIND_3XTF32, false>(maps, p, ctl, s);
+  return c_tma ? launch_pair_t<KIND_3XTF32, true>(maps, p, after_prepass, ctl, s)
+               : launch_pair_t<KIND_3XTF32, false>(maps, p, after_prepass, ctl, s);
 }
 
 }  // namespace tc

@@ -215,14 +215,17 @@ def test_pair_kernel_split_last_round(mhr, path):
     that are reduce-added into C. Build a problem with 3 more pair tiles than
     co-resident clusters, so exactly 3 tiles are split, and compare it in full
     with the oracle, through the TMA reduce path (aligned C) and the atomic
-    path (ldc odd), and for bitwise repeatability."""
+    path (ldc odd), and for bitwise repeatability. With every buffer one
+    element off 16-byte alignment, the pre-pass (the bf16 repacks, or the
+    3xTF32 split with 4-byte loads) runs alongside the kernel zeroing C's
+    split tiles, which then writes 4-byte stores."""
     old = mhr.gemm_testing_set_cta_pair_mode(2)
     try:
         clusters = pair_clusters(mhr, path)
         M, N, K = 256 * (clusters + 3), 256, 320
-        for ldc in (None, N + 1):
+        for ldc, offset in ((None, 0), (N + 1, 0), (None, 1)):
             A, B, Ab, Bb = operands(M, N, K, 3103, "normal", path)
-            call = DeviceCall(path, A, B, Ab, Bb, ldc=ldc)
+            call = DeviceCall(path, A, B, Ab, Bb, ldc=ldc, offset=offset)
             C = call.run(mhr).result()
             assert f"tiles={clusters + 3}" in mhr.gemm_testing_last_main_kernel()
             Cref, S = oracle.gemm(A, B, with_abs=True)
