@@ -195,19 +195,36 @@ __device__ __forceinline__ void stage_and_store_chunk(const uint32_t (&r)[32], u
     }
   } else {
     __syncwarp();
-    const int col = col0 + lane;
+    // Two rows per step, two adjacent columns per lane: lanes 0-15 take row
+    // i, lanes 16-31 row i + 1.  A pair whose address is 8-byte aligned (all
+    // of them when C and ldc are even) goes out as one 8-byte store or atomic
+    // add, else as two 4-byte ones.
+    const int half = lane >> 4;
+    const int cp = (lane & 15) * 2;  // column pair within the chunk
+    const int col = col0 + cp;
 #pragma unroll 4
-    for (int i = 0; i < 32; ++i) {
-      const int row = row0 + i;
-      const uint32_t a = stg + i * 128 + ((((lane >> 2) ^ i) & 7) << 4) + (lane & 3) * 4;
-      float v;
-      asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+    for (int i = 0; i < 32; i += 2) {
+      const int rr = i + half;
+      const int row = row0 + rr;
+      const uint32_t a = stg + rr * 128 + ((((cp >> 2) ^ rr) & 7) << 4) + (cp & 3) * 4;
+      float2 v;
+      asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a) : "memory");
       if (row < p.M && col < p.N) {
         float* dst = p.C + static_cast<int64_t>(row) * p.ldc + col;
-        if (reduce)
-          atomicAdd(dst, v);
-        else
-          *dst = v;
+        if (col + 1 < p.N && (reinterpret_cast<uintptr_t>(dst) & 7u) == 0) {
+          if (reduce)
+            atomicAdd(reinterpret_cast<float2*>(dst), v);
+          else
+            *reinterpret_cast<float2*>(dst) = v;
+        } else {
+          if (reduce) {
+            atomicAdd(dst, v.x);
+            if (col + 1 < p.N) atomicAdd(dst + 1, v.y);
+          } else {
+            dst[0] = v.x;
+            if (col + 1 < p.N) dst[1] = v.y;
+          }
+        }
       }
     }
     __syncwarp();  // the box is free for the next chunk

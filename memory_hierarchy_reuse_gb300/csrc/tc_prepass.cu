@@ -29,15 +29,16 @@ __global__ void pack_u16_kernel(const uint16_t* __restrict__ src, int64_t rows, 
 
 // Split of both operands in one launch.  Blocks [0, a_blocks) split rows of
 // A in place order; the remaining blocks split 64 x 64 tiles of B and write
-// them transposed.  VA / VB select 16-byte loads when the operand's address,
-// leading dimension (and, for A, K) allow them, else 4-byte loads; the
-// outputs (pitch Kp, a multiple of 4, in the 16-byte-aligned workspace) are
-// always written with 16-byte stores.  Each thread keeps several loads in
-// flight.
+// them transposed.  VA selects 16-byte loads of A when its address, leading
+// dimension and K allow them, else 4-byte loads; VB is the width in floats of
+// B's loads, 4, 2 or 1, the widest that B's address, leading dimension and N
+// allow.  The outputs (pitch Kp, a multiple of 4, in the 16-byte-aligned
+// workspace) are always written with 16-byte stores.  Each thread keeps
+// several loads in flight.
 constexpr int SPLIT_THREADS = 256;
 constexpr int SPLIT_TILE = 64;
 
-template <bool VA, bool VB>
+template <bool VA, int VB>
 __global__ void __launch_bounds__(SPLIT_THREADS)
     split_vec_kernel(const float* __restrict__ A, const float* __restrict__ B, int64_t M,
                      int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t Kp, int a_blocks,
@@ -89,7 +90,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS)
   const int64_t nb = gridDim.x - a_blocks;
   for (int64_t tile = blockIdx.x - a_blocks; tile < tiles; tile += nb) {
     const int64_t n0 = (tile % tiles_n) * SPLIT_TILE, k0 = (tile / tiles_n) * SPLIT_TILE;
-    if (VB) {
+    if constexpr (VB == 4) {
       float4 v[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {  // read: 64 k-rows x 16 float4 along n
@@ -106,6 +107,25 @@ __global__ void __launch_bounds__(SPLIT_THREADS)
         split4<true>(v[j], b, s);
         tb[kr][nc] = b.x; tb[kr][nc + 1] = b.y; tb[kr][nc + 2] = b.z; tb[kr][nc + 3] = b.w;
         ts[kr][nc] = s.x; ts[kr][nc + 1] = s.y; ts[kr][nc + 2] = s.z; ts[kr][nc + 3] = s.w;
+      }
+    } else if constexpr (VB == 2) {
+      float2 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {  // read: 64 k-rows x 32 float2 along n
+        const int idx = t + j * SPLIT_THREADS;
+        const int64_t k = k0 + (idx >> 5), n = n0 + (idx & 31) * 2;
+        v[j] = (k < K && n < N) ? __ldg(reinterpret_cast<const float2*>(B + k * ldb + n))
+                                : make_float2(0.f, 0.f);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int idx = t + j * SPLIT_THREADS;
+        const int kr = idx >> 5, nc = (idx & 31) * 2;
+        float b0, s0, b1, s1;
+        split_tf32<false>(v[j].x, b0, s0);
+        split_tf32<false>(v[j].y, b1, s1);
+        tb[kr][nc] = b0; tb[kr][nc + 1] = b1;
+        ts[kr][nc] = s0; ts[kr][nc + 1] = s1;
       }
     } else {
       float v[16];
@@ -168,7 +188,9 @@ cudaError_t launch_split_tf32(const float* A, const float* B, int64_t M, int64_t
   if (Kp % 4 != 0 || !al16(a_big) || !al16(a_small) || !al16(bt_big) || !al16(bt_small))
     return cudaErrorInvalidValue;  // the workspace layout guarantees these
   const bool va = al16(A) && lda % 4 == 0 && K % 4 == 0;
-  const bool vb = al16(B) && ldb % 4 == 0 && N % 4 == 0;
+  const int vb = al16(B) && ldb % 4 == 0 && N % 4 == 0                                   ? 4
+                 : (reinterpret_cast<uintptr_t>(B) & 7u) == 0 && ldb % 2 == 0 && N % 2 == 0 ? 2
+                                                                                          : 1;
   // One wave of resident blocks (6 per SM fit), shared between the operands
   // in proportion to their sizes.
   int dev = 0, sms = 148;
@@ -184,18 +206,14 @@ cudaError_t launch_split_tf32(const float* A, const float* B, int64_t M, int64_t
   const unsigned grid = static_cast<unsigned>(a_blocks + b_blocks);
   const int ab = static_cast<int>(a_blocks);
   note_launch();
-  if (va && vb)
-    split_vec_kernel<true, true><<<grid, SPLIT_THREADS, 0, s>>>(A, B, M, N, K, lda, ldb, Kp, ab,
-                                                                a_big, a_small, bt_big, bt_small);
-  else if (va)
-    split_vec_kernel<true, false><<<grid, SPLIT_THREADS, 0, s>>>(A, B, M, N, K, lda, ldb, Kp, ab,
-                                                                 a_big, a_small, bt_big, bt_small);
-  else if (vb)
-    split_vec_kernel<false, true><<<grid, SPLIT_THREADS, 0, s>>>(A, B, M, N, K, lda, ldb, Kp, ab,
-                                                                 a_big, a_small, bt_big, bt_small);
-  else
-    split_vec_kernel<false, false><<<grid, SPLIT_THREADS, 0, s>>>(A, B, M, N, K, lda, ldb, Kp, ab,
-                                                                  a_big, a_small, bt_big, bt_small);
+  using Kern = void (*)(const float*, const float*, int64_t, int64_t, int64_t, int64_t, int64_t,
+                       int64_t, int, float*, float*, float*, float*);
+  const Kern kerns[2][3] = {{split_vec_kernel<false, 1>, split_vec_kernel<false, 2>,
+                             split_vec_kernel<false, 4>},
+                            {split_vec_kernel<true, 1>, split_vec_kernel<true, 2>,
+                             split_vec_kernel<true, 4>}};
+  kerns[va ? 1 : 0][vb == 4 ? 2 : vb - 1]<<<grid, SPLIT_THREADS, 0, s>>>(
+      A, B, M, N, K, lda, ldb, Kp, ab, a_big, a_small, bt_big, bt_small);
   return cudaGetLastError();
 }
 

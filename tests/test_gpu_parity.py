@@ -39,11 +39,12 @@ def path(request, mhr):
 # (M, N, K): single elements, thin shapes, several tiles with ragged tails in
 # every dimension, and K long enough to wrap every ring several times
 # (bf16: 64-wide K steps x 4 stages, 1-CTA, or 128-wide x 3, pair; tf32: 32-wide x 3;
-# SIMT: 8-wide x 2).
+# SIMT: 8-wide x 2). N = 130 and 1026 (2 mod 4) take the 3xTF32 split's
+# 8-byte loads of B and the epilogue's 8-byte stores of C.
 SMALL_SHAPES = [
     (1, 1, 1), (1, 300, 7), (7, 1, 300), (2, 3, 5), (127, 129, 65), (129, 257, 127),
     (256, 256, 256), (300, 520, 200), (255, 513, 1000), (130, 260, 769), (200, 200, 289),
-    (64, 1100, 33),
+    (64, 1100, 33), (200, 130, 300), (70, 1026, 65),
 ]
 
 
