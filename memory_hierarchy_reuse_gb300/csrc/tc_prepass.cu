@@ -50,6 +50,48 @@ __global__ void __launch_bounds__(SPLIT_THREADS)
   const int t = threadIdx.x;
   if (static_cast<int>(blockIdx.x) < a_blocks) {
     const int64_t k4 = Kp / 4;  // 16-byte chunks of an output row (pad columns get zeros)
+    if (k4 < 4 * SPLIT_THREADS) {
+      // Short rows: a pass covers `rows` whole rows, slot t + 256 j taking
+      // chunk co[j] of row ro[j], so every thread has four loads in flight.
+      const int rows = static_cast<int>((4 * SPLIT_THREADS) / k4);
+      int ro[4], co[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int slot = t + j * SPLIT_THREADS;
+        ro[j] = slot < rows * k4 ? slot / static_cast<int>(k4) : -1;
+        co[j] = slot - ro[j] * static_cast<int>(k4);
+      }
+      for (int64_t r0 = static_cast<int64_t>(blockIdx.x) * rows; r0 < M;
+           r0 += static_cast<int64_t>(a_blocks) * rows) {
+        float4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int64_t r = r0 + ro[j];
+          v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (ro[j] < 0 || r >= M) continue;
+          const float* src = A + r * lda;
+          if (VA) {
+            v[j] = __ldg(reinterpret_cast<const float4*>(src) + co[j]);
+          } else {
+            const int64_t k = 4 * co[j];
+            v[j].x = k < K ? __ldg(src + k) : 0.f;
+            v[j].y = k + 1 < K ? __ldg(src + k + 1) : 0.f;
+            v[j].z = k + 2 < K ? __ldg(src + k + 2) : 0.f;
+            v[j].w = k + 3 < K ? __ldg(src + k + 3) : 0.f;
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int64_t r = r0 + ro[j];
+          if (ro[j] < 0 || r >= M) continue;
+          float4 b, s;
+          split4<VA>(v[j], b, s);
+          reinterpret_cast<float4*>(a_big + r * Kp)[co[j]] = b;
+          reinterpret_cast<float4*>(a_small + r * Kp)[co[j]] = s;
+        }
+      }
+      return;
+    }
     for (int64_t r = blockIdx.x; r < M; r += a_blocks) {
       const float* src = A + r * lda;
       float4* db = reinterpret_cast<float4*>(a_big + r * Kp);
@@ -191,12 +233,26 @@ cudaError_t launch_split_tf32(const float* A, const float* B, int64_t M, int64_t
   const int vb = al16(B) && ldb % 4 == 0 && N % 4 == 0                                   ? 4
                  : (reinterpret_cast<uintptr_t>(B) & 7u) == 0 && ldb % 2 == 0 && N % 2 == 0 ? 2
                                                                                           : 1;
-  // One wave of resident blocks (6 per SM fit), shared between the operands
-  // in proportion to their sizes.
-  int dev = 0, sms = 148;
+  using Kern = void (*)(const float*, const float*, int64_t, int64_t, int64_t, int64_t, int64_t,
+                       int64_t, int, float*, float*, float*, float*);
+  const Kern kerns[2][3] = {{split_vec_kernel<false, 1>, split_vec_kernel<false, 2>,
+                             split_vec_kernel<false, 4>},
+                            {split_vec_kernel<true, 1>, split_vec_kernel<true, 2>,
+                             split_vec_kernel<true, 4>}};
+  const Kern kern = kerns[va ? 1 : 0][vb == 4 ? 2 : vb - 1];
+  // Exactly one wave of resident blocks (registers decide how many fit: 5
+  // per SM at 45 registers a thread, 3 at 70), shared between the operands in
+  // proportion to their sizes.  Every block has an equal share of the work,
+  // so a block left for a second wave would start when the others end and
+  // run with too few loads in flight to keep HBM busy.
+  int dev = 0, sms = 148, per_sm = 0;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t total = static_cast<int64_t>(sms) * 6;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, SPLIT_THREADS, 0) !=
+          cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const int64_t total = static_cast<int64_t>(sms) * per_sm;
   const int64_t b_tiles = ((N + SPLIT_TILE - 1) / SPLIT_TILE) * ((K + SPLIT_TILE - 1) / SPLIT_TILE);
   const double a_share = static_cast<double>(M) / static_cast<double>(M + N);
   int64_t a_blocks = static_cast<int64_t>(a_share * total);
@@ -206,14 +262,8 @@ cudaError_t launch_split_tf32(const float* A, const float* B, int64_t M, int64_t
   const unsigned grid = static_cast<unsigned>(a_blocks + b_blocks);
   const int ab = static_cast<int>(a_blocks);
   note_launch();
-  using Kern = void (*)(const float*, const float*, int64_t, int64_t, int64_t, int64_t, int64_t,
-                       int64_t, int, float*, float*, float*, float*);
-  const Kern kerns[2][3] = {{split_vec_kernel<false, 1>, split_vec_kernel<false, 2>,
-                             split_vec_kernel<false, 4>},
-                            {split_vec_kernel<true, 1>, split_vec_kernel<true, 2>,
-                             split_vec_kernel<true, 4>}};
-  kerns[va ? 1 : 0][vb == 4 ? 2 : vb - 1]<<<grid, SPLIT_THREADS, 0, s>>>(
-      A, B, M, N, K, lda, ldb, Kp, ab, a_big, a_small, bt_big, bt_small);
+  kern<<<grid, SPLIT_THREADS, 0, s>>>(A, B, M, N, K, lda, ldb, Kp, ab, a_big, a_small, bt_big,
+                                      bt_small);
   return cudaGetLastError();
 }
 
