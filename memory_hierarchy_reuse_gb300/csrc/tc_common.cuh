@@ -271,14 +271,18 @@ struct TcMaps {
 
 // tc_gemm_1cta.cu
 cudaError_t launch_single_cta(int kind, const TcMaps& maps, float* C, int64_t M, int64_t N,
-                              int64_t K, int64_t ldc, bool c_tma, const DeviceCtl& ctl,
-                              cudaStream_t s);
+                              int64_t K, int64_t ldc, bool c_tma, bool after_prepass,
+                              const DeviceCtl& ctl, cudaStream_t s);
 // tc_gemm_pair.cu.  after_prepass: the call launched a pre-pass (split or
 // repack) just before this, in plain stream order; a kernel zeroing C for a
 // K-split schedule then runs alongside it as a programmatic dependent.
 cudaError_t launch_cta_pair(int kind, const TcMaps& maps, float* C, int64_t M, int64_t N,
                             int64_t K, int64_t ldc, bool c_tma, bool after_prepass,
                             const DeviceCtl& ctl, cudaStream_t s);
+// Zero the C tiles [q.full_units, q.num_tiles) of tile_rows x tile_cols that
+// a K-split schedule reduce-adds into; after_prepass as for launch_cta_pair.
+cudaError_t launch_zero_split_tiles(const TcParams& q, int tile_rows, int tile_cols,
+                                    bool after_prepass, cudaStream_t s);
 // The CTA-pair kernel with the 3xTF32 split done in the kernel (no workspace):
 // A (M x K, pitch lda) and B (K x N, pitch ldb) row-major fp32.
 cudaError_t launch_cta_pair_split(const float* A, const float* B, const CUtensorMap& c_map,

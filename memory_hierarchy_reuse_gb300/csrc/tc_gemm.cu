@@ -35,7 +35,7 @@ cudaError_t launch_tc_any(int kind, const TcMaps& maps, float* C, int64_t M, int
                           cudaStream_t s) {
   return tc_pair_chosen(kind, M, N, K, ctl)
              ? launch_cta_pair(kind, maps, C, M, N, K, ldc, c_tma, after_prepass, ctl, s)
-             : launch_single_cta(kind, maps, C, M, N, K, ldc, c_tma, ctl, s);
+             : launch_single_cta(kind, maps, C, M, N, K, ldc, c_tma, after_prepass, ctl, s);
 }
 
 CUresult encode_c_map(CUtensorMap* cm, float* C, int64_t M, int64_t N, int64_t ldc, bool c_tma) {

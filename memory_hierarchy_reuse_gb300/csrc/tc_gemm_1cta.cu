@@ -109,11 +109,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t it = 0;
       uint32_t inflight = 0;  // bit s: the latest fill of stage s had a TMA issued
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+        const Unit w = unit_of(u, p);
         int tm, tn;
-        tile_coords(t, p, tm, tn);
+        tile_coords(w.tile, p, tm, tn);
         const int m0 = tm * Cf::BM, n0 = tn * Cf::BN;
-        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
           const uint32_t s = it % Cf::STAGES, ph = (it / Cf::STAGES) & 1u;
           if (!mbar_wait_bounded(empty_bar(s), ph ^ 1u, limit, abort_flag)) {
             give_up_one(p, abort_flag, kErrTimeoutProducer);
@@ -159,7 +160,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       uint32_t it = 0, tcount = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++tcount) {
+      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++tcount) {
+        const Unit w = unit_of(u, p);
         const uint32_t buf = tcount & 1u, aph = (tcount >> 1) & 1u;
         if (!mbar_wait_bounded(acce_bar(buf), aph ^ 1u, limit, abort_flag)) {
           give_up_one(p, abort_flag, kErrTimeoutMma);
@@ -167,7 +169,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_after();  // the epilogue's TMEM reads precede these MMAs' writes
         const uint32_t d_tmem = tmem_base + buf * Cf::BN;
-        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
           const uint32_t s = it % Cf::STAGES, ph = (it / Cf::STAGES) & 1u;
           if (!mbar_wait_bounded(full_bar(s), ph, limit, abort_flag)) {
             give_up_one(p, abort_flag, kErrTimeoutMma);
@@ -183,7 +185,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int kk = 0; kk < Cf::BK / Cf::INSTR_K; ++kk) {
               const uint64_t ad = smem_desc_sw128(st + kk * 32, 16, 1024);
               const uint64_t bd = smem_desc_sw128(st + Cf::A_BYTES + kk * 2048, Cf::B_BOX_BYTES, 1024);
-              mma_f16(d_tmem, ad, bd, Cf::IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+              mma_f16(d_tmem, ad, bd, Cf::IDESC, (kb > w.kb0 || kk > 0) ? 1u : 0u);
             }
           } else {
             // All four operands K-major, 128 B rows (32 floats), 8-row groups
@@ -197,7 +199,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               const uint64_t asd = smem_desc_sw128(a_small + off, 16, 1024);
               const uint64_t bbd = smem_desc_sw128(b_big + off, 16, 1024);
               const uint64_t bsd = smem_desc_sw128(b_small + off, 16, 1024);
-              mma_tf32(d_tmem, asd, bbd, Cf::IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+              mma_tf32(d_tmem, asd, bbd, Cf::IDESC, (kb > w.kb0 || kk > 0) ? 1u : 0u);
               mma_tf32(d_tmem, abd, bsd, Cf::IDESC, 1u);
               mma_tf32(d_tmem, abd, bbd, Cf::IDESC, 1u);
             }
@@ -218,7 +220,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int q = warp & 3;           // TMEM lane quarter this warp may access
     const int ew = warp - 2;          // epilogue warp index 0..3
     uint32_t tcount = 0, chunk = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++tcount) {
+    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++tcount) {
+      const Unit w = unit_of(u, p);
       const uint32_t buf = tcount & 1u, aph = (tcount >> 1) & 1u;
       if (!warp_wait(accf_bar(buf), aph, limit, abort_flag, 128)) {
         give_up(p, abort_flag, kErrTimeoutEpilogue, lane);
@@ -226,7 +229,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       tc_fence_after();
       int tm, tn;
-      tile_coords(t, p, tm, tn);
+      tile_coords(w.tile, p, tm, tn);
       const int m0 = tm * Cf::BM, n0 = tn * Cf::BN;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * Cf::BN;
 #pragma unroll 1
@@ -235,7 +238,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tmem_ld_32cols(taddr + c * 32, r);
         tmem_ld_wait();
         stage_and_store_chunk<TMA_STORE>(r, sbase + L::EPI_OFF, ew, chunk, lane, &tmC, p,
-                                         m0 + q * 32, n0 + c * 32, false);
+                                         m0 + q * 32, n0 + c * 32, w.reduce);
         ++chunk;
       }
       tc_fence_before();
@@ -265,10 +268,28 @@ cudaError_t prepare_kernel() {
 
 template <int KIND>
 cudaError_t launch_t(const TcMaps& mp, float* C, int64_t M, int64_t N, int64_t K, int64_t ldc,
-                     bool c_tma, const DeviceCtl& ctl, cudaStream_t s) {
+                     bool c_tma, bool after_prepass, const DeviceCtl& ctl, cudaStream_t s) {
   using Cf = Cfg<KIND>;
-  const TcParams p = make_params(M, N, K, Cf::BM, Cf::BN, Cf::BK, C, ldc, ctl);
-  const int grid = p.num_tiles < ctl.sm_count ? p.num_tiles : ctl.sm_count;
+  TcParams p = make_params(M, N, K, Cf::BM, Cf::BN, Cf::BK, C, ldc, ctl);
+  cudaError_t e;
+  // Few tiles (all of them, halved, fit on the SMs at once): split every tile
+  // into two half-K units that reduce-add into C, zeroed first, so that twice
+  // as many SMs share the work.  Two addends onto zero give the same sum in
+  // either order: results stay bit-reproducible.  The zeroing runs alongside
+  // a pre-pass when there is one; without, it is a launch of its own, which
+  // only pays for itself with a long K loop.  GB300, whole calls, 1-CTA:
+  // 3xTF32 1024 x 1024 x 4096 95.9 -> 63.1 us, 512 x 512 x 8192 163.5 ->
+  // 94.9, 1024^3 31.4 -> 24.2, 256^3 15.0 -> 14.0; bf16 1024 x 1024 x 4096
+  // (64 K-steps) 31.4 -> 23.2, 1024^3 (16) 15.0 either way, 256^3 (4) 10.9
+  // -> 13.0.
+  if (2 * p.num_tiles <= ctl.sm_count && p.num_kb >= (after_prepass ? 4 : 32)) {
+    p.full_units = 0;
+    p.num_units = 2 * p.num_tiles;
+    p.kb_mid = p.num_kb / 2;
+    if ((e = launch_zero_split_tiles(p, Cf::BM, Cf::BN, after_prepass, s)) != cudaSuccess)
+      return e;
+  }
+  const int grid = p.num_units < ctl.sm_count ? p.num_units : ctl.sm_count;
   note_main_kernel(KIND == KIND_BF16 ? "tc_gemm_kernel<bf16>" : "tc_gemm_kernel<3xtf32>", grid,
                    p.num_tiles);
   cudaLaunchAttribute attr[1];
@@ -281,7 +302,6 @@ cudaError_t launch_t(const TcMaps& mp, float* C, int64_t M, int64_t N, int64_t K
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e;
   if (c_tma) {
     if ((e = prepare_kernel<KIND, true>()) != cudaSuccess) return e;
     e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<KIND, true>, mp.a0, mp.a1, mp.b0, mp.b1, mp.c, p);
@@ -296,10 +316,11 @@ cudaError_t launch_t(const TcMaps& mp, float* C, int64_t M, int64_t N, int64_t K
 }  // namespace
 
 cudaError_t launch_single_cta(int kind, const TcMaps& maps, float* C, int64_t M, int64_t N,
-                              int64_t K, int64_t ldc, bool c_tma, const DeviceCtl& ctl,
-                              cudaStream_t s) {
-  return kind == KIND_BF16 ? launch_t<KIND_BF16>(maps, C, M, N, K, ldc, c_tma, ctl, s)
-                           : launch_t<KIND_3XTF32>(maps, C, M, N, K, ldc, c_tma, ctl, s);
+                              int64_t K, int64_t ldc, bool c_tma, bool after_prepass,
+                              const DeviceCtl& ctl, cudaStream_t s) {
+  return kind == KIND_BF16
+             ? launch_t<KIND_BF16>(maps, C, M, N, K, ldc, c_tma, after_prepass, ctl, s)
+             : launch_t<KIND_3XTF32>(maps, C, M, N, K, ldc, c_tma, after_prepass, ctl, s);
 }
 
 }  // namespace tc

@@ -678,16 +678,8 @@ cudaError_t launch_pair_t(const TcMaps& mp, const TcParams& p, bool after_prepas
     q.full_units = p.num_tiles - rem;
     q.num_units = q.full_units + 2 * rem;
     q.kb_mid = p.num_kb / 2;
-    const bool vec = (reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 && p.ldc % 4 == 0;
-    note_launch();
-    cudaLaunchConfig_t zcfg = {};
-    zcfg.gridDim = dim3(rem, 8);
-    zcfg.blockDim = dim3(64, 4);
-    zcfg.stream = s;
-    zcfg.attrs = &attr[1];
-    zcfg.numAttrs = after_prepass ? 1 : 0;  // see zero_split_tiles_kernel
-    if ((e = cudaLaunchKernelEx(&zcfg, zero_split_tiles_kernel, q, 2 * PairCfg<KIND>::BM,
-                                static_cast<int>(PairCfg<KIND>::BN), vec)) != cudaSuccess)
+    if ((e = launch_zero_split_tiles(q, 2 * PairCfg<KIND>::BM, PairCfg<KIND>::BN, after_prepass,
+                                     s)) != cudaSuccess)
       return e;
   }
   cfg.gridDim = dim3(2 * clusters);
@@ -702,6 +694,24 @@ cudaError_t launch_pair_t(const TcMaps& mp, const TcParams& p, bool after_prepas
 }
 
 }  // namespace
+
+cudaError_t launch_zero_split_tiles(const TcParams& q, int tile_rows, int tile_cols,
+                                    bool after_prepass, cudaStream_t s) {
+  const int split = q.num_tiles - q.full_units;
+  if (split <= 0) return cudaSuccess;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(split, 8);
+  cfg.blockDim = dim3(64, 4);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_prepass ? 1 : 0;  // see zero_split_tiles_kernel
+  const bool vec = (reinterpret_cast<uintptr_t>(q.C) & 15u) == 0 && q.ldc % 4 == 0;
+  note_launch();
+  return cudaLaunchKernelEx(&cfg, zero_split_tiles_kernel, q, tile_rows, tile_cols, vec);
+}
 
 cudaError_t launch_cta_pair_split(const float* A, const float* B, const CUtensorMap& c_map,
                                   float* C, int64_t M, int64_t N, int64_t K, int64_t lda,

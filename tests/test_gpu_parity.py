@@ -259,6 +259,41 @@ def test_pair_kernel_schedule_bit_exact(mhr, path, extra):
         mhr.gemm_testing_set_cta_pair_mode(old)
 
 
+@pytest.mark.parametrize("path", ["3xtf32", "bf16"])
+def test_single_cta_k_halves(mhr, path):
+    """The single-CTA kernel splits every tile into two K halves, reduce-added
+    into a zeroed C, when the halves of all tiles fit on the SMs at once (and,
+    without a pre-pass to overlap the zeroing, K has at least 32 steps). Tile
+    counts of half the SM count (split) and one more (not split), a ragged K,
+    integer inputs (bit-exact against the oracle) through the TMA reduce path
+    and the atomic path (ldc odd), and bitwise repeatability on real inputs."""
+    import re
+
+    import torch
+
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tile_n = 256 if path == "bf16" else 128  # single-CTA tiles: 128 x tile_n
+    old = mhr.gemm_testing_set_cta_pair_mode(1)
+    try:
+        for tiles, split in ((sms // 2, True), (sms // 2 + 1, False)):
+            M, N, K = 128 * tiles, tile_n, (32 if path == "bf16" else 8) * 64 + 40
+            for ldc in (None, N + 1):
+                A, B, Ab, Bb = operands(M, N, K, 3112 + tiles, "int", path)
+                C = DeviceCall(path, A, B, Ab, Bb, ldc=ldc).run(mhr).result()
+                label = mhr.gemm_testing_last_main_kernel()
+                grid = int(re.search(r"grid=(\d+)", label).group(1))
+                assert grid == (min(2 * tiles, sms) if split else min(tiles, sms)), label
+                assert np.array_equal(C, oracle.gemm(A, B))
+        A, B, Ab, Bb = operands(128 * (sms // 2), tile_n, 1000, 3113, "normal", path)
+        call = DeviceCall(path, A, B, Ab, Bb)
+        C = call.run(mhr).result()
+        Cref, S = oracle.gemm(A, B, with_abs=True)
+        assert normalised_error(C, Cref, S) <= TOL[path]
+        assert np.array_equal(call.run(mhr).result(), C)
+    finally:
+        mhr.gemm_testing_set_cta_pair_mode(old)
+
+
 @pytest.mark.parametrize("shape", [(300, 520, 1000), (255, 513, 1001), (130, 260, 37),
                                    (512, 512, 4096), (256 * 79, 256, 320)],
                          ids=lambda s: "x".join(map(str, s)))
