@@ -17,7 +17,11 @@
 //     other buffer);
 //   * edge tiles: elements outside the matrix are loaded as zero and outputs
 //     outside it are not stored ("矩阵乘法 tiling", section 六;
-//     "CUDA 编程系列之三", section 7).
+//     "CUDA 编程系列之三", section 7);
+//   * problems with few tiles: a thread-block cluster of up to 8 CTAs shares
+//     each tile, each CTA taking one run of K-steps, and the partial tiles
+//     are summed through distributed shared memory -- the pages' reuse idea
+//     applied to the partial sums, which never travel to global memory.
 //
 // Loads are coalesced where the tile crosses the global-memory boundary (a
 // warp reads consecutive addresses of one row), the A tile is stored
@@ -42,6 +46,37 @@ namespace {
 
 constexpr int BM = 128, BN = 128, BK = 8, NT = 256, APAD = 4;
 constexpr int GROUP_M = 8;  // tile rows swept together (L2 reuse of B column strips)
+// Cluster split: each CTA's partial 128 x 128 tile in shared memory, rows
+// padded by 4 floats.
+constexpr int RLD = BN + 4;
+constexpr int RED_BYTES = BM * RLD * 4;
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// 16-byte load of shared address `addr` in the cluster's CTA `rank`.
+__device__ __forceinline__ float4 ld_peer_v4(uint32_t addr, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(addr), "r"(rank));
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(a)
+               : "memory");
+  return v;
+}
 
 // d = a * b + c on two fp32 lanes packed in 64-bit registers.
 __device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
@@ -65,7 +100,15 @@ __device__ __forceinline__ float2 unpack2(uint64_t v) {
 // and both add their partial sums into C, which the caller has zeroed.  Two
 // addends onto zero give the same fp32 sum in either order, so the result is
 // reproducible bit for bit.
-template <bool VA, bool VB, bool VC>
+//
+// CLUSTER: the kernel is launched in clusters of S CTAs (2, 4 or 8), one
+// cluster per tile; rank r takes the r-th of S equal runs of K-steps (the
+// last runs may be short or empty).  The S partial tiles meet in distributed
+// shared memory: rank r sums rows [r * 128 / S, (r + 1) * 128 / S) of all S
+// partial tiles, in rank order, and stores them.  One fixed order per
+// element: bit-reproducible, with no atomics and no zeroing of C.  Used when
+// the tiles alone would leave most SMs idle.
+template <bool VA, bool VB, bool VC, bool CLUSTER>
 __global__ void __launch_bounds__(NT, 2)
     simt_f32_kernel(const float* __restrict__ A, const float* __restrict__ B,
                     float* __restrict__ C, int64_t M, int64_t N, int64_t K, int64_t lda,
@@ -74,13 +117,24 @@ __global__ void __launch_bounds__(NT, 2)
   __shared__ __align__(16) float Bs[2][BK][BN];
 
   const int tid = threadIdx.x;
-  const int64_t tiles = tiles_m * tiles_n;
-  const bool second_half = k_mid > 0 && static_cast<int64_t>(blockIdx.x) >= tiles;
-  const int64_t k_begin = second_half ? k_mid : 0;
-  const int64_t k_end = k_mid > 0 && !second_half ? k_mid : K;
+  int64_t t, k_begin, k_end;
+  uint32_t crank = 0, csize = 1;
+  if constexpr (CLUSTER) {
+    crank = cluster_rank();
+    csize = cluster_size();
+    t = blockIdx.x / csize;
+    const int64_t per = ((K + BK - 1) / BK + csize - 1) / csize * BK;  // K per rank
+    k_begin = crank * per < K ? crank * per : K;
+    k_end = k_begin + per < K ? k_begin + per : K;
+  } else {
+    const int64_t tiles = tiles_m * tiles_n;
+    const bool second_half = k_mid > 0 && static_cast<int64_t>(blockIdx.x) >= tiles;
+    k_begin = second_half ? k_mid : 0;
+    k_end = k_mid > 0 && !second_half ? k_mid : K;
+    t = second_half ? blockIdx.x - tiles : blockIdx.x;
+  }
   // Grouped raster over a 1-D grid: blocks launched together cover GROUP_M
   // tile rows, column by column.
-  const int64_t t = second_half ? blockIdx.x - tiles : blockIdx.x;
   const int64_t group_size = GROUP_M * tiles_n;
   const int64_t first_m = (t / group_size) * GROUP_M;
   const int64_t gm = tiles_m - first_m < GROUP_M ? tiles_m - first_m : GROUP_M;
@@ -170,31 +224,71 @@ __global__ void __launch_bounds__(NT, 2)
       acc[i][2 * p] = v.x;
       acc[i][2 * p + 1] = v.y;
     }
+  if constexpr (CLUSTER) {
+    extern __shared__ __align__(16) float red[];  // BM x RLD: this rank's partial tile
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int64_t row = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
-    if (row >= M) continue;
-    float* crow = C + row * ldc;
+    for (int i = 0; i < 8; ++i) {
+      const int row = i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4);
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int64_t col = n0 + h * 64 + tx * 4;
-      const float4 v =
-          make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2], acc[i][4 * h + 3]);
+      for (int h = 0; h < 2; ++h)
+        *reinterpret_cast<float4*>(&red[row * RLD + h * 64 + tx * 4]) =
+            make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2], acc[i][4 * h + 3]);
+    }
+    cluster_barrier();  // every rank's partial tile is written
+    const uint32_t red0 = static_cast<uint32_t>(__cvta_generic_to_shared(red));
+    const int rows = BM / static_cast<int>(csize);
+    for (int idx = tid; idx < rows * (BN / 4); idx += NT) {
+      const int r = static_cast<int>(crank) * rows + idx / (BN / 4);
+      const int c = (idx % (BN / 4)) * 4;
+      const uint32_t addr = red0 + static_cast<uint32_t>((r * RLD + c) * 4);
+      float4 v = ld_peer_v4(addr, 0);
+      for (uint32_t q = 1; q < csize; ++q) {
+        const float4 w = ld_peer_v4(addr, q);
+        v.x += w.x;
+        v.y += w.y;
+        v.z += w.z;
+        v.w += w.w;
+      }
+      const int64_t row = m0 + r, col = n0 + c;
+      if (row >= M) continue;
+      float* crow = C + row * ldc;
       if (VC && col + 4 <= N) {
-        if (k_mid > 0)
-          atomicAdd(reinterpret_cast<float4*>(crow + col), v);
-        else
-          *reinterpret_cast<float4*>(crow + col) = v;
+        *reinterpret_cast<float4*>(crow + col) = v;
       } else {
         const float w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          if (col + j < N) {
-            if (k_mid > 0)
-              atomicAdd(crow + col + j, w[j]);
-            else
-              crow[col + j] = w[j];
-          }
+          if (col + j < N) crow[col + j] = w[j];
+      }
+    }
+    cluster_barrier();  // no rank leaves while another still reads its tile
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int64_t row = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
+      if (row >= M) continue;
+      float* crow = C + row * ldc;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t col = n0 + h * 64 + tx * 4;
+        const float4 v =
+            make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2], acc[i][4 * h + 3]);
+        if (VC && col + 4 <= N) {
+          if (k_mid > 0)
+            atomicAdd(reinterpret_cast<float4*>(crow + col), v);
+          else
+            *reinterpret_cast<float4*>(crow + col) = v;
+        } else {
+          const float w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (col + j < N) {
+              if (k_mid > 0)
+                atomicAdd(crow + col + j, w[j]);
+              else
+                crow[col + j] = w[j];
+            }
+        }
       }
     }
   }
@@ -217,17 +311,52 @@ cudaError_t launch_t(const float* A, const float* B, float* C, int64_t M, int64_
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaError_t e;
+  // Few tiles (at most half as many as SMs): a cluster of S CTAs per tile,
+  // the largest S in {8, 4, 2} that keeps one CTA per SM and at least two
+  // K-steps per rank.
+  const int64_t nk = (K + BK - 1) / BK;
+  int cs = 1;
+  if (2 * tiles <= sms)
+    for (int c = 8; c >= 2; c /= 2)
+      if (tiles * c <= sms && nk >= 2 * c) {
+        cs = c;
+        break;
+      }
+  if (cs > 1) {
+    auto kern = simt_f32_kernel<VA, VB, VC, true>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  RED_BYTES)) != cudaSuccess)
+      return e;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(tiles * cs));
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = RED_BYTES;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    note_main_kernel("simt_f32_kernel<cluster-K>", static_cast<int>(tiles * cs),
+                     static_cast<int>(tiles));
+    if ((e = cudaLaunchKernelEx(&cfg, kern, A, B, C, M, N, K, lda, ldb, ldc, tiles_m, tiles_n,
+                                int64_t{0})) != cudaSuccess)
+      return e;
+    return cudaGetLastError();
+  }
   const int64_t whole = (tiles + sms - 1) / sms;
   const int64_t halves = (2 * tiles + sms - 1) / sms;  // in half-block times
   int64_t k_mid = 0;
   if (K >= 2 * 64 * BK && tiles < (int64_t{1} << 30) && halves < 2 * whole * 0.93)
     k_mid = (K / 2 + BK - 1) / BK * BK;
-  cudaError_t e;
   if (k_mid > 0 && (e = launch_zero_fill(C, M, N, ldc, s)) != cudaSuccess) return e;
   const int64_t blocks = k_mid > 0 ? 2 * tiles : tiles;
   note_main_kernel(k_mid > 0 ? "simt_f32_kernel<split-K>" : "simt_f32_kernel",
                    static_cast<int>(blocks), static_cast<int>(tiles));
-  simt_f32_kernel<VA, VB, VC><<<static_cast<unsigned>(blocks), NT, 0, s>>>(
+  simt_f32_kernel<VA, VB, VC, false><<<static_cast<unsigned>(blocks), NT, 0, s>>>(
       A, B, C, M, N, K, lda, ldb, ldc, tiles_m, tiles_n, k_mid);
   return cudaGetLastError();
 }

@@ -368,6 +368,32 @@ def test_simt_split_k(mhr):
     assert np.array_equal(call.run(mhr).result(), C)
 
 
+@pytest.mark.parametrize("shape,grid", [((256, 256, 256), 32), ((300, 520, 200), 120),
+                                        ((129, 257, 100), 24)],
+                         ids=["256-c8", "300x520x200-c8-empty-rank", "129x257x100-c4"])
+def test_simt_cluster_split_k(mhr, shape, grid):
+    """With few tiles the SIMT kernel runs a cluster of 8, 4 or 2 CTAs per
+    tile, each on its own run of K-steps, and sums the partial tiles in
+    distributed shared memory in rank order. 256^3: 4 tiles x 8 ranks of 4
+    K-steps. 300 x 520 x 200: 15 tiles x 8 ranks; 25 K-steps in runs of 4
+    leave rank 6 one step and rank 7 none. 129 x 257 x 100: 6 tiles x 4 ranks,
+    K ragged (100 = 12 x 8 + 4). Integer inputs match the oracle bit for bit;
+    real inputs (and C with an odd pitch: scalar stores) meet the tolerance,
+    bitwise repeatably."""
+    M, N, K = shape
+    A, B, _, _ = operands(M, N, K, 3501 + K, "int", "f32")
+    C = DeviceCall("f32", A, B).run(mhr).result()
+    assert mhr.gemm_testing_last_main_kernel().startswith(
+        f"simt_f32_kernel<cluster-K> grid={grid} ")
+    assert np.array_equal(C, oracle.gemm(A, B))
+    A, B, _, _ = operands(M, N, K, 3502 + K, "normal", "f32")
+    call = DeviceCall("f32", A, B, ldc=N + 1)
+    C = call.run(mhr).result()
+    Cref, S = oracle.gemm(A, B, with_abs=True)
+    assert normalised_error(C, Cref, S) <= TOL["f32"]
+    assert np.array_equal(call.run(mhr).result(), C)
+
+
 @pytest.mark.parametrize("N", [182, 195, 1], ids=lambda n: f"N{n}")
 def test_ragged_n_with_tma_aligned_c(mhr, path, N):
     """C 16-byte aligned with ldc % 4 == 0 but N % 4 != 0: C's padding columns
