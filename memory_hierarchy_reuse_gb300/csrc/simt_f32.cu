@@ -241,14 +241,20 @@ __global__ void __launch_bounds__(NT, 2)
       const int r = static_cast<int>(crank) * rows + idx / (BN / 4);
       const int c = (idx % (BN / 4)) * 4;
       const uint32_t addr = red0 + static_cast<uint32_t>((r * RLD + c) * 4);
-      float4 v = ld_peer_v4(addr, 0);
-      for (uint32_t q = 1; q < csize; ++q) {
-        const float4 w = ld_peer_v4(addr, q);
-        v.x += w.x;
-        v.y += w.y;
-        v.z += w.z;
-        v.w += w.w;
-      }
+      // all loads first (their latencies overlap), then the sum in rank order
+      float4 w[8];
+#pragma unroll
+      for (uint32_t q = 0; q < 8; ++q)
+        if (q < csize) w[q] = ld_peer_v4(addr, q);
+      float4 v = w[0];
+#pragma unroll
+      for (uint32_t q = 1; q < 8; ++q)
+        if (q < csize) {
+          v.x += w[q].x;
+          v.y += w[q].y;
+          v.z += w[q].z;
+          v.w += w[q].w;
+        }
       const int64_t row = m0 + r, col = n0 + c;
       if (row >= M) continue;
       float* crow = C + row * ldc;

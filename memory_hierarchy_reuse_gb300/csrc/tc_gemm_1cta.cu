@@ -35,6 +35,56 @@ struct Cfg<KIND_3XTF32> {
   static constexpr uint32_t TMEM_COLS = 2 * BN;            // 256
 };
 
+// ------------------------------------------------------------------ cluster split
+//
+// Few tiles: the kernel can run as clusters of S CTAs (2, 4 or 8), one
+// cluster per output tile.  Rank r takes the r-th run of ceil(num_kb / S)
+// K-blocks (trailing runs may be short or empty), accumulates it in TMEM as
+// usual, and its epilogue writes the partial 128 x BN fp32 tile into its own
+// shared memory, over the ring, which no longer holds operands once the
+// accumulator is complete.  After a cluster barrier rank r sums rows
+// [r * 128 / S, (r + 1) * 128 / S) of all S partial tiles through distributed
+// shared memory, in rank order, and stores them to C; a second barrier keeps
+// every partial tile alive until the peers have read it.  One fixed order
+// per element: bit-reproducible, with no zeroing of C and no atomics.
+
+__device__ __forceinline__ uint32_t cluster_ctas() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ float4 ld_cluster_v4(uint32_t cluster_addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(cluster_addr)
+               : "memory");
+  return v;
+}
+
+// Work unit u: the persistent schedule's (tile, K range), or with CLUSTER
+// tile u / S and the K-run u % S.
+template <bool CLUSTER>
+__device__ __forceinline__ Unit unit_1cta(int u, const TcParams& p) {
+  if constexpr (CLUSTER) {
+    const int S = static_cast<int>(cluster_ctas());
+    const int per = (p.num_kb + S - 1) / S;
+    Unit w;
+    w.tile = u / S;
+    w.kb0 = min(p.num_kb, (u % S) * per);
+    w.kb1 = min(p.num_kb, w.kb0 + per);
+    w.reduce = false;
+    return w;
+  } else {
+    return unit_of(u, p);
+  }
+}
+
+// Row pitch (floats) of the cluster split's partial tile: BN + 4.
+template <int KIND>
+constexpr int PART_LD = Cfg<KIND>::BN + 4;
+
 template <int KIND>
 struct Layout {
   using C = Cfg<KIND>;
@@ -44,9 +94,11 @@ struct Layout {
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;   // tmem slot, abort flag
   static constexpr int USED = MISC_OFF + 16;
   static constexpr int ALLOC = USED + 1024;                 // slack for 1024-byte alignment
+  // the cluster split's partial tile lives over the ring
+  static_assert(C::BM * PART_LD<KIND> * 4 <= C::STAGES * C::STAGE_BYTES, "partial tile");
 };
 
-template <int KIND, bool TMA_STORE>
+template <int KIND, bool TMA_STORE, bool CLUSTER>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                    const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
@@ -110,7 +162,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t inflight = 0;  // bit s: the latest fill of stage s had a TMA issued
       bool ok = true;
       for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-        const Unit w = unit_of(u, p);
+        const Unit w = unit_1cta<CLUSTER>(u, p);
         int tm, tn;
         tile_coords(w.tile, p, tm, tn);
         const int m0 = tm * Cf::BM, n0 = tn * Cf::BN;
@@ -161,7 +213,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t it = 0, tcount = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++tcount) {
-        const Unit w = unit_of(u, p);
+        const Unit w = unit_1cta<CLUSTER>(u, p);
         const uint32_t buf = tcount & 1u, aph = (tcount >> 1) & 1u;
         if (!mbar_wait_bounded(acce_bar(buf), aph ^ 1u, limit, abort_flag)) {
           give_up_one(p, abort_flag, kErrTimeoutMma);
@@ -221,7 +273,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int ew = warp - 2;          // epilogue warp index 0..3
     uint32_t tcount = 0, chunk = 0;
     for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++tcount) {
-      const Unit w = unit_of(u, p);
+      const Unit w = unit_1cta<CLUSTER>(u, p);
       const uint32_t buf = tcount & 1u, aph = (tcount >> 1) & 1u;
       if (!warp_wait(accf_bar(buf), aph, limit, abort_flag, 128)) {
         give_up(p, abort_flag, kErrTimeoutEpilogue, lane);
@@ -232,14 +284,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tile_coords(w.tile, p, tm, tn);
       const int m0 = tm * Cf::BM, n0 = tn * Cf::BN;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * Cf::BN;
+      if constexpr (CLUSTER) {
+        // this thread's row of the partial tile, into shared memory (a rank
+        // with no K-blocks contributes zeros)
+        const uint32_t prow = sbase + static_cast<uint32_t>((q * 32 + lane) * PART_LD<KIND> * 4);
+        const bool has_k = w.kb1 > w.kb0;
 #pragma unroll 1
-      for (int c = 0; c < Cf::BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_32cols(taddr + c * 32, r);
-        tmem_ld_wait();
-        stage_and_store_chunk<TMA_STORE>(r, sbase + L::EPI_OFF, ew, chunk, lane, &tmC, p,
-                                         m0 + q * 32, n0 + c * 32, w.reduce);
-        ++chunk;
+        for (int c = 0; c < Cf::BN / 32; ++c) {
+          uint32_t r[32];
+          if (has_k) {
+            tmem_ld_32cols(taddr + c * 32, r);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = 0u;
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            st_shared_v4(prow + static_cast<uint32_t>((c * 32 + 4 * j) * 4),
+                         make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                     __uint_as_float(r[4 * j + 2]),
+                                     __uint_as_float(r[4 * j + 3])));
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < Cf::BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32cols(taddr + c * 32, r);
+          tmem_ld_wait();
+          stage_and_store_chunk<TMA_STORE>(r, sbase + L::EPI_OFF, ew, chunk, lane, &tmC, p,
+                                           m0 + q * 32, n0 + c * 32, w.reduce);
+          ++chunk;
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -253,17 +329,94 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (CLUSTER) {
+    cluster_sync_all();  // every rank's partial tile is in its shared memory
+    const int S = static_cast<int>(cluster_ctas());
+    const int rank = static_cast<int>(cluster_ctarank());
+    const int rows = Cf::BM / S;
+    int tm, tn;
+    tile_coords(static_cast<int>(blockIdx.x) / S, p, tm, tn);
+    const int64_t m0 = static_cast<int64_t>(tm) * Cf::BM;
+    const int n0 = tn * Cf::BN;
+    const bool vec = (reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 && (p.ldc & 3) == 0;
+    for (int idx = threadIdx.x; idx < rows * (Cf::BN / 4); idx += NUM_THREADS) {
+      const int r = rank * rows + idx / (Cf::BN / 4);
+      const int c = (idx % (Cf::BN / 4)) * 4;
+      const uint32_t off = sbase + static_cast<uint32_t>((r * PART_LD<KIND> + c) * 4);
+      // all loads first (their latencies overlap), then the sum in rank order
+      float4 t[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (k < S) t[k] = ld_cluster_v4(mapa_shared(off, static_cast<uint32_t>(k)));
+      float4 v = t[0];
+#pragma unroll
+      for (int k = 1; k < 8; ++k)
+        if (k < S) {
+          v.x += t[k].x;
+          v.y += t[k].y;
+          v.z += t[k].z;
+          v.w += t[k].w;
+        }
+      const int64_t row = m0 + r;
+      const int col = n0 + c;
+      if (row >= p.M || col >= p.N) continue;
+      float* dst = p.C + row * p.ldc + col;
+      if (vec && col + 4 <= p.N) {
+        *reinterpret_cast<float4*>(dst) = v;
+      } else {
+        dst[0] = v.x;
+        if (col + 1 < p.N) dst[1] = v.y;
+        if (col + 2 < p.N) dst[2] = v.z;
+        if (col + 3 < p.N) dst[3] = v.w;
+      }
+    }
+    cluster_sync_all();  // no rank leaves while a peer still reads its partial tile
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, Cf::TMEM_COLS);
   }
 }
 
-template <int KIND, bool TMA_STORE>
+template <int KIND, bool TMA_STORE, bool CLUSTER>
 cudaError_t prepare_kernel() {
   // cudaFuncSetAttribute is per device; callers run it on every launch (cheap).
-  return cudaFuncSetAttribute(tc_gemm_kernel<KIND, TMA_STORE>,
+  return cudaFuncSetAttribute(tc_gemm_kernel<KIND, TMA_STORE, CLUSTER>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<KIND>::ALLOC);
+}
+
+// Cluster size for the cluster split of a problem with few tiles: the
+// largest S in {8, 4} with one CTA per SM for all tiles x S CTAs, at least
+// 16 K-blocks per rank, and every cluster co-resident; 1 = no cluster split.
+// Measured on GB300 (whole calls), the split's fixed costs -- the cluster
+// launch, the partial tiles through shared memory, two cluster barriers --
+// pay off only on long K runs: 512 x 512 x 8192 3xTF32 95.9 -> 64.1 us (S =
+// 4, against two K halves), bf16 33.4 -> 21.1 us (S = 8); 1024 x 1024 x 4096
+// bf16 23.2 -> 21.2 us (S = 4); but 256^3 3xTF32 14.0 -> 15.0 us (S = 8, one
+// K-block per rank), bf16 10.9 -> 12.9 us, and S = 2 in place of the K
+// halves 63.1 -> 66.2 us (1024 x 1024 x 4096 3xTF32).
+template <int KIND>
+int cluster_split_size(const TcParams& p, cudaLaunchConfig_t cfg, const DeviceCtl& ctl) {
+  if (2 * p.num_tiles > ctl.sm_count) return 1;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  for (int S = 8; S >= 4; S /= 2) {
+    if (p.num_tiles * S > ctl.sm_count || p.num_kb < 16 * S) continue;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+    cfg.gridDim = dim3(static_cast<unsigned>(p.num_tiles * S));
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, tc_gemm_kernel<KIND, false, true>, &cfg) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      continue;
+    }
+    if (clusters >= p.num_tiles) return S;
+  }
+  return 1;
 }
 
 template <int KIND>
@@ -272,16 +425,44 @@ cudaError_t launch_t(const TcMaps& mp, float* C, int64_t M, int64_t N, int64_t K
   using Cf = Cfg<KIND>;
   TcParams p = make_params(M, N, K, Cf::BM, Cf::BN, Cf::BK, C, ldc, ctl);
   cudaError_t e;
-  // Few tiles (all of them, halved, fit on the SMs at once): split every tile
-  // into two half-K units that reduce-add into C, zeroed first, so that twice
-  // as many SMs share the work.  Two addends onto zero give the same sum in
-  // either order: results stay bit-reproducible.  The zeroing runs alongside
-  // a pre-pass when there is one; without, it is a launch of its own, which
-  // only pays for itself with a long K loop.  GB300, whole calls, 1-CTA:
-  // 3xTF32 1024 x 1024 x 4096 95.9 -> 63.1 us, 512 x 512 x 8192 163.5 ->
-  // 94.9, 1024^3 31.4 -> 24.2, 256^3 15.0 -> 14.0; bf16 1024 x 1024 x 4096
-  // (64 K-steps) 31.4 -> 23.2, 1024^3 (16) 15.0 either way, 256^3 (4) 10.9
-  // -> 13.0.
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = Layout<KIND>::ALLOC;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // Few tiles with long K runs: a cluster of S CTAs per tile, each on one
+  // run of K-blocks, summing through distributed shared memory (see above).
+  if ((e = prepare_kernel<KIND, false, true>()) != cudaSuccess) return e;
+  const int S = cluster_split_size<KIND>(p, cfg, ctl);
+  if (S > 1) {
+    p.num_units = p.num_tiles * S;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(S);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+    cfg.gridDim = dim3(static_cast<unsigned>(p.num_units));
+    note_main_kernel(KIND == KIND_BF16 ? "tc_gemm_kernel<bf16,cluster-K>"
+                                       : "tc_gemm_kernel<3xtf32,cluster-K>",
+                     p.num_units, p.num_tiles);
+    e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<KIND, false, true>, mp.a0, mp.a1, mp.b0, mp.b1,
+                           mp.c, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  }
+  // Otherwise, few tiles (all of them, halved, fit on the SMs at once):
+  // split every tile into two half-K units that reduce-add into C, zeroed
+  // first, so that twice as many SMs share the work.  Two addends onto zero
+  // give the same sum in either order: results stay bit-reproducible.  The
+  // zeroing runs alongside a pre-pass when there is one; without, it is a
+  // launch of its own, which only pays for itself with a long K loop.  GB300,
+  // whole calls: 3xTF32 1024 x 1024 x 4096 95.9 -> 63.1 us, 1024^3 31.4 ->
+  // 24.2, 256^3 15.0 -> 14.0; bf16 1024^3 (16 K-steps) 15.0 either way, 256^3
+  // (4) 10.9 -> 13.0.
   if (2 * p.num_tiles <= ctl.sm_count && p.num_kb >= (after_prepass ? 4 : 32)) {
     p.full_units = 0;
     p.num_units = 2 * p.num_tiles;
@@ -292,22 +473,15 @@ cudaError_t launch_t(const TcMaps& mp, float* C, int64_t M, int64_t N, int64_t K
   const int grid = p.num_units < ctl.sm_count ? p.num_units : ctl.sm_count;
   note_main_kernel(KIND == KIND_BF16 ? "tc_gemm_kernel<bf16>" : "tc_gemm_kernel<3xtf32>", grid,
                    p.num_tiles);
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(NUM_THREADS);
-  cfg.dynamicSmemBytes = Layout<KIND>::ALLOC;
-  cfg.stream = s;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   if (c_tma) {
-    if ((e = prepare_kernel<KIND, true>()) != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<KIND, true>, mp.a0, mp.a1, mp.b0, mp.b1, mp.c, p);
+    if ((e = prepare_kernel<KIND, true, false>()) != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<KIND, true, false>, mp.a0, mp.a1, mp.b0, mp.b1,
+                           mp.c, p);
   } else {
-    if ((e = prepare_kernel<KIND, false>()) != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<KIND, false>, mp.a0, mp.a1, mp.b0, mp.b1, mp.c, p);
+    if ((e = prepare_kernel<KIND, false, false>()) != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<KIND, false, false>, mp.a0, mp.a1, mp.b0, mp.b1,
+                           mp.c, p);
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

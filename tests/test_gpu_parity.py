@@ -260,36 +260,45 @@ def test_pair_kernel_schedule_bit_exact(mhr, path, extra):
 
 
 @pytest.mark.parametrize("path", ["3xtf32", "bf16"])
-def test_single_cta_k_halves(mhr, path):
-    """The single-CTA kernel splits every tile into two K halves, reduce-added
-    into a zeroed C, when the halves of all tiles fit on the SMs at once (and,
-    without a pre-pass to overlap the zeroing, K has at least 32 steps). Tile
-    counts of half the SM count (split) and one more (not split), a ragged K,
-    integer inputs (bit-exact against the oracle) through the TMA reduce path
-    and the atomic path (ldc odd), and bitwise repeatability on real inputs."""
-    import re
-
+def test_single_cta_few_tiles(mhr, path):
+    """Few tiles on the single-CTA kernel. With long K runs (at least 16
+    K-blocks per rank) it runs a cluster of 8 or 4 CTAs per tile, each on one
+    run of K-blocks, and sums the partial tiles through distributed shared
+    memory in rank order. Otherwise, when the halves of all tiles fit on the
+    SMs at once (and, without a pre-pass to overlap the zeroing, K has at
+    least 32 steps), every tile becomes two K halves reduce-added into a
+    zeroed C. Cases: 4 tiles with 129-130 K-blocks (cluster of 8) and 65-66
+    (cluster of 4, ragged runs), half the SM count in tiles (K halves) and one
+    more (no split); K ragged throughout. Integer inputs bit-exact against the
+    oracle through vector and scalar stores (ldc odd), real inputs within
+    tolerance and bitwise repeatable."""
     import torch
 
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     tile_n = 256 if path == "bf16" else 128  # single-CTA tiles: 128 x tile_n
+    bk = 64 if path == "bf16" else 32
+    name = "tc_gemm_kernel<bf16" if path == "bf16" else "tc_gemm_kernel<3xtf32"
     old = mhr.gemm_testing_set_cta_pair_mode(1)
     try:
-        for tiles, split in ((sms // 2, True), (sms // 2 + 1, False)):
-            M, N, K = 128 * tiles, tile_n, (32 if path == "bf16" else 8) * 64 + 40
+        cases = [(4, bk * 128 + 40, f"{name},cluster-K> grid=32 "),
+                 (4, bk * 64 + 40, f"{name},cluster-K> grid=16 "),
+                 (sms // 2, bk * 32 + 40, f"{name}> grid={sms} "),
+                 (sms // 2 + 1, bk * 32 + 40, f"{name}> grid={sms // 2 + 1} ")]
+        for tiles, K, want in cases:
+            M, N = 128 * tiles, tile_n
             for ldc in (None, N + 1):
-                A, B, Ab, Bb = operands(M, N, K, 3112 + tiles, "int", path)
+                A, B, Ab, Bb = operands(M, N, K, 3112 + tiles + K, "int", path)
                 C = DeviceCall(path, A, B, Ab, Bb, ldc=ldc).run(mhr).result()
                 label = mhr.gemm_testing_last_main_kernel()
-                grid = int(re.search(r"grid=(\d+)", label).group(1))
-                assert grid == (min(2 * tiles, sms) if split else min(tiles, sms)), label
+                assert label.startswith(want), (label, want)
                 assert np.array_equal(C, oracle.gemm(A, B))
-        A, B, Ab, Bb = operands(128 * (sms // 2), tile_n, 1000, 3113, "normal", path)
-        call = DeviceCall(path, A, B, Ab, Bb)
-        C = call.run(mhr).result()
-        Cref, S = oracle.gemm(A, B, with_abs=True)
-        assert normalised_error(C, Cref, S) <= TOL[path]
-        assert np.array_equal(call.run(mhr).result(), C)
+        for tiles, K in ((4, bk * 128 + 40), (sms // 2, 1000)):
+            A, B, Ab, Bb = operands(128 * tiles, tile_n, K, 3113 + tiles, "normal", path)
+            call = DeviceCall(path, A, B, Ab, Bb)
+            C = call.run(mhr).result()
+            Cref, S = oracle.gemm(A, B, with_abs=True)
+            assert normalised_error(C, Cref, S) <= TOL[path]
+            assert np.array_equal(call.run(mhr).result(), C)
     finally:
         mhr.gemm_testing_set_cta_pair_mode(old)
 
