@@ -397,7 +397,11 @@ cudaError_t prepare_kernel() {
 // halves 63.1 -> 66.2 us (1024 x 1024 x 4096 3xTF32).
 template <int KIND>
 int cluster_split_size(const TcParams& p, cudaLaunchConfig_t cfg, const DeviceCtl& ctl) {
-  if (2 * p.num_tiles > ctl.sm_count) return 1;
+  if (2 * p.num_tiles > ctl.sm_count || p.num_kb < 16 * 4) return 1;
+  if (prepare_kernel<KIND, false, true>() != cudaSuccess) {
+    cudaGetLastError();
+    return 1;
+  }
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.y = 1;
@@ -436,7 +440,6 @@ cudaError_t launch_t(const TcMaps& mp, float* C, int64_t M, int64_t N, int64_t K
   cfg.numAttrs = 1;
   // Few tiles with long K runs: a cluster of S CTAs per tile, each on one
   // run of K-blocks, summing through distributed shared memory (see above).
-  if ((e = prepare_kernel<KIND, false, true>()) != cudaSuccess) return e;
   const int S = cluster_split_size<KIND>(p, cfg, ctl);
   if (S > 1) {
     p.num_units = p.num_tiles * S;
