@@ -601,6 +601,7 @@ def main():
     if w["also"]:
         also = w["also"]
         call(also)
+        simt_label = lib.gemm_testing_last_main_kernel().decode()
         n_also = max(3, min(args.steps, 50))
         s_ms = timed_steps(also, n_also, kernel_events=False)
         s_k = timed_steps(also, n_also, kernel_events=True)
@@ -612,7 +613,8 @@ def main():
         extra[ENTRY[also]] = {
             "value": aggregate_tflops(world, flop, simt_ms), "unit": "TFLOPS", "ms_per_step": simt_ms,
             "roofline": {"bound": "alu", "achieved": flop / (simt_k * 1e-3) / 1e12,
-                         "traffic": stored_traffic("simt_f32_kernel", args.workload),
+                         "traffic": stored_traffic(simt_label.split(" ")[0], args.workload),
+                         "kernel": simt_label,
                          "peak": fp32_peak, "unit": "TFLOP/s",
                          "frac": flop / (simt_k * 1e-3) / 1e12 / fp32_peak,
                          "peak_note": f"{sms} SMs x {FP32_LANES_PER_SM} fp32 lanes x 2 x "
