@@ -380,22 +380,28 @@ def test_simt_split_k(mhr):
 @pytest.mark.parametrize("shape,label", [
     ((2048, 2560, 1032), "simt_f32_kernel<wide,split-K> grid=320 "),
     ((2048, 4864, 64), "simt_f32_kernel<wide> grid=304 "),
-    ((2048, 4864 + 4, 64), "simt_f32_kernel grid=")],
-    ids=["160-tiles-split", "304-tiles", "ragged-n-standard"])
-def test_simt_wide_tiles(mhr, shape, label):
+    ((2048, 4864 + 4, 64), "simt_f32_kernel grid="),
+    ((2048, 2560, 1032), "simt_f32_kernel<wide,split-K> grid=320 ")],
+    ids=["160-tiles-split", "304-tiles", "ragged-n-standard", "160-tiles-padded-ld"])
+def test_simt_wide_tiles(mhr, shape, label, request):
     """Aligned problems whose sizes are multiples of 128 x 256 x 8 and that
     fill the SMs take the wide-tile SIMT kernel (8 x 16 outputs per thread,
     no masks): 160 tiles with K halves added into a zeroed C (K = 1032), 304
     tiles unsplit; N one vector wider leaves the shape to the masked kernel.
-    Integer inputs bit-exact against the oracle, real inputs within tolerance
-    and bitwise repeatable."""
+    The last case pads every leading dimension by a multiple of 4 with NaN in
+    the pads: a read outside the logical matrices poisons C, a write outside
+    C breaks its guard band. Integer inputs bit-exact against the oracle,
+    real inputs within tolerance and bitwise repeatable."""
     M, N, K = shape
+    lds = {}
+    if request.node.callspec.id.endswith("padded-ld"):
+        lds = dict(lda=K + 4, ldb=N + 8, ldc=N + 4)
     A, B, _, _ = operands(M, N, K, 3601 + K, "int", "f32")
-    C = DeviceCall("f32", A, B).run(mhr).result()
+    C = DeviceCall("f32", A, B, **lds).run(mhr).result()
     assert mhr.gemm_testing_last_main_kernel().startswith(label)
     assert np.array_equal(C, oracle.gemm(A, B))
     A, B, _, _ = operands(M, N, K, 3602 + K, "normal", "f32")
-    call = DeviceCall("f32", A, B)
+    call = DeviceCall("f32", A, B, **lds)
     C = call.run(mhr).result()
     Cref, S = oracle.gemm(A, B, with_abs=True)
     assert normalised_error(C, Cref, S) <= TOL["f32"]
