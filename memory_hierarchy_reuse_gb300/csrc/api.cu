@@ -322,11 +322,15 @@ MHR_API int gemm_f32_3xtf32(const float* A, const float* B, float* C, int64_t M,
   float* a_small = a_big + M * Kp;
   float* bt_big = a_small + M * Kp;
   float* bt_small = bt_big + N * Kp;
-  cudaError_t e = launch_split_tf32(A, B, M, N, K, lda, ldb, Kp, a_big, a_small, bt_big, bt_small, s);
+  // A itself serves as A_big when TMA can read it (the tensor core truncates
+  // it to tf32, which is the split's big part); then only A_small is written.
+  const bool a_raw = a_serves_as_big(A, lda);
+  cudaError_t e = launch_split_tf32(A, B, M, N, K, lda, ldb, Kp, a_raw ? nullptr : a_big, a_small,
+                                    bt_big, bt_small, s);
   if (e != cudaSuccess) return from_cuda(e);
   MainKernelEvents ev(s);
-  return from_cuda(launch_tc_3xtf32(a_big, a_small, bt_big, bt_small, C, M, N, K, Kp, ldc, c_tma,
-                                    ctl, s));
+  return from_cuda(launch_tc_3xtf32(a_raw ? A : a_big, a_raw ? lda : Kp, a_small, bt_big,
+                                    bt_small, C, M, N, K, Kp, ldc, c_tma, ctl, s));
 }
 
 MHR_API int gemm_bf16_f32acc(const uint16_t* A, const uint16_t* B, float* C, int64_t M, int64_t N,

@@ -36,8 +36,10 @@ cudaError_t launch_zero_fill(float* C, int64_t M, int64_t N, int64_t ldc, cudaSt
 cudaError_t launch_pack_u16(const uint16_t* src, int64_t rows, int64_t cols, int64_t src_ld,
                             uint16_t* dst, int64_t dst_ld, cudaStream_t s);
 
-// 3xTF32 split: A (M x K, lda) -> a_big, a_small (M x Kp, K-contiguous);
-// B (K x N, ldb) -> bt_big, bt_small (N x Kp, K-contiguous, i.e. B transposed).
+// 3xTF32 split: A (M x K, lda) -> a_big, a_small (M x Kp, K-contiguous; big
+// truncated to tf32, a_big may be null when A itself serves as A_big);
+// B (K x N, ldb) -> bt_big, bt_small (N x Kp, K-contiguous, i.e. B transposed;
+// big rounded to tf32).
 cudaError_t launch_split_tf32(const float* A, const float* B, int64_t M, int64_t N, int64_t K,
                               int64_t lda, int64_t ldb, int64_t Kp, float* a_big, float* a_small,
                               float* bt_big, float* bt_small, cudaStream_t s);
@@ -51,12 +53,19 @@ cudaError_t launch_tc_bf16(const uint16_t* A, const uint16_t* B, float* C, int64
                            int64_t K, int64_t lda, int64_t ldb, int64_t ldc, bool c_tma,
                            bool after_prepass, const DeviceCtl& ctl, cudaStream_t s);
 
-// 3xTF32 main loop over the split operands (pitch Kp floats), launched right
-// after the split pre-pass that writes them.
-cudaError_t launch_tc_3xtf32(const float* a_big, const float* a_small, const float* bt_big,
-                             const float* bt_small, float* C, int64_t M, int64_t N, int64_t K,
-                             int64_t Kp, int64_t ldc, bool c_tma, const DeviceCtl& ctl,
-                             cudaStream_t s);
+// 3xTF32 main loop over the split operands (pitch Kp floats; a_big with
+// pitch a_big_ld, which is A itself when a_big_ld = lda), launched right after
+// the split pre-pass that writes them.
+cudaError_t launch_tc_3xtf32(const float* a_big, int64_t a_big_ld, const float* a_small,
+                             const float* bt_big, const float* bt_small, float* C, int64_t M,
+                             int64_t N, int64_t K, int64_t Kp, int64_t ldc, bool c_tma,
+                             const DeviceCtl& ctl, cudaStream_t s);
+
+// Whether the 3xTF32 path may read A itself as its big part: TMA needs a
+// 16-byte aligned base and a row pitch that is a multiple of 16 bytes.
+inline bool a_serves_as_big(const float* A, int64_t lda) {
+  return (reinterpret_cast<uintptr_t>(A) & 15u) == 0 && lda % 4 == 0;
+}
 
 // 3xTF32 with the split done inside the CTA-pair kernel: A (M x K, lda) and
 // B (K x N, ldb) row-major fp32, read directly; no workspace.

@@ -97,10 +97,13 @@ MHR_API int gemm_f32_3xtf32_noalloc(const float* A, const float* B, float* C, in
     float* a_small = a_big + M * Kp;
     float* bt_big = a_small + M * Kp;
     float* bt_small = bt_big + N * Kp;
-    e = launch_split_tf32(A, B, M, N, K, lda, ldb, Kp, a_big, a_small, bt_big, bt_small, s);
+    const bool a_raw = a_serves_as_big(A, lda);  // as in gemm_f32_3xtf32
+    e = launch_split_tf32(A, B, M, N, K, lda, ldb, Kp, a_raw ? nullptr : a_big, a_small, bt_big,
+                          bt_small, s);
     if (e == cudaSuccess) {
       const bool c_tma = c_tma_eligible(C, N, ldc);
-      e = launch_tc_3xtf32(a_big, a_small, bt_big, bt_small, C, M, N, K, Kp, ldc, c_tma, ctl, s);
+      e = launch_tc_3xtf32(a_raw ? A : a_big, a_raw ? lda : Kp, a_small, bt_big, bt_small, C, M,
+                           N, K, Kp, ldc, c_tma, ctl, s);
     }
   }
   if (e != cudaSuccess) {

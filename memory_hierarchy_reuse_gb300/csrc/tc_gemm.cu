@@ -62,14 +62,14 @@ cudaError_t launch_tc_bf16(const uint16_t* A, const uint16_t* B, float* C, int64
   return launch_tc_any(KIND_BF16, mp, C, M, N, K, ldc, c_tma, after_prepass, ctl, s);
 }
 
-cudaError_t launch_tc_3xtf32(const float* a_big, const float* a_small, const float* bt_big,
-                             const float* bt_small, float* C, int64_t M, int64_t N, int64_t K,
-                             int64_t Kp, int64_t ldc, bool c_tma, const DeviceCtl& ctl,
-                             cudaStream_t s) {
+cudaError_t launch_tc_3xtf32(const float* a_big, int64_t a_big_ld, const float* a_small,
+                             const float* bt_big, const float* bt_small, float* C, int64_t M,
+                             int64_t N, int64_t K, int64_t Kp, int64_t ldc, bool c_tma,
+                             const DeviceCtl& ctl, cudaStream_t s) {
   TcMaps mp;
   const auto f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
-  if (encode_tmap_2d(&mp.a0, f32, a_big, K, M, Kp * 4, 32, 128, sw) != CUDA_SUCCESS ||
+  if (encode_tmap_2d(&mp.a0, f32, a_big, K, M, a_big_ld * 4, 32, 128, sw) != CUDA_SUCCESS ||
       encode_tmap_2d(&mp.a1, f32, a_small, K, M, Kp * 4, 32, 128, sw) != CUDA_SUCCESS ||
       encode_tmap_2d(&mp.b0, f32, bt_big, K, N, Kp * 4, 32, 128, sw) != CUDA_SUCCESS ||
       encode_tmap_2d(&mp.b1, f32, bt_small, K, N, Kp * 4, 32, 128, sw) != CUDA_SUCCESS ||

@@ -260,7 +260,7 @@ __device__ __forceinline__ void split_store(const SplitRegs& r, uint32_t st, int
     const int row = idx >> 3, c = idx & 7;
     const uint32_t off = row * 128 + ((c ^ (row & 7)) << 4);
     float4 big, small;
-    split4<true>(r.a[j], big, small);
+    split4_trunc<true>(r.a[j], big, small);  // as the pre-pass splits A
     st_shared_v4(st + off, big);
     st_shared_v4(st + Cf::A_BYTES + off, small);
   }

@@ -28,8 +28,10 @@ __global__ void pack_u16_kernel(const uint16_t* __restrict__ src, int64_t rows, 
 }
 
 // Split of both operands in one launch.  Blocks [0, a_blocks) split rows of
-// A in place order; the remaining blocks split 64 x 64 tiles of B and write
-// them transposed.  VA selects 16-byte loads of A when its address, leading
+// A in place order (big part truncated, see split_tf32_trunc; with a_big null
+// only the small part is written, A itself serving as A_big); the remaining
+// blocks split 64 x 64 tiles of B (big part rounded) and write them
+// transposed.  VA selects 16-byte loads of A when its address, leading
 // dimension and K allow them, else 4-byte loads; VB is the width in floats of
 // B's loads, 4, 2 or 1, the widest that B's address, leading dimension and N
 // allow.  The outputs (pitch Kp, a multiple of 4, in the 16-byte-aligned
@@ -85,8 +87,8 @@ __global__ void __launch_bounds__(SPLIT_THREADS)
           const int64_t r = r0 + ro[j];
           if (ro[j] < 0 || r >= M) continue;
           float4 b, s;
-          split4<VA>(v[j], b, s);
-          reinterpret_cast<float4*>(a_big + r * Kp)[co[j]] = b;
+          split4_trunc<VA>(v[j], b, s);
+          if (a_big) reinterpret_cast<float4*>(a_big + r * Kp)[co[j]] = b;
           reinterpret_cast<float4*>(a_small + r * Kp)[co[j]] = s;
         }
       }
@@ -94,7 +96,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS)
     }
     for (int64_t r = blockIdx.x; r < M; r += a_blocks) {
       const float* src = A + r * lda;
-      float4* db = reinterpret_cast<float4*>(a_big + r * Kp);
+      float4* db = a_big ? reinterpret_cast<float4*>(a_big + r * Kp) : nullptr;
       float4* ds = reinterpret_cast<float4*>(a_small + r * Kp);
       for (int64_t c0 = t; c0 < k4; c0 += 4 * SPLIT_THREADS) {
         float4 v[4];
@@ -117,8 +119,8 @@ __global__ void __launch_bounds__(SPLIT_THREADS)
           const int64_t c = c0 + j * SPLIT_THREADS;
           if (c < k4) {
             float4 b, s;
-            split4<VA>(v[j], b, s);  // conversion where 16-byte loads keep this memory-bound
-            db[c] = b;
+            split4_trunc<VA>(v[j], b, s);  // conversion where 16-byte loads keep this memory-bound
+            if (db) db[c] = b;
             ds[c] = s;
           }
         }
@@ -228,7 +230,7 @@ cudaError_t launch_split_tf32(const float* A, const float* B, int64_t M, int64_t
                               float* bt_big, float* bt_small, cudaStream_t s) {
   auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
   if (Kp % 4 != 0 || !al16(a_big) || !al16(a_small) || !al16(bt_big) || !al16(bt_small))
-    return cudaErrorInvalidValue;  // the workspace layout guarantees these
+    return cudaErrorInvalidValue;  // the workspace layout guarantees these (a_big may be null)
   const bool va = al16(A) && lda % 4 == 0 && K % 4 == 0;
   const int vb = al16(B) && ldb % 4 == 0 && N % 4 == 0                                   ? 4
                  : (reinterpret_cast<uintptr_t>(B) & 7u) == 0 && ldb % 2 == 0 && N % 2 == 0 ? 2
@@ -254,7 +256,9 @@ cudaError_t launch_split_tf32(const float* A, const float* B, int64_t M, int64_t
     per_sm = 1;
   const int64_t total = static_cast<int64_t>(sms) * per_sm;
   const int64_t b_tiles = ((N + SPLIT_TILE - 1) / SPLIT_TILE) * ((K + SPLIT_TILE - 1) / SPLIT_TILE);
-  const double a_share = static_cast<double>(M) / static_cast<double>(M + N);
+  // bytes per element: A 4 read + 8 written (4 without A_big), B 4 + 8
+  const double a_w = a_big ? 12.0 : 8.0;
+  const double a_share = a_w * M / (a_w * M + 12.0 * N);
   int64_t a_blocks = static_cast<int64_t>(a_share * total);
   a_blocks = a_blocks < 1 ? 1 : (a_blocks > M ? M : a_blocks);
   int64_t b_blocks = total - a_blocks;

@@ -1,9 +1,10 @@
 // The 3xTF32 split of one fp32 value into two tf32 parts, big + small, used
 // by the split pre-pass (tc_prepass.cu) and by the CTA-pair kernel's in-kernel
 // converter warps (tc_gemm_pair.cu).  big keeps the top 11 significant bits
-// of x, rounded to nearest-even; small is the exact remainder x - big, itself
-// rounded to tf32.  Products big*big + big*small + small*big then carry about
-// 22 significant bits, against 11 for one tf32 product.
+// of x -- rounded to nearest-even for B, truncated for A (below) -- and small
+// is the exact remainder x - big, itself rounded to tf32.  Products
+// big*big + big*small + small*big then carry about 22 significant bits,
+// against 11 for one tf32 product.
 #pragma once
 
 #include <cstdint>
@@ -46,6 +47,26 @@ __device__ __forceinline__ void split_tf32(float x, float& big, float& small) {
   big = tf32_rne<CVT>(x);
   const float rest = x - big;  // exact: the discarded low bits
   small = big == x ? 0.f : tf32_rne<CVT>(rest);
+}
+
+// The split with a truncated big part, used for A: big = x with its low 13
+// bits cleared, which is what the tensor core itself reads from an fp32
+// operand under kind::tf32 (measured on GB300: u & ~0x1FFF for every value of
+// a sweep), so A itself can serve as A_big; small = the exact remainder x -
+// big, below 2^-10 |x|, rounded to tf32 to nearest.
+template <bool CVT>
+__device__ __forceinline__ void split_tf32_trunc(float x, float& big, float& small) {
+  big = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+  const float rest = x - big;  // exact
+  small = big == x ? 0.f : tf32_rne<CVT>(rest);
+}
+
+template <bool CVT>
+__device__ __forceinline__ void split4_trunc(const float4 v, float4& b, float4& s) {
+  split_tf32_trunc<CVT>(v.x, b.x, s.x);
+  split_tf32_trunc<CVT>(v.y, b.y, s.y);
+  split_tf32_trunc<CVT>(v.z, b.z, s.z);
+  split_tf32_trunc<CVT>(v.w, b.w, s.w);
 }
 
 template <bool CVT>
