@@ -50,3 +50,32 @@ def test_injected_stall_reports_timeout(mhr, variant):
     Cref, S = oracle.gemm(A, B, with_abs=True)
     assert normalised_error(C, Cref, S) <= TOL[path]
 
+
+@pytest.mark.parametrize("path,K", [("3xtf32", 32 * 128 + 40), ("bf16", 64 * 128 + 40)],
+                         ids=["3xtf32", "bf16"])
+def test_injected_stall_in_cluster_split(mhr, path, K):
+    """The single-CTA kernel's cluster split (few tiles, long K runs): block 0,
+    rank 0 of the first cluster, times out on its first stage while its peers
+    finish and wait for it at the cluster barrier; the timeout is reported, the
+    kernel exits, and the next call on the context is correct."""
+    A, B, Ab, Bb = operands(300, 520, K, 6002, "normal", path)
+    call = DeviceCall(path, A, B, Ab, Bb)
+    old_mode = mhr.gemm_testing_set_cta_pair_mode(1)
+    old_limit = mhr.gemm_testing_set_wait_limit_ns(50_000_000)  # 50 ms
+    mhr.gemm_testing_set_inject_stall(1)
+    try:
+        call.run(mhr, check=False)
+        assert ",cluster-K> " in mhr.gemm_testing_last_main_kernel()
+        bits = mhr.gemm_testing_peek_status(None)
+        assert bits > 0 and (bits & 0x8) == 0, bits
+        assert mhr.gemm_check(None) == mhr.MHR_ERR_TIMEOUT
+        assert mhr.gemm_check(None) == mhr.MHR_OK
+    finally:
+        mhr.gemm_testing_set_inject_stall(0)
+        mhr.gemm_testing_set_wait_limit_ns(old_limit)
+    try:
+        C = call.run(mhr).result()
+    finally:
+        mhr.gemm_testing_set_cta_pair_mode(old_mode)
+    Cref, S = oracle.gemm(A, B, with_abs=True)
+    assert normalised_error(C, Cref, S) <= TOL[path]
