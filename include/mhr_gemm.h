@@ -70,19 +70,28 @@ typedef enum mhr_status {
  * double-buffered shared-memory ring, each thread accumulating an 8 x 8
  * register block ("矩阵乘法 tiling", sections 四 and 五: thread coarsening,
  * accumulator in registers; "CUDA 编程系列之三", section 6: register tiling).
- * Any alignment and any leading dimension are accepted.
+ * Aligned problems whose sizes are multiples of 128 x 256 x 8 and that fill
+ * the SMs use 128 x 256 tiles with 8 x 16 register blocks; problems with few
+ * tiles give each tile a cluster of CTAs that split K and sum their partial
+ * tiles in distributed shared memory.  Every output is summed in one fixed
+ * order per shape: results are bitwise repeatable.  Any alignment and any
+ * leading dimension are accepted.
  */
 int gemm_f32(const float* A, const float* B, float* C, int64_t M, int64_t N, int64_t K,
              int64_t lda, int64_t ldb, int64_t ldc, void* stream);
 
 /*
  * FP32-accurate path on the tensor cores: each operand is split as
- * x = big + small with big = tf32(x) and small = tf32(x - big) (round to
+ * x = big + small, where big keeps the top 11 significant bits of x
+ * (rounded to nearest even for B; truncated for A, which is what the tensor
+ * core reads from an fp32 operand) and small = tf32(x - big) (round to
  * nearest even), and C accumulates small*big + big*small + big*big with
  * tcgen05.mma kind::tf32 into a TMEM accumulator (the small*small term is
- * dropped).  A split pre-pass writes the four tf32 operands into the
- * library's workspace (B transposed to K-major, 8 (M + N) K bytes in all),
- * then a TMA + mbarrier ring feeds the tensor cores.  If that workspace cannot
+ * dropped).  A split pre-pass writes the tf32 operands into the library's
+ * workspace (B transposed to K-major; A's big part is A itself when A is
+ * 16-byte aligned with lda a multiple of 4; the workspace takes
+ * 8 (M + N) K bytes in all), then a TMA + mbarrier ring feeds the tensor
+ * cores.  If that workspace cannot
  * be allocated, converter warps of the CTA-pair kernel load A and B directly
  * and split them on chip instead: the same MMAs in the same order, so the
  * same C bit for bit, at about 60 % of the speed on GB300.  Any alignment and
