@@ -381,13 +381,18 @@ def test_simt_split_k(mhr):
     ((2048, 2560, 1032), "simt_f32_kernel<wide,split-K> grid=320 "),
     ((2048, 4864, 64), "simt_f32_kernel<wide> grid=304 "),
     ((2048, 4864 + 4, 64), "simt_f32_kernel grid="),
-    ((2048, 2560, 1032), "simt_f32_kernel<wide,split-K> grid=320 ")],
-    ids=["160-tiles-split", "304-tiles", "ragged-n-standard", "160-tiles-padded-ld"])
+    ((2048, 2560, 1032), "simt_f32_kernel<wide,split-K> grid=320 "),
+    ((2048, 2048, 512), "simt_f32_kernel<wide> grid=128 "),
+    ((1024, 2048, 512), "simt_f32_kernel grid=")],
+    ids=["160-tiles-split", "304-tiles", "ragged-n-standard", "160-tiles-padded-ld",
+         "128-tiles", "64-tiles-standard"])
 def test_simt_wide_tiles(mhr, shape, label, request):
     """Aligned problems whose sizes are multiples of 128 x 256 x 8 and that
     fill the SMs take the wide-tile SIMT kernel (8 x 16 outputs per thread,
-    no masks): 160 tiles with K halves added into a zeroed C (K = 1032), 304
-    tiles unsplit; N one vector wider leaves the shape to the masked kernel.
+    no masks) when they have at least half as many such tiles as SMs: 160
+    tiles with K halves added into a zeroed C (K = 1032), 304 and 128 tiles
+    unsplit; N one vector wider, or 64 tiles, leave the shape to the masked
+    kernel.
     The last case pads every leading dimension by a multiple of 4 with NaN in
     the pads: a read outside the logical matrices poisons C, a write outside
     C breaks its guard band. Integer inputs bit-exact against the oracle,
