@@ -24,8 +24,8 @@
  * Precision: every product is formed in double from the fp32 operands (the
  * product of two fp32 values is exact in double), summed in ascending k in
  * double, and rounded once to fp32 (round to nearest even).  The pages
- * accumulate in fp32; the fp64 sum is the stricter reading used to judge
- * every GPU path against one tolerance.
+ * accumulate in fp32; the fp64 sum is the stricter reading, against which
+ * every GPU path is checked with one tolerance.
  *
  * Layout: row-major with leading dimensions, A[i*lda + k], B[k*ldb + j],
  * C[i*ldc + j].  Rectangular shapes and leading dimensions generalise the
