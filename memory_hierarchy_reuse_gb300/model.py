@@ -81,8 +81,9 @@ def compulsory_bytes(M: int, N: int, K: int, in_bytes: int, out_bytes: int = 4) 
     return in_bytes * (M * K + K * N) + out_bytes * M * N
 
 
-def split_bytes(M: int, N: int, K: int) -> int:
+def split_bytes(M: int, N: int, K: int, a_big_written: bool = False) -> int:
     """HBM bytes of the 3xTF32 split pre-pass: read A and B (fp32) once, write
-    their big and small tf32 parts (fp32 containers, K padded to 4)."""
+    A's small part and B's big and small parts (fp32 containers, K padded to
+    4); A's big part too when TMA cannot read A itself as that part."""
     Kp = cdiv(K, 4) * 4
-    return 4 * (M * K + K * N) + 8 * Kp * (M + N)
+    return 4 * (M * K + K * N) + 4 * Kp * ((2 if a_big_written else 1) * M + 2 * N)

@@ -83,5 +83,9 @@ def test_roofline_examples():
 
 
 def test_split_bytes():
-    # 4096^3: read 2 x 64 MiB, write 4 x 64 MiB
-    assert model.split_bytes(4096, 4096, 4096) == 6 * 4096 * 4096 * 4
+    # 4096^3: read 2 x 64 MiB, write A_small, Bt_big, Bt_small (3 x 64 MiB),
+    # and A_big as well when A cannot serve as it
+    assert model.split_bytes(4096, 4096, 4096) == 5 * 4096 * 4096 * 4
+    assert model.split_bytes(4096, 4096, 4096, a_big_written=True) == 6 * 4096 * 4096 * 4
+    # K padded to a multiple of 4 in the written parts only
+    assert model.split_bytes(3, 5, 7) == 4 * (3 * 7 + 7 * 5) + 4 * 8 * (3 + 2 * 5)
