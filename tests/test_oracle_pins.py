@@ -174,3 +174,56 @@ def test_threads_do_not_change_results(oracle_lib):
     B = si.matrix(200, 48, 62, "normal")
     assert np.array_equal(bits(oracle_lib.gemm(A, B, nthreads=1)),
                           bits(oracle_lib.gemm(A, B, nthreads=4)))
+
+
+# ---------------------------------------------------------------- invariants
+# Identities of the exact product that hold bit for bit for the oracle's
+# definition (each product exact in fp64, summed in ascending k, rounded once),
+# checked on seeded real-valued inputs that are larger than the brute-force
+# cases above. Each one fails on a plausible mistake elsewhere in the code:
+# an index swap, a stride, a dropped or duplicated term, a rounding.
+
+def test_transpose_identity(oracle_lib):
+    """(A B)^T = B^T A^T: the same products summed in the same k order."""
+    A = si.matrix(37, 53, 8101, "normal")
+    B = si.matrix(53, 29, 8102, "normal")
+    C = oracle_lib.gemm(A, B)
+    Ct = oracle_lib.gemm(np.ascontiguousarray(B.T), np.ascontiguousarray(A.T))
+    assert np.array_equal(bits(C.T), bits(Ct))
+
+
+def test_row_and_column_permutations(oracle_lib):
+    """Permuting the rows of A permutes the rows of C; permuting the columns
+    of B permutes the columns of C."""
+    A = si.matrix(31, 40, 8103, "uniform")
+    B = si.matrix(40, 23, 8104, "uniform")
+    C = oracle_lib.gemm(A, B)
+    p = np.random.default_rng(1).permutation(31)
+    q = np.random.default_rng(2).permutation(23)
+    assert np.array_equal(bits(oracle_lib.gemm(np.ascontiguousarray(A[p]), B)), bits(C[p]))
+    assert np.array_equal(bits(oracle_lib.gemm(A, np.ascontiguousarray(B[:, q]))), bits(C[:, q]))
+
+
+def test_power_of_two_scaling(oracle_lib):
+    """Scaling A by 2^5 and B by 2^-3 scales every product, every partial sum
+    and the rounded result by exactly 2^2."""
+    A = si.matrix(19, 33, 8105, "normal")
+    B = si.matrix(33, 17, 8106, "normal")
+    C = oracle_lib.gemm(A, B)
+    C2 = oracle_lib.gemm(A * np.float32(32.0), B * np.float32(0.125))
+    assert np.array_equal(bits(C2), bits(C * np.float32(4.0)))
+
+
+def test_integer_linearity_and_k_split(oracle_lib):
+    """On small integers every sum is exact: C(A1 + A2, B) = C(A1, B) +
+    C(A2, B), and C(A, B) equals the sum of the products of any split of K
+    (the block decomposition of the pages, for every cut)."""
+    A1 = si.matrix(24, 50, 8107, "int")
+    A2 = si.matrix(24, 50, 8108, "int")
+    B = si.matrix(50, 18, 8109, "int")
+    C = oracle_lib.gemm(A1 + A2, B)
+    assert np.array_equal(C, oracle_lib.gemm(A1, B) + oracle_lib.gemm(A2, B))
+    for cut in (1, 17, 32, 49):
+        left = oracle_lib.gemm(np.ascontiguousarray(A1[:, :cut]), np.ascontiguousarray(B[:cut]))
+        right = oracle_lib.gemm(np.ascontiguousarray(A1[:, cut:]), np.ascontiguousarray(B[cut:]))
+        assert np.array_equal(oracle_lib.gemm(A1, B), left + right)
