@@ -21,7 +21,10 @@
 //   * problems with few tiles: a thread-block cluster of up to 8 CTAs shares
 //     each tile, each CTA taking one run of K-steps, and the partial tiles
 //     are summed through distributed shared memory -- the pages' reuse idea
-//     applied to the partial sums, which never travel to global memory.
+//     applied to the partial sums, which never travel to global memory;
+//   * aligned problems whose sizes are multiples of 128 x 256 x 8 go one
+//     level further still: 128 x 256 tiles, 8 x 16 outputs per thread
+//     (simt_f32_wide_kernel, below).
 //
 // Loads are coalesced where the tile crosses the global-memory boundary (a
 // warp reads consecutive addresses of one row), the A tile is stored
