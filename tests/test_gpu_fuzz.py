@@ -1,11 +1,12 @@
 """Seeded random sweep of every path variant against the oracle (GB300 only).
 
-Sixty cases with dimensions anywhere in 1..700, and sixty with every
-dimension at or next to a tile boundary (1, 8, 16, ..., 512, each +-1), each drawing a path variant (SIMT fp32; 3xTF32 on the single-CTA
-kernel, on the CTA-pair kernel with the split pre-pass, and with the split on
-chip; bf16 on either kernel), a shape with each of M, N, K in 1..700, padded
-leading dimensions (0 to 9 extra elements), an element offset that breaks
-16-byte alignment or not, and integer or real inputs. Integer inputs must
+Sixty cases with dimensions anywhere in 1..700, sixty with every dimension at
+or next to a tile boundary (1, 8, 16, ..., 512, each +-1), and twenty-four
+drawn onto the schedules that split or widen tiles. Each draws a path variant
+(SIMT fp32; 3xTF32 on the single-CTA kernel, on the CTA-pair kernel with the
+split pre-pass, and with the split on chip; bf16 on either kernel), a shape,
+padded leading dimensions (0 to 9 extra elements), an element offset that
+breaks 16-byte alignment or not, and integer or real inputs. Integer inputs must
 match the oracle bit for bit, real ones within the path's tolerance; the
 padding of C must keep its guard value (checked by DeviceCall.result)."""
 import numpy as np
@@ -49,7 +50,37 @@ def edge_cases(n=60, seed=20261203):
     return out
 
 
-@pytest.mark.parametrize("case", cases() + edge_cases(),
+def schedule_cases(n=24, seed=20261204):
+    """Shapes drawn to land on the schedules that split or widen tiles:
+    aligned 128 x 256 x 8 multiples with 76-120 such tiles (the wide SIMT
+    kernel), few single-CTA tiles with long K (clusters of 4 or 8 CTAs summing
+    through distributed shared memory, 3xTF32 and bf16), and few SIMT tiles
+    (clusters of 2-8). Alignment-preserving pads for the wide kernel; any
+    pads and offsets otherwise."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        kind = i % 4
+        dist = "int" if rng.random() < 0.5 else "normal"
+        if kind == 0:
+            while True:
+                a, b = int(rng.integers(2, 17)), int(rng.integers(1, 21))
+                if 76 <= a * b <= 120:
+                    break
+            M, N, K = 128 * a, 256 * b, 8 * int(rng.integers(1, 34))
+            pads = [4 * int(x) for x in rng.integers(0, 3, 3)]
+            out.append((("f32", 0, 0), M, N, K, pads, 0, dist, 9500 + i))
+            continue
+        M, N = (int(x) for x in rng.integers(1, 401, 2))
+        K = {1: int(rng.integers(2048, 4501)), 2: int(rng.integers(4096, 8401)),
+             3: int(rng.integers(16, 3001))}[kind]
+        v = {1: ("3xtf32", 1, 1), 2: ("bf16", 1, 0), 3: ("f32", 0, 0)}[kind]
+        pads = [int(x) for x in rng.integers(0, 10, 3)]
+        out.append((v, M, N, K, pads, int(rng.integers(0, 2)), dist, 9500 + i))
+    return out
+
+
+@pytest.mark.parametrize("case", cases() + edge_cases() + schedule_cases(),
                          ids=lambda c: f"{c[0][0]}-{c[0][1]}{c[0][2]}-{c[1]}x{c[2]}x{c[3]}-{c[6]}")
 def test_random_case(mhr, case):
     (path, pair_mode, split_mode), M, N, K, pads, offset, dist, seed = case
