@@ -6,7 +6,8 @@ problem, with inputs resident in HBM. The default workload is 4096^3 fp32
 pre-pass, TMA ring, tcgen05 main loop and epilogue -- and the same problem
 through the strict-fp32 SIMT path is reported beside it. Other workloads:
 --workload c1 (256^3), c3 (3000 x 2050 x 1000), c4 (8192^3 3xTF32),
-c5 (8192^3 bf16).
+c5 (8192^3 bf16); s1 / s2 (512 x 512 x 8192, 3xTF32 / bf16: few tiles and a
+long K, the single-CTA kernel's cluster split).
 
 Prints ONE JSON line (rank 0). Metric: 2MNK / t in TFLOPS. L2 is flushed
 (a 256 MiB write) between timed steps, outside the per-step CUDA events.
@@ -48,6 +49,11 @@ WORKLOADS = {
                also=None, desc="fp32-accurate 8192^3 via 3xTF32, uniform[-1,1)"),
     "c5": dict(M=8192, N=8192, K=8192, dist="normal", seeds=(5001, 5002), path="bf16",
                also=None, desc="bf16 inputs (normal(0,1) rounded), fp32 accumulate, 8192^3"),
+    # extra measurements (not parity configurations): few tiles, long K
+    "s1": dict(M=512, N=512, K=8192, dist="uniform", seeds=(6001, 6002), path="3xtf32",
+               also="f32", desc="fp32 skinny-deep 512x512x8192 (few tiles, long K)"),
+    "s2": dict(M=512, N=512, K=8192, dist="normal", seeds=(6101, 6102), path="bf16",
+               also=None, desc="bf16 skinny-deep 512x512x8192 (few tiles, long K)"),
 }
 ENTRY = {"f32": "gemm_f32", "3xtf32": "gemm_f32_3xtf32", "bf16": "gemm_bf16_f32acc"}
 DTYPE = {"f32": "f32", "3xtf32": "tf32x3", "bf16": "bf16"}
