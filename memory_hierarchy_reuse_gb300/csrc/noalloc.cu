@@ -83,9 +83,12 @@ MHR_API int gemm_f32_3xtf32_noalloc(const float* A, const float* B, float* C, in
   // 8 * Kp * (M + N) bytes must fit; M, N, K are below 2^31, so no overflow.
   if (K > 0 && static_cast<uint64_t>(Kp) * static_cast<uint64_t>(M + N) * 8u > kScratchBytes)
     return MHR_ERR_INVALID_ARG;
+  // The same lock as every other entry point: the settings, the profiling
+  // events and the launch counters are shared library state.
+  std::lock_guard<std::mutex> lock(library_mutex());
   DeviceCtl ctl;
   int dev = 0;
-  if ((rc = current_device_ctl(&ctl, &dev)) != MHR_OK) return rc;
+  if ((rc = device_ctl_locked(&ctl, &dev)) != MHR_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (K == 0) {
@@ -102,6 +105,7 @@ MHR_API int gemm_f32_3xtf32_noalloc(const float* A, const float* B, float* C, in
                           bt_small, s);
     if (e == cudaSuccess) {
       const bool c_tma = c_tma_eligible(C, N, ldc);
+      MainKernelEvents ev(s);
       e = launch_tc_3xtf32(a_raw ? A : a_big, a_raw ? lda : Kp, a_small, bt_big, bt_small, C, M,
                            N, K, Kp, ldc, c_tma, ctl, s);
     }
