@@ -36,9 +36,14 @@
  * Scratch: gemm_f32_3xtf32 (normally) and gemm_bf16_f32acc (only when an
  * operand's address or leading dimension is not 16-byte aligned) need a
  * device workspace.  The library owns it: one buffer per (device, stream),
- * grown with cudaMalloc on demand and kept until gemm_release().  When the
- * 3xTF32 workspace cannot be allocated, gemm_f32_3xtf32 splits its operands
- * inside the kernel instead (same result bit for bit, slower, no workspace).
+ * grown with cudaMalloc on demand and kept until gemm_release(), for at most
+ * four streams per device -- a call on a fifth stream first frees the least
+ * recently used stream's buffer, after waiting for that stream's last call
+ * to finish.  Each call makes its stream wait for the previous call that used
+ * the same buffer, so a stream handle that comes back after cudaStreamDestroy
+ * (with the destroyed stream's work still running) is safe.  When the 3xTF32
+ * workspace cannot be allocated, gemm_f32_3xtf32 splits its operands inside
+ * the kernel instead (same result bit for bit, slower, no workspace).
  *
  * Errors: every entry point returns an int status (mhr_status below); none
  * throws, none traps on the device.  Thread safety: calls from several host
@@ -155,9 +160,11 @@ int gemm_f32_ladder(int rung, const float* A, const float* B, float* C, int64_t 
                     int64_t K, int64_t lda, int64_t ldb, int64_t ldc, void* stream);
 
 /*
- * Synchronises `stream`, then reads and clears the current device's status
- * word.  Returns MHR_OK, MHR_ERR_TIMEOUT (some kernel since the last check hit
- * a wait limit) or MHR_ERR_CUDA (the synchronisation itself failed).
+ * Reads and clears the current device's status word in stream order on
+ * `stream`, then waits for `stream` alone (other streams keep running).
+ * Returns MHR_OK, MHR_ERR_TIMEOUT (some kernel that finished before this
+ * point hit a wait limit since the last check) or MHR_ERR_CUDA (the launch,
+ * copy or synchronisation failed).
  */
 int gemm_check(void* stream);
 
@@ -165,8 +172,8 @@ int gemm_check(void* stream);
 const char* gemm_status_string(int status);
 
 /*
- * Frees every workspace the library holds (all devices, all streams).  The
- * caller must ensure no library work is still running on any stream.
+ * Frees every workspace the library holds (all devices, all streams), each
+ * after the last call that used it has finished.
  */
 void gemm_release(void);
 

@@ -27,47 +27,53 @@ constexpr int64_t kMaxDim = (int64_t{1} << 31) - 512;  // tile/TMA coordinates a
 
 // Per-device status word: tensor-core kernels OR their timeout bits into it.
 __device__ uint32_t g_status_word;
+// gemm_check's copy of the status word, taken and cleared in one atomic step
+// on the caller's stream.
+__device__ uint32_t g_status_taken;
+
+__global__ void take_status_kernel(uint32_t* status, uint32_t* out) {
+  *out = atomicExch(status, 0u);
+}
 
 struct DeviceState {
   int checked = 0;  // 0 = not yet, 1 = sm_103, 2 = unsupported
   uint32_t* status = nullptr;
+  uint32_t* taken = nullptr;
   int sm_count = 0;
 };
 
+// A workspace belongs to one (device, stream).  `last_use` is recorded on the
+// stream after every call that used the buffer; a call waits for it on its
+// own stream before touching the buffer, so a stream handle reused after
+// cudaStreamDestroy (whose last kernels may still be running) cannot overwrite
+// data they read, and the host waits for it before freeing the buffer.
 struct Workspace {
   void* ptr = nullptr;
   size_t bytes = 0;
+  cudaEvent_t last_use = nullptr;
+  uint64_t stamp = 0;  // least recently used workspaces are freed first
 };
+// Workspaces kept per device; a call on a further stream frees the least
+// recently used one first.
+constexpr int kMaxWorkspacesPerDevice = 4;
 
 std::mutex g_mu;
 std::map<int, DeviceState> g_devices;
 std::map<std::pair<int, cudaStream_t>, Workspace> g_workspaces;
+uint64_t g_workspace_clock = 0;
 uint64_t g_wait_limit_ns = 2000000000ull;
 int g_inject_stall = 0;
 int g_pair_mode = 0;
 int g_raster_group = 0;
 int g_split_mode = 0;
 uint64_t g_workspace_limit = UINT64_MAX;
+int g_zero_a_small = 0;
 cudaEvent_t g_main_start = nullptr, g_main_stop = nullptr;
 
-// Brackets the main kernel launch with the caller's profiling events, if set:
-// the start event is recorded by note_main_kernel(), right before the launch
-// (after any pre-pass or zeroing kernel), the stop event when the entry point
-// returns.  Entry points hold g_mu meanwhile.
+// The caller's profiling events around the main kernel launch, if set (see
+// MainKernelEvents in mhr_internal.h).  Entry points hold g_mu meanwhile.
 cudaStream_t g_events_stream = nullptr;
 bool g_events_armed = false;
-struct MainKernelEvents {
-  explicit MainKernelEvents(cudaStream_t st) {
-    if (g_main_start && g_main_stop) {
-      g_events_stream = st;
-      g_events_armed = true;
-    }
-  }
-  ~MainKernelEvents() {
-    if (g_events_armed) cudaEventRecord(g_main_stop, g_events_stream);
-    g_events_armed = false;
-  }
-};
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -102,8 +108,14 @@ int device_state(DeviceState** out, int* dev_out) {
       st.checked = 2;
     } else {
       void* p = nullptr;
-      if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return MHR_ERR_CUDA;
+      void* q = nullptr;
+      if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess ||
+          cudaGetSymbolAddress(&q, g_status_taken) != cudaSuccess) {
+        cudaGetLastError();
+        return MHR_ERR_CUDA;
+      }
       st.status = static_cast<uint32_t*>(p);
+      st.taken = static_cast<uint32_t*>(q);
       st.sm_count = sms;
       st.checked = 1;
     }
@@ -152,16 +164,52 @@ int validate(const void* A, const void* B, const void* C, int64_t M, int64_t N, 
   return MHR_OK;
 }
 
-// Workspace of at least `bytes` for (device, stream).  Growing frees the old
-// buffer first (cudaFree waits for the device), so earlier calls on the same
-// stream that still read it have finished.
-int workspace(int dev, cudaStream_t s, size_t bytes, void** out) {
+// Frees a workspace once the last call that used it has finished.
+void free_workspace(int dev, Workspace& w) {
+  int cur = 0;
+  cudaGetDevice(&cur);
+  if (cur != dev) cudaSetDevice(dev);
+  if (w.last_use) {
+    cudaEventSynchronize(w.last_use);
+    cudaEventDestroy(w.last_use);
+  }
+  if (w.ptr) cudaFree(w.ptr);
+  cudaGetLastError();
+  if (cur != dev) cudaSetDevice(cur);
+  w = Workspace{};
+}
+
+// Workspace of at least `bytes` for (device, stream), ready for use on `s`:
+// the stream has been made to wait for the buffer's previous use.  The caller
+// records that use with workspace_used() after its launches.  At most
+// kMaxWorkspacesPerDevice are kept per device.
+int workspace(int dev, cudaStream_t s, size_t bytes, void** out, Workspace** ws_out) {
   constexpr size_t kGrain = size_t{2} << 20;
   if (bytes > SIZE_MAX - kGrain) return MHR_ERR_CUDA;  // no such allocation exists
   if (bytes > g_workspace_limit) return MHR_ERR_CUDA;  // test hook: as if cudaMalloc failed
-  Workspace& w = g_workspaces[{dev, s}];
+  const auto key = std::make_pair(dev, s);
+  if (g_workspaces.find(key) == g_workspaces.end()) {
+    int kept = 0;
+    auto lru = g_workspaces.end();
+    for (auto it = g_workspaces.begin(); it != g_workspaces.end(); ++it) {
+      if (it->first.first != dev) continue;
+      ++kept;
+      if (lru == g_workspaces.end() || it->second.stamp < lru->second.stamp) lru = it;
+    }
+    if (kept >= kMaxWorkspacesPerDevice && lru != g_workspaces.end()) {
+      free_workspace(dev, lru->second);
+      g_workspaces.erase(lru);
+    }
+  }
+  Workspace& w = g_workspaces[key];
+  if (!w.last_use && cudaEventCreateWithFlags(&w.last_use, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    w.last_use = nullptr;
+    return MHR_ERR_CUDA;
+  }
   if (w.bytes < bytes) {
     if (w.ptr) {
+      cudaEventSynchronize(w.last_use);  // the previous calls' kernels have read it
       cudaFree(w.ptr);
       w.ptr = nullptr;
       w.bytes = 0;
@@ -173,9 +221,19 @@ int workspace(int dev, cudaStream_t s, size_t bytes, void** out) {
       return MHR_ERR_CUDA;
     }
     w.bytes = rounded;
+  } else if (cudaStreamWaitEvent(s, w.last_use, 0) != cudaSuccess) {
+    cudaGetLastError();
+    return MHR_ERR_CUDA;
   }
+  w.stamp = ++g_workspace_clock;
   *out = w.ptr;
+  *ws_out = &w;
   return MHR_OK;
+}
+
+// Records the end of this call's use of the workspace on its stream.
+void workspace_used(Workspace* w, cudaStream_t s) {
+  if (w && w->last_use) cudaEventRecord(w->last_use, s);
 }
 
 DeviceCtl make_ctl(const DeviceState& st) {
@@ -239,12 +297,25 @@ int check_gemm_args(const void* A, const void* B, const void* C, int64_t M, int6
   return validate(A, B, C, M, N, K, lda, ldb, ldc, esz_ab, noop);
 }
 
-int current_device_ctl(DeviceCtl* ctl, int* dev) {
-  std::lock_guard<std::mutex> g(g_mu);
+std::mutex& library_mutex() { return g_mu; }
+
+int device_ctl_locked(DeviceCtl* ctl, int* dev) {
   DeviceState* st;
   const int rc = device_state(&st, dev);
   if (rc == MHR_OK) *ctl = make_ctl(*st);
   return rc;
+}
+
+void main_events_arm(cudaStream_t s) {
+  if (g_main_start && g_main_stop) {
+    g_events_stream = s;
+    g_events_armed = true;
+  }
+}
+
+void main_events_disarm() {
+  if (g_events_armed) cudaEventRecord(g_main_stop, g_events_stream);
+  g_events_armed = false;
 }
 
 }  // namespace mhr
@@ -311,13 +382,14 @@ MHR_API int gemm_f32_3xtf32(const float* A, const float* B, float* C, int64_t M,
                     !__builtin_add_overflow(a_bytes, b_bytes, &ws_bytes) &&
                     !__builtin_mul_overflow(ws_bytes, size_t{2}, &ws_bytes);
   void* ws = nullptr;
+  Workspace* wsd = nullptr;
   if (ctl.split_mode == 2 ||
-      (ctl.split_mode == 0 && (!fits || workspace(dev, s, ws_bytes, &ws) != MHR_OK))) {
+      (ctl.split_mode == 0 && (!fits || workspace(dev, s, ws_bytes, &ws, &wsd) != MHR_OK))) {
     MainKernelEvents ev(s);
     return from_cuda(launch_tc_3xtf32_split(A, B, C, M, N, K, lda, ldb, ldc, c_tma, ctl, s));
   }
   if (!fits) return MHR_ERR_CUDA;
-  if (!ws && (rc = workspace(dev, s, ws_bytes, &ws)) != MHR_OK) return rc;
+  if (!ws && (rc = workspace(dev, s, ws_bytes, &ws, &wsd)) != MHR_OK) return rc;
   float* a_big = static_cast<float*>(ws);
   float* a_small = a_big + M * Kp;
   float* bt_big = a_small + M * Kp;
@@ -327,10 +399,15 @@ MHR_API int gemm_f32_3xtf32(const float* A, const float* B, float* C, int64_t M,
   const bool a_raw = a_serves_as_big(A, lda);
   cudaError_t e = launch_split_tf32(A, B, M, N, K, lda, ldb, Kp, a_raw ? nullptr : a_big, a_small,
                                     bt_big, bt_small, s);
-  if (e != cudaSuccess) return from_cuda(e);
-  MainKernelEvents ev(s);
-  return from_cuda(launch_tc_3xtf32(a_raw ? A : a_big, a_raw ? lda : Kp, a_small, bt_big,
-                                    bt_small, C, M, N, K, Kp, ldc, c_tma, ctl, s));
+  if (e == cudaSuccess && g_zero_a_small)  // test hook: the tensor core sees A alone
+    e = cudaMemsetAsync(a_small, 0, static_cast<size_t>(M) * Kp * 4, s);
+  if (e == cudaSuccess) {
+    MainKernelEvents ev(s);
+    e = launch_tc_3xtf32(a_raw ? A : a_big, a_raw ? lda : Kp, a_small, bt_big, bt_small, C, M, N,
+                         K, Kp, ldc, c_tma, ctl, s);
+  }
+  workspace_used(wsd, s);
+  return from_cuda(e);
 }
 
 MHR_API int gemm_bf16_f32acc(const uint16_t* A, const uint16_t* B, float* C, int64_t M, int64_t N,
@@ -345,6 +422,7 @@ MHR_API int gemm_bf16_f32acc(const uint16_t* A, const uint16_t* B, float* C, int
   if ((rc = device_state(&st, &dev)) != MHR_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (K == 0) return from_cuda(launch_zero_fill(C, M, N, ldc, s));
+  Workspace* wsd = nullptr;
   const bool a_ok = aligned16(A) && (lda % 8) == 0;
   const bool b_ok = aligned16(B) && (ldb % 8) == 0;
   if (!a_ok || !b_ok) {
@@ -356,25 +434,35 @@ MHR_API int gemm_bf16_f32acc(const uint16_t* A, const uint16_t* B, float* C, int
     if (__builtin_add_overflow(static_cast<size_t>(round_up(a_bytes, 256)), b_bytes, &ws_bytes))
       return MHR_ERR_CUDA;
     void* ws;
-    if ((rc = workspace(dev, s, ws_bytes, &ws)) != MHR_OK) return rc;
+    if ((rc = workspace(dev, s, ws_bytes, &ws, &wsd)) != MHR_OK) return rc;
     uint16_t* pa = static_cast<uint16_t*>(ws);
     uint16_t* pb = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + round_up(a_bytes, 256));
     cudaError_t e;
     if (!a_ok) {
-      if ((e = launch_pack_u16(A, M, K, lda, pa, lda_p, s)) != cudaSuccess) return from_cuda(e);
+      if ((e = launch_pack_u16(A, M, K, lda, pa, lda_p, s)) != cudaSuccess) {
+        workspace_used(wsd, s);
+        return from_cuda(e);
+      }
       A = pa;
       lda = lda_p;
     }
     if (!b_ok) {
-      if ((e = launch_pack_u16(B, K, N, ldb, pb, ldb_p, s)) != cudaSuccess) return from_cuda(e);
+      if ((e = launch_pack_u16(B, K, N, ldb, pb, ldb_p, s)) != cudaSuccess) {
+        workspace_used(wsd, s);
+        return from_cuda(e);
+      }
       B = pb;
       ldb = ldb_p;
     }
   }
   const bool c_tma = c_tma_eligible(C, N, ldc);
-  MainKernelEvents ev(s);
-  return from_cuda(launch_tc_bf16(A, B, C, M, N, K, lda, ldb, ldc, c_tma, !a_ok || !b_ok,
-                                  make_ctl(*st), s));
+  cudaError_t e;
+  {
+    MainKernelEvents ev(s);
+    e = launch_tc_bf16(A, B, C, M, N, K, lda, ldb, ldc, c_tma, !a_ok || !b_ok, make_ctl(*st), s);
+  }
+  workspace_used(wsd, s);
+  return from_cuda(e);
 }
 
 MHR_API int gemm_check(void* stream) {
@@ -382,14 +470,14 @@ MHR_API int gemm_check(void* stream) {
   DeviceState* st;
   int rc;
   if ((rc = device_state(&st, nullptr)) != MHR_OK) return rc;
-  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
-    cudaGetLastError();
-    return MHR_ERR_CUDA;
-  }
+  // Take and clear the status word in one atomic step, in stream order, then
+  // wait for this stream alone.
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint32_t bits = 0;
-  if (cudaMemcpy(&bits, st->status, sizeof(bits), cudaMemcpyDeviceToHost) != cudaSuccess ||
-      cudaMemset(st->status, 0, sizeof(bits)) != cudaSuccess ||
-      cudaDeviceSynchronize() != cudaSuccess) {
+  take_status_kernel<<<1, 1, 0, s>>>(st->status, st->taken);
+  if (cudaGetLastError() != cudaSuccess ||
+      cudaMemcpyAsync(&bits, st->taken, sizeof(bits), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
     cudaGetLastError();
     return MHR_ERR_CUDA;
   }
@@ -409,16 +497,8 @@ MHR_API const char* gemm_status_string(int status) {
 
 MHR_API void gemm_release(void) {
   std::lock_guard<std::mutex> g(g_mu);
-  int cur = 0;
-  cudaGetDevice(&cur);
-  for (auto& kv : g_workspaces) {
-    if (kv.second.ptr) {
-      cudaSetDevice(kv.first.first);
-      cudaFree(kv.second.ptr);
-    }
-  }
+  for (auto& kv : g_workspaces) free_workspace(kv.first.first, kv.second);
   g_workspaces.clear();
-  cudaSetDevice(cur);
 }
 
 MHR_API int gemm_version(void) { return kVersion; }
@@ -462,6 +542,13 @@ MHR_API uint64_t gemm_testing_set_workspace_limit(uint64_t bytes) {
   std::lock_guard<std::mutex> g(g_mu);
   const uint64_t old = g_workspace_limit;
   g_workspace_limit = bytes;
+  return old;
+}
+
+MHR_API int gemm_testing_set_zero_a_small(int enable) {
+  std::lock_guard<std::mutex> g(g_mu);
+  const int old = g_zero_a_small;
+  g_zero_a_small = enable ? 1 : 0;
   return old;
 }
 

@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
+#include <mutex>
 
 namespace mhr {
 
@@ -107,8 +108,27 @@ const char* last_main_kernel();
 int check_gemm_args(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
                     int64_t lda, int64_t ldb, int64_t ldc, int64_t esz_ab, bool* noop);
 
+// The library lock (api.cu).  Every entry point holds it while it reads the
+// settings, looks up device state and scratch, and enqueues its kernels.
+std::mutex& library_mutex();
+
 // The current device's kernel controls (status word, wait limit, SM count);
-// MHR_ERR_UNSUPPORTED unless the device is sm_103.
-int current_device_ctl(DeviceCtl* ctl, int* dev);
+// MHR_ERR_UNSUPPORTED unless the device is sm_103.  The caller holds
+// library_mutex().
+int device_ctl_locked(DeviceCtl* ctl, int* dev);
+
+// The caller's profiling events around the main kernel of a call
+// (gemm_testing_set_main_kernel_events): while armed, note_main_kernel()
+// records the start event on the call's stream right before the main kernel
+// launch; disarming records the stop event.  The caller holds
+// library_mutex().
+void main_events_arm(cudaStream_t s);
+void main_events_disarm();
+struct MainKernelEvents {
+  explicit MainKernelEvents(cudaStream_t s) { main_events_arm(s); }
+  ~MainKernelEvents() { main_events_disarm(); }
+  MainKernelEvents(const MainKernelEvents&) = delete;
+  MainKernelEvents& operator=(const MainKernelEvents&) = delete;
+};
 
 }  // namespace mhr

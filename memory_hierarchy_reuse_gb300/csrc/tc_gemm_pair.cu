@@ -281,18 +281,11 @@ struct PairLayout {
   using C = PairCfg<KIND>;
   static constexpr int EPI_OFF = C::STAGES * C::STAGE_BYTES;
   static constexpr int BAR_OFF = EPI_OFF + EPI_BYTES;
-  static constexpr int NUM_BARS = 2 * C::STAGES + 5;
+  static constexpr int NUM_BARS = 2 * C::STAGES + 6;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int USED = MISC_OFF + 16;
   static constexpr int ALLOC = USED + 1024;
 };
-
-// Pause for `ns` nanoseconds (bounded).
-__device__ __forceinline__ void pause_ns(uint64_t ns) {
-  const uint64_t t0 = global_timer_ns();
-  while (global_timer_ns() - t0 < ns) {
-  }
-}
 
 template <int KIND, bool TMA_STORE>
 __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
@@ -313,8 +306,12 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
   auto accf_bar = [&](uint32_t b) { return bar0 + 8u * (2 * Cf::STAGES + b); };
   auto acce_bar = [&](uint32_t b) { return bar0 + 8u * (2 * Cf::STAGES + 2 + b); };
   const uint32_t drain_bar = bar0 + 8u * (2 * Cf::STAGES + 4);
+  // rank 0 only: rank 1's producer arrives here once it has issued its last load
+  const uint32_t peer_done_bar = bar0 + 8u * (2 * Cf::STAGES + 5);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
+  // rank 0 only: how many ring stages rank 1's producer loaded
+  volatile uint32_t* peer_loaded = reinterpret_cast<volatile uint32_t*>(smem + L::MISC_OFF + 8);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -336,7 +333,9 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
       mbar_init(acce_bar(b), 2 * EPI_WARPS);
     }
     mbar_init(drain_bar, 1);
+    mbar_init(peer_done_bar, 1);
     *abort_flag = 0;
+    *peer_loaded = 0;
     fence_mbar_init();
     if constexpr (KIND != KIND_3XTF32_SPLIT) {
       tma_prefetch_desc(&tmA0);
@@ -377,15 +376,18 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
     // One thread waits, arms and issues; the rest of the warp idles.  (The
     // split kind has converter warps instead; its warp 0 only idles.)
     if (KIND != KIND_3XTF32_SPLIT && lane == 0) {
-      uint32_t it = 0, inflight = 0;
-      bool ok = true;
-      for (int u = cluster; ok && u < p.num_units; u += num_clusters) {
+      // `it` counts the ring stages this producer armed (rank 0) and loaded;
+      // with the injected stall, block 0's first stage is armed but not loaded.
+      uint32_t it = 0;
+      bool stalled_first = false;
+      for (int u = cluster; u < p.num_units; u += num_clusters) {
         const Unit w = unit_of(u, p);
         int tm, tn;
         tile_coords(w.tile, p, tm, tn);
         const int m0 = tm * 2 * Cf::BM + static_cast<int>(rank) * Cf::BM;
         const int nb0 = tn * Cf::BN + static_cast<int>(rank) * Cf::BN_HALF;
-        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+        bool ok = true;
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
           const uint32_t s = it % Cf::STAGES, ph = (it / Cf::STAGES) & 1u;
           if (!mbar_wait_bounded(empty_bar(s), ph ^ 1u, limit, abort_flag)) {
             give_up_one(kErrTimeoutProducer);
@@ -414,26 +416,51 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
               tma_load_2d_pair(st + 2 * Cf::A_BYTES, &tmB0, fb, k0, nb0);
               tma_load_2d_pair(st + 2 * Cf::A_BYTES + Cf::B_BYTES, &tmB1, fb, k0, nb0);
             }
-            inflight |= 1u << s;
           } else {
-            inflight &= ~(1u << s);
+            stalled_first = true;
           }
+          ++it;
         }
+        if (!ok) break;
       }
-      if (leader) {
-        // Rank 0 can see its full barriers: wait for every fill it armed and loaded.
-        for (uint32_t s = 0; s < static_cast<uint32_t>(Cf::STAGES) && s < it; ++s) {
-          if (!(inflight & (1u << s))) continue;
-          const uint32_t last = it - 1 - ((it - 1 - s) % Cf::STAGES);
-          volatile int never = 0;
-          if (!mbar_wait_bounded(full_bar(s), (last / Cf::STAGES) & 1u, limit, &never))
+      // Drain.  Both CTAs' loads complete on rank 0's full barriers, which
+      // rank 1 cannot poll, so rank 0 waits for them all: rank 1 tells it how
+      // many stages it loaded; rank 0 then completes the phase of each of the
+      // last STAGES iterations -- arming it for rank 1's bytes if rank 0 never
+      // got that far, or counting as done the bytes that either CTA never
+      // issued -- and waits for it.  Earlier phases are complete already: a
+      // stage is armed or loaded again only after the MMAs have consumed it.
+      // Neither CTA passes the final cluster barrier before this ends, so no
+      // load can land in the shared memory of a CTA that has exited.
+      volatile int never = 0;
+      if (!leader) {
+        st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<uint32_t*>(peer_loaded)), 0), it);
+        mbar_arrive_cluster(mapa_shared(peer_done_bar, 0));
+      } else {
+        uint32_t it1 = 0;
+        if (mbar_wait_bounded<true>(peer_done_bar, 0, limit, &never)) {
+          it1 = *peer_loaded;
+        } else {
+          atomicOr(p.status, kErrTimeoutDrain);
+          it1 = it;  // unknown: wait for what rank 0 armed
+        }
+        const uint32_t hi = it > it1 ? it : it1;
+        for (uint32_t i = hi > static_cast<uint32_t>(Cf::STAGES) ? hi - Cf::STAGES : 0; i < hi;
+             ++i) {
+          const uint32_t s = i % Cf::STAGES, ph = (i / Cf::STAGES) & 1u;
+          const bool armed0 = i < it, loaded0 = armed0 && !(stalled_first && i == 0);
+          const bool loaded1 = i < it1;
+          if (!armed0) {
+            mbar_arrive_expect_tx(full_bar(s), Cf::STAGE_BYTES);  // rank 1's bytes only
+          } else {
+            const uint32_t missing = (loaded0 ? 0u : static_cast<uint32_t>(Cf::STAGE_BYTES)) +
+                                     (loaded1 ? 0u : static_cast<uint32_t>(Cf::STAGE_BYTES));
+            if (missing) mbar_complete_tx(full_bar(s), missing);
+          }
+          if (!mbar_wait_bounded(full_bar(s), ph, limit, &never))
             atomicOr(p.status, kErrTimeoutDrain);
         }
       }
-      // After an abort, the loads this CTA issued signal rank 0's barriers,
-      // which rank 1 cannot poll: give them time to land (a TMA load takes
-      // microseconds) before the CTA may leave.
-      if (*abort_flag) pause_ns(100000);
     }
     __syncwarp();
   } else if (warp == 1) {
