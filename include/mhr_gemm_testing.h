@@ -60,6 +60,17 @@ int gemm_testing_set_cta_pair_mode(int mode);
 int gemm_testing_set_split_mode(int mode);
 
 /*
+ * When `enable` is nonzero, gemm_f32_3xtf32 calls that split in a pre-pass
+ * (split mode 0 or 1 with a workspace) clear A's small part after the split,
+ * so the main kernel accumulates A_big * (B_big + B_small) only.  With B the
+ * identity that exposes what the tensor core reads from an fp32 A operand
+ * under kind::tf32 -- the library relies on it being A with the low 13 bits
+ * of each value cleared, so that A itself can serve as A's big part.  Test
+ * use only; returns the previous setting.
+ */
+int gemm_testing_set_zero_a_small(int enable);
+
+/*
  * Caps the bytes the library's workspace may grow to (process-wide), so that
  * a larger request fails as an allocation failure would.  UINT64_MAX (the
  * initial value) removes the cap.  Returns the previous cap.

@@ -47,7 +47,8 @@ EXPORTS = ("gemm_f32", "gemm_f32_3xtf32", "gemm_bf16_f32acc", "gemm_f32_3xtf32_n
            "gemm_testing_peek_status", "gemm_testing_set_main_kernel_events",
            "gemm_testing_set_cta_pair_mode", "gemm_testing_last_main_kernel",
            "gemm_testing_set_raster_group", "gemm_testing_set_split_mode",
-           "gemm_testing_last_launches", "gemm_testing_set_workspace_limit")
+           "gemm_testing_last_launches", "gemm_testing_set_workspace_limit",
+           "gemm_testing_set_zero_a_small")
 
 _lib = None
 
@@ -96,6 +97,8 @@ def load(path: str | None = None):
     lib.gemm_testing_last_main_kernel.restype = ctypes.c_char_p
     lib.gemm_testing_set_cta_pair_mode.argtypes = [ctypes.c_int]
     lib.gemm_testing_set_cta_pair_mode.restype = ctypes.c_int
+    lib.gemm_testing_set_zero_a_small.argtypes = [ctypes.c_int]
+    lib.gemm_testing_set_zero_a_small.restype = ctypes.c_int
     lib.gemm_testing_set_split_mode.argtypes = [ctypes.c_int]
     lib.gemm_testing_set_split_mode.restype = ctypes.c_int
     lib.gemm_testing_set_workspace_limit.argtypes = [ctypes.c_uint64]
@@ -186,6 +189,11 @@ def gemm_testing_set_split_mode(mode: int) -> int:
     """3xTF32 split: 0 = automatic (pre-pass; on chip without workspace), 1 = pre-pass,
     2 = inside the CTA-pair kernel."""
     return load().gemm_testing_set_split_mode(int(mode))
+
+
+def gemm_testing_set_zero_a_small(enable: int) -> int:
+    """Clear A's small part after the 3xTF32 split pre-pass (test hook)."""
+    return load().gemm_testing_set_zero_a_small(int(enable))
 
 
 def gemm_testing_set_main_kernel_events(start=None, stop=None) -> None:
