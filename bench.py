@@ -122,33 +122,84 @@ def stored_traffic(kernel: str, workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons, sampled every 100 ms in the background."""
+    """SM clock, power and clock-event (throttle) reasons of this process's GPU,
+    sampled in the background: through NVML every 2 ms where libnvidia-ml can
+    be loaded (read-only queries), else by nvidia-smi's own loop.  Each row is
+    (sm MHz, max sm MHz, power W, hw_slowdown, hw_thermal_slowdown,
+    sw_thermal_slowdown, sw_power_cap), the reasons as "Active"/"Not Active"."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits, in the order of the row's last four fields
+    REASON_BITS = (0x8, 0x40, 0x20, 0x4)
+    PERIOD_S = 0.002
 
     def __init__(self, device_index: int):
         self.rows = []
         self.proc = None
+        self.source = None
+        self._stop = threading.Event()
         import torch
 
-        ident = []
+        uuid = None
         try:
-            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
-            ident = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+            u = str(torch.cuda.get_device_properties(device_index).uuid)
+            uuid = u if u.startswith("GPU-") else "GPU-" + u
         except Exception:
-            ident = []
-        cmd = ["nvidia-smi", *ident, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-               "-lms", "100"]
+            uuid = None
+        if self._start_nvml(uuid):
+            return
+        cmd = ["nvidia-smi", *(["-i", uuid] if uuid else []), f"--query-gpu={self.FIELDS}",
+               "--format=csv,noheader,nounits", "-lms", "25"]
         try:
             self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
                                          text=True)
         except OSError:
             self.proc = None
             return
+        self.source = "nvidia-smi -lms 25"
         self.t = threading.Thread(target=self._read, daemon=True)
         self.t.start()
+
+    def _start_nvml(self, uuid) -> bool:
+        import ctypes
+
+        if not uuid:
+            return False
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return False
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) != 0:
+                return False
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) != 0:  # 1 = SM clock
+                return False
+            reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        except (OSError, AttributeError):
+            return False
+        self._nv, self._h, self._max, self._reasons_fn = nv, h, mx.value, reasons_fn
+        self.source = f"NVML every {self.PERIOD_S * 1e3:.0f} ms"
+        self.t = threading.Thread(target=self._poll, daemon=True)
+        self.t.start()
+        return True
+
+    def _poll(self):
+        import ctypes
+
+        nv, h = self._nv, self._h
+        clk, mw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if (nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and
+                    self._reasons_fn(h, ctypes.byref(rs)) == 0):
+                pw = mw.value / 1e3 if nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw)) == 0 else 0.0
+                flags = ["Active" if rs.value & b else "Not Active" for b in self.REASON_BITS]
+                self.rows.append((time.time(), [str(clk.value), str(self._max), f"{pw:.1f}",
+                                                *flags]))
+            time.sleep(self.PERIOD_S)
 
     def _read(self):
         for line in self.proc.stdout:
@@ -160,6 +211,7 @@ class ClockSampler:
         return [r for (t, r) in self.rows if t0 <= t <= t1]
 
     def stop(self):
+        self._stop.set()
         if self.proc:
             self.proc.terminate()
             try:
@@ -176,7 +228,8 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[3 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows),
+                "sm_mhz_min": min(sm) if sm else None}
 
 
 def dist_setup():
@@ -407,6 +460,227 @@ def run_reference(args, w, world, rank):
     }), flush=True)
 
 
+def sampled_error(A, B, c_dev, M, N, K, seed, n_random=4096):
+    """Normalised error max |C - C_ref| / sum_k |A_ik||B_kj| of the GPU result
+    on sampled entries (random ones plus the first and last row and column),
+    each computed by the CPU oracle."""
+    import numpy as np
+    import torch
+
+    import oracle
+
+    rng = np.random.default_rng(seed)
+    r = np.concatenate([rng.integers(0, M, n_random), np.zeros(N, np.int64),
+                        np.full(N, M - 1), np.arange(M), np.arange(M)]).astype(np.int64)
+    c = np.concatenate([rng.integers(0, N, n_random), np.arange(N), np.arange(N),
+                        np.zeros(M, np.int64), np.full(M, N - 1)]).astype(np.int64)
+    ref, S = oracle.gemm_entries(A, B, r, c, M, N, K)
+    got = c_dev[torch.from_numpy(r).to(c_dev.device), torch.from_numpy(c).to(c_dev.device)]
+    got = got.cpu().numpy().astype(np.float64)
+    ok = S > 0
+    return {"value": float(np.max(np.abs(got - ref)[ok] / S[ok])) if ok.any() else 0.0,
+            "entries": int(r.size), "all_finite": bool(np.all(np.isfinite(got)))}
+
+
+def cublas_tf32_peak(dev, stream, flush, sampler, reps=10, n=8192):
+    """The tf32 tensor-pipe ceiling measured on this GPU: cuBLAS single-pass
+    tf32 (torch.matmul with TF32 allowed) on n^3 fp32 operands, uniform[-1, 1),
+    best of `reps` calls, each timed with CUDA events after an L2 flush."""
+    import torch
+
+    old = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        a = torch.rand(n, n, device=dev) * 2 - 1
+        b = torch.rand(n, n, device=dev) * 2 - 1
+        for _ in range(3):
+            torch.matmul(a, b)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)]
+        torch.cuda.synchronize(dev)
+        t0 = time.time()
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(stream)
+            torch.matmul(a, b)
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        t1 = time.time()
+        ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+        flop = 2.0 * n ** 3
+        out = {"tflops": flop / (min(ms) * 1e-3) / 1e12,
+               "mean_tflops": flop / (sum(ms) / len(ms) * 1e-3) / 1e12,
+               "how": f"cuBLAS single-pass tf32 (torch.matmul, TF32 allowed) at {n}^3 fp32, "
+                      f"best of {reps} calls, L2 flushed before each, in this run"}
+        if sampler:
+            out["clocks"] = ClockSampler.summary(sampler.window(t0 - 0.05, t1 + 0.05))
+        del a, b
+        return out
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = old
+
+
+class Bench:
+    """One GPU's measurement context: the library, the launching stream, the
+    L2-flush buffer, the ranks and the clock sampler."""
+
+    def __init__(self, lib, mhr, dev, stream, flush, ranks, sampler):
+        self.lib, self.mhr, self.dev, self.stream = lib, mhr, dev, stream
+        self.sh = stream.cuda_stream
+        self.flush, self.ranks, self.sampler = flush, ranks, sampler
+
+    def call(self, path, a, b, c, M, N, K):
+        rc = getattr(self.lib, ENTRY[path])(a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K, K,
+                                            N, N, self.sh)
+        if rc != self.mhr.MHR_OK:
+            raise self.mhr.GemmError(rc, ENTRY[path])
+
+    def timed_steps(self, path, steps, kernel_events, a, b, c, M, N, K):
+        """Per-step CUDA events around each call (L2 flushed before each,
+        outside the events).  With kernel_events, events around the main
+        kernel of each call instead: recorded between a pre-pass and the main
+        kernel, they stop the main kernel from starting programmatically
+        behind the pre-pass, so the step times of such a loop are not used."""
+        import torch
+
+        stream, lib = self.stream, self.lib
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for e in ev:  # create the underlying events
+            for x in e:
+                x.record(stream)
+        torch.cuda.synchronize(self.dev)
+        for e0, e1 in ev:
+            self.flush.zero_()
+            if kernel_events:
+                lib.gemm_testing_set_main_kernel_events(e0.cuda_event, e1.cuda_event)
+            else:
+                e0.record(stream)
+            self.call(path, a, b, c, M, N, K)
+            if not kernel_events:
+                e1.record(stream)
+        lib.gemm_testing_set_main_kernel_events(None, None)
+        torch.cuda.synchronize(self.dev)
+        return [e0.elapsed_time(e1) for e0, e1 in ev]
+
+    def measure(self, path, a, b, c, M, N, K, steps, warmup):
+        """Warm-up, then `steps` timed calls (the step time), then as many
+        again with events around the main kernel alone; max over ranks."""
+        import torch
+
+        for _ in range(warmup):
+            self.call(path, a, b, c, M, N, K)
+        rc = self.lib.gemm_check(self.sh)
+        if rc != self.mhr.MHR_OK:
+            raise self.mhr.GemmError(rc, "warm-up")
+        main_kernel = self.lib.gemm_testing_last_main_kernel().decode()
+        # our kernels per call, as counted by the library (pre-passes, zero
+        # fills of split tiles, the main kernel)
+        launches = self.lib.gemm_testing_last_launches()
+        time.sleep(0.2)  # a few clock samples before the timed region
+        self.ranks.barrier()
+        torch.cuda.synchronize(self.dev)
+        t0 = time.time()
+        step_ms = self.timed_steps(path, steps, False, a, b, c, M, N, K)
+        torch.cuda.synchronize(self.dev)
+        self.ranks.barrier()
+        t1 = time.time()
+        kern_ms = self.timed_steps(path, steps, True, a, b, c, M, N, K)
+        rc = self.lib.gemm_check(self.sh)
+        if rc != self.mhr.MHR_OK:
+            raise self.mhr.GemmError(rc, "timed region")
+        clocks = None
+        if self.sampler:
+            clocks = ClockSampler.summary(self.sampler.window(t0, t1))
+        return {"ms_step": self.ranks.max(sum(step_ms) / len(step_ms)),
+                "ms_kern": self.ranks.max(sum(kern_ms) / len(kern_ms)),
+                "main_kernel": main_kernel, "launches_per_call": launches, "clocks": clocks,
+                "t0": t0, "t1": t1}
+
+
+def tensor_roofline(path, flop, meas, workload, tf32, sms):
+    """Roofline of the dominant (main) kernel of a tensor-core path."""
+    pk = peaks()
+    if path == "bf16":
+        tensor_flop, peak, src = flop, pk["bf16_tflops"], (
+            f"{pk['source']} (MEASURED_PEAKS bf16 dense burst; the kernel is timed alone)")
+    else:
+        tensor_flop = 3 * flop  # three tf32 MMAs per product
+        peak = tf32["tflops"] if tf32 else pk["bf16_tflops"] * TF32_OVER_BF16
+        src = ("measured in this run: " + tf32["how"]) if tf32 else (
+            f"{pk['source']} bf16 burst x 1.1/2.25 (nominal tf32/bf16 ratio)")
+    achieved = tensor_flop / (meas["ms_kern"] * 1e-3) / 1e12
+    kernel_name = meas["main_kernel"].split(" ")[0]
+    out = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+           "frac": achieved / peak, "traffic": stored_traffic(kernel_name, workload),
+           "kernel": meas["main_kernel"], "kernel_ms": meas["ms_kern"],
+           "kernel_timing": "CUDA events around the main kernel on its stream, over a second "
+                            "loop of the same steps right after the timed loop (events between "
+                            "a pre-pass and the main kernel would serialise them)",
+           "work": "3 x 2MNK tf32 MMA FLOPs (3xTF32)" if path != "bf16" else "2MNK bf16 FLOPs",
+           "peak_source": src}
+    if path != "bf16":
+        nominal = pk["bf16_tflops"] * TF32_OVER_BF16
+        out["peak_nominal_ratio"] = {"peak": nominal, "frac": achieved / nominal,
+                                     "note": "bf16 burst x 1.1/2.25 (nominal dense tf32/bf16)"}
+    per_clk = TENSOR_FLOP_PER_CLK_SM["bf16" if path == "bf16" else "tf32"]
+    mhz = ((meas.get("clocks") or {}).get("sm_mhz")) or pk["sm_max_mhz"]
+    pclk = per_clk * sms * mhz * 1e6 / 1e12
+    out["peak_at_sm_clock"] = {
+        "peak": pclk, "frac": achieved / pclk, "unit": "TFLOP/s",
+        "note": f"{per_clk} dense FLOP/clk/SM x {sms} SMs x {mhz:.0f} MHz (median SM clock "
+                "in the timed region)"}
+    return out
+
+
+def device_operands(w, dev):
+    """Host operands of workload w, pinned host copies and device copies."""
+    import numpy as np
+    import torch
+
+    M, N, K = w["M"], w["N"], w["K"]
+    A_h, B_h, Ab_h, Bb_h = host_operands(w)
+    if w["path"] == "bf16":
+        a_pin = torch.from_numpy(Ab_h.view(np.int16).reshape(M, K)).pin_memory()
+        b_pin = torch.from_numpy(Bb_h.view(np.int16).reshape(K, N)).pin_memory()
+    else:
+        a_pin = torch.from_numpy(A_h).pin_memory()
+        b_pin = torch.from_numpy(B_h).pin_memory()
+    return A_h, B_h, a_pin, b_pin, a_pin.to(dev), b_pin.to(dev)
+
+
+def extra_workload(bench, name, args, tf32, sms, want_error):
+    """A further workload of the default run: its own timed steps, main-kernel
+    time, roofline and clocks, and the sampled GPU-vs-oracle error."""
+    import torch
+
+    w = WORKLOADS[name]
+    M, N, K, path = w["M"], w["N"], w["K"], w["path"]
+    A_h, B_h, _, _, a_d, b_d = device_operands(w, bench.dev)
+    c_d = torch.empty((M, N), dtype=torch.float32, device=bench.dev)
+    meas = bench.measure(path, a_d, b_d, c_d, M, N, K, args.steps, args.warmup)
+    flop = 2.0 * M * N * K
+    roof = tensor_roofline(path, flop, meas, name, tf32, sms)
+    roof["cublas_same_run"] = cublas_reference(path, M, N, K, bench.dev, bench.stream,
+                                               roof["achieved"], args.steps, bench.flush,
+                                               w["dist"])
+    out = {"workload": w["desc"], "M": M, "N": N, "K": K, "entry": ENTRY[path],
+           "dtype": DTYPE[path], "dist": w["dist"], "seeds": list(w["seeds"]),
+           "value": aggregate_tflops(bench.ranks.world, flop, meas["ms_step"]), "unit": "TFLOPS",
+           "ms_per_step": meas["ms_step"], "main_kernel_ms": meas["ms_kern"],
+           "roofline": roof, "clocks": meas["clocks"],
+           "gpu_launches": meas["launches_per_call"] * args.steps}
+    if want_error:
+        bench.call(path, a_d, b_d, c_d, M, N, K)
+        torch.cuda.synchronize(bench.dev)
+        out["gpu_vs_oracle_sampled_error"] = sampled_error(A_h, B_h, c_d, M, N, K,
+                                                           w["seeds"][0])
+        out["gpu_vs_oracle_sampled_error"]["tolerance"] = 1e-2 if path == "bf16" else 1e-5
+    del a_d, b_d, c_d
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -417,6 +691,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="with the default workload, skip the 8192^3 3xTF32 and bf16 entries")
     ap.add_argument("--ladder", action="store_true",
                     help="time the pages' naive/tiled kernels beside the build's paths at 4096^3")
     ap.add_argument("--split", default="auto", choices=["auto", "onchip"],
@@ -452,90 +728,23 @@ def main():
     if args.split == "onchip":
         lib.gemm_testing_set_split_mode(2)
     M, N, K = w["M"], w["N"], w["K"]
-    A_h, B_h, Ab_h, Bb_h = host_operands(w)
     path = w["path"]
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
-
-    def device_operands(p):
-        if p == "bf16":
-            a = torch.from_numpy(Ab_h.view(np.int16).reshape(M, K)).pin_memory()
-            b = torch.from_numpy(Bb_h.view(np.int16).reshape(K, N)).pin_memory()
-        else:
-            a = torch.from_numpy(A_h).pin_memory()
-            b = torch.from_numpy(B_h).pin_memory()
-        return a, b, a.to(dev), b.to(dev)
-
-    a_pin, b_pin, a_d, b_d = device_operands(path)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    A_h, B_h, a_pin, b_pin, a_d, b_d = device_operands(w, dev)
     c_d = torch.empty((M, N), dtype=torch.float32, device=dev)
     c_pin = torch.empty((M, N), dtype=torch.float32).pin_memory()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    entry = getattr(lib, ENTRY[path])
-
-    def call(p=path, a=None, b=None):
-        a = a_d if a is None else a
-        b = b_d if b is None else b
-        rc = getattr(lib, ENTRY[p])(a.data_ptr(), b.data_ptr(), c_d.data_ptr(), M, N, K, K, N, N, sh)
-        if rc != mhr.MHR_OK:
-            raise mhr.GemmError(rc, ENTRY[p])
-
-    def timed_steps(p, steps, kernel_events, a=None, b=None):
-        """Per-step CUDA events around each call (L2 flushed before each, outside
-        the events).  With kernel_events, events around the main kernel of each
-        call instead: recorded between a pre-pass and the main kernel, they
-        stop the main kernel from starting programmatically behind the
-        pre-pass, so the step times of such a loop are not used."""
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(steps)]
-        for e in ev:  # create the underlying events
-            for x in e:
-                x.record(stream)
-        torch.cuda.synchronize(dev)
-        for e0, e1 in ev:
-            flush.zero_()
-            if kernel_events:
-                lib.gemm_testing_set_main_kernel_events(e0.cuda_event, e1.cuda_event)
-            else:
-                e0.record(stream)
-            call(p, a, b)
-            if not kernel_events:
-                e1.record(stream)
-        lib.gemm_testing_set_main_kernel_events(None, None)
-        torch.cuda.synchronize(dev)
-        return [e0.elapsed_time(e1) for e0, e1 in ev]
-
+    sampler = ClockSampler(local) if rank == 0 else None
+    bench = Bench(lib, mhr, dev, stream, flush, ranks, sampler)
     barrier = ranks.barrier
     max_over_ranks = ranks.max
 
-    sampler = ClockSampler(local) if rank == 0 else None
-    # ---------------------------------------------------------------- warm-up
-    for _ in range(args.warmup):
-        call()
-    rc = lib.gemm_check(sh)
-    if rc != mhr.MHR_OK:
-        raise mhr.GemmError(rc, "warm-up")
-    main_kernel = lib.gemm_testing_last_main_kernel().decode()
-    # our kernels per call, as counted by the library (pre-passes, zero fills
-    # of split tiles, the main kernel)
-    launches_per_call = lib.gemm_testing_last_launches()
-
     # ---------------------------------------------------------------- timed
-    time.sleep(0.5)  # let the clock sampler start
-    barrier()
-    torch.cuda.synchronize(dev)
-    t_wall0 = time.time()
-    step_ms = timed_steps(path, args.steps, kernel_events=False)
-    torch.cuda.synchronize(dev)
-    barrier()
-    t_wall1 = time.time()
-    # the main kernel alone, over as many steps again, right after (inside the
-    # clock-sampling window); see timed_steps
-    kern_ms = timed_steps(path, args.steps, kernel_events=True)
-    rc = lib.gemm_check(sh)
-    if rc != mhr.MHR_OK:
-        raise mhr.GemmError(rc, "timed region")
-    ms_step = max_over_ranks(sum(step_ms) / len(step_ms))
-    ms_kern = max_over_ranks(sum(kern_ms) / len(kern_ms))
+    time.sleep(0.3)  # let the clock sampler start
+    head = bench.measure(path, a_d, b_d, c_d, M, N, K, args.steps, args.warmup)
+    ms_step, ms_kern = head["ms_step"], head["ms_kern"]
     flop = model.flops(M, N, K)
     value = aggregate_tflops(world, flop, ms_step)
 
@@ -555,7 +764,7 @@ def main():
     for _ in range(e2e_steps):
         a_d.copy_(a_pin, non_blocking=True)
         b_d.copy_(b_pin, non_blocking=True)
-        call()
+        bench.call(path, a_d, b_d, c_d, M, N, K)
         c_pin.copy_(c_d, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize(dev)
@@ -601,20 +810,20 @@ def main():
     t_e2e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(t_e2e0.elapsed_time(t_e2e1) / e2e_steps)
+    del sets[1]
 
     # ------------------------------------- the strict-fp32 SIMT path, same problem
     extra = {}
     if w["also"]:
         also = w["also"]
-        call(also)
+        bench.call(also, a_d, b_d, c_d, M, N, K)
         simt_label = lib.gemm_testing_last_main_kernel().decode()
         n_also = max(3, min(args.steps, 50))
-        s_ms = timed_steps(also, n_also, kernel_events=False)
-        s_k = timed_steps(also, n_also, kernel_events=True)
+        s_ms = bench.timed_steps(also, n_also, False, a_d, b_d, c_d, M, N, K)
+        s_k = bench.timed_steps(also, n_also, True, a_d, b_d, c_d, M, N, K)
         simt_ms = max_over_ranks(sum(s_ms) / len(s_ms))
         simt_k = max_over_ranks(sum(s_k) / len(s_k))
         clock_mhz = peaks()["sm_max_mhz"]
-        sms = torch.cuda.get_device_properties(dev).multi_processor_count
         fp32_peak = sms * FP32_LANES_PER_SM * 2 * clock_mhz * 1e6 / 1e12
         extra[ENTRY[also]] = {
             "value": aggregate_tflops(world, flop, simt_ms), "unit": "TFLOPS", "ms_per_step": simt_ms,
@@ -627,45 +836,25 @@ def main():
                                       f"{clock_mhz:.0f} MHz (max SM clock)"},
         }
 
-    clocks = None
-    if sampler:
-        sampler.stop()
-        clocks = ClockSampler.summary(sampler.window(t_wall0, t_wall1))
+    # ------------------------------------------- the tf32 tensor-pipe ceiling
+    extras_wanted = args.workload == "c2" and not args.no_extra
+    tf32 = None
+    if path == "3xtf32" or extras_wanted:
+        tf32 = cublas_tf32_peak(dev, stream, flush, sampler)
 
     # ---------------------------------------------------------------- roofline
-    pk = peaks()
-    if path == "bf16":
-        tensor_flop, peak_tf, peak_note = flop, pk["bf16_tflops"], "bf16 dense, burst"
-    elif path == "3xtf32":
-        tensor_flop = 3 * flop
-        peak_tf = pk["bf16_tflops"] * TF32_OVER_BF16
-        peak_note = "tf32 = bf16 burst x 1.1/2.25 (nominal tf32/bf16 ratio); 3 MMAs per product"
-    else:
-        tensor_flop, peak_tf, peak_note = flop, None, ""
-    kernel_name = main_kernel.split(" ")[0]
-    achieved = tensor_flop / (ms_kern * 1e-3) / 1e12
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
-                "frac": achieved / peak_tf if peak_tf else None,
-                "traffic": stored_traffic(kernel_name, args.workload),
-                "kernel": main_kernel, "kernel_ms": ms_kern,
-                "kernel_timing": "CUDA events around the main kernel on its stream, over a second "
-                                 "loop of the same steps right after the timed loop (events between "
-                                 "a pre-pass and the main kernel would serialise them)",
-                "peak_source": f"{pk['source']} ({peak_note})"}
+    roofline = None
     if path in ("3xtf32", "bf16"):
-        roofline["cublas_same_run"] = cublas_reference(path, M, N, K, dev, stream, achieved,
-                                                       args.steps, flush, w["dist"])
-        # The nominal tf32 rate corresponds to a lower clock than this kernel
-        # sustains, so also give the dense rate per SM per clock at the SM
-        # clock sampled during the timed region.
-        per_clk = TENSOR_FLOP_PER_CLK_SM["bf16" if path == "bf16" else "tf32"]
-        sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        mhz = (clocks or {}).get("sm_mhz") or pk["sm_max_mhz"]
-        pclk = per_clk * sms * mhz * 1e6 / 1e12
-        roofline["peak_at_sm_clock"] = {
-            "peak": pclk, "frac": achieved / pclk, "unit": "TFLOP/s",
-            "note": f"{per_clk} dense FLOP/clk/SM x {sms} SMs x {mhz:.0f} MHz (median SM clock "
-                    "in the timed region)"}
+        roofline = tensor_roofline(path, flop, head, args.workload, tf32, sms)
+        roofline["cublas_same_run"] = cublas_reference(path, M, N, K, dev, stream,
+                                                       roofline["achieved"], args.steps, flush,
+                                                       w["dist"])
+
+    # ------------------- the two 8192^3 tensor-core configurations of the target
+    if extras_wanted:
+        for name in ("c4", "c5"):
+            extra[name] = extra_workload(bench, name, args, tf32, sms,
+                                         want_error=rank == 0 and not args.no_cpu_baseline)
 
     # ---------------------------------------------------------------- CPU baseline
     cpu = None
@@ -675,8 +864,8 @@ def main():
         oracle.build()
         rows, _ = calibrate_rows(A_h, B_h, args.cpu_budget, M)
         C_ref, t_cpu = oracle_rows(A_h, B_h, rows)
-        # the same rows from the GPU (last timed call's output)
-        call()
+        # the same rows from the GPU
+        bench.call(path, a_d, b_d, c_d, M, N, K)
         torch.cuda.synchronize(dev)
         c_rows = c_d[:rows].cpu().numpy()
         S = np.abs(A_h[:rows].astype(np.float64)) @ np.abs(B_h.astype(np.float64))
@@ -708,6 +897,9 @@ def main():
                           "cores": cpu_tiled.max_threads(), "kind": "cache-blocked fp32 CPU GEMM",
                           "sample": f"the whole {M}x{N}x{K} product, {t_ct:.2f} s"}
 
+    if sampler:
+        sampler.stop()
+
     if rank == 0:
         out = {
             "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
@@ -729,8 +921,9 @@ def main():
                     "note": "per step: pinned host A, B -> device, C API call, C -> pinned host; "
                             "value pipelines consecutive steps over three streams, serial_value "
                             "runs them one after another on one stream"},
-            "gpu_launches": launches_per_call * args.steps,
-            "clocks": clocks,
+            "gpu_launches": head["launches_per_call"] * args.steps,
+            "clocks": dict(head["clocks"] or {}, source=sampler.source if sampler else None),
+            "tf32_peak": tf32,
             "paths": extra,
             "source_digest": source_digest(),
         }

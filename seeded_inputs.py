@@ -27,6 +27,9 @@ and returns both the 16-bit patterns and their exact fp32 widening.
 """
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 
 GOLDEN = np.uint64(0x9E3779B97F4A7C15)
@@ -48,25 +51,47 @@ def splitmix64(seed: int, start: int, count: int) -> np.ndarray:
         return _mix(np.uint64(seed & 0xFFFFFFFFFFFFFFFF) + idx * GOLDEN)
 
 
+def _fill(out: np.ndarray, seed: int, dist: str, s: int, e: int) -> None:
+    """Elements s .. e-1 of the matrix (draws depend only on the index)."""
+    if dist == "uniform":
+        x = splitmix64(seed, s, e - s)
+        out[s:e] = ((x >> np.uint64(40)).astype(np.float64) * 2.0 ** -23 - 1.0)
+    elif dist == "int":
+        x = splitmix64(seed, s, e - s)
+        out[s:e] = ((x >> np.uint64(32)) % np.uint64(5)).astype(np.int64) - 2
+    elif dist == "normal":
+        x = splitmix64(seed, 2 * s, 2 * (e - s))
+        u1 = ((x[0::2] >> np.uint64(11)).astype(np.float64) + 1.0) * 2.0 ** -53
+        u2 = (x[1::2] >> np.uint64(11)).astype(np.float64) * 2.0 ** -53
+        out[s:e] = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
+    else:
+        raise ValueError(f"unknown distribution {dist!r}")
+
+
+def _threads() -> int:
+    try:
+        return max(1, min(16, len(os.sched_getaffinity(0))))
+    except (AttributeError, OSError):
+        return max(1, min(16, os.cpu_count() or 1))
+
+
 def matrix(rows: int, cols: int, seed: int, dist: str = "uniform") -> np.ndarray:
-    """A C-contiguous float32 ``rows x cols`` matrix drawn from ``dist``."""
+    """A C-contiguous float32 ``rows x cols`` matrix drawn from ``dist``.
+
+    Element ``(r, c)`` depends only on its index ``r * cols + c``, so large
+    matrices are filled in chunks on several host threads with identical
+    results."""
+    if dist not in ("uniform", "int", "normal"):
+        raise ValueError(f"unknown distribution {dist!r}")
     n = rows * cols
     out = np.empty(n, dtype=np.float32)
-    for s in range(0, n, _CHUNK):
-        e = min(n, s + _CHUNK)
-        if dist == "uniform":
-            x = splitmix64(seed, s, e - s)
-            out[s:e] = ((x >> np.uint64(40)).astype(np.float64) * 2.0 ** -23 - 1.0)
-        elif dist == "int":
-            x = splitmix64(seed, s, e - s)
-            out[s:e] = ((x >> np.uint64(32)) % np.uint64(5)).astype(np.int64) - 2
-        elif dist == "normal":
-            x = splitmix64(seed, 2 * s, 2 * (e - s))
-            u1 = ((x[0::2] >> np.uint64(11)).astype(np.float64) + 1.0) * 2.0 ** -53
-            u2 = (x[1::2] >> np.uint64(11)).astype(np.float64) * 2.0 ** -53
-            out[s:e] = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
-        else:
-            raise ValueError(f"unknown distribution {dist!r}")
+    chunks = [(s, min(n, s + _CHUNK)) for s in range(0, n, _CHUNK)]
+    if len(chunks) > 1 and _threads() > 1:
+        with ThreadPoolExecutor(max_workers=_threads()) as ex:
+            list(ex.map(lambda se: _fill(out, seed, dist, *se), chunks))
+    else:
+        for s, e in chunks:
+            _fill(out, seed, dist, s, e)
     return out.reshape(rows, cols)
 
 
@@ -76,9 +101,24 @@ def bf16_rne(x: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     Returns ``(bits, widened)``: the uint16 bf16 patterns and the same values
     widened back to fp32 (exact).
     """
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    bias = ((u >> np.uint64(16)) & np.uint64(1)) + np.uint64(0x7FFF)
-    bits = ((u + bias) >> np.uint64(16)).astype(np.uint16)
+    src = np.ascontiguousarray(x, dtype=np.float32)
+    flat = src.reshape(-1).view(np.uint32)
+    bits = np.empty(flat.size, dtype=np.uint16)
+
+    def one(se):
+        s, e = se
+        u = flat[s:e].astype(np.uint64)
+        bias = ((u >> np.uint64(16)) & np.uint64(1)) + np.uint64(0x7FFF)
+        bits[s:e] = ((u + bias) >> np.uint64(16)).astype(np.uint16)
+
+    chunks = [(s, min(flat.size, s + _CHUNK)) for s in range(0, flat.size, _CHUNK)]
+    if len(chunks) > 1 and _threads() > 1:
+        with ThreadPoolExecutor(max_workers=_threads()) as ex:
+            list(ex.map(one, chunks))
+    else:
+        for se in chunks:
+            one(se)
+    bits = bits.reshape(src.shape)
     widened = (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
     return bits, widened
 
