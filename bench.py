@@ -56,6 +56,7 @@ WORKLOADS = {
                also=None, desc="bf16 skinny-deep 512x512x8192 (few tiles, long K)"),
 }
 ENTRY = {"f32": "gemm_f32", "3xtf32": "gemm_f32_3xtf32", "bf16": "gemm_bf16_f32acc"}
+SPLIT_MODES = {"auto": 0, "prepass": 1, "onchip": 2}  # gemm_testing_set_split_mode
 DTYPE = {"f32": "f32", "3xtf32": "tf32x3", "bf16": "bf16"}
 TF32_OVER_BF16 = 1.1 / 2.25   # nominal dense tensor rates (PFLOP/s) of GB300
 # Dense tensor-core rate of one Blackwell SM per clock: 2.25 PFLOP/s bf16 over
@@ -695,10 +696,10 @@ def main():
                     help="with the default workload, skip the 8192^3 3xTF32 and bf16 entries")
     ap.add_argument("--ladder", action="store_true",
                     help="time the pages' naive/tiled kernels beside the build's paths at 4096^3")
-    ap.add_argument("--split", default="auto", choices=["auto", "onchip"],
+    ap.add_argument("--split", default="auto", choices=sorted(SPLIT_MODES),
                     help="3xTF32 workloads: where the operands are split into tf32 parts "
-                         "(auto: the library's choice, a pre-pass; onchip: inside the CTA-pair "
-                         "kernel)")
+                         "(auto: the library's choice; prepass: a split pre-pass; onchip: "
+                         "converter warps of the CTA-pair kernel)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -725,8 +726,7 @@ def main():
     from memory_hierarchy_reuse_gb300 import model
 
     lib = mhr.load()
-    if args.split == "onchip":
-        lib.gemm_testing_set_split_mode(2)
+    lib.gemm_testing_set_split_mode(SPLIT_MODES[args.split])
     M, N, K = w["M"], w["N"], w["K"]
     path = w["path"]
     stream = torch.cuda.current_stream(dev)
@@ -910,8 +910,7 @@ def main():
                        "dist": w["dist"], "seeds": list(w["seeds"]),
                        "l2": "flushed before every timed step (256 MiB write, outside the step events)",
                        "parallelism": "replicas" if world > 1 else "single GPU",
-                       **({"split": "on chip (CTA-pair kernel)" if args.split == "onchip"
-                           else "pre-pass"} if path == "3xtf32" else {})},
+                       **({"split": args.split} if path == "3xtf32" else {})},
             "roofline": roofline,
             "cpu_baseline": cpu,
             "cpu_tiled": cpu_tiled_line,

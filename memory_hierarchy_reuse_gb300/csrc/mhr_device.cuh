@@ -182,6 +182,15 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, const float4 v) {
                : "memory");
 }
 
+__device__ __forceinline__ float4 ld_shared_v4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
 // Make generic-proxy writes to shared memory visible to the async proxy (TMA,
 // tcgen05.mma operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -27,13 +27,14 @@
 //   warp 0     TMA producer (lane 0 issues)
 //   warp 1     TMEM allocator + MMA issuer (lane 0 issues)
 //   warps 2-5  epilogue; warp w reads TMEM lanes 32*(w%4) .. 32*(w%4)+31
-//   (KIND_3XTF32_SPLIT adds warps 6-13 as converters; its warp 0 idles)
+//   (the in-kernel split kinds add warps 6-13 as converters; in
+//   KIND_3XTF32_SPLIT warp 0 idles)
 // The accumulator is double-buffered in TMEM so the epilogue of tile i runs
 // while the MMAs of tile i+1 are issued.  The kernels are launched with
 // programmatic stream serialisation: their set-up overlaps the kernel before
 // them, and griddepcontrol.wait precedes every access to inputs or C.
 //
-// Three kinds:
+// Four kinds:
 //   KIND_BF16:   A bf16 K-major (row-major M x K), B bf16 MN-major (row-major
 //                K x N), kind::f16.
 //   KIND_3XTF32: A_big, A_small K-major; B_big^T, B_small^T K-major (N x K),
@@ -43,6 +44,11 @@
 //                done in the kernel: converter warps load the fp32 operands
 //                from global memory, split them and write the four tf32 parts
 //                into the shared-memory ring in the layout TMA would produce.
+//   KIND_3XTF32_SPLIT_TMA_A (CTA-pair kernel only): the same, except that TMA
+//                stages A itself into the A_big box (the tensor core reads an
+//                fp32 operand as its truncated tf32 big part) and the
+//                converter warps read it there to write A_small; B goes
+//                through the converters' registers as above.
 //
 // Every wait is bounded (DeviceCtl::wait_limit_ns).  A role that runs out of
 // time sets its bit in the device status word and an abort flag in shared
@@ -63,6 +69,7 @@ namespace tc {
 constexpr int KIND_BF16 = 0;
 constexpr int KIND_3XTF32 = 1;
 constexpr int KIND_3XTF32_SPLIT = 2;
+constexpr int KIND_3XTF32_SPLIT_TMA_A = 3;
 
 constexpr int EPI_WARPS = 4;
 constexpr int EPI_BUF_BYTES = 32 * 32 * 4;                 // 32 rows x 32 fp32
@@ -88,12 +95,13 @@ struct TcParams {
   uint32_t* status;
   uint64_t wait_limit_ns;
   int32_t inject_stall;
-  // KIND_3XTF32_SPLIT only: the fp32 operands, row-major, and whether A rows
-  // may be read with 16-byte loads (A 16-byte aligned, lda % 4 == 0).
+  // The in-kernel split kinds only: the fp32 operands, row-major, and whether
+  // A rows and B rows may be read with 16-byte loads (16-byte aligned,
+  // leading dimension a multiple of 4).
   const float* A;
   const float* B;
   int64_t lda, ldb;
-  int32_t vec_a;
+  int32_t vec_a, vec_b;
 };
 
 // Grouped raster: consecutive work units sweep GROUP_M tile rows column by
@@ -256,7 +264,7 @@ inline TcParams make_params(int64_t M, int64_t N, int64_t K, int tile_m, int til
   p.A = nullptr;
   p.B = nullptr;
   p.lda = p.ldb = 0;
-  p.vec_a = 0;
+  p.vec_a = p.vec_b = 0;
   return p;
 }
 
@@ -284,8 +292,10 @@ cudaError_t launch_cta_pair(int kind, const TcMaps& maps, float* C, int64_t M, i
 cudaError_t launch_zero_split_tiles(const TcParams& q, int tile_rows, int tile_cols,
                                     bool after_prepass, cudaStream_t s);
 // The CTA-pair kernel with the 3xTF32 split done in the kernel (no workspace):
-// A (M x K, pitch lda) and B (K x N, pitch ldb) row-major fp32.
-cudaError_t launch_cta_pair_split(const float* A, const float* B, const CUtensorMap& c_map,
+// A (M x K, pitch lda) and B (K x N, pitch ldb) row-major fp32.  `maps` holds
+// the C map (TMA stores) and, with tma_a, A's map (K-major boxes of 32 k x
+// 128 rows) for KIND_3XTF32_SPLIT_TMA_A; else KIND_3XTF32_SPLIT runs.
+cudaError_t launch_cta_pair_split(bool tma_a, const float* A, const float* B, const TcMaps& maps,
                                   float* C, int64_t M, int64_t N, int64_t K, int64_t lda,
                                   int64_t ldb, int64_t ldc, bool c_tma, const DeviceCtl& ctl,
                                   cudaStream_t s);

@@ -82,9 +82,14 @@ cudaError_t launch_tc_3xtf32(const float* a_big, int64_t a_big_ld, const float* 
 cudaError_t launch_tc_3xtf32_split(const float* A, const float* B, float* C, int64_t M,
                                    int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                                    bool c_tma, const DeviceCtl& ctl, cudaStream_t s) {
-  CUtensorMap cm = {};
-  if (encode_c_map(&cm, C, M, N, ldc, c_tma) != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  return launch_cta_pair_split(A, B, cm, C, M, N, K, lda, ldb, ldc, c_tma, ctl, s);
+  TcMaps mp = {};
+  if (encode_c_map(&mp.c, C, M, N, ldc, c_tma) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  // A itself, staged by TMA as its big part, when TMA can address it.
+  const bool tma_a = a_serves_as_big(A, lda);
+  if (tma_a && encode_tmap_2d(&mp.a0, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, K, M, lda * 4, 32, 128,
+                              CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  return launch_cta_pair_split(tma_a, A, B, mp, C, M, N, K, lda, ldb, ldc, c_tma, ctl, s);
 }
 
 }  // namespace mhr

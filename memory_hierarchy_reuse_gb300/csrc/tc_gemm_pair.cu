@@ -73,6 +73,14 @@ struct PairCfg<KIND_3XTF32> {
 // differs (converter warps instead of TMA).
 template <>
 struct PairCfg<KIND_3XTF32_SPLIT> : PairCfg<KIND_3XTF32> {};
+template <>
+struct PairCfg<KIND_3XTF32_SPLIT_TMA_A> : PairCfg<KIND_3XTF32> {};
+
+// Kinds whose ring stages are filled (wholly or partly) by converter warps.
+template <int KIND>
+__host__ __device__ constexpr bool has_converters() {
+  return KIND == KIND_3XTF32_SPLIT || KIND == KIND_3XTF32_SPLIT_TMA_A;
+}
 
 // ------------------------------------------------------------------ in-kernel split
 //
@@ -83,21 +91,27 @@ struct PairCfg<KIND_3XTF32_SPLIT> : PairCfg<KIND_3XTF32> {};
 // operands produce: 128-row x 128-byte K-major boxes with the 128-byte swizzle,
 // 16-byte chunk c of row r at r * 128 + ((c ^ (r % 8)) * 16).  Compared with
 // the split pre-pass, the split operands never exist in HBM, and the kernel
-// needs no workspace.  On GB300 it runs at about 60 % of the speed of the
-// pre-pass path, though: the converter warps are issue-bound (some 16
-// instructions per element at about 1.2 instructions per SM cycle), so the
-// C ABI uses it only when the pre-pass's workspace cannot be allocated.
+// needs no workspace.
 //
-// Thread ct (0..255) of the converter warps owns four chunks of each box per
+// The big part is stored as the fp32 value itself: the tensor core reads an
+// fp32 operand of kind::tf32 as its top 19 bits, which is the truncated big
+// part.  Only the small part takes arithmetic: small = tf32_rn(x - x with its
+// low 13 bits cleared), three instructions per element (finite inputs; an
+// infinite one gives a NaN small part).
+//
+// Thread ct (0..255) of the converter warps, with w = ct % 8, owns per
 // K-block:
-//   A (this CTA's 128 rows x 32 k): chunk (row ct/8 + 32j, k-chunk ct%8) -- one
-//     16-byte load when A allows it; a warp reads 4 rows x 128 contiguous bytes;
-//   B (32 k x this CTA's 128 columns): chunk (column ct%128, k-chunk ct/128 + 2j)
-//     -- four 4-byte loads, one per k, each coalesced across the warp along a
-//     row of B -- stored as row `column` of the K-major box: B is transposed on
-//     the way in.
+//   A (this CTA's 128 rows x 32 k): the 16-byte chunks (row ct/8 + 32j,
+//     k-chunk w), j = 0..3 -- a warp reads 4 rows x 128 contiguous bytes;
+//   B (32 k x this CTA's 128 columns): a 4 x 4 block, k-rows 4w .. 4w+3 of
+//     columns 4nb .. 4nb+3, nb = (ct % 32) / 8 + 4 (ct / 32) -- four 16-byte
+//     row pieces (a warp reads 8 k-rows x 64 contiguous bytes per load),
+//     transposed in registers: column 4nb + i is the 16-byte chunk w of row
+//     4nb + i of the K-major box.  The 8 lanes sharing nb write 8 different
+//     chunk positions w ^ (row % 8).
 // Both store patterns write 8 distinct 16-byte slots per 8 lanes: no bank
-// conflicts.
+// conflicts.  When A or B is not 16-byte aligned with a leading dimension
+// that is a multiple of 4, its pieces are read element by element.
 //
 // Latency: a thread keeps two K-blocks of loads in flight in two register
 // sets used in turn, issuing a block's loads after the proxy fence of the
@@ -109,13 +123,21 @@ constexpr int SPLIT_THREADS = 32 * SPLIT_WARPS;
 constexpr int SPLIT_CHUNKS = 4;    // per thread, per operand, per K-block
 constexpr int SPLIT_PREFETCH = 4;  // K-blocks between the L2 prefetches and the loads
 
+// Groups of SPLIT_WARPS converter warps that take K-blocks in turn (see the
+// split kinds below).
+template <int KIND>
+constexpr int converter_groups() {
+  return KIND == KIND_3XTF32_SPLIT_TMA_A ? 2 : has_converters<KIND>() ? 1 : 0;
+}
+
 template <int KIND>
 constexpr int pair_threads() {
-  return KIND == KIND_3XTF32_SPLIT ? NUM_THREADS + SPLIT_THREADS : NUM_THREADS;
+  return NUM_THREADS + converter_groups<KIND>() * SPLIT_THREADS;
 }
 
 struct SplitRegs {
-  float4 a[SPLIT_CHUNKS], b[SPLIT_CHUNKS];
+  float4 a[SPLIT_CHUNKS];  // A chunk j
+  float4 b[SPLIT_CHUNKS];  // B k-row 4w + j, columns 4nb .. 4nb+3
 };
 
 // This CTA's boxes of work unit u, and the unit's K-block range.
@@ -132,26 +154,35 @@ __device__ __forceinline__ bool unit_boxes(const TcParams& p, int u, uint32_t ra
   return true;
 }
 
-// The next K-block whose loads a converter thread issues: its chunk-0
-// addresses at k = 0, the row of its A chunk 0 and the column of its B chunks.
+// The next K-block whose loads a converter thread issues: pointers to its A
+// chunk 0 and its B row 4w at that K-block, and whether the unit's boxes lie
+// inside the matrices in M and N (only K is then checked, per block).
 struct LoadCursor {
   const float* a;
   const float* b;
   int arow, bcol, u, kb, kb1;
-  bool valid;
+  bool valid, interior;
 
   __device__ __forceinline__ void seek(const TcParams& p, int unit, uint32_t rank, int ct) {
     int m0, nb0;
     valid = unit_boxes(p, unit, rank, m0, nb0, kb, kb1);
     if (!valid) return;
     u = unit;
+    const int w = ct & 7, nb = ((ct & 31) >> 3) + 4 * (ct >> 5);
     arow = m0 + (ct >> 3);
-    bcol = nb0 + (ct & 127);
-    a = p.A + static_cast<int64_t>(arow) * p.lda + 4 * (ct & 7);
-    b = p.B + static_cast<int64_t>(4 * (ct >> 7)) * p.ldb + bcol;
+    bcol = nb0 + 4 * nb;
+    interior = m0 + PAIR_TILE_M / 2 <= p.M && nb0 + PAIR_TILE_N / 2 <= p.N;
+    a = p.A + static_cast<int64_t>(arow) * p.lda + 32 * kb + 4 * w;
+    b = p.B + static_cast<int64_t>(32 * kb + 4 * w) * p.ldb + bcol;
   }
   __device__ __forceinline__ void advance(const TcParams& p, int stride, uint32_t rank, int ct) {
-    if (valid && ++kb == kb1) seek(p, u + stride, rank, ct);
+    if (!valid) return;
+    if (++kb == kb1) {
+      seek(p, u + stride, rank, ct);
+    } else {
+      a += 32;
+      b += 32 * p.ldb;
+    }
   }
 };
 
@@ -168,55 +199,59 @@ struct PrefetchCursor {
   }
 };
 
-// Loads of K-block c.kb into r.  Blocks wholly inside K (all but a ragged
-// last one) skip the per-element K checks.
-template <bool VA>
+template <bool VEC>
+__device__ __forceinline__ float4 load4(const float* src) {
+  if constexpr (VEC) {
+    return __ldg(reinterpret_cast<const float4*>(src));
+  } else {
+    return make_float4(__ldg(src), __ldg(src + 1), __ldg(src + 2), __ldg(src + 3));
+  }
+}
+
+// The first `n` (0..3) of 4 consecutive elements, the rest zero.
+__device__ __forceinline__ float4 load_partial(const float* src, int n, int64_t stride) {
+  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (n > 0) v.x = __ldg(src);
+  if (n > 1) v.y = __ldg(src + stride);
+  if (n > 2) v.z = __ldg(src + 2 * stride);
+  return v;
+}
+
+// Loads of K-block c.kb into r; elements outside the matrices read as zero.
+template <bool VA, bool VB>
 __device__ __forceinline__ void split_load(SplitRegs& r, const TcParams& p, const LoadCursor& c,
                                            int ct) {
+  const int64_t lda32 = 32 * p.lda;
   const int k0 = c.kb * 32;
-  const bool full_k = k0 + 32 <= p.K;
-  const int ka = k0 + 4 * (ct & 7);  // first k of the thread's A chunks
+  if (c.interior && k0 + 32 <= p.K) {  // the whole box is inside: no checks
+#pragma unroll
+    for (int j = 0; j < SPLIT_CHUNKS; ++j) r.a[j] = load4<VA>(c.a + j * lda32);
+#pragma unroll
+    for (int j = 0; j < SPLIT_CHUNKS; ++j) r.b[j] = load4<VB>(c.b + j * p.ldb);
+    return;
+  }
+  const int ka = k0 + 4 * (ct & 7);  // first k of the thread's A chunks and B rows
 #pragma unroll
   for (int j = 0; j < SPLIT_CHUNKS; ++j) {
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (c.arow + 32 * j < p.M) {
-      const float* src = c.a + static_cast<int64_t>(32 * j) * p.lda + k0;
-      if (full_k) {
-        if (VA) {
-          v = __ldg(reinterpret_cast<const float4*>(src));
-        } else {
-          v.x = __ldg(src);
-          v.y = __ldg(src + 1);
-          v.z = __ldg(src + 2);
-          v.w = __ldg(src + 3);
-        }
-      } else if (ka < p.K) {
-        v.x = __ldg(src);
-        if (ka + 1 < p.K) v.y = __ldg(src + 1);
-        if (ka + 2 < p.K) v.z = __ldg(src + 2);
-        if (ka + 3 < p.K) v.w = __ldg(src + 3);
-      }
+      const float* src = c.a + j * lda32;
+      if (ka + 4 <= p.K)
+        v = load4<VA>(src);
+      else if (ka < p.K)
+        v = load_partial(src, p.K - ka, 1);
     }
     r.a[j] = v;
   }
-  const int kb_first = k0 + 4 * (ct >> 7);  // first k of the thread's B chunk 0
 #pragma unroll
   for (int j = 0; j < SPLIT_CHUNKS; ++j) {
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    const int k = kb_first + 8 * j;
-    if (c.bcol < p.N) {
-      const float* src = c.b + static_cast<int64_t>(k0 + 8 * j) * p.ldb;
-      if (full_k) {
-        v.x = __ldg(src);
-        v.y = __ldg(src + p.ldb);
-        v.z = __ldg(src + 2 * p.ldb);
-        v.w = __ldg(src + 3 * p.ldb);
-      } else if (k < p.K) {
-        v.x = __ldg(src);
-        if (k + 1 < p.K) v.y = __ldg(src + p.ldb);
-        if (k + 2 < p.K) v.z = __ldg(src + 2 * p.ldb);
-        if (k + 3 < p.K) v.w = __ldg(src + 3 * p.ldb);
-      }
+    if (ka + j < p.K) {
+      const float* src = c.b + j * p.ldb;
+      if (c.bcol + 4 <= p.N)
+        v = load4<VB>(src);
+      else if (c.bcol < p.N)
+        v = load_partial(src, p.N - c.bcol, 1);
     }
     r.b[j] = v;
   }
@@ -250,29 +285,108 @@ __device__ __forceinline__ void split_prefetch_l2(const TcParams& p, int ct,
   }
 }
 
+// A converter thread's fixed store offsets within a stage's boxes: its A
+// chunk 0 (chunk j is 4 KB further: 32 rows) and its four B columns' chunks.
+struct StoreOffsets {
+  uint32_t a;
+  uint32_t b[4];
+  __device__ __forceinline__ explicit StoreOffsets(int ct) {
+    const int w = ct & 7, row = ct >> 3;
+    a = row * 128 + ((w ^ (row & 7)) << 4);
+    const int nb = ((ct & 31) >> 3) + 4 * (ct >> 5);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int n = 4 * nb + i;
+      b[i] = n * 128 + ((w ^ (n & 7)) << 4);
+    }
+  }
+};
+
 // Split the registers of one K-block into ring stage `st`: A_big, A_small,
-// B_big^T, B_small^T boxes of 16 KB each, in that order.
-__device__ __forceinline__ void split_store(const SplitRegs& r, uint32_t st, int ct) {
+// B_big^T, B_small^T boxes of 16 KB each, in that order; the big parts are the
+// values themselves (see above).
+__device__ __forceinline__ void split_store(const SplitRegs& r, uint32_t st,
+                                            const StoreOffsets& o) {
   using Cf = PairCfg<KIND_3XTF32>;
 #pragma unroll
   for (int j = 0; j < SPLIT_CHUNKS; ++j) {
-    const int idx = ct + SPLIT_THREADS * j;
-    const int row = idx >> 3, c = idx & 7;
-    const uint32_t off = row * 128 + ((c ^ (row & 7)) << 4);
-    float4 big, small;
-    split4_trunc<true>(r.a[j], big, small);  // as the pre-pass splits A
-    st_shared_v4(st + off, big);
-    st_shared_v4(st + Cf::A_BYTES + off, small);
+    const uint32_t off = o.a + j * 4096;
+    st_shared_v4(st + off, r.a[j]);
+    st_shared_v4(st + Cf::A_BYTES + off, small4_tf32_trunc(r.a[j]));
   }
+  const float4 col[4] = {make_float4(r.b[0].x, r.b[1].x, r.b[2].x, r.b[3].x),
+                         make_float4(r.b[0].y, r.b[1].y, r.b[2].y, r.b[3].y),
+                         make_float4(r.b[0].z, r.b[1].z, r.b[2].z, r.b[3].z),
+                         make_float4(r.b[0].w, r.b[1].w, r.b[2].w, r.b[3].w)};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    st_shared_v4(st + 2 * Cf::A_BYTES + o.b[i], col[i]);
+    st_shared_v4(st + 2 * Cf::A_BYTES + Cf::B_BYTES + o.b[i], small4_tf32_trunc(col[i]));
+  }
+}
+
+// ------------------------------------------------- in-kernel split, A staged by TMA
+//
+// KIND_3XTF32_SPLIT_TMA_A: when A is 16-byte aligned with lda a multiple of 4,
+// each CTA's producer warp TMA-loads A's box (128 rows x 32 k) into the stage's
+// A_big box, completing on a barrier of its own CTA (a_full[s]); the tensor
+// core reads it there as A's truncated big part.  The converter warps read
+// their A chunks back from that box (the positions they would have stored
+// to), write A_small, and take B through registers as in KIND_3XTF32_SPLIT.
+//
+// Two groups of SPLIT_WARPS converter warps take the K-blocks in turn (even
+// and odd).  A thread issues the B loads of its group's next K-block right
+// after handing over the current one, so they have two K-block times to land,
+// and it never has loads outstanding when it executes its proxy fence: on
+// GB300 that fence also waits for the thread's outstanding global loads,
+// which made one group with several register sets no faster than one load
+// round trip per K-block (1.7 us against 0.8 us of MMAs, measured).
+// Shared memory carries per stage TMA's 16 KB of A, the converters' 16 KB of
+// A reads and 48 KB of stores, and the MMAs' 96 KB of operand reads.
+struct BRegs {
+  float4 b[SPLIT_CHUNKS];  // B k-row 4w + j, columns 4nb .. 4nb+3
+};
+
+template <bool VB>
+__device__ __forceinline__ void load_b(BRegs& r, const TcParams& p, const LoadCursor& c, int ct) {
+  const int k0 = c.kb * 32;
+  if (c.bcol + 4 <= p.N && k0 + 32 <= p.K) {
+#pragma unroll
+    for (int j = 0; j < SPLIT_CHUNKS; ++j) r.b[j] = load4<VB>(c.b + j * p.ldb);
+    return;
+  }
+  const int kb_row = k0 + 4 * (ct & 7);
 #pragma unroll
   for (int j = 0; j < SPLIT_CHUNKS; ++j) {
-    const int idx = ct + SPLIT_THREADS * j;
-    const int row = idx & 127, c = idx >> 7;
-    const uint32_t off = row * 128 + ((c ^ (row & 7)) << 4);
-    float4 big, small;
-    split4<true>(r.b[j], big, small);
-    st_shared_v4(st + 2 * Cf::A_BYTES + off, big);
-    st_shared_v4(st + 2 * Cf::A_BYTES + Cf::B_BYTES + off, small);
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (kb_row + j < p.K) {
+      const float* src = c.b + j * p.ldb;
+      if (c.bcol + 4 <= p.N)
+        v = load4<VB>(src);
+      else if (c.bcol < p.N)
+        v = load_partial(src, p.N - c.bcol, 1);
+    }
+    r.b[j] = v;
+  }
+}
+
+// A_small from the staged A box, and B_big^T, B_small^T from registers.
+__device__ __forceinline__ void split_store_tma_a(const BRegs& r, uint32_t st,
+                                                  const StoreOffsets& o) {
+  using Cf = PairCfg<KIND_3XTF32>;
+#pragma unroll
+  for (int j = 0; j < SPLIT_CHUNKS; ++j) {
+    const uint32_t off = o.a + j * 4096;
+    st_shared_v4(st + Cf::A_BYTES + off, small4_tf32_trunc(ld_shared_v4(st + off)));
+  }
+  const float4 col[4] = {make_float4(r.b[0].x, r.b[1].x, r.b[2].x, r.b[3].x),
+                         make_float4(r.b[0].y, r.b[1].y, r.b[2].y, r.b[3].y),
+                         make_float4(r.b[0].z, r.b[1].z, r.b[2].z, r.b[3].z),
+                         make_float4(r.b[0].w, r.b[1].w, r.b[2].w, r.b[3].w)};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    st_shared_v4(st + 2 * Cf::A_BYTES + o.b[i], col[i]);
+    st_shared_v4(st + 2 * Cf::A_BYTES + Cf::B_BYTES + o.b[i], small4_tf32_trunc(col[i]));
   }
 }
 
@@ -281,7 +395,7 @@ struct PairLayout {
   using C = PairCfg<KIND>;
   static constexpr int EPI_OFF = C::STAGES * C::STAGE_BYTES;
   static constexpr int BAR_OFF = EPI_OFF + EPI_BYTES;
-  static constexpr int NUM_BARS = 2 * C::STAGES + 6;
+  static constexpr int NUM_BARS = 3 * C::STAGES + 6;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int USED = MISC_OFF + 16;
   static constexpr int ALLOC = USED + 1024;
@@ -308,6 +422,8 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
   const uint32_t drain_bar = bar0 + 8u * (2 * Cf::STAGES + 4);
   // rank 0 only: rank 1's producer arrives here once it has issued its last load
   const uint32_t peer_done_bar = bar0 + 8u * (2 * Cf::STAGES + 5);
+  // KIND_3XTF32_SPLIT_TMA_A, each CTA: its own TMA load of A's box into stage s
+  auto a_full_bar = [&](uint32_t s) { return bar0 + 8u * (2 * Cf::STAGES + 6 + s); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
   // rank 0 only: how many ring stages rank 1's producer loaded
@@ -323,10 +439,11 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
   if (threadIdx.x == 0) {
     // full[s]: one arrive.expect_tx by the TMA producer, or one arrive per
     // converter warp of both CTAs (split kind)
-    constexpr uint32_t full_count = KIND == KIND_3XTF32_SPLIT ? 2 * SPLIT_WARPS : 1;
+    constexpr uint32_t full_count = has_converters<KIND>() ? 2 * SPLIT_WARPS : 1;
     for (int s = 0; s < Cf::STAGES; ++s) {
       mbar_init(full_bar(s), full_count);
       mbar_init(empty_bar(s), 1);
+      if constexpr (KIND == KIND_3XTF32_SPLIT_TMA_A) mbar_init(a_full_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
@@ -337,10 +454,8 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
     *abort_flag = 0;
     *peer_loaded = 0;
     fence_mbar_init();
-    if constexpr (KIND != KIND_3XTF32_SPLIT) {
-      tma_prefetch_desc(&tmA0);
-      tma_prefetch_desc(&tmB0);
-    }
+    if constexpr (KIND != KIND_3XTF32_SPLIT) tma_prefetch_desc(&tmA0);
+    if constexpr (!has_converters<KIND>()) tma_prefetch_desc(&tmB0);
     if constexpr (KIND == KIND_3XTF32) {
       tma_prefetch_desc(&tmA1);
       tma_prefetch_desc(&tmB1);
@@ -375,7 +490,46 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
     // ------------------------------------------------------------ producers (both CTAs)
     // One thread waits, arms and issues; the rest of the warp idles.  (The
     // split kind has converter warps instead; its warp 0 only idles.)
-    if (KIND != KIND_3XTF32_SPLIT && lane == 0) {
+    if (KIND == KIND_3XTF32_SPLIT_TMA_A && lane == 0) {
+      // This CTA's A boxes, into the A_big box of each stage, on its own
+      // barriers (its converter warps wait for them).
+      uint32_t it = 0;
+      bool stalled_first = false;
+      for (int u = cluster; u < p.num_units; u += num_clusters) {
+        const Unit w = unit_of(u, p);
+        int tm, tn;
+        tile_coords(w.tile, p, tm, tn);
+        const int m0 = tm * 2 * Cf::BM + static_cast<int>(rank) * Cf::BM;
+        bool ok = true;
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+          const uint32_t s = it % Cf::STAGES, ph = (it / Cf::STAGES) & 1u;
+          if (!mbar_wait_bounded(empty_bar(s), ph ^ 1u, limit, abort_flag)) {
+            give_up_one(kErrTimeoutProducer);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(a_full_bar(s), Cf::A_BYTES);
+          // test hook: block 0 arms its first stage without loading it
+          if (!(p.inject_stall && blockIdx.x == 0 && it == 0))
+            tma_load_2d(sbase + s * Cf::STAGE_BYTES, &tmA0, a_full_bar(s), kb * Cf::BK, m0);
+          else
+            stalled_first = true;
+          ++it;
+        }
+        if (!ok) break;
+      }
+      // Drain: wait for this CTA's loads of the last STAGES iterations (earlier
+      // phases were waited for by the converters before the stage was reused).
+      // A stage armed without its load is counted as done.
+      volatile int never = 0;
+      for (uint32_t i = it > static_cast<uint32_t>(Cf::STAGES) ? it - Cf::STAGES : 0; i < it;
+           ++i) {
+        const uint32_t s = i % Cf::STAGES, ph = (i / Cf::STAGES) & 1u;
+        if (stalled_first && i == 0) mbar_complete_tx(a_full_bar(s), Cf::A_BYTES);
+        if (!mbar_wait_bounded(a_full_bar(s), ph, limit, &never))
+          atomicOr(p.status, kErrTimeoutDrain);
+      }
+    } else if (!has_converters<KIND>() && lane == 0) {
       // `it` counts the ring stages this producer armed (rank 0) and loaded;
       // with the injected stall, block 0's first stage is armed but not loaded.
       uint32_t it = 0;
@@ -482,7 +636,7 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
           const uint32_t s = it % Cf::STAGES, ph = (it / Cf::STAGES) & 1u;
           // the split kind's stages are completed by plain stores from both
           // CTAs, released at cluster scope
-          if (!mbar_wait_bounded<KIND == KIND_3XTF32_SPLIT>(full_bar(s), ph, limit, abort_flag)) {
+          if (!mbar_wait_bounded<has_converters<KIND>()>(full_bar(s), ph, limit, abort_flag)) {
             give_up_one(kErrTimeoutMma);
             ok = false;
             break;
@@ -563,11 +717,60 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
       if (lane == 0) bulk_wait_group<0>();
       __syncwarp();
     }
+  } else if constexpr (KIND == KIND_3XTF32_SPLIT_TMA_A) {
+    // ------------------------------------------------------------ converters (both CTAs)
+    // Group g takes the cluster's K-blocks g, g + 2, g + 4, ...
+    const int g = (threadIdx.x - NUM_THREADS) / SPLIT_THREADS;
+    const int ct = (threadIdx.x - NUM_THREADS) % SPLIT_THREADS;
+    const StoreOffsets so(ct);
+    auto convert = [&](auto vec_b) {
+      constexpr bool VB = decltype(vec_b)::value;
+      int total = 0;  // how many K-blocks this cluster stores
+      for (int u = cluster; u < p.num_units; u += num_clusters) {
+        const Unit w = unit_of(u, p);
+        total += w.kb1 - w.kb0;
+      }
+      LoadCursor ld;
+      ld.seek(p, cluster, rank, ct);
+      PrefetchCursor pf;
+      pf.seek(p, cluster, rank);
+      for (int d = 0; d < g; ++d) ld.advance(p, num_clusters, rank, ct);
+      for (int d = 0; d < g + 2 + SPLIT_PREFETCH; ++d) {
+        if (d >= g + 2 && ((d - g) & 1) == 0) split_prefetch_l2(p, ct, pf);
+        pf.advance(p, num_clusters, rank);
+      }
+      BRegs r;
+      if (g < total) load_b<VB>(r, p, ld, ct);
+      for (int it = g; it < total; it += 2) {
+        const uint32_t s = it % Cf::STAGES, ph = (it / Cf::STAGES) & 1u;
+        if (!warp_wait(empty_bar(s), ph ^ 1u, limit, abort_flag) ||
+            !warp_wait(a_full_bar(s), ph, limit, abort_flag)) {
+          give_up_pair(kErrTimeoutProducer);
+          break;
+        }
+        split_store_tma_a(r, sbase + s * Cf::STAGE_BYTES, so);
+        fence_proxy_async_smem();  // the stores, visible to the pair's MMA reads
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(full_bar(s), 0));
+        // the group's next K-block: its loads, and a prefetch two blocks further
+        ld.advance(p, num_clusters, rank, ct);
+        ld.advance(p, num_clusters, rank, ct);
+        if (it + 2 < total) load_b<VB>(r, p, ld, ct);
+        split_prefetch_l2(p, ct, pf);
+        pf.advance(p, num_clusters, rank);
+        pf.advance(p, num_clusters, rank);
+      }
+    };
+    if (p.vec_b)
+      convert(std::true_type{});
+    else
+      convert(std::false_type{});
   } else if constexpr (KIND == KIND_3XTF32_SPLIT) {
     // ------------------------------------------------------------ converters (both CTAs)
     const int ct = threadIdx.x - NUM_THREADS;
-    auto convert = [&](auto vec_a) {
-      constexpr bool VA = decltype(vec_a)::value;
+    const StoreOffsets so(ct);
+    auto convert = [&](auto vec_a, auto vec_b) {
+      constexpr bool VA = decltype(vec_a)::value, VB = decltype(vec_b)::value;
       // how many K-blocks this cluster stores
       int left = 0;
       for (int u = cluster; u < p.num_units; u += num_clusters) {
@@ -584,9 +787,9 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
         pf.advance(p, num_clusters, rank);
       }
       SplitRegs r0, r1;
-      split_load<VA>(r0, p, ld, ct);
+      split_load<VA, VB>(r0, p, ld, ct);
       ld.advance(p, num_clusters, rank, ct);
-      if (ld.valid) split_load<VA>(r1, p, ld, ct);
+      if (ld.valid) split_load<VA, VB>(r1, p, ld, ct);
       ld.advance(p, num_clusters, rank, ct);
       uint32_t it = 0;
       // Store the K-block held in r, then reuse r for the loads two blocks on.
@@ -596,7 +799,7 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
           give_up_pair(kErrTimeoutProducer);
           return false;
         }
-        split_store(r, sbase + s * Cf::STAGE_BYTES, ct);
+        split_store(r, sbase + s * Cf::STAGE_BYTES, so);
         fence_proxy_async_smem();  // the stores, visible to the pair's MMA reads
         __syncwarp();
         // test hook: block 0 never completes its first stage
@@ -604,7 +807,7 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
         if (lane == 0 && !stall) mbar_arrive_cluster(mapa_shared(full_bar(s), 0));
         ++it;
         if (--left == 0) return false;
-        if (ld.valid) split_load<VA>(r, p, ld, ct);
+        if (ld.valid) split_load<VA, VB>(r, p, ld, ct);
         ld.advance(p, num_clusters, rank, ct);
         split_prefetch_l2(p, ct, pf);
         pf.advance(p, num_clusters, rank);
@@ -613,10 +816,14 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
       while (step(r0) && step(r1)) {
       }
     };
-    if (p.vec_a)
-      convert(std::true_type{});
+    if (p.vec_a && p.vec_b)
+      convert(std::true_type{}, std::true_type{});
+    else if (p.vec_a)
+      convert(std::true_type{}, std::false_type{});
+    else if (p.vec_b)
+      convert(std::false_type{}, std::true_type{});
     else
-      convert(std::false_type{});
+      convert(std::false_type{}, std::false_type{});
   }
 
   tc_fence_before();
@@ -711,9 +918,10 @@ cudaError_t launch_pair_t(const TcMaps& mp, const TcParams& p, bool after_prepas
   }
   cfg.gridDim = dim3(2 * clusters);
   cfg.numAttrs = 2;  // and programmatic serialisation behind the kernel before
-  note_main_kernel(KIND == KIND_BF16     ? "tc_gemm_pair_kernel<bf16>"
-                   : KIND == KIND_3XTF32 ? "tc_gemm_pair_kernel<3xtf32>"
-                                         : "tc_gemm_pair_kernel<3xtf32,split>",
+  note_main_kernel(KIND == KIND_BF16                 ? "tc_gemm_pair_kernel<bf16>"
+                   : KIND == KIND_3XTF32             ? "tc_gemm_pair_kernel<3xtf32>"
+                   : KIND == KIND_3XTF32_SPLIT_TMA_A ? "tc_gemm_pair_kernel<3xtf32,split,tma-a>"
+                                                     : "tc_gemm_pair_kernel<3xtf32,split>",
                    2 * clusters, p.num_tiles);
   e = cudaLaunchKernelEx(&cfg, kern, mp.a0, mp.a1, mp.b0, mp.b1, mp.c, q);
   if (e != cudaSuccess) return e;
@@ -740,7 +948,7 @@ cudaError_t launch_zero_split_tiles(const TcParams& q, int tile_rows, int tile_c
   return cudaLaunchKernelEx(&cfg, zero_split_tiles_kernel, q, tile_rows, tile_cols, vec);
 }
 
-cudaError_t launch_cta_pair_split(const float* A, const float* B, const CUtensorMap& c_map,
+cudaError_t launch_cta_pair_split(bool tma_a, const float* A, const float* B, const TcMaps& maps,
                                   float* C, int64_t M, int64_t N, int64_t K, int64_t lda,
                                   int64_t ldb, int64_t ldc, bool c_tma, const DeviceCtl& ctl,
                                   cudaStream_t s) {
@@ -751,10 +959,12 @@ cudaError_t launch_cta_pair_split(const float* A, const float* B, const CUtensor
   p.lda = lda;
   p.ldb = ldb;
   p.vec_a = (reinterpret_cast<uintptr_t>(A) % 16 == 0) && (lda % 4 == 0);
-  TcMaps mp;  // only the C map is read (TMA stores); the operand maps are unused
-  mp.a0 = mp.a1 = mp.b0 = mp.b1 = mp.c = c_map;
-  return c_tma ? launch_pair_t<KIND_3XTF32_SPLIT, true>(mp, p, false, ctl, s)
-               : launch_pair_t<KIND_3XTF32_SPLIT, false>(mp, p, false, ctl, s);
+  p.vec_b = (reinterpret_cast<uintptr_t>(B) % 16 == 0) && (ldb % 4 == 0);
+  if (tma_a)
+    return c_tma ? launch_pair_t<KIND_3XTF32_SPLIT_TMA_A, true>(maps, p, false, ctl, s)
+                 : launch_pair_t<KIND_3XTF32_SPLIT_TMA_A, false>(maps, p, false, ctl, s);
+  return c_tma ? launch_pair_t<KIND_3XTF32_SPLIT, true>(maps, p, false, ctl, s)
+               : launch_pair_t<KIND_3XTF32_SPLIT, false>(maps, p, false, ctl, s);
 }
 
 cudaError_t launch_cta_pair(int kind, const TcMaps& maps, float* C, int64_t M, int64_t N,

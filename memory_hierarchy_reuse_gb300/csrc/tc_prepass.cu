@@ -30,8 +30,8 @@ __global__ void pack_u16_kernel(const uint16_t* __restrict__ src, int64_t rows, 
 // Split of both operands in one launch.  Blocks [0, a_blocks) split rows of
 // A in place order (big part truncated, see split_tf32_trunc; with a_big null
 // only the small part is written, A itself serving as A_big); the remaining
-// blocks split 64 x 64 tiles of B (big part rounded) and write them
-// transposed.  VA selects 16-byte loads of A when its address, leading
+// blocks split 64 x 64 tiles of B (big part truncated too, as the fused split
+// reads B itself as its big part) and write them transposed.  VA selects 16-byte loads of A when its address, leading
 // dimension and K allow them, else 4-byte loads; VB is the width in floats of
 // B's loads, 4, 2 or 1, the widest that B's address, leading dimension and N
 // allow.  The outputs (pitch Kp, a multiple of 4, in the 16-byte-aligned
@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS)
         const int idx = t + j * SPLIT_THREADS;
         const int kr = idx >> 4, nc = (idx & 15) * 4;
         float4 b, s;
-        split4<true>(v[j], b, s);
+        split4_trunc<true>(v[j], b, s);
         tb[kr][nc] = b.x; tb[kr][nc + 1] = b.y; tb[kr][nc + 2] = b.z; tb[kr][nc + 3] = b.w;
         ts[kr][nc] = s.x; ts[kr][nc + 1] = s.y; ts[kr][nc + 2] = s.z; ts[kr][nc + 3] = s.w;
       }
@@ -166,8 +166,8 @@ __global__ void __launch_bounds__(SPLIT_THREADS)
         const int idx = t + j * SPLIT_THREADS;
         const int kr = idx >> 5, nc = (idx & 31) * 2;
         float b0, s0, b1, s1;
-        split_tf32<false>(v[j].x, b0, s0);
-        split_tf32<false>(v[j].y, b1, s1);
+        split_tf32_trunc<false>(v[j].x, b0, s0);
+        split_tf32_trunc<false>(v[j].y, b1, s1);
         tb[kr][nc] = b0; tb[kr][nc + 1] = b1;
         ts[kr][nc] = s0; ts[kr][nc + 1] = s1;
       }
@@ -183,7 +183,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS)
       for (int j = 0; j < 16; ++j) {
         const int idx = t + j * SPLIT_THREADS;
         float b, sm;
-        split_tf32<false>(v[j], b, sm);  // integer rounding: this 4-byte-load branch is latency-bound
+        split_tf32_trunc<false>(v[j], b, sm);  // integer rounding: this 4-byte-load branch is latency-bound
         tb[idx >> 6][idx & 63] = b;
         ts[idx >> 6][idx & 63] = sm;
       }

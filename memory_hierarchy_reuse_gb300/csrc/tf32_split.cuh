@@ -1,8 +1,9 @@
 // The 3xTF32 split of one fp32 value into two tf32 parts, big + small, used
 // by the split pre-pass (tc_prepass.cu) and by the CTA-pair kernel's in-kernel
 // converter warps (tc_gemm_pair.cu).  big keeps the top 11 significant bits
-// of x -- rounded to nearest-even for B, truncated for A (below) -- and small
-// is the exact remainder x - big, itself rounded to tf32.  Products
+// of x, truncated (below: that is what the tensor core reads from an fp32
+// operand, so A and B themselves can serve as their big parts), and small is
+// the exact remainder x - big, itself rounded to tf32.  Products
 // big*big + big*small + small*big then carry about 22 significant bits,
 // against 11 for one tf32 product.
 #pragma once
@@ -40,25 +41,31 @@ __device__ __forceinline__ float tf32_rne(float x) {
   }
 }
 
-// small is zero when big already equals x, which also covers infinities
-// (where x - big would be NaN).
-template <bool CVT>
-__device__ __forceinline__ void split_tf32(float x, float& big, float& small) {
-  big = tf32_rne<CVT>(x);
-  const float rest = x - big;  // exact: the discarded low bits
-  small = big == x ? 0.f : tf32_rne<CVT>(rest);
-}
-
-// The split with a truncated big part, used for A: big = x with its low 13
-// bits cleared, which is what the tensor core itself reads from an fp32
-// operand under kind::tf32 (measured on GB300: u & ~0x1FFF for every value of
-// a sweep), so A itself can serve as A_big; small = the exact remainder x -
-// big, below 2^-10 |x|, rounded to tf32 to nearest.
+// The split: big = x with its low 13 bits cleared, which is what the tensor
+// core itself reads from an fp32 operand under kind::tf32 (measured on GB300:
+// u & ~0x1FFF for every value of a sweep), so A and B themselves can serve as
+// their big parts; small = the exact remainder x - big, below 2^-10 |x|,
+// rounded to tf32 to nearest.  small is zero when big already equals x, which
+// also covers infinities (where x - big would be NaN).
 template <bool CVT>
 __device__ __forceinline__ void split_tf32_trunc(float x, float& big, float& small) {
   big = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
   const float rest = x - big;  // exact
   small = big == x ? 0.f : tf32_rne<CVT>(rest);
+}
+
+// The small part alone for a truncated big part, small = tf32_rn(x - (x with
+// its low 13 bits cleared)), for finite x (an infinite x gives NaN here, where
+// split_tf32_trunc gives 0).  Used where the big part is x itself, read by the
+// tensor core.
+__device__ __forceinline__ float small_tf32_trunc(float x) {
+  const float big = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+  return tf32_rne<true>(x - big);  // x - big is exact
+}
+
+__device__ __forceinline__ float4 small4_tf32_trunc(const float4 v) {
+  return make_float4(small_tf32_trunc(v.x), small_tf32_trunc(v.y), small_tf32_trunc(v.z),
+                     small_tf32_trunc(v.w));
 }
 
 template <bool CVT>
@@ -67,14 +74,6 @@ __device__ __forceinline__ void split4_trunc(const float4 v, float4& b, float4& 
   split_tf32_trunc<CVT>(v.y, b.y, s.y);
   split_tf32_trunc<CVT>(v.z, b.z, s.z);
   split_tf32_trunc<CVT>(v.w, b.w, s.w);
-}
-
-template <bool CVT>
-__device__ __forceinline__ void split4(const float4 v, float4& b, float4& s) {
-  split_tf32<CVT>(v.x, b.x, s.x);
-  split_tf32<CVT>(v.y, b.y, s.y);
-  split_tf32<CVT>(v.z, b.z, s.z);
-  split_tf32<CVT>(v.w, b.w, s.w);
 }
 
 }  // namespace mhr

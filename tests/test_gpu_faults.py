@@ -1,9 +1,9 @@
 """Failure detection on the GPU without a fault (GB300 only).
 
 A test hook makes block 0 of a tensor-core kernel leave its first ring stage
-incomplete (the TMA producer arms it without loading it; the in-kernel split's
-converter warps fill it without arriving), so its consumers' bounded waits run
-out. The kernel must record
+incomplete (a TMA producer arms it without loading it; the in-kernel split's
+converter warps, where they fill it alone, fill it without arriving), so its
+consumers' bounded waits run out. The kernel must record
 the timeout, free its TMEM and exit; gemm_check() must report
 MHR_ERR_TIMEOUT; and the context must stay usable (a following call is
 correct). Nothing traps, faults or hangs.
@@ -17,17 +17,21 @@ from parity_util import TOL, DeviceCall, normalised_error, operands
 pytestmark = pytest.mark.gpu
 
 
-# (path, CTA-pair mode, 3xTF32 split mode): every producer kind -- TMA loads
-# in both kernels, and the converter warps of the in-kernel split
-VARIANTS = [("3xtf32", 1, 1), ("3xtf32", 2, 1), ("3xtf32", 2, 2), ("bf16", 1, 0), ("bf16", 2, 0)]
-IDS = ["3xtf32-1cta", "3xtf32-pair-prepass", "3xtf32-pair-insplit", "bf16-1cta", "bf16-pair"]
+# Every producer kind: TMA loads in both kernels, the TMA loads of A beside
+# the converter warps of the in-kernel split (aligned operands), and the
+# converter warps alone (operands one element off alignment)
+# (path, CTA-pair mode, 3xTF32 split mode, operand offset)
+VARIANTS = [("3xtf32", 1, 1, 0), ("3xtf32", 2, 1, 0), ("3xtf32", 2, 2, 0), ("3xtf32", 2, 2, 1),
+            ("bf16", 1, 0, 0), ("bf16", 2, 0, 0)]
+IDS = ["3xtf32-1cta", "3xtf32-pair-prepass", "3xtf32-pair-insplit-tma-a",
+       "3xtf32-pair-insplit-registers", "bf16-1cta", "bf16-pair"]
 
 
 @pytest.mark.parametrize("variant", VARIANTS, ids=IDS)
 def test_injected_stall_reports_timeout(mhr, variant):
-    path, mode, split = variant
+    path, mode, split, offset = variant
     A, B, Ab, Bb = operands(300, 520, 700, 6001, "normal", path)
-    call = DeviceCall(path, A, B, Ab, Bb)
+    call = DeviceCall(path, A, B, Ab, Bb, offset=offset)
     old_split = mhr.gemm_testing_set_split_mode(split)
     old_mode = mhr.gemm_testing_set_cta_pair_mode(mode)
     old_limit = mhr.gemm_testing_set_wait_limit_ns(50_000_000)  # 50 ms

@@ -80,7 +80,27 @@ def schedule_cases(n=24, seed=20261204):
     return out
 
 
-@pytest.mark.parametrize("case", cases() + edge_cases() + schedule_cases(),
+def aligned_split_cases(n=24, seed=20261205):
+    """Shapes for the in-kernel 3xTF32 split with A and B 16-byte aligned and
+    leading dimensions multiples of 4, so that its converter warps read both
+    operands with 16-byte loads, at random and at tile-boundary sizes, ragged
+    N and K included."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        if i % 2:
+            M, N, K = (EDGES[int(x)] for x in rng.integers(0, len(EDGES), 3))
+        else:
+            M, N, K = (int(x) for x in rng.integers(1, 1101, 3))
+        # lda, ldb: the next multiple of 4, plus 0-2 more groups of 4
+        pa, pb = ((-d) % 4 + 4 * int(rng.integers(0, 3)) for d in (K, N))
+        dist = "int" if rng.random() < 0.4 else "normal"
+        out.append((("3xtf32", 2, 2), M, N, K, [pa, pb, int(rng.integers(0, 6))], 0, dist,
+                    9700 + i))
+    return out
+
+
+@pytest.mark.parametrize("case", cases() + edge_cases() + schedule_cases() + aligned_split_cases(),
                          ids=lambda c: f"{c[0][0]}-{c[0][1]}{c[0][2]}-{c[1]}x{c[2]}x{c[3]}-{c[6]}")
 def test_random_case(mhr, case):
     (path, pair_mode, split_mode), M, N, K, pads, offset, dist, seed = case

@@ -304,15 +304,17 @@ def test_single_cta_few_tiles(mhr, path):
 
 
 @pytest.mark.parametrize("shape", [(300, 520, 1000), (255, 513, 1001), (130, 260, 37),
-                                   (512, 512, 4096), (256 * 79, 256, 320)],
+                                   (512, 512, 4096), (256 * 79, 256, 320), (300, 130, 1000)],
                          ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("offset", [0, 1], ids=["aligned", "offset1"])
 def test_in_kernel_split_matches_prepass_bitwise(mhr, shape, offset):
     """The CTA-pair kernel with the split inside the kernel computes exactly
     what it computes on pre-split operands: the same tf32 parts, the same
-    MMAs in the same order. Ragged K (not a multiple of 4, of the 32-wide K
-    step), operands one element off 16-byte alignment (A read with 4-byte
-    loads), and 79 tiles (a split last round on 76 clusters) included."""
+    MMAs in the same order. Aligned operands take the kind that stages A by
+    TMA; operands one element off 16-byte alignment the one that reads both
+    through registers, element by element. Ragged K (not a multiple of 4, of
+    the 32-wide K step), ragged N (not a multiple of 4), and 79 tiles (a split
+    last round on 76 clusters) included."""
     M, N, K = shape
     A, B, _, _ = operands(M, N, K, 3201 + K, "normal", "3xtf32")
     old = mhr.gemm_testing_set_cta_pair_mode(2)
@@ -323,8 +325,9 @@ def test_in_kernel_split_matches_prepass_bitwise(mhr, shape, offset):
             try:
                 outs.append(DeviceCall("3xtf32", A, B, offset=offset).run(mhr).result())
                 label = mhr.gemm_testing_last_main_kernel()
-                assert label.startswith("tc_gemm_pair_kernel<3xtf32" +
-                                        (",split>" if split == 2 else ">")), label
+                tma_a = offset == 0 and K % 4 == 0  # A 16-byte aligned, lda = K a multiple of 4
+                want = ">" if split == 1 else (",split,tma-a>" if tma_a else ",split>")
+                assert label.startswith("tc_gemm_pair_kernel<3xtf32" + want), label
             finally:
                 mhr.gemm_testing_set_split_mode(old_split)
     finally:
@@ -335,18 +338,20 @@ def test_in_kernel_split_matches_prepass_bitwise(mhr, shape, offset):
 
 
 def test_workspace_fallback_splits_in_kernel(mhr):
-    """When the split operands' workspace cannot be allocated (a cap set by a
-    test hook stands in for an allocation failure), gemm_f32_3xtf32 splits
-    inside the CTA-pair kernel instead and returns the same C bit for bit."""
+    """Operands one element off 16-byte alignment cannot be their own big
+    parts, so the split runs in a pre-pass into the workspace. When that
+    workspace cannot be allocated (a cap set by a test hook stands in for an
+    allocation failure), gemm_f32_3xtf32 splits inside the CTA-pair kernel
+    instead and returns the same C bit for bit."""
     A, B, _, _ = operands(300, 520, 1000, 3301, "normal", "3xtf32")
     old = mhr.gemm_testing_set_cta_pair_mode(2)
     try:
-        ref = DeviceCall("3xtf32", A, B).run(mhr).result()
+        ref = DeviceCall("3xtf32", A, B, offset=1).run(mhr).result()
         assert mhr.gemm_testing_last_main_kernel().startswith("tc_gemm_pair_kernel<3xtf32> ")
         assert mhr.gemm_testing_last_launches() == 2  # split pre-pass + main kernel
         old_limit = mhr.gemm_testing_set_workspace_limit(0)
         try:
-            C = DeviceCall("3xtf32", A, B).run(mhr).result()
+            C = DeviceCall("3xtf32", A, B, offset=1).run(mhr).result()
             assert mhr.gemm_testing_last_main_kernel().startswith(
                 "tc_gemm_pair_kernel<3xtf32,split> ")
             assert mhr.gemm_testing_last_launches() == 1
