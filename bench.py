@@ -57,6 +57,7 @@ WORKLOADS = {
 }
 ENTRY = {"f32": "gemm_f32", "3xtf32": "gemm_f32_3xtf32", "bf16": "gemm_bf16_f32acc"}
 SPLIT_MODES = {"auto": 0, "prepass": 1, "onchip": 2}  # gemm_testing_set_split_mode
+PAIR_MODES = {"auto": 0, "single": 1, "pair": 2}  # gemm_testing_set_cta_pair_mode
 DTYPE = {"f32": "f32", "3xtf32": "tf32x3", "bf16": "bf16"}
 TF32_OVER_BF16 = 1.1 / 2.25   # nominal dense tensor rates (PFLOP/s) of GB300
 # Dense tensor-core rate of one Blackwell SM per clock: 2.25 PFLOP/s bf16 over
@@ -700,6 +701,9 @@ def main():
                     help="3xTF32 workloads: where the operands are split into tf32 parts "
                          "(auto: the library's choice; prepass: a split pre-pass; onchip: "
                          "converter warps of the CTA-pair kernel)")
+    ap.add_argument("--cta-pair", default="auto", choices=sorted(PAIR_MODES),
+                    help="tensor-core kernel (auto: the library's choice; single: the single-CTA "
+                         "kernel; pair: the CTA-pair kernel)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -727,6 +731,7 @@ def main():
 
     lib = mhr.load()
     lib.gemm_testing_set_split_mode(SPLIT_MODES[args.split])
+    lib.gemm_testing_set_cta_pair_mode(PAIR_MODES[args.cta_pair])
     M, N, K = w["M"], w["N"], w["K"]
     path = w["path"]
     stream = torch.cuda.current_stream(dev)
@@ -910,7 +915,8 @@ def main():
                        "dist": w["dist"], "seeds": list(w["seeds"]),
                        "l2": "flushed before every timed step (256 MiB write, outside the step events)",
                        "parallelism": "replicas" if world > 1 else "single GPU",
-                       **({"split": args.split} if path == "3xtf32" else {})},
+                       **({"split": args.split} if path == "3xtf32" else {}),
+                       **({"cta_pair": args.cta_pair} if args.cta_pair != "auto" else {})},
             "roofline": roofline,
             "cpu_baseline": cpu,
             "cpu_tiled": cpu_tiled_line,

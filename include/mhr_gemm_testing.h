@@ -53,8 +53,10 @@ int gemm_testing_set_cta_pair_mode(int mode);
  * Chooses where gemm_f32_3xtf32 splits its operands into tf32 big and small
  * parts (process-wide): 0 = automatic (a pre-pass into the workspace, or
  * inside the CTA-pair kernel when the workspace cannot be allocated), 1 =
- * always a pre-pass, 2 = always inside the CTA-pair kernel (which is then
- * used whatever the CTA-pair mode says).  Other values mean 0.  Both give
+ * always a pre-pass, 2 = always inside a kernel: the single-CTA kernel's
+ * one-launch form when the CTA-pair mode is 1 and A is 16-byte aligned with
+ * lda a multiple of 4, else the CTA-pair kernel's (used whatever the CTA-pair
+ * mode says).  Other values mean 0.  Pre-pass and in-kernel split give
  * bit-identical results for the same kernel.  Returns the previous mode.
  */
 int gemm_testing_set_split_mode(int mode);

@@ -74,6 +74,13 @@ cudaError_t launch_tc_3xtf32_split(const float* A, const float* B, float* C, int
                                    int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                                    bool c_tma, const DeviceCtl& ctl, cudaStream_t s);
 
+// 3xTF32 in one launch of the single-CTA kernel, split inside it (A staged by
+// TMA as its own big part, so a_serves_as_big(A, lda) must hold); for
+// problems small enough that a pre-pass launch would dominate.
+cudaError_t launch_tc_3xtf32_small(const float* A, const float* B, float* C, int64_t M, int64_t N,
+                                   int64_t K, int64_t lda, int64_t ldb, int64_t ldc, bool c_tma,
+                                   const DeviceCtl& ctl, cudaStream_t s);
+
 // Whether the tensor-core path of `kind` (KIND_BF16 or KIND_3XTF32, in
 // tc_common.cuh) runs the CTA-pair kernel for this shape (else the
 // single-CTA kernel).

@@ -281,6 +281,13 @@ struct TcMaps {
 cudaError_t launch_single_cta(int kind, const TcMaps& maps, float* C, int64_t M, int64_t N,
                               int64_t K, int64_t ldc, bool c_tma, bool after_prepass,
                               const DeviceCtl& ctl, cudaStream_t s);
+// tc_gemm_1cta.cu: KIND_3XTF32_SPLIT_TMA_A on the single-CTA kernel, for small
+// problems (one launch): maps.a0 is A's map (K-major boxes of 32 k x 128
+// rows), maps.c C's map when c_tma.
+cudaError_t launch_single_cta_split(const TcMaps& maps, const float* A, const float* B, float* C,
+                                    int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                                    int64_t ldc, bool c_tma, const DeviceCtl& ctl,
+                                    cudaStream_t s);
 // tc_gemm_pair.cu.  after_prepass: the call launched a pre-pass (split or
 // repack) just before this, in plain stream order; a kernel zeroing C for a
 // K-split schedule then runs alongside it as a programmatic dependent.

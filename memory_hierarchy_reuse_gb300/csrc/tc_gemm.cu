@@ -92,4 +92,15 @@ cudaError_t launch_tc_3xtf32_split(const float* A, const float* B, float* C, int
   return launch_cta_pair_split(tma_a, A, B, mp, C, M, N, K, lda, ldb, ldc, c_tma, ctl, s);
 }
 
+cudaError_t launch_tc_3xtf32_small(const float* A, const float* B, float* C, int64_t M, int64_t N,
+                                   int64_t K, int64_t lda, int64_t ldb, int64_t ldc, bool c_tma,
+                                   const DeviceCtl& ctl, cudaStream_t s) {
+  TcMaps mp = {};
+  if (encode_c_map(&mp.c, C, M, N, ldc, c_tma) != CUDA_SUCCESS ||
+      encode_tmap_2d(&mp.a0, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, K, M, lda * 4, 32, 128,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  return launch_single_cta_split(mp, A, B, C, M, N, K, lda, ldb, ldc, c_tma, ctl, s);
+}
+
 }  // namespace mhr

@@ -3,7 +3,10 @@
 //   3xTF32: 128 x 128 x 32 tiles, 3 stages of 64 KB, kind::tf32 M128 N128 K8.
 // Used for problems whose 256-row CTA-pair tiles would not keep the GPU busy.
 // The method and the warp roles are described in tc_common.cuh.
+#include <type_traits>
+
 #include "tc_common.cuh"
+#include "tc_split.cuh"
 
 namespace mhr {
 namespace tc {
@@ -34,6 +37,18 @@ struct Cfg<KIND_3XTF32> {
   static constexpr uint32_t IDESC = make_idesc(2, false, false, BM, BN);
   static constexpr uint32_t TMEM_COLS = 2 * BN;            // 256
 };
+
+// The 3xTF32 split done in the kernel, for problems too small to amortise a
+// pre-pass launch: TMA stages A itself into the A_big box and two groups of
+// converter warps (tc_split.cuh) write A_small, B_big^T and B_small^T.  One
+// launch, no workspace.
+template <>
+struct Cfg<KIND_3XTF32_SPLIT_TMA_A> : Cfg<KIND_3XTF32> {};
+
+template <int KIND>
+__host__ __device__ constexpr int cta_threads() {
+  return KIND == KIND_3XTF32_SPLIT_TMA_A ? NUM_THREADS + 2 * SPLIT_THREADS : NUM_THREADS;
+}
 
 // ------------------------------------------------------------------ cluster split
 //
@@ -90,7 +105,8 @@ struct Layout {
   using C = Cfg<KIND>;
   static constexpr int EPI_OFF = C::STAGES * C::STAGE_BYTES;
   static constexpr int BAR_OFF = EPI_OFF + EPI_BYTES;
-  static constexpr int NUM_BARS = 2 * C::STAGES + 5;        // full, empty, acc_full x2, acc_empty x2, drain
+  // full, empty, acc_full x2, acc_empty x2, drain, and the converters' stores
+  static constexpr int NUM_BARS = 3 * C::STAGES + 5;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;   // tmem slot, abort flag
   static constexpr int USED = MISC_OFF + 16;
   static constexpr int ALLOC = USED + 1024;                 // slack for 1024-byte alignment
@@ -98,8 +114,26 @@ struct Layout {
   static_assert(C::BM * PART_LD<KIND> * 4 <= C::STAGES * C::STAGE_BYTES, "partial tile");
 };
 
+// The converter warps' walk over this CTA's units (A rows m0.., B columns
+// n0.., 128 each, and a K-block range).
+template <bool CLUSTER>
+struct SingleWalk {
+  __device__ __forceinline__ bool box(const TcParams& p, int u, int& m0, int& nb0, int& kb0,
+                                      int& kb1) const {
+    if (u >= p.num_units) return false;
+    const Unit w = unit_1cta<CLUSTER>(u, p);
+    int tm, tn;
+    tile_coords(w.tile, p, tm, tn);
+    m0 = tm * SPLIT_BOX_ROWS;
+    nb0 = tn * SPLIT_BOX_ROWS;
+    kb0 = w.kb0;
+    kb1 = w.kb1;
+    return true;
+  }
+};
+
 template <int KIND, bool TMA_STORE, bool CLUSTER>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(cta_threads<KIND>(), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                    const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                    const __grid_constant__ CUtensorMap tmC, const TcParams p) {
@@ -115,6 +149,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto accf_bar = [&](uint32_t b) { return bar0 + 8u * (2 * Cf::STAGES + b); };
   auto acce_bar = [&](uint32_t b) { return bar0 + 8u * (2 * Cf::STAGES + 2 + b); };
   const uint32_t drain_bar = bar0 + 8u * (2 * Cf::STAGES + 4);
+  // KIND_3XTF32_SPLIT_TMA_A: the converter warps' stores of stage s are done
+  auto cvt_bar = [&](uint32_t s) { return bar0 + 8u * (2 * Cf::STAGES + 5 + s); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
 
@@ -125,6 +161,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int s = 0; s < Cf::STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
+      if constexpr (KIND == KIND_3XTF32_SPLIT_TMA_A) mbar_init(cvt_bar(s), SPLIT_WARPS);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
@@ -134,7 +171,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA0);
-    tma_prefetch_desc(&tmB0);
+    if constexpr (KIND != KIND_3XTF32_SPLIT_TMA_A) tma_prefetch_desc(&tmB0);
     if constexpr (KIND == KIND_3XTF32) {
       tma_prefetch_desc(&tmA1);
       tma_prefetch_desc(&tmB1);
@@ -175,10 +212,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           const uint32_t st = sbase + s * Cf::STAGE_BYTES;
           const int k0 = kb * Cf::BK;
-          mbar_arrive_expect_tx(full_bar(s), Cf::STAGE_BYTES);
+          // the split kind loads A alone (its converters fill the rest)
+          mbar_arrive_expect_tx(full_bar(s), KIND == KIND_3XTF32_SPLIT_TMA_A ? Cf::A_BYTES
+                                                                             : Cf::STAGE_BYTES);
           const bool stall = p.inject_stall && blockIdx.x == 0 && it == 0;
           if (!stall) {
-            if constexpr (KIND == KIND_BF16) {
+            if constexpr (KIND == KIND_3XTF32_SPLIT_TMA_A) {
+              tma_load_2d(st, &tmA0, full_bar(s), k0, m0);
+            } else if constexpr (KIND == KIND_BF16) {
               tma_load_2d(st, &tmA0, full_bar(s), k0, m0);
 #pragma unroll
               for (int j = 0; j < Cf::BN / 64; ++j)
@@ -223,11 +264,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t d_tmem = tmem_base + buf * Cf::BN;
         for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
           const uint32_t s = it % Cf::STAGES, ph = (it / Cf::STAGES) & 1u;
-          if (!mbar_wait_bounded(full_bar(s), ph, limit, abort_flag)) {
+          // the split kind: the converters' stores, which follow the A load
+          if (!mbar_wait_bounded(KIND == KIND_3XTF32_SPLIT_TMA_A ? cvt_bar(s) : full_bar(s), ph,
+                                 limit, abort_flag)) {
             give_up_one(p, abort_flag, kErrTimeoutMma);
             ok = false;
             break;
           }
+          tc_fence_after();
           const uint32_t st = sbase + s * Cf::STAGE_BYTES;
           if constexpr (KIND == KIND_BF16) {
             // A: 128 rows x 128 B, K-major, 8-row groups 1024 B apart.
@@ -267,6 +311,55 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!mbar_wait_bounded(drain_bar, 0, limit, &never)) atomicOr(p.status, kErrTimeoutDrain);
     }
     __syncwarp();
+  } else if (KIND == KIND_3XTF32_SPLIT_TMA_A && warp >= NUM_THREADS / 32) {
+    // ------------------------------------------------------------ converters
+    // Group g takes this CTA's K-blocks g, g + 2, ... (tc_split.cuh).
+    const int g = (threadIdx.x - NUM_THREADS) / SPLIT_THREADS;
+    const int ct = (threadIdx.x - NUM_THREADS) % SPLIT_THREADS;
+    const StoreOffsets so(ct);
+    const SingleWalk<CLUSTER> walk;
+    const int stride = static_cast<int>(gridDim.x);
+    auto convert = [&](auto vec_b) {
+      constexpr bool VB = decltype(vec_b)::value;
+      int total = 0;  // how many K-blocks this CTA stores
+      for (int u = blockIdx.x; u < p.num_units; u += stride) {
+        const Unit w = unit_1cta<CLUSTER>(u, p);
+        total += w.kb1 - w.kb0;
+      }
+      LoadCursor<SingleWalk<CLUSTER>> ld;
+      ld.seek_work(p, walk, blockIdx.x, stride, ct);  // (a cluster rank's K run may be empty)
+      PrefetchCursor<SingleWalk<CLUSTER>> pf;
+      pf.seek_work(p, walk, blockIdx.x, stride);
+      for (int d = 0; d < g; ++d) ld.advance(p, walk, stride, ct);
+      for (int d = 0; d < g + 2 + SPLIT_PREFETCH; ++d) {
+        if (d >= g + 2 && ((d - g) & 1) == 0) split_prefetch_l2(p, ct, pf);
+        pf.advance(p, walk, stride);
+      }
+      BRegs r;
+      if (g < total) load_b<VB>(r, p, ld, ct);
+      for (int it = g; it < total; it += 2) {
+        const uint32_t s = it % Cf::STAGES, ph = (it / Cf::STAGES) & 1u;
+        if (!warp_wait(empty_bar(s), ph ^ 1u, limit, abort_flag) ||
+            !warp_wait(full_bar(s), ph, limit, abort_flag)) {
+          give_up(p, abort_flag, kErrTimeoutProducer, lane);
+          break;
+        }
+        split_store_tma_a(r, sbase + s * Cf::STAGE_BYTES, so);
+        fence_proxy_async_smem();  // the stores, visible to the MMA's reads
+        __syncwarp();
+        if (lane == 0) mbar_arrive(cvt_bar(s));
+        ld.advance(p, walk, stride, ct);
+        ld.advance(p, walk, stride, ct);
+        if (it + 2 < total) load_b<VB>(r, p, ld, ct);
+        split_prefetch_l2(p, ct, pf);
+        pf.advance(p, walk, stride);
+        pf.advance(p, walk, stride);
+      }
+    };
+    if (p.vec_b)
+      convert(std::true_type{});
+    else
+      convert(std::false_type{});
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;           // TMEM lane quarter this warp may access
@@ -339,7 +432,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int64_t m0 = static_cast<int64_t>(tm) * Cf::BM;
     const int n0 = tn * Cf::BN;
     const bool vec = (reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 && (p.ldc & 3) == 0;
-    for (int idx = threadIdx.x; idx < rows * (Cf::BN / 4); idx += NUM_THREADS) {
+    for (int idx = threadIdx.x; idx < rows * (Cf::BN / 4); idx += cta_threads<KIND>()) {
       const int r = rank * rows + idx / (Cf::BN / 4);
       const int c = (idx % (Cf::BN / 4)) * 4;
       const uint32_t off = sbase + static_cast<uint32_t>((r * PART_LD<KIND> + c) * 4);
@@ -491,6 +584,77 @@ cudaError_t launch_t(const TcMaps& mp, float* C, int64_t M, int64_t N, int64_t K
 }
 
 }  // namespace
+
+cudaError_t launch_single_cta_split(const TcMaps& maps, const float* A, const float* B, float* C,
+                                    int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                                    int64_t ldc, bool c_tma, const DeviceCtl& ctl,
+                                    cudaStream_t s) {
+  constexpr int KIND = KIND_3XTF32_SPLIT_TMA_A;
+  using Cf = Cfg<KIND>;
+  TcParams p = make_params(M, N, K, Cf::BM, Cf::BN, Cf::BK, C, ldc, ctl);
+  p.A = A;
+  p.B = B;
+  p.lda = lda;
+  p.ldb = ldb;
+  p.vec_a = 1;  // the TMA map of A requires what the 16-byte loads do
+  p.vec_b = (reinterpret_cast<uintptr_t>(B) % 16 == 0) && (ldb % 4 == 0);
+  cudaError_t e;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(cta_threads<KIND>());
+  cfg.dynamicSmemBytes = Layout<KIND>::ALLOC;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // With few tiles, a cluster of S CTAs per tile, each on one run of
+  // K-blocks, summing through distributed shared memory: the largest S in
+  // {8, 4, 2} that gives every rank a K-block and every CTA its own SM.
+  if ((e = prepare_kernel<KIND, false, true>()) != cudaSuccess) return e;
+  int S = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  for (int c = 8; c >= 2 && S == 1; c /= 2) {
+    if (p.num_tiles * c > ctl.sm_count || p.num_kb < c) continue;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(c);
+    cfg.numAttrs = 2;
+    cfg.gridDim = dim3(static_cast<unsigned>(p.num_tiles * c));
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, tc_gemm_kernel<KIND, false, true>, &cfg) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      continue;
+    }
+    if (clusters >= p.num_tiles) S = c;
+  }
+  if (S > 1) {
+    attr[1].val.clusterDim.x = static_cast<unsigned>(S);
+    p.num_units = p.num_tiles * S;
+    cfg.numAttrs = 2;
+    cfg.gridDim = dim3(static_cast<unsigned>(p.num_units));
+    note_main_kernel("tc_gemm_kernel<3xtf32,split,tma-a,cluster-K>", p.num_units, p.num_tiles);
+    e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<KIND, false, true>, maps.a0, maps.a1, maps.b0,
+                           maps.b1, maps.c, p);
+  } else {
+    cfg.numAttrs = 1;
+    const int grid = p.num_units < ctl.sm_count ? p.num_units : ctl.sm_count;
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    note_main_kernel("tc_gemm_kernel<3xtf32,split,tma-a>", grid, p.num_tiles);
+    if (c_tma) {
+      if ((e = prepare_kernel<KIND, true, false>()) != cudaSuccess) return e;
+      e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<KIND, true, false>, maps.a0, maps.a1, maps.b0,
+                             maps.b1, maps.c, p);
+    } else {
+      if ((e = prepare_kernel<KIND, false, false>()) != cudaSuccess) return e;
+      e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<KIND, false, false>, maps.a0, maps.a1, maps.b0,
+                             maps.b1, maps.c, p);
+    }
+  }
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
 
 cudaError_t launch_single_cta(int kind, const TcMaps& maps, float* C, int64_t M, int64_t N,
                               int64_t K, int64_t ldc, bool c_tma, bool after_prepass,

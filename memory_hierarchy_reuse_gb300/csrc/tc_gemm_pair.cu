@@ -5,6 +5,7 @@
 #include <type_traits>
 
 #include "tc_common.cuh"
+#include "tc_split.cuh"
 #include "tf32_split.cuh"
 
 namespace mhr {
@@ -82,49 +83,8 @@ __host__ __device__ constexpr bool has_converters() {
   return KIND == KIND_3XTF32_SPLIT || KIND == KIND_3XTF32_SPLIT_TMA_A;
 }
 
-// ------------------------------------------------------------------ in-kernel split
-//
-// KIND_3XTF32_SPLIT replaces the TMA producer by SPLIT_WARPS converter warps
-// per CTA.  They read the fp32 operands straight from global memory, split
-// each value into tf32 big + small in registers, and store the four parts
-// into the ring stage in exactly the layout the TMA loads of the pre-split
-// operands produce: 128-row x 128-byte K-major boxes with the 128-byte swizzle,
-// 16-byte chunk c of row r at r * 128 + ((c ^ (r % 8)) * 16).  Compared with
-// the split pre-pass, the split operands never exist in HBM, and the kernel
-// needs no workspace.
-//
-// The big part is stored as the fp32 value itself: the tensor core reads an
-// fp32 operand of kind::tf32 as its top 19 bits, which is the truncated big
-// part.  Only the small part takes arithmetic: small = tf32_rn(x - x with its
-// low 13 bits cleared), three instructions per element (finite inputs; an
-// infinite one gives a NaN small part).
-//
-// Thread ct (0..255) of the converter warps, with w = ct % 8, owns per
-// K-block:
-//   A (this CTA's 128 rows x 32 k): the 16-byte chunks (row ct/8 + 32j,
-//     k-chunk w), j = 0..3 -- a warp reads 4 rows x 128 contiguous bytes;
-//   B (32 k x this CTA's 128 columns): a 4 x 4 block, k-rows 4w .. 4w+3 of
-//     columns 4nb .. 4nb+3, nb = (ct % 32) / 8 + 4 (ct / 32) -- four 16-byte
-//     row pieces (a warp reads 8 k-rows x 64 contiguous bytes per load),
-//     transposed in registers: column 4nb + i is the 16-byte chunk w of row
-//     4nb + i of the K-major box.  The 8 lanes sharing nb write 8 different
-//     chunk positions w ^ (row % 8).
-// Both store patterns write 8 distinct 16-byte slots per 8 lanes: no bank
-// conflicts.  When A or B is not 16-byte aligned with a leading dimension
-// that is a multiple of 4, its pieces are read element by element.
-//
-// Latency: a thread keeps two K-blocks of loads in flight in two register
-// sets used in turn, issuing a block's loads after the proxy fence of the
-// block before, so that no fence has the thread's own loads outstanding to
-// order.  A third stream of prefetches pulls the K-block SPLIT_PREFETCH ahead
-// of the loads from HBM into L2, so that the register loads hit there.
-constexpr int SPLIT_WARPS = 8;
-constexpr int SPLIT_THREADS = 32 * SPLIT_WARPS;
-constexpr int SPLIT_CHUNKS = 4;    // per thread, per operand, per K-block
-constexpr int SPLIT_PREFETCH = 4;  // K-blocks between the L2 prefetches and the loads
-
-// Groups of SPLIT_WARPS converter warps that take K-blocks in turn (see the
-// split kinds below).
+// Groups of SPLIT_WARPS converter warps that take K-blocks in turn (see
+// tc_split.cuh and the split kinds below).
 template <int KIND>
 constexpr int converter_groups() {
   return KIND == KIND_3XTF32_SPLIT_TMA_A ? 2 : has_converters<KIND>() ? 1 : 0;
@@ -134,11 +94,6 @@ template <int KIND>
 constexpr int pair_threads() {
   return NUM_THREADS + converter_groups<KIND>() * SPLIT_THREADS;
 }
-
-struct SplitRegs {
-  float4 a[SPLIT_CHUNKS];  // A chunk j
-  float4 b[SPLIT_CHUNKS];  // B k-row 4w + j, columns 4nb .. 4nb+3
-};
 
 // This CTA's boxes of work unit u, and the unit's K-block range.
 __device__ __forceinline__ bool unit_boxes(const TcParams& p, int u, uint32_t rank, int& m0,
@@ -154,241 +109,15 @@ __device__ __forceinline__ bool unit_boxes(const TcParams& p, int u, uint32_t ra
   return true;
 }
 
-// The next K-block whose loads a converter thread issues: pointers to its A
-// chunk 0 and its B row 4w at that K-block, and whether the unit's boxes lie
-// inside the matrices in M and N (only K is then checked, per block).
-struct LoadCursor {
-  const float* a;
-  const float* b;
-  int arow, bcol, u, kb, kb1;
-  bool valid, interior;
-
-  __device__ __forceinline__ void seek(const TcParams& p, int unit, uint32_t rank, int ct) {
-    int m0, nb0;
-    valid = unit_boxes(p, unit, rank, m0, nb0, kb, kb1);
-    if (!valid) return;
-    u = unit;
-    const int w = ct & 7, nb = ((ct & 31) >> 3) + 4 * (ct >> 5);
-    arow = m0 + (ct >> 3);
-    bcol = nb0 + 4 * nb;
-    interior = m0 + PAIR_TILE_M / 2 <= p.M && nb0 + PAIR_TILE_N / 2 <= p.N;
-    a = p.A + static_cast<int64_t>(arow) * p.lda + 32 * kb + 4 * w;
-    b = p.B + static_cast<int64_t>(32 * kb + 4 * w) * p.ldb + bcol;
-  }
-  __device__ __forceinline__ void advance(const TcParams& p, int stride, uint32_t rank, int ct) {
-    if (!valid) return;
-    if (++kb == kb1) {
-      seek(p, u + stride, rank, ct);
-    } else {
-      a += 32;
-      b += 32 * p.ldb;
-    }
+// The converter warps' walk over this CTA's boxes: units cluster,
+// cluster + clusters, ...
+struct PairWalk {
+  uint32_t rank;
+  __device__ __forceinline__ bool box(const TcParams& p, int u, int& m0, int& nb0, int& kb0,
+                                      int& kb1) const {
+    return unit_boxes(p, u, rank, m0, nb0, kb0, kb1);
   }
 };
-
-struct PrefetchCursor {
-  int m0, nb0, u, kb, kb1;
-  bool valid;
-
-  __device__ __forceinline__ void seek(const TcParams& p, int unit, uint32_t rank) {
-    valid = unit_boxes(p, unit, rank, m0, nb0, kb, kb1);
-    u = unit;
-  }
-  __device__ __forceinline__ void advance(const TcParams& p, int stride, uint32_t rank) {
-    if (valid && ++kb == kb1) seek(p, u + stride, rank);
-  }
-};
-
-template <bool VEC>
-__device__ __forceinline__ float4 load4(const float* src) {
-  if constexpr (VEC) {
-    return __ldg(reinterpret_cast<const float4*>(src));
-  } else {
-    return make_float4(__ldg(src), __ldg(src + 1), __ldg(src + 2), __ldg(src + 3));
-  }
-}
-
-// The first `n` (0..3) of 4 consecutive elements, the rest zero.
-__device__ __forceinline__ float4 load_partial(const float* src, int n, int64_t stride) {
-  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (n > 0) v.x = __ldg(src);
-  if (n > 1) v.y = __ldg(src + stride);
-  if (n > 2) v.z = __ldg(src + 2 * stride);
-  return v;
-}
-
-// Loads of K-block c.kb into r; elements outside the matrices read as zero.
-template <bool VA, bool VB>
-__device__ __forceinline__ void split_load(SplitRegs& r, const TcParams& p, const LoadCursor& c,
-                                           int ct) {
-  const int64_t lda32 = 32 * p.lda;
-  const int k0 = c.kb * 32;
-  if (c.interior && k0 + 32 <= p.K) {  // the whole box is inside: no checks
-#pragma unroll
-    for (int j = 0; j < SPLIT_CHUNKS; ++j) r.a[j] = load4<VA>(c.a + j * lda32);
-#pragma unroll
-    for (int j = 0; j < SPLIT_CHUNKS; ++j) r.b[j] = load4<VB>(c.b + j * p.ldb);
-    return;
-  }
-  const int ka = k0 + 4 * (ct & 7);  // first k of the thread's A chunks and B rows
-#pragma unroll
-  for (int j = 0; j < SPLIT_CHUNKS; ++j) {
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (c.arow + 32 * j < p.M) {
-      const float* src = c.a + j * lda32;
-      if (ka + 4 <= p.K)
-        v = load4<VA>(src);
-      else if (ka < p.K)
-        v = load_partial(src, p.K - ka, 1);
-    }
-    r.a[j] = v;
-  }
-#pragma unroll
-  for (int j = 0; j < SPLIT_CHUNKS; ++j) {
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (ka + j < p.K) {
-      const float* src = c.b + j * p.ldb;
-      if (c.bcol + 4 <= p.N)
-        v = load4<VB>(src);
-      else if (c.bcol < p.N)
-        v = load_partial(src, p.N - c.bcol, 1);
-    }
-    r.b[j] = v;
-  }
-}
-
-// Pull one future K-block of this CTA's boxes into L2: each of the first 128
-// converter threads takes one row of the A box (128 bytes), each of the others
-// one 128-byte quarter of a row of the B box (32 rows x 512 bytes).  Both ends
-// of each piece are touched, in case it straddles two lines.  Addresses
-// outside the matrices are skipped.
-__device__ __forceinline__ void prefetch_l2(const float* a) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
-}
-
-__device__ __forceinline__ void split_prefetch_l2(const TcParams& p, int ct,
-                                                  const PrefetchCursor& c) {
-  if (!c.valid) return;
-  const int k0 = c.kb * 32;
-  if (ct < 128) {
-    const int row = c.m0 + ct;
-    if (row >= p.M || k0 >= p.K) return;
-    const float* a = p.A + static_cast<int64_t>(row) * p.lda + k0;
-    prefetch_l2(a);
-    prefetch_l2(a + (min(k0 + 31, p.K - 1) - k0));
-  } else {
-    const int q = ct - 128, k = k0 + (q >> 2), col = c.nb0 + 32 * (q & 3);
-    if (k >= p.K || col >= p.N) return;
-    const float* b = p.B + static_cast<int64_t>(k) * p.ldb + col;
-    prefetch_l2(b);
-    prefetch_l2(b + (min(col + 31, p.N - 1) - col));
-  }
-}
-
-// A converter thread's fixed store offsets within a stage's boxes: its A
-// chunk 0 (chunk j is 4 KB further: 32 rows) and its four B columns' chunks.
-struct StoreOffsets {
-  uint32_t a;
-  uint32_t b[4];
-  __device__ __forceinline__ explicit StoreOffsets(int ct) {
-    const int w = ct & 7, row = ct >> 3;
-    a = row * 128 + ((w ^ (row & 7)) << 4);
-    const int nb = ((ct & 31) >> 3) + 4 * (ct >> 5);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int n = 4 * nb + i;
-      b[i] = n * 128 + ((w ^ (n & 7)) << 4);
-    }
-  }
-};
-
-// Split the registers of one K-block into ring stage `st`: A_big, A_small,
-// B_big^T, B_small^T boxes of 16 KB each, in that order; the big parts are the
-// values themselves (see above).
-__device__ __forceinline__ void split_store(const SplitRegs& r, uint32_t st,
-                                            const StoreOffsets& o) {
-  using Cf = PairCfg<KIND_3XTF32>;
-#pragma unroll
-  for (int j = 0; j < SPLIT_CHUNKS; ++j) {
-    const uint32_t off = o.a + j * 4096;
-    st_shared_v4(st + off, r.a[j]);
-    st_shared_v4(st + Cf::A_BYTES + off, small4_tf32_trunc(r.a[j]));
-  }
-  const float4 col[4] = {make_float4(r.b[0].x, r.b[1].x, r.b[2].x, r.b[3].x),
-                         make_float4(r.b[0].y, r.b[1].y, r.b[2].y, r.b[3].y),
-                         make_float4(r.b[0].z, r.b[1].z, r.b[2].z, r.b[3].z),
-                         make_float4(r.b[0].w, r.b[1].w, r.b[2].w, r.b[3].w)};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    st_shared_v4(st + 2 * Cf::A_BYTES + o.b[i], col[i]);
-    st_shared_v4(st + 2 * Cf::A_BYTES + Cf::B_BYTES + o.b[i], small4_tf32_trunc(col[i]));
-  }
-}
-
-// ------------------------------------------------- in-kernel split, A staged by TMA
-//
-// KIND_3XTF32_SPLIT_TMA_A: when A is 16-byte aligned with lda a multiple of 4,
-// each CTA's producer warp TMA-loads A's box (128 rows x 32 k) into the stage's
-// A_big box, completing on a barrier of its own CTA (a_full[s]); the tensor
-// core reads it there as A's truncated big part.  The converter warps read
-// their A chunks back from that box (the positions they would have stored
-// to), write A_small, and take B through registers as in KIND_3XTF32_SPLIT.
-//
-// Two groups of SPLIT_WARPS converter warps take the K-blocks in turn (even
-// and odd).  A thread issues the B loads of its group's next K-block right
-// after handing over the current one, so they have two K-block times to land,
-// and it never has loads outstanding when it executes its proxy fence: on
-// GB300 that fence also waits for the thread's outstanding global loads,
-// which made one group with several register sets no faster than one load
-// round trip per K-block (1.7 us against 0.8 us of MMAs, measured).
-// Shared memory carries per stage TMA's 16 KB of A, the converters' 16 KB of
-// A reads and 48 KB of stores, and the MMAs' 96 KB of operand reads.
-struct BRegs {
-  float4 b[SPLIT_CHUNKS];  // B k-row 4w + j, columns 4nb .. 4nb+3
-};
-
-template <bool VB>
-__device__ __forceinline__ void load_b(BRegs& r, const TcParams& p, const LoadCursor& c, int ct) {
-  const int k0 = c.kb * 32;
-  if (c.bcol + 4 <= p.N && k0 + 32 <= p.K) {
-#pragma unroll
-    for (int j = 0; j < SPLIT_CHUNKS; ++j) r.b[j] = load4<VB>(c.b + j * p.ldb);
-    return;
-  }
-  const int kb_row = k0 + 4 * (ct & 7);
-#pragma unroll
-  for (int j = 0; j < SPLIT_CHUNKS; ++j) {
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (kb_row + j < p.K) {
-      const float* src = c.b + j * p.ldb;
-      if (c.bcol + 4 <= p.N)
-        v = load4<VB>(src);
-      else if (c.bcol < p.N)
-        v = load_partial(src, p.N - c.bcol, 1);
-    }
-    r.b[j] = v;
-  }
-}
-
-// A_small from the staged A box, and B_big^T, B_small^T from registers.
-__device__ __forceinline__ void split_store_tma_a(const BRegs& r, uint32_t st,
-                                                  const StoreOffsets& o) {
-  using Cf = PairCfg<KIND_3XTF32>;
-#pragma unroll
-  for (int j = 0; j < SPLIT_CHUNKS; ++j) {
-    const uint32_t off = o.a + j * 4096;
-    st_shared_v4(st + Cf::A_BYTES + off, small4_tf32_trunc(ld_shared_v4(st + off)));
-  }
-  const float4 col[4] = {make_float4(r.b[0].x, r.b[1].x, r.b[2].x, r.b[3].x),
-                         make_float4(r.b[0].y, r.b[1].y, r.b[2].y, r.b[3].y),
-                         make_float4(r.b[0].z, r.b[1].z, r.b[2].z, r.b[3].z),
-                         make_float4(r.b[0].w, r.b[1].w, r.b[2].w, r.b[3].w)};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    st_shared_v4(st + 2 * Cf::A_BYTES + o.b[i], col[i]);
-    st_shared_v4(st + 2 * Cf::A_BYTES + Cf::B_BYTES + o.b[i], small4_tf32_trunc(col[i]));
-  }
-}
 
 template <int KIND>
 struct PairLayout {
@@ -723,6 +452,7 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
     const int g = (threadIdx.x - NUM_THREADS) / SPLIT_THREADS;
     const int ct = (threadIdx.x - NUM_THREADS) % SPLIT_THREADS;
     const StoreOffsets so(ct);
+    const PairWalk walk{rank};
     auto convert = [&](auto vec_b) {
       constexpr bool VB = decltype(vec_b)::value;
       int total = 0;  // how many K-blocks this cluster stores
@@ -730,14 +460,14 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
         const Unit w = unit_of(u, p);
         total += w.kb1 - w.kb0;
       }
-      LoadCursor ld;
-      ld.seek(p, cluster, rank, ct);
-      PrefetchCursor pf;
-      pf.seek(p, cluster, rank);
-      for (int d = 0; d < g; ++d) ld.advance(p, num_clusters, rank, ct);
+      LoadCursor<PairWalk> ld;
+      ld.seek(p, walk, cluster, ct);
+      PrefetchCursor<PairWalk> pf;
+      pf.seek(p, walk, cluster);
+      for (int d = 0; d < g; ++d) ld.advance(p, walk, num_clusters, ct);
       for (int d = 0; d < g + 2 + SPLIT_PREFETCH; ++d) {
         if (d >= g + 2 && ((d - g) & 1) == 0) split_prefetch_l2(p, ct, pf);
-        pf.advance(p, num_clusters, rank);
+        pf.advance(p, walk, num_clusters);
       }
       BRegs r;
       if (g < total) load_b<VB>(r, p, ld, ct);
@@ -753,12 +483,12 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(mapa_shared(full_bar(s), 0));
         // the group's next K-block: its loads, and a prefetch two blocks further
-        ld.advance(p, num_clusters, rank, ct);
-        ld.advance(p, num_clusters, rank, ct);
+        ld.advance(p, walk, num_clusters, ct);
+        ld.advance(p, walk, num_clusters, ct);
         if (it + 2 < total) load_b<VB>(r, p, ld, ct);
         split_prefetch_l2(p, ct, pf);
-        pf.advance(p, num_clusters, rank);
-        pf.advance(p, num_clusters, rank);
+        pf.advance(p, walk, num_clusters);
+        pf.advance(p, walk, num_clusters);
       }
     };
     if (p.vec_b)
@@ -769,6 +499,7 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
     // ------------------------------------------------------------ converters (both CTAs)
     const int ct = threadIdx.x - NUM_THREADS;
     const StoreOffsets so(ct);
+    const PairWalk walk{rank};
     auto convert = [&](auto vec_a, auto vec_b) {
       constexpr bool VA = decltype(vec_a)::value, VB = decltype(vec_b)::value;
       // how many K-blocks this cluster stores
@@ -778,19 +509,19 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
         left += w.kb1 - w.kb0;
       }
       if (left == 0) return;
-      LoadCursor ld;
-      ld.seek(p, cluster, rank, ct);
-      PrefetchCursor pf;
-      pf.seek(p, cluster, rank);
+      LoadCursor<PairWalk> ld;
+      ld.seek(p, walk, cluster, ct);
+      PrefetchCursor<PairWalk> pf;
+      pf.seek(p, walk, cluster);
       for (int d = 0; d < 2 + SPLIT_PREFETCH; ++d) {
         if (d >= 2) split_prefetch_l2(p, ct, pf);
-        pf.advance(p, num_clusters, rank);
+        pf.advance(p, walk, num_clusters);
       }
       SplitRegs r0, r1;
       split_load<VA, VB>(r0, p, ld, ct);
-      ld.advance(p, num_clusters, rank, ct);
+      ld.advance(p, walk, num_clusters, ct);
       if (ld.valid) split_load<VA, VB>(r1, p, ld, ct);
-      ld.advance(p, num_clusters, rank, ct);
+      ld.advance(p, walk, num_clusters, ct);
       uint32_t it = 0;
       // Store the K-block held in r, then reuse r for the loads two blocks on.
       auto step = [&](SplitRegs& r) -> bool {
@@ -808,9 +539,9 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
         ++it;
         if (--left == 0) return false;
         if (ld.valid) split_load<VA, VB>(r, p, ld, ct);
-        ld.advance(p, num_clusters, rank, ct);
+        ld.advance(p, walk, num_clusters, ct);
         split_prefetch_l2(p, ct, pf);
-        pf.advance(p, num_clusters, rank);
+        pf.advance(p, walk, num_clusters);
         return true;
       };
       while (step(r0) && step(r1)) {

@@ -21,9 +21,9 @@ pytestmark = pytest.mark.gpu
 # the converter warps of the in-kernel split (aligned operands), and the
 # converter warps alone (operands one element off alignment)
 # (path, CTA-pair mode, 3xTF32 split mode, operand offset)
-VARIANTS = [("3xtf32", 1, 1, 0), ("3xtf32", 2, 1, 0), ("3xtf32", 2, 2, 0), ("3xtf32", 2, 2, 1),
-            ("bf16", 1, 0, 0), ("bf16", 2, 0, 0)]
-IDS = ["3xtf32-1cta", "3xtf32-pair-prepass", "3xtf32-pair-insplit-tma-a",
+VARIANTS = [("3xtf32", 1, 1, 0), ("3xtf32", 1, 2, 0), ("3xtf32", 2, 1, 0), ("3xtf32", 2, 2, 0),
+            ("3xtf32", 2, 2, 1), ("bf16", 1, 0, 0), ("bf16", 2, 0, 0)]
+IDS = ["3xtf32-1cta", "3xtf32-1cta-insplit", "3xtf32-pair-prepass", "3xtf32-pair-insplit-tma-a",
        "3xtf32-pair-insplit-registers", "bf16-1cta", "bf16-pair"]
 
 

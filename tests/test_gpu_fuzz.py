@@ -18,8 +18,8 @@ from parity_util import TOL, DeviceCall, normalised_error, operands
 pytestmark = pytest.mark.gpu
 
 # (path, CTA-pair mode, split mode)
-VARIANTS = [("f32", 0, 0), ("3xtf32", 1, 1), ("3xtf32", 2, 1), ("3xtf32", 2, 2), ("bf16", 1, 0),
-            ("bf16", 2, 0)]
+VARIANTS = [("f32", 0, 0), ("3xtf32", 1, 1), ("3xtf32", 1, 2), ("3xtf32", 2, 1), ("3xtf32", 2, 2),
+            ("bf16", 1, 0), ("bf16", 2, 0)]
 
 
 def cases(n=60, seed=20261202):
@@ -95,8 +95,8 @@ def aligned_split_cases(n=24, seed=20261205):
         # lda, ldb: the next multiple of 4, plus 0-2 more groups of 4
         pa, pb = ((-d) % 4 + 4 * int(rng.integers(0, 3)) for d in (K, N))
         dist = "int" if rng.random() < 0.4 else "normal"
-        out.append((("3xtf32", 2, 2), M, N, K, [pa, pb, int(rng.integers(0, 6))], 0, dist,
-                    9700 + i))
+        out.append((("3xtf32", 1 + (i % 3 == 0), 2), M, N, K, [pa, pb, int(rng.integers(0, 6))],
+                    0, dist, 9700 + i))
     return out
 
 

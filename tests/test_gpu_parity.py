@@ -16,15 +16,17 @@ pytestmark = pytest.mark.gpu
 
 PATHS = ["f32", "3xtf32", "bf16"]
 # Each tensor-core path has two kernels: the single-CTA kernel (128-row tiles)
-# and the CTA-pair kernel (256-row tiles over a cluster of 2); 3xTF32 on the
-# CTA-pair kernel splits its operands either in a pre-pass or inside the
-# kernel. Every combination is forced in turn on every small shape; full-size
-# checks use the automatic choice, as the benchmark does.
+# and the CTA-pair kernel (256-row tiles over a cluster of 2); 3xTF32 splits
+# its operands either in a pre-pass or inside the kernel (the single-CTA
+# kernel's in-kernel split needs A 16-byte aligned with lda a multiple of 4,
+# and hands other operands to the CTA-pair kernel's). Every combination is
+# forced in turn on every small shape; full-size checks use the automatic
+# choice, as the benchmark does.
 # (path, CTA-pair mode, split mode)
-VARIANTS = [("f32", 0, 0), ("3xtf32", 1, 1), ("3xtf32", 2, 1), ("3xtf32", 2, 2), ("bf16", 1, 0),
-            ("bf16", 2, 0)]
-VARIANT_IDS = ["f32", "3xtf32-1cta", "3xtf32-pair-prepass", "3xtf32-pair-insplit", "bf16-1cta",
-               "bf16-pair"]
+VARIANTS = [("f32", 0, 0), ("3xtf32", 1, 1), ("3xtf32", 1, 2), ("3xtf32", 2, 1), ("3xtf32", 2, 2),
+            ("bf16", 1, 0), ("bf16", 2, 0)]
+VARIANT_IDS = ["f32", "3xtf32-1cta", "3xtf32-1cta-insplit", "3xtf32-pair-prepass",
+               "3xtf32-pair-insplit", "bf16-1cta", "bf16-pair"]
 
 
 @pytest.fixture(params=VARIANTS, ids=VARIANT_IDS)
@@ -335,6 +337,34 @@ def test_in_kernel_split_matches_prepass_bitwise(mhr, shape, offset):
     assert np.array_equal(outs[0], outs[1])
     Cref, S = oracle.gemm(A, B, with_abs=True)
     assert normalised_error(outs[1], Cref, S) <= TOL["3xtf32"]
+
+
+@pytest.mark.parametrize("shape", [(256, 256, 256), (200, 300, 520), (512, 512, 8192),
+                                   (1024, 1024, 1024), (130, 1000, 64)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_single_cta_in_kernel_split_is_one_launch(mhr, shape):
+    """The single-CTA kernel's in-kernel split does the whole 3xTF32 product
+    in one launch (no pre-pass, no zeroing of C), with clusters splitting K
+    when the tiles are few, and matches the oracle; on integer inputs bit for
+    bit."""
+    M, N, K = shape
+    old = mhr.gemm_testing_set_cta_pair_mode(1)
+    old_split = mhr.gemm_testing_set_split_mode(2)
+    try:
+        for dist in ("normal", "int"):
+            A, B, _, _ = operands(M, N, K, 3401 + K, dist, "3xtf32")
+            C = DeviceCall("3xtf32", A, B).run(mhr).result()
+            assert mhr.gemm_testing_last_main_kernel().startswith(
+                "tc_gemm_kernel<3xtf32,split,tma-a"), mhr.gemm_testing_last_main_kernel()
+            assert mhr.gemm_testing_last_launches() == 1
+            if dist == "int":
+                assert np.array_equal(C, oracle.gemm(A, B))
+            else:
+                Cref, S = oracle.gemm(A, B, with_abs=True)
+                assert normalised_error(C, Cref, S) <= TOL["3xtf32"]
+    finally:
+        mhr.gemm_testing_set_split_mode(old_split)
+        mhr.gemm_testing_set_cta_pair_mode(old)
 
 
 def test_workspace_fallback_splits_in_kernel(mhr):
