@@ -79,8 +79,10 @@ def peaks():
 
 
 KERNEL_SOURCES = {  # the files whose text determines each kernel
-    "tc_gemm_pair_kernel": ["tc_gemm_pair.cu", "tc_common.cuh", "mhr_device.cuh", "tf32_split.cuh"],
-    "tc_gemm_kernel": ["tc_gemm_1cta.cu", "tc_common.cuh", "mhr_device.cuh"],
+    "tc_gemm_pair_kernel": ["tc_gemm_pair.cu", "tc_common.cuh", "mhr_device.cuh", "tf32_split.cuh",
+                            "tc_split.cuh"],
+    "tc_gemm_kernel": ["tc_gemm_1cta.cu", "tc_common.cuh", "mhr_device.cuh", "tf32_split.cuh",
+                       "tc_split.cuh"],
     "simt_f32_kernel": ["simt_f32.cu"],
     "split_vec_kernel": ["tc_prepass.cu", "tf32_split.cuh"],
 }
