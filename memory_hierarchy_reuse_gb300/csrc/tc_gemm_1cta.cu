@@ -585,6 +585,11 @@ cudaError_t launch_t(const TcMaps& mp, float* C, int64_t M, int64_t N, int64_t K
 
 }  // namespace
 
+// The largest cluster size the one-launch split tries (8, 4 or 2; 1 = none).
+#ifndef MHR_SMALL_MAX_CLUSTER
+#define MHR_SMALL_MAX_CLUSTER 8
+#endif
+
 cudaError_t launch_single_cta_split(const TcMaps& maps, const float* A, const float* B, float* C,
                                     int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
                                     int64_t ldc, bool c_tma, const DeviceCtl& ctl,
@@ -616,7 +621,7 @@ cudaError_t launch_single_cta_split(const TcMaps& maps, const float* A, const fl
   attr[1].id = cudaLaunchAttributeClusterDimension;
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
-  for (int c = 8; c >= 2 && S == 1; c /= 2) {
+  for (int c = MHR_SMALL_MAX_CLUSTER; c >= 2 && S == 1; c /= 2) {
     if (p.num_tiles * c > ctl.sm_count || p.num_kb < c) continue;
     attr[1].val.clusterDim.x = static_cast<unsigned>(c);
     cfg.numAttrs = 2;
