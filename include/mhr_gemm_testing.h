@@ -113,6 +113,28 @@ const char* gemm_testing_last_main_kernel(void);
  */
 void gemm_testing_set_main_kernel_events(void* start, void* stop);
 
+/*
+ * Forces the width of the CTA-pair kernel's 3xTF32 output tiles (256 rows x
+ * `columns`) for the following calls (process-wide): a multiple of 16 in
+ * [128, 256]; any other value, 0 included, restores the planner's choice.  A
+ * width that is not a multiple of 32 writes C with register stores even where
+ * C could take TMA stores.  The single-CTA kernel and the bf16 path ignore
+ * it.  Returns the previous setting.
+ */
+int gemm_testing_set_pair_tile_n(int columns);
+
+/*
+ * The planner's choice of those tile columns for an M x N x K 3xTF32 problem
+ * on `clusters` co-resident CTA pairs, with C written by TMA stores when
+ * c_tma is nonzero (a multiple of 32 then) or by register stores.  Host
+ * arithmetic only: it needs no GPU.  It weighs the tile-size trade-off of
+ * "矩阵乘法 tiling", section 五 (a wider tile reuses each staged B element over
+ * more columns; fewer, wider tiles fill the SMs in fewer, coarser rounds):
+ * rounds of tiles over the clusters against the shared-memory bytes per
+ * tensor cycle that narrower tiles need.
+ */
+int gemm_testing_plan_pair_tile_n(int64_t M, int64_t N, int64_t K, int clusters, int c_tma);
+
 #ifdef __cplusplus
 }
 #endif

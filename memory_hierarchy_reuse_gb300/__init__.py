@@ -48,7 +48,8 @@ EXPORTS = ("gemm_f32", "gemm_f32_3xtf32", "gemm_bf16_f32acc", "gemm_f32_3xtf32_n
            "gemm_testing_set_cta_pair_mode", "gemm_testing_last_main_kernel",
            "gemm_testing_set_raster_group", "gemm_testing_set_split_mode",
            "gemm_testing_last_launches", "gemm_testing_set_workspace_limit",
-           "gemm_testing_set_zero_a_small")
+           "gemm_testing_set_zero_a_small", "gemm_testing_set_pair_tile_n",
+           "gemm_testing_plan_pair_tile_n")
 
 _lib = None
 
@@ -99,6 +100,10 @@ def load(path: str | None = None):
     lib.gemm_testing_set_cta_pair_mode.restype = ctypes.c_int
     lib.gemm_testing_set_zero_a_small.argtypes = [ctypes.c_int]
     lib.gemm_testing_set_zero_a_small.restype = ctypes.c_int
+    lib.gemm_testing_set_pair_tile_n.argtypes = [ctypes.c_int]
+    lib.gemm_testing_set_pair_tile_n.restype = ctypes.c_int
+    lib.gemm_testing_plan_pair_tile_n.argtypes = [i64, i64, i64, ctypes.c_int, ctypes.c_int]
+    lib.gemm_testing_plan_pair_tile_n.restype = ctypes.c_int
     lib.gemm_testing_set_split_mode.argtypes = [ctypes.c_int]
     lib.gemm_testing_set_split_mode.restype = ctypes.c_int
     lib.gemm_testing_set_workspace_limit.argtypes = [ctypes.c_uint64]
@@ -194,6 +199,17 @@ def gemm_testing_set_split_mode(mode: int) -> int:
 def gemm_testing_set_zero_a_small(enable: int) -> int:
     """Clear A's small part after the 3xTF32 split pre-pass (test hook)."""
     return load().gemm_testing_set_zero_a_small(int(enable))
+
+
+def gemm_testing_set_pair_tile_n(columns: int) -> int:
+    """Force the 3xTF32 CTA-pair tiles' columns (a multiple of 16 in
+    [128, 256]); 0 restores the planner (test hook)."""
+    return load().gemm_testing_set_pair_tile_n(int(columns))
+
+
+def gemm_testing_plan_pair_tile_n(M: int, N: int, K: int, clusters: int, c_tma: bool) -> int:
+    """The 3xTF32 CTA-pair tile columns the planner picks (host logic only)."""
+    return load().gemm_testing_plan_pair_tile_n(M, N, K, int(clusters), int(bool(c_tma)))
 
 
 def gemm_testing_set_main_kernel_events(start=None, stop=None) -> None:

@@ -66,6 +66,7 @@ int g_inject_stall = 0;
 int g_pair_mode = 0;
 int g_raster_group = 0;
 int g_split_mode = 0;
+int g_pair_tile_n = 0;
 uint64_t g_workspace_limit = UINT64_MAX;
 int g_zero_a_small = 0;
 cudaEvent_t g_main_start = nullptr, g_main_stop = nullptr;
@@ -245,6 +246,7 @@ DeviceCtl make_ctl(const DeviceState& st) {
   c.pair_mode = g_pair_mode;
   c.raster_group = g_raster_group;
   c.split_mode = g_split_mode;
+  c.pair_tile_n = g_pair_tile_n;
   return c;
 }
 
@@ -549,6 +551,18 @@ MHR_API uint64_t gemm_testing_set_workspace_limit(uint64_t bytes) {
   const uint64_t old = g_workspace_limit;
   g_workspace_limit = bytes;
   return old;
+}
+
+MHR_API int gemm_testing_set_pair_tile_n(int columns) {
+  std::lock_guard<std::mutex> g(g_mu);
+  const int old = g_pair_tile_n;
+  g_pair_tile_n = (columns >= 128 && columns <= 256 && columns % 16 == 0) ? columns : 0;
+  return old;
+}
+
+MHR_API int gemm_testing_plan_pair_tile_n(int64_t M, int64_t N, int64_t K, int clusters,
+                                          int c_tma) {
+  return tc::plan_pair_tile_n(M, N, K, clusters, c_tma != 0);
 }
 
 MHR_API int gemm_testing_set_zero_a_small(int enable) {

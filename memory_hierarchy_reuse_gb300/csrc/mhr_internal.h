@@ -19,6 +19,7 @@ struct DeviceCtl {
   int pair_mode = 0;                   // 0 auto, 1 single-CTA kernel, 2 CTA-pair kernel (test hook)
   int raster_group = 0;                // tile rows per raster group, 0 = default (tuning hook)
   int split_mode = 0;                  // 3xTF32: 0 auto, 1 split pre-pass, 2 in-kernel split (test hook)
+  int pair_tile_n = 0;                 // 3xTF32 CTA-pair tile columns, 0 = planned (test hook)
 };
 
 cudaError_t launch_simt_f32(const float* A, const float* B, float* C, int64_t M, int64_t N,
@@ -40,7 +41,7 @@ cudaError_t launch_pack_u16(const uint16_t* src, int64_t rows, int64_t cols, int
 // 3xTF32 split: A (M x K, lda) -> a_big, a_small (M x Kp, K-contiguous; big
 // truncated to tf32, a_big may be null when A itself serves as A_big);
 // B (K x N, ldb) -> bt_big, bt_small (N x Kp, K-contiguous, i.e. B transposed;
-// big rounded to tf32).
+// big truncated to tf32).
 cudaError_t launch_split_tf32(const float* A, const float* B, int64_t M, int64_t N, int64_t K,
                               int64_t lda, int64_t ldb, int64_t Kp, float* a_big, float* a_small,
                               float* bt_big, float* bt_small, cudaStream_t s);
@@ -85,6 +86,13 @@ cudaError_t launch_tc_3xtf32_small(const float* A, const float* B, float* C, int
 // tc_common.cuh) runs the CTA-pair kernel for this shape (else the
 // single-CTA kernel).
 bool tc_pair_chosen(int kind, int64_t M, int64_t N, int64_t K, const DeviceCtl& ctl);
+namespace tc {
+// Columns of the CTA-pair kernel's 3xTF32 tiles (256, or a narrower multiple
+// of 16 -- of 32 when C is written by TMA -- down to 128) for an M x N x K
+// problem with up to `clusters` co-resident clusters; tc_gemm.cu gives the
+// cost model.
+int plan_pair_tile_n(int64_t M, int64_t N, int64_t K, int clusters, bool c_tma);
+}  // namespace tc
 
 // Whether C can be written with TMA stores: 16-byte aligned base and pitch,
 // and N a multiple of 4.  A TMA store clips a box at the tensor's inner extent

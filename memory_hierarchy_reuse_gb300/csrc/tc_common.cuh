@@ -84,6 +84,10 @@ constexpr int GROUP_M = 8;
 
 struct TcParams {
   int32_t M, N, K;
+  // Output tile columns: 256 for the CTA-pair kernel's tiles unless the host
+  // chose narrower ones (3xTF32 only, a multiple of 16), the kernel's BN
+  // otherwise.
+  int32_t bn;
   int32_t tiles_m, tiles_n, num_tiles, num_kb;
   // Work units of the pair kernel: tiles [0, full_units) whole; tiles
   // [full_units, num_tiles) split into two K halves, [0, kb_mid) and
@@ -92,6 +96,10 @@ struct TcParams {
   int32_t group_m;  // tile rows per raster group
   float* C;
   int64_t ldc;
+  // C not TMA-aligned but its even rows are (16-byte aligned C, ldc even):
+  // chunks wholly inside the tile and C store their even rows by TMA through
+  // a map over rows 0, 2, 4, ... and only the odd rows from registers.
+  int32_t c_even;
   uint32_t* status;
   uint64_t wait_limit_ns;
   int32_t inject_stall;
@@ -170,17 +178,76 @@ __device__ __forceinline__ void give_up(const TcParams& p, volatile int* abort_f
 // swizzle: 16-byte piece j of row r sits at position j ^ (r % 8), so both the
 // row-wise writes here and the column-wise reads below are conflict-free),
 // then either hand the box to one TMA store / reduce-add, or -- when C is not
-// TMA-aligned -- store it row by row so each warp instruction writes 32
-// consecutive floats of one row of C (masked at the edges; atomic adds for
-// split-K units).
+// TMA-aligned -- store it two rows per warp instruction, masked to rows < M
+// and columns < col_end (atomic adds for split-K units).  col_end is N, or
+// the tile's last column + 1 when the tile is narrower than its last chunk
+// (the TMA path is used only for tiles that are whole chunks).
 template <bool TMA_STORE>
 __device__ __forceinline__ void stage_and_store_chunk(const uint32_t (&r)[32], uint32_t epi_base,
                                                       int ew, uint32_t chunk, int lane,
                                                       const CUtensorMap* tmC, const TcParams& p,
-                                                      int row0, int col0, bool reduce) {
+                                                      int row0, int col0, int col_end,
+                                                      bool reduce) {
   const uint32_t stg = epi_base + (ew * 2 + (chunk & 1u)) * EPI_BUF_BYTES;
+  const bool even_rows = !TMA_STORE && p.c_even;
+  if (even_rows && col0 + 32 <= col_end) {
+    // Even rows 0, 2, .., 30 of the chunk into the buffer's first 16 swizzled
+    // rows, odd rows into the last 16; one TMA store (or reduce-add) writes
+    // the even half to rows row0 / 2 .. of the even-row map, and the odd half
+    // goes out from registers two rows per warp instruction as below.  A
+    // register chunk commits no bulk group, so wait for all of them: the
+    // buffer may have been handed to a store two or more groups back.
+    if (lane == 0) bulk_wait_group_read<0>();
+    __syncwarp();
+    const int brow = (lane >> 1) + (lane & 1) * 16;
+    const uint32_t brow_addr = stg + brow * 128;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t a = brow_addr + ((j ^ (brow & 7)) << 4);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(r[4 * j]),
+                   "r"(r[4 * j + 1]), "r"(r[4 * j + 2]), "r"(r[4 * j + 3])
+                   : "memory");
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if (reduce)
+        tma_reduce_add_2d(tmC, stg, col0, row0 / 2);
+      else
+        tma_store_2d(tmC, stg, col0, row0 / 2);
+      bulk_commit_group();
+    }
+    const int half = lane >> 4;
+    const int cp = (lane & 15) * 2;
+    const int col = col0 + cp;
+    float2 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int rr = 16 + 2 * i + half;  // buffer row: odd row 2 (rr - 16) + 1
+      const uint32_t a = stg + rr * 128 + ((((cp >> 2) ^ rr) & 7) << 4) + (cp & 3) * 4;
+      asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];"
+                   : "=f"(v[i].x), "=f"(v[i].y)
+                   : "r"(a)
+                   : "memory");
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int row = row0 + 2 * (2 * i + half) + 1;
+      if (row < p.M) {
+        float* dst = p.C + static_cast<int64_t>(row) * p.ldc + col;  // 8-byte aligned: ldc even
+        if (reduce)
+          atomicAdd(reinterpret_cast<float2*>(dst), v[i]);
+        else
+          *reinterpret_cast<float2*>(dst) = v[i];
+      }
+    }
+    __syncwarp();
+    return;
+  }
   if (TMA_STORE) {
     if (lane == 0) bulk_wait_group_read<1>();  // the store that last used this buffer has read it
+  } else if (even_rows) {
+    if (lane == 0) bulk_wait_group_read<0>();  // (a chunk at the tile's edge; see above)
   }
   __syncwarp();
   const uint32_t row_addr = stg + lane * 128;
@@ -206,31 +273,39 @@ __device__ __forceinline__ void stage_and_store_chunk(const uint32_t (&r)[32], u
     // Two rows per step, two adjacent columns per lane: lanes 0-15 take row
     // i, lanes 16-31 row i + 1.  A pair whose address is 8-byte aligned (all
     // of them when C and ldc are even) goes out as one 8-byte store or atomic
-    // add, else as two 4-byte ones.
+    // add, else as two 4-byte ones.  All sixteen shared-memory reads are
+    // issued before the first store, so the chunk waits for one shared-memory
+    // round trip, not one per step.
     const int half = lane >> 4;
     const int cp = (lane & 15) * 2;  // column pair within the chunk
     const int col = col0 + cp;
-#pragma unroll 4
-    for (int i = 0; i < 32; i += 2) {
-      const int rr = i + half;
-      const int row = row0 + rr;
+    float2 v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int rr = 2 * i + half;
       const uint32_t a = stg + rr * 128 + ((((cp >> 2) ^ rr) & 7) << 4) + (cp & 3) * 4;
-      float2 v;
-      asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a) : "memory");
-      if (row < p.M && col < p.N) {
+      asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];"
+                   : "=f"(v[i].x), "=f"(v[i].y)
+                   : "r"(a)
+                   : "memory");
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int row = row0 + 2 * i + half;
+      if (row < p.M && col < col_end) {
         float* dst = p.C + static_cast<int64_t>(row) * p.ldc + col;
-        if (col + 1 < p.N && (reinterpret_cast<uintptr_t>(dst) & 7u) == 0) {
+        if (col + 1 < col_end && (reinterpret_cast<uintptr_t>(dst) & 7u) == 0) {
           if (reduce)
-            atomicAdd(reinterpret_cast<float2*>(dst), v);
+            atomicAdd(reinterpret_cast<float2*>(dst), v[i]);
           else
-            *reinterpret_cast<float2*>(dst) = v;
+            *reinterpret_cast<float2*>(dst) = v[i];
         } else {
           if (reduce) {
-            atomicAdd(dst, v.x);
-            if (col + 1 < p.N) atomicAdd(dst + 1, v.y);
+            atomicAdd(dst, v[i].x);
+            if (col + 1 < col_end) atomicAdd(dst + 1, v[i].y);
           } else {
-            dst[0] = v.x;
-            if (col + 1 < p.N) dst[1] = v.y;
+            dst[0] = v[i].x;
+            if (col + 1 < col_end) dst[1] = v[i].y;
           }
         }
       }
@@ -248,6 +323,7 @@ inline TcParams make_params(int64_t M, int64_t N, int64_t K, int tile_m, int til
   p.M = static_cast<int32_t>(M);
   p.N = static_cast<int32_t>(N);
   p.K = static_cast<int32_t>(K);
+  p.bn = tile_n;
   p.tiles_m = static_cast<int32_t>((M + tile_m - 1) / tile_m);
   p.tiles_n = static_cast<int32_t>((N + tile_n - 1) / tile_n);
   p.num_tiles = p.tiles_m * p.tiles_n;
@@ -258,6 +334,7 @@ inline TcParams make_params(int64_t M, int64_t N, int64_t K, int tile_m, int til
   p.group_m = ctl.raster_group > 0 ? ctl.raster_group : GROUP_M;
   p.C = C;
   p.ldc = ldc;
+  p.c_even = 0;
   p.status = ctl.status;
   p.wait_limit_ns = ctl.wait_limit_ns;
   p.inject_stall = ctl.inject_stall;
@@ -272,9 +349,11 @@ inline TcParams make_params(int64_t M, int64_t N, int64_t K, int tile_m, int til
 constexpr int PAIR_TILE_M = 256, PAIR_TILE_N = 256;
 
 // Tensor maps of one launch: A parts, B parts (the bf16 kind uses a0 / b0
-// only) and C (unused without TMA stores).
+// only) and C (unused without TMA stores).  c_even: `c` maps C's even rows
+// (boxes of 32 columns x 16 of those rows) for the register-store kernels.
 struct TcMaps {
   CUtensorMap a0, a1, b0, b1, c;
+  bool c_even = false;
 };
 
 // tc_gemm_1cta.cu
@@ -290,9 +369,11 @@ cudaError_t launch_single_cta_split(const TcMaps& maps, const float* A, const fl
                                     cudaStream_t s);
 // tc_gemm_pair.cu.  after_prepass: the call launched a pre-pass (split or
 // repack) just before this, in plain stream order; a kernel zeroing C for a
-// K-split schedule then runs alongside it as a programmatic dependent.
+// K-split schedule then runs alongside it as a programmatic dependent.  bn:
+// the pair tiles' columns (256; KIND_3XTF32 also a multiple of 16 from 128,
+// a multiple of 32 with c_tma), matching the B maps' boxes of bn / 2 rows.
 cudaError_t launch_cta_pair(int kind, const TcMaps& maps, float* C, int64_t M, int64_t N,
-                            int64_t K, int64_t ldc, bool c_tma, bool after_prepass,
+                            int64_t K, int64_t ldc, bool c_tma, bool after_prepass, int bn,
                             const DeviceCtl& ctl, cudaStream_t s);
 // Zero the C tiles [q.full_units, q.num_tiles) of tile_rows x tile_cols that
 // a K-split schedule reduce-adds into; after_prepass as for launch_cta_pair.

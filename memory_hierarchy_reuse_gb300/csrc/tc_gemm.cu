@@ -15,6 +15,65 @@ bool tc_pair_chosen(int kind, int64_t M, int64_t N, int64_t K, const DeviceCtl& 
   return kind != tc::KIND_BF16 || K >= 2048 || pair_tiles >= 2 * clusters;
 }
 
+namespace tc {
+
+// Pair tile width for 3xTF32.  Each CTA of a pair computes 128 rows x bn
+// columns, so a tile's MMA time is proportional to bn and to its K-blocks;
+// what varies with bn is how many tiles the problem needs (ceil(N / bn) per
+// row of tiles), how the tiles fall into rounds over the co-resident
+// clusters, whether the last round is split along K (then C is zeroed and
+// both halves add into it), and how many shared-memory bytes each tensor
+// cycle needs.  Per instruction-K step a CTA's MMAs read its 128 x 8 A part
+// (4 KB) and bn / 2 x 8 of B (16 bn bytes) while the tensor pipe works bn / 2
+// cycles, and TMA writes 32 KB of A and 128 bn bytes of B per K-block of 12
+// MMAs: 13653 / bn + 53.3 bytes per cycle in all, 107 at bn = 256.  Shared
+// memory delivers about 125 bytes per cycle (the bf16 kernels' measured
+// ceiling), so narrower tiles run below the full tensor rate.  The estimate
+// below is the busiest cluster's MMA cycles plus the last epilogue, which
+// nothing overlaps (TMA stores or, when C is not TMA-aligned, register stores
+// at about a third of their rate; atomic adds after a K split).  bn = 256
+// unless a narrower width is at least 5 % faster by this estimate.
+double pair_cycles_estimate(int64_t M, int64_t N, int64_t K, int clusters_max, bool c_tma,
+                            int bn) {
+  const int64_t tiles = ((M + PAIR_TILE_M - 1) / PAIR_TILE_M) * ((N + bn - 1) / bn);
+  const int64_t clusters = tiles < clusters_max ? tiles : clusters_max;
+  const int64_t kb = (K + 31) / 32;
+  const double demand = 13653.3 / bn + 53.3;
+  const double eff = demand > 125.0 ? 125.0 / demand : 1.0;
+  const double tile = static_cast<double>(kb) * 6.0 * bn / eff;
+  const int64_t full = tiles / clusters, rem = tiles % clusters;
+  double rounds;
+  bool split = false;
+  if (rem == 0) {
+    rounds = static_cast<double>(full);
+  } else if (tiles > clusters && 2 * rem <= clusters && kb >= 2) {
+    rounds = full + 0.5;
+    split = true;
+  } else {
+    rounds = static_cast<double>(full + 1);
+  }
+  const double epi_per_col = split ? (c_tma ? 20.0 : 58.0) : (c_tma ? 25.0 : 61.0);
+  return rounds * tile + epi_per_col * bn;
+}
+
+int plan_pair_tile_n(int64_t M, int64_t N, int64_t K, int clusters, bool c_tma) {
+  if (clusters < 1) return PAIR_TILE_N;
+  const double full_width = pair_cycles_estimate(M, N, K, clusters, c_tma, PAIR_TILE_N);
+  int best = PAIR_TILE_N;
+  double best_t = full_width;
+  // TMA stores write C in chunks of 32 columns, so their tiles are whole chunks
+  for (int bn = PAIR_TILE_N - (c_tma ? 32 : 16); bn >= 128; bn -= c_tma ? 32 : 16) {
+    const double t = pair_cycles_estimate(M, N, K, clusters, c_tma, bn);
+    if (t < best_t) {
+      best_t = t;
+      best = bn;
+    }
+  }
+  return best_t <= 0.95 * full_width ? best : PAIR_TILE_N;
+}
+
+}  // namespace tc
+
 namespace {
 
 using namespace tc;
@@ -34,14 +93,26 @@ cudaError_t launch_tc_any(int kind, const TcMaps& maps, float* C, int64_t M, int
                           int64_t ldc, bool c_tma, bool after_prepass, const DeviceCtl& ctl,
                           cudaStream_t s) {
   return tc_pair_chosen(kind, M, N, K, ctl)
-             ? launch_cta_pair(kind, maps, C, M, N, K, ldc, c_tma, after_prepass, ctl, s)
+             ? launch_cta_pair(kind, maps, C, M, N, K, ldc, c_tma, after_prepass, PAIR_TILE_N,
+                               ctl, s)
              : launch_single_cta(kind, maps, C, M, N, K, ldc, c_tma, after_prepass, ctl, s);
 }
 
-CUresult encode_c_map(CUtensorMap* cm, float* C, int64_t M, int64_t N, int64_t ldc, bool c_tma) {
-  if (!c_tma) return CUDA_SUCCESS;
-  return encode_tmap_2d(cm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, N, M, ldc * 4, 32, 32,
-                        CU_TENSOR_MAP_SWIZZLE_128B);
+// C's map: the whole of C in boxes of 32 x 32 when TMA can store C.
+// Otherwise, when C is 16-byte aligned and ldc even (so that every other row
+// starts on a 16-byte boundary: the case of an ldc that is 2 mod 4), a map
+// over C's even rows (pitch 2 ldc, boxes of 32 columns x 16 rows) with which
+// the register-store kernels write half of each chunk by TMA (TcMaps::c_even).
+CUresult encode_c_map(TcMaps* mp, float* C, int64_t M, int64_t N, int64_t ldc, bool c_tma) {
+  mp->c_even = false;
+  if (c_tma)
+    return encode_tmap_2d(&mp->c, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, N, M, ldc * 4, 32, 32,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+  if ((reinterpret_cast<uintptr_t>(C) & 15u) == 0 && ldc % 2 == 0 &&
+      encode_tmap_2d(&mp->c, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, N, (M + 1) / 2, ldc * 8, 32, 16,
+                     CU_TENSOR_MAP_SWIZZLE_128B) == CUDA_SUCCESS)
+    mp->c_even = true;
+  return CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -54,11 +125,11 @@ cudaError_t launch_tc_bf16(const uint16_t* A, const uint16_t* B, float* C, int64
                      CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
       encode_tmap_2d(&mp.b0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, N, K, ldb * 2, 64, 64,
                      CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
-      encode_c_map(&mp.c, C, M, N, ldc, c_tma) != CUDA_SUCCESS)
+      encode_c_map(&mp, C, M, N, ldc, c_tma) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   mp.a1 = mp.a0;  // unused by the bf16 kernels
   mp.b1 = mp.b0;
-  if (!c_tma) mp.c = mp.a0;  // unused without TMA stores
+  if (!c_tma && !mp.c_even) mp.c = mp.a0;  // unused without TMA stores
   return launch_tc_any(KIND_BF16, mp, C, M, N, K, ldc, c_tma, after_prepass, ctl, s);
 }
 
@@ -69,21 +140,32 @@ cudaError_t launch_tc_3xtf32(const float* a_big, int64_t a_big_ld, const float* 
   TcMaps mp;
   const auto f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  // The CTA-pair kernel's tiles are 256 x bn (each CTA loads bn / 2 rows of
+  // B^T per part); the single-CTA kernel's 128 x 128.  A tile width the
+  // planner would not give with TMA stores (one that is not whole 32-column
+  // chunks, forced by the test hook) writes C with register stores instead.
+  const bool pair = tc_pair_chosen(KIND_3XTF32, M, N, K, ctl);
+  const int bn = !pair                ? PAIR_TILE_N
+                 : ctl.pair_tile_n > 0 ? ctl.pair_tile_n
+                                       : plan_pair_tile_n(M, N, K, ctl.sm_count / 2, c_tma);
+  const bool tma_c = c_tma && bn % 32 == 0;
+  const int b_box_rows = pair ? bn / 2 : 128;
   if (encode_tmap_2d(&mp.a0, f32, a_big, K, M, a_big_ld * 4, 32, 128, sw) != CUDA_SUCCESS ||
       encode_tmap_2d(&mp.a1, f32, a_small, K, M, Kp * 4, 32, 128, sw) != CUDA_SUCCESS ||
-      encode_tmap_2d(&mp.b0, f32, bt_big, K, N, Kp * 4, 32, 128, sw) != CUDA_SUCCESS ||
-      encode_tmap_2d(&mp.b1, f32, bt_small, K, N, Kp * 4, 32, 128, sw) != CUDA_SUCCESS ||
-      encode_c_map(&mp.c, C, M, N, ldc, c_tma) != CUDA_SUCCESS)
+      encode_tmap_2d(&mp.b0, f32, bt_big, K, N, Kp * 4, 32, b_box_rows, sw) != CUDA_SUCCESS ||
+      encode_tmap_2d(&mp.b1, f32, bt_small, K, N, Kp * 4, 32, b_box_rows, sw) != CUDA_SUCCESS ||
+      encode_c_map(&mp, C, M, N, ldc, tma_c) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  if (!c_tma) mp.c = mp.a0;  // unused without TMA stores
-  return launch_tc_any(KIND_3XTF32, mp, C, M, N, K, ldc, c_tma, true, ctl, s);
+  if (!tma_c && !mp.c_even) mp.c = mp.a0;  // unused without TMA stores
+  return pair ? launch_cta_pair(KIND_3XTF32, mp, C, M, N, K, ldc, tma_c, true, bn, ctl, s)
+              : launch_single_cta(KIND_3XTF32, mp, C, M, N, K, ldc, tma_c, true, ctl, s);
 }
 
 cudaError_t launch_tc_3xtf32_split(const float* A, const float* B, float* C, int64_t M,
                                    int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                                    bool c_tma, const DeviceCtl& ctl, cudaStream_t s) {
   TcMaps mp = {};
-  if (encode_c_map(&mp.c, C, M, N, ldc, c_tma) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  if (encode_c_map(&mp, C, M, N, ldc, c_tma) != CUDA_SUCCESS) return cudaErrorInvalidValue;
   // A itself, staged by TMA as its big part, when TMA can address it.
   const bool tma_a = a_serves_as_big(A, lda);
   if (tma_a && encode_tmap_2d(&mp.a0, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, K, M, lda * 4, 32, 128,
@@ -96,7 +178,7 @@ cudaError_t launch_tc_3xtf32_small(const float* A, const float* B, float* C, int
                                    int64_t K, int64_t lda, int64_t ldb, int64_t ldc, bool c_tma,
                                    const DeviceCtl& ctl, cudaStream_t s) {
   TcMaps mp = {};
-  if (encode_c_map(&mp.c, C, M, N, ldc, c_tma) != CUDA_SUCCESS ||
+  if (encode_c_map(&mp, C, M, N, ldc, c_tma) != CUDA_SUCCESS ||
       encode_tmap_2d(&mp.a0, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, K, M, lda * 4, 32, 128,
                      CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;

@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
           tmem_ld_32cols(taddr + c * 32, r);
           tmem_ld_wait();
           stage_and_store_chunk<TMA_STORE>(r, sbase + L::EPI_OFF, ew, chunk, lane, &tmC, p,
-                                           m0 + q * 32, n0 + c * 32, w.reduce);
+                                           m0 + q * 32, n0 + c * 32, p.N, w.reduce);
           ++chunk;
         }
       }
@@ -414,7 +414,7 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(acce_bar(buf));  // TMEM buffer `buf` may be overwritten
     }
-    if constexpr (TMA_STORE) {
+    if (TMA_STORE || p.c_even) {  // every store of this warp has completed
       if (lane == 0) bulk_wait_group<0>();
       __syncwarp();
     }
@@ -521,6 +521,7 @@ cudaError_t launch_t(const TcMaps& mp, float* C, int64_t M, int64_t N, int64_t K
                      bool c_tma, bool after_prepass, const DeviceCtl& ctl, cudaStream_t s) {
   using Cf = Cfg<KIND>;
   TcParams p = make_params(M, N, K, Cf::BM, Cf::BN, Cf::BK, C, ldc, ctl);
+  p.c_even = !c_tma && mp.c_even;
   cudaError_t e;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -603,6 +604,7 @@ cudaError_t launch_single_cta_split(const TcMaps& maps, const float* A, const fl
   p.ldb = ldb;
   p.vec_a = 1;  // the TMA map of A requires what the 16-byte loads do
   p.vec_b = (reinterpret_cast<uintptr_t>(B) % 16 == 0) && (ldb % 4 == 0);
+  p.c_even = !c_tma && maps.c_even;
   cudaError_t e;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -2,6 +2,7 @@
 // two SMs share one 256 x 256 output tile; persistent over tiles, with the
 // sparse last round split along K.  Used for large problems.  The method and
 // the warp roles are described in tc_common.cuh.
+#include <cstdio>
 #include <type_traits>
 
 #include "tc_common.cuh"
@@ -58,6 +59,9 @@ struct PairCfg<KIND_BF16> {
   static constexpr uint32_t TMEM_COLS = 2 * BN;             // 512
 };
 
+// BN is the widest tile; the kernel runs the tile width the host planned
+// (TcParams::bn, a multiple of 16), loading bn / 2 rows of each B part per CTA
+// into the start of its 16 KB box.
 template <>
 struct PairCfg<KIND_3XTF32> {
   static constexpr int BM = 128;
@@ -164,6 +168,11 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
   const bool leader = rank == 0;
   const int cluster = blockIdx.x >> 1, num_clusters = gridDim.x >> 1;
   const uint32_t peer_abort = mapa_shared(smem_u32(const_cast<int*>(abort_flag)), rank ^ 1u);
+  // The pair tile's columns, and the bytes one CTA loads into a ring stage.
+  const int bn = KIND == KIND_3XTF32 ? p.bn : Cf::BN;
+  const uint32_t stage_tx =
+      KIND == KIND_3XTF32 ? static_cast<uint32_t>(2 * Cf::A_BYTES + 2 * (bn / 2) * Cf::BK * 4)
+                          : static_cast<uint32_t>(Cf::STAGE_BYTES);
 
   if (threadIdx.x == 0) {
     // full[s]: one arrive.expect_tx by the TMA producer, or one arrive per
@@ -268,7 +277,7 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
         int tm, tn;
         tile_coords(w.tile, p, tm, tn);
         const int m0 = tm * 2 * Cf::BM + static_cast<int>(rank) * Cf::BM;
-        const int nb0 = tn * Cf::BN + static_cast<int>(rank) * Cf::BN_HALF;
+        const int nb0 = tn * bn + static_cast<int>(rank) * (bn / 2);
         bool ok = true;
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
           const uint32_t s = it % Cf::STAGES, ph = (it / Cf::STAGES) & 1u;
@@ -280,7 +289,7 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
           const uint32_t st = sbase + s * Cf::STAGE_BYTES;
           const uint32_t fb = mapa_shared(full_bar(s), 0);  // rank 0's full[s]
           const int k0 = kb * Cf::BK;
-          if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * Cf::STAGE_BYTES);
+          if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * stage_tx);
           const bool stall = p.inject_stall && blockIdx.x == 0 && it == 0;
           if (!stall) {
             if constexpr (KIND == KIND_BF16) {
@@ -334,10 +343,9 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
           const bool armed0 = i < it, loaded0 = armed0 && !(stalled_first && i == 0);
           const bool loaded1 = i < it1;
           if (!armed0) {
-            mbar_arrive_expect_tx(full_bar(s), Cf::STAGE_BYTES);  // rank 1's bytes only
+            mbar_arrive_expect_tx(full_bar(s), stage_tx);  // rank 1's bytes only
           } else {
-            const uint32_t missing = (loaded0 ? 0u : static_cast<uint32_t>(Cf::STAGE_BYTES)) +
-                                     (loaded1 ? 0u : static_cast<uint32_t>(Cf::STAGE_BYTES));
+            const uint32_t missing = (loaded0 ? 0u : stage_tx) + (loaded1 ? 0u : stage_tx);
             if (missing) mbar_complete_tx(full_bar(s), missing);
           }
           if (!mbar_wait_bounded(full_bar(s), ph, limit, &never))
@@ -352,6 +360,9 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
     if (leader && lane == 0) {
       uint32_t it = 0, tcount = 0;
       bool ok = true;
+      // M = 256 (the pair), N = the tile's columns
+      const uint32_t idesc =
+          KIND == KIND_3XTF32 ? make_idesc(2, false, false, 2 * Cf::BM, bn) : Cf::IDESC;
       for (int u = cluster; ok && u < p.num_units; u += num_clusters, ++tcount) {
         const Unit w = unit_of(u, p);
         const uint32_t buf = tcount & 1u, aph = (tcount >> 1) & 1u;
@@ -382,7 +393,7 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
                   smem_desc_sw128(st + (kk / 4) * Cf::A_BOX_BYTES + (kk % 4) * 32, 16, 1024);
               const uint64_t bd =
                   smem_desc_sw128(st + Cf::A_BYTES + kk * 2048, Cf::B_BOX_BYTES, 1024);
-              mma_f16_pair(d_tmem, ad, bd, Cf::IDESC, (kb > w.kb0 || kk > 0) ? 1u : 0u);
+              mma_f16_pair(d_tmem, ad, bd, idesc, (kb > w.kb0 || kk > 0) ? 1u : 0u);
             }
           } else {
             const uint32_t a_big = st, a_small = st + Cf::A_BYTES;
@@ -394,9 +405,9 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
               const uint64_t asd = smem_desc_sw128(a_small + off, 16, 1024);
               const uint64_t bbd = smem_desc_sw128(b_big + off, 16, 1024);
               const uint64_t bsd = smem_desc_sw128(b_small + off, 16, 1024);
-              mma_tf32_pair(d_tmem, asd, bbd, Cf::IDESC, (kb > w.kb0 || kk > 0) ? 1u : 0u);
-              mma_tf32_pair(d_tmem, abd, bsd, Cf::IDESC, 1u);
-              mma_tf32_pair(d_tmem, abd, bbd, Cf::IDESC, 1u);
+              mma_tf32_pair(d_tmem, asd, bbd, idesc, (kb > w.kb0 || kk > 0) ? 1u : 0u);
+              mma_tf32_pair(d_tmem, abd, bsd, idesc, 1u);
+              mma_tf32_pair(d_tmem, abd, bbd, idesc, 1u);
             }
           }
           mma_commit_pair_multicast(empty_bar(s), 0x3);  // stage s free in both CTAs
@@ -427,22 +438,25 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
       int tm, tn;
       tile_coords(w.tile, p, tm, tn);
       const int m0 = tm * 2 * Cf::BM + static_cast<int>(rank) * Cf::BM;
-      const int n0 = tn * Cf::BN;
+      const int n0 = tn * bn;
+      const int col_end = n0 + bn < p.N ? n0 + bn : p.N;
+      // (accumulator b occupies TMEM columns [256 b, 256 b + bn); a last
+      // chunk of 16 columns reads 16 allocated, unwritten ones, masked off)
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * Cf::BN;
 #pragma unroll 1
-      for (int c = 0; c < Cf::BN / 32; ++c) {
+      for (int c = 0; c < (bn + 31) / 32; ++c) {
         uint32_t r[32];
         tmem_ld_32cols(taddr + c * 32, r);
         tmem_ld_wait();
         stage_and_store_chunk<TMA_STORE>(r, sbase + L::EPI_OFF, ew, chunk, lane, &tmC, p,
-                                         m0 + q * 32, n0 + c * 32, w.reduce);
+                                         m0 + q * 32, n0 + c * 32, col_end, w.reduce);
         ++chunk;
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(buf), 0));
     }
-    if constexpr (TMA_STORE) {
+    if (TMA_STORE || p.c_even) {  // every store of this warp has completed
       if (lane == 0) bulk_wait_group<0>();
       __syncwarp();
     }
@@ -638,22 +652,28 @@ cudaError_t launch_pair_t(const TcMaps& mp, const TcParams& p, bool after_prepas
   // C (zeroed first).  Two addends onto zero give the same sum in either
   // order, so results stay bit-reproducible.
   TcParams q = p;
+  q.c_even = !TMA_STORE && mp.c_even;
   const int rem = p.num_tiles % clusters;
   if (p.num_tiles > clusters && rem > 0 && 2 * rem <= clusters && p.num_kb >= 2) {
     q.full_units = p.num_tiles - rem;
     q.num_units = q.full_units + 2 * rem;
     q.kb_mid = p.num_kb / 2;
-    if ((e = launch_zero_split_tiles(q, 2 * PairCfg<KIND>::BM, PairCfg<KIND>::BN, after_prepass,
-                                     s)) != cudaSuccess)
+    if ((e = launch_zero_split_tiles(q, 2 * PairCfg<KIND>::BM, q.bn, after_prepass, s)) !=
+        cudaSuccess)
       return e;
   }
   cfg.gridDim = dim3(2 * clusters);
   cfg.numAttrs = 2;  // and programmatic serialisation behind the kernel before
-  note_main_kernel(KIND == KIND_BF16                 ? "tc_gemm_pair_kernel<bf16>"
-                   : KIND == KIND_3XTF32             ? "tc_gemm_pair_kernel<3xtf32>"
-                   : KIND == KIND_3XTF32_SPLIT_TMA_A ? "tc_gemm_pair_kernel<3xtf32,split,tma-a>"
-                                                     : "tc_gemm_pair_kernel<3xtf32,split>",
-                   2 * clusters, p.num_tiles);
+  char name[64];
+  if (KIND == KIND_3XTF32 && p.bn != PairCfg<KIND>::BN)
+    snprintf(name, sizeof(name), "tc_gemm_pair_kernel<3xtf32,n%d>", p.bn);
+  else
+    snprintf(name, sizeof(name), "%s",
+             KIND == KIND_BF16                 ? "tc_gemm_pair_kernel<bf16>"
+             : KIND == KIND_3XTF32             ? "tc_gemm_pair_kernel<3xtf32>"
+             : KIND == KIND_3XTF32_SPLIT_TMA_A ? "tc_gemm_pair_kernel<3xtf32,split,tma-a>"
+                                               : "tc_gemm_pair_kernel<3xtf32,split>");
+  note_main_kernel(name, 2 * clusters, p.num_tiles);
   e = cudaLaunchKernelEx(&cfg, kern, mp.a0, mp.a1, mp.b0, mp.b1, mp.c, q);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -699,7 +719,7 @@ cudaError_t launch_cta_pair_split(bool tma_a, const float* A, const float* B, co
 }
 
 cudaError_t launch_cta_pair(int kind, const TcMaps& maps, float* C, int64_t M, int64_t N,
-                            int64_t K, int64_t ldc, bool c_tma, bool after_prepass,
+                            int64_t K, int64_t ldc, bool c_tma, bool after_prepass, int bn,
                             const DeviceCtl& ctl, cudaStream_t s) {
   if (kind == KIND_BF16) {
     const TcParams p = make_params(M, N, K, PAIR_TILE_M, PAIR_TILE_N, PairCfg<KIND_BF16>::BK, C,
@@ -707,8 +727,7 @@ cudaError_t launch_cta_pair(int kind, const TcMaps& maps, float* C, int64_t M, i
     return c_tma ? launch_pair_t<KIND_BF16, true>(maps, p, after_prepass, ctl, s)
                  : launch_pair_t<KIND_BF16, false>(maps, p, after_prepass, ctl, s);
   }
-  const TcParams p = make_params(M, N, K, PAIR_TILE_M, PAIR_TILE_N, PairCfg<KIND_3XTF32>::BK, C,
-                                 ldc, ctl);
+  const TcParams p = make_params(M, N, K, PAIR_TILE_M, bn, PairCfg<KIND_3XTF32>::BK, C, ldc, ctl);
   return c_tma ? launch_pair_t<KIND_3XTF32, true>(maps, p, after_prepass, ctl, s)
                : launch_pair_t<KIND_3XTF32, false>(maps, p, after_prepass, ctl, s);
 }

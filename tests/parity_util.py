@@ -3,6 +3,7 @@ C ABI on device buffers with poisoned padding, and the comparison with the CPU
 oracle by the normalised error max |C - C_ref| / sum_k |A_ik||B_kj|."""
 from __future__ import annotations
 
+import contextlib
 import ctypes
 
 import numpy as np
@@ -113,3 +114,14 @@ def sample_indices(M, N, seed, n_random=4096, rows=(), cols=()):
         r.append(np.arange(M))
         c.append(np.full(M, col))
     return np.concatenate(r).astype(np.int64), np.concatenate(c).astype(np.int64)
+
+
+@contextlib.contextmanager
+def pair_tile_n(mhr, columns):
+    """Run the enclosed calls with the 3xTF32 CTA-pair tiles forced to
+    `columns` wide (0: the planner's choice)."""
+    old = mhr.gemm_testing_set_pair_tile_n(columns)
+    try:
+        yield
+    finally:
+        mhr.gemm_testing_set_pair_tile_n(old)

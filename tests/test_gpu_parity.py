@@ -10,7 +10,8 @@ import numpy as np
 import pytest
 
 import oracle
-from parity_util import TOL, DeviceCall, normalised_error, operands, sample_indices
+from parity_util import (TOL, DeviceCall, normalised_error, operands, pair_tile_n,
+                         sample_indices)
 
 pytestmark = pytest.mark.gpu
 
@@ -171,6 +172,17 @@ def test_config3_rectangular_full(mhr):
         C = DeviceCall(path, A, B).run(mhr).result()
         err = normalised_error(C, Cref, S)
         assert err <= TOL[path], (path, err)
+        if path == "3xtf32":
+            # C's pitch rules out TMA stores; the pair tiles are as wide as the
+            # planner says for this GPU (176 columns on 76 clusters)
+            label = mhr.gemm_testing_last_main_kernel()
+            if label.startswith("tc_gemm_pair_kernel<3xtf32"):
+                import re
+
+                clusters = int(re.search(r"grid=(\d+)", label).group(1)) // 2
+                bn = mhr.gemm_testing_plan_pair_tile_n(M, N, K, clusters, False)
+                want = "tc_gemm_pair_kernel<3xtf32" + ("> " if bn == 256 else f",n{bn}> ")
+                assert label.startswith(want), (label, want)
 
 
 def sampled_check(mhr, path, M, N, K, seed, dist):
@@ -200,6 +212,15 @@ def test_config5_8192_bf16_sampled(mhr):
     sampled_check(mhr, "bf16", 8192, 8192, 8192, 5001, "normal")
 
 
+@pytest.fixture
+def full_width_tiles(mhr):
+    """The 3xTF32 CTA-pair tiles at their full 256 columns, for tests that
+    count tiles or compare the pre-pass path with the in-kernel split (which
+    always runs 256-column tiles) bit for bit."""
+    with pair_tile_n(mhr, 256):
+        yield
+
+
 def pair_clusters(mhr, path):
     """The number of clusters the CTA-pair kernel runs on this GPU."""
     import re
@@ -212,6 +233,7 @@ def pair_clusters(mhr, path):
     return clusters
 
 
+@pytest.mark.usefixtures("full_width_tiles")
 @pytest.mark.parametrize("path", ["3xtf32", "bf16"])
 def test_pair_kernel_split_last_round(mhr, path):
     """The CTA-pair kernel splits a sparse last round of tiles into two K halves
@@ -221,12 +243,14 @@ def test_pair_kernel_split_last_round(mhr, path):
     path (ldc odd), and for bitwise repeatability. With every buffer one
     element off 16-byte alignment, the pre-pass (the bf16 repacks, or the
     3xTF32 split with 4-byte loads) runs alongside the kernel zeroing C's
-    split tiles, which then writes 4-byte stores."""
+    split tiles, which then writes 4-byte stores. ldc = N + 2 (2 mod 4)
+    takes the mixed path: TMA reduce-adds into C's even rows, atomic adds
+    into the odd ones."""
     old = mhr.gemm_testing_set_cta_pair_mode(2)
     try:
         clusters = pair_clusters(mhr, path)
         M, N, K = 256 * (clusters + 3), 256, 320
-        for ldc, offset in ((None, 0), (N + 1, 0), (None, 1)):
+        for ldc, offset in ((None, 0), (N + 1, 0), (N + 2, 0), (None, 1)):
             A, B, Ab, Bb = operands(M, N, K, 3103, "normal", path)
             call = DeviceCall(path, A, B, Ab, Bb, ldc=ldc, offset=offset)
             C = call.run(mhr).result()
@@ -238,6 +262,7 @@ def test_pair_kernel_split_last_round(mhr, path):
         mhr.gemm_testing_set_cta_pair_mode(old)
 
 
+@pytest.mark.usefixtures("full_width_tiles")
 @pytest.mark.parametrize("path", ["3xtf32", "bf16"])
 @pytest.mark.parametrize("extra", [1, -1, 5, 28], ids=["c+1", "2c-1", "2c+5", "3c+28"])
 def test_pair_kernel_schedule_bit_exact(mhr, path, extra):
@@ -257,6 +282,41 @@ def test_pair_kernel_schedule_bit_exact(mhr, path, extra):
         C = DeviceCall(path, A, B, Ab, Bb).run(mhr).result()
         assert f"tiles={tiles}" in mhr.gemm_testing_last_main_kernel()
         assert np.array_equal(C, oracle.gemm(A, B))
+    finally:
+        mhr.gemm_testing_set_cta_pair_mode(old)
+
+
+@pytest.mark.parametrize("bn", [240, 224, 176, 144, 128])
+def test_pair_kernel_narrow_tiles(mhr, bn):
+    """3xTF32 CTA-pair tiles narrower than 256 columns: each CTA loads bn / 2
+    rows of each B part, the MMAs run with N = bn, and the epilogue writes
+    ceil(bn / 32) chunks per tile, the last one masked at the tile's edge when
+    bn is not a multiple of 32. 10 tile columns (N = 10 bn - 8 or 10 bn - 7,
+    a short last column) by 8 tile rows (M = 1948, ragged) are 80 tiles: one
+    round plus 4 tiles split into K halves on 76 clusters. Integer inputs
+    match the oracle bit for bit through TMA stores (N a multiple of 4 with C
+    aligned, for widths that are whole chunks) and register stores (N odd,
+    ldc = N + 1); real inputs meet the tolerance, bitwise repeatably."""
+    import re
+
+    M, K = 1948, 96 + 5
+    old = mhr.gemm_testing_set_cta_pair_mode(2)
+    try:
+        with pair_tile_n(mhr, bn):
+            for N, ldc in ((10 * bn - 8, None), (10 * bn - 7, 10 * bn - 6)):
+                A, B, _, _ = operands(M, N, K, 3701 + bn, "int", "3xtf32")
+                C = DeviceCall("3xtf32", A, B, ldc=ldc).run(mhr).result()
+                label = mhr.gemm_testing_last_main_kernel()
+                assert label.startswith(f"tc_gemm_pair_kernel<3xtf32,n{bn}> "), label
+                clusters = int(re.search(r"grid=(\d+)", label).group(1)) // 2
+                assert f"tiles={8 * 10}" in label, label
+                assert np.array_equal(C, oracle.gemm(A, B)), (bn, ldc, clusters)
+            A, B, _, _ = operands(M, N, K, 3702 + bn, "normal", "3xtf32")
+            call = DeviceCall("3xtf32", A, B, ldc=ldc)
+            C = call.run(mhr).result()
+            Cref, S = oracle.gemm(A, B, with_abs=True)
+            assert normalised_error(C, Cref, S) <= TOL["3xtf32"]
+            assert np.array_equal(call.run(mhr).result(), C)
     finally:
         mhr.gemm_testing_set_cta_pair_mode(old)
 
@@ -288,7 +348,7 @@ def test_single_cta_few_tiles(mhr, path):
                  (sms // 2 + 1, bk * 32 + 40, f"{name}> grid={sms // 2 + 1} ")]
         for tiles, K, want in cases:
             M, N = 128 * tiles, tile_n
-            for ldc in (None, N + 1):
+            for ldc in (None, N + 1, N + 2):
                 A, B, Ab, Bb = operands(M, N, K, 3112 + tiles + K, "int", path)
                 C = DeviceCall(path, A, B, Ab, Bb, ldc=ldc).run(mhr).result()
                 label = mhr.gemm_testing_last_main_kernel()
@@ -309,6 +369,7 @@ def test_single_cta_few_tiles(mhr, path):
                                    (512, 512, 4096), (256 * 79, 256, 320), (300, 130, 1000)],
                          ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("offset", [0, 1], ids=["aligned", "offset1"])
+@pytest.mark.usefixtures("full_width_tiles")
 def test_in_kernel_split_matches_prepass_bitwise(mhr, shape, offset):
     """The CTA-pair kernel with the split inside the kernel computes exactly
     what it computes on pre-split operands: the same tf32 parts, the same
@@ -367,6 +428,7 @@ def test_single_cta_in_kernel_split_is_one_launch(mhr, shape):
         mhr.gemm_testing_set_cta_pair_mode(old)
 
 
+@pytest.mark.usefixtures("full_width_tiles")
 def test_workspace_fallback_splits_in_kernel(mhr):
     """Operands one element off 16-byte alignment cannot be their own big
     parts, so the split runs in a pre-pass into the workspace. When that

@@ -1,0 +1,48 @@
+"""The tile-width planner of the 3xTF32 CTA-pair kernel (host arithmetic in
+libmhr_gemm.so, no GPU needed): which width it picks for the listed
+workloads on GB300's 76 co-resident CTA pairs, and that every pick is a width
+the kernel supports."""
+import numpy as np
+import pytest
+
+import memory_hierarchy_reuse_gb300 as mhr
+
+CLUSTERS = 76  # 152 SMs in pairs
+
+
+@pytest.fixture(scope="module")
+def lib():
+    try:
+        return mhr.load()
+    except OSError as e:  # the library is built by __graft_entry__.build()
+        pytest.skip(f"libmhr_gemm.so not built: {e}")
+
+
+@pytest.mark.parametrize("shape,c_tma,want", [
+    ((4096, 4096, 4096), True, 256),   # 256 tiles: 3 rounds + a split one, whole-width best
+    ((8192, 8192, 8192), True, 256),   # 1024 tiles: 13 rounds + a split one
+    ((3000, 2048, 1000), True, 256),
+    # 3000 x 2050 x 1000 with C's odd pitch (register stores): 108 tiles of 256
+    # columns need a K-split last round ending in atomic adds; 144 tiles of 176
+    # columns fill two whole rounds
+    ((3000, 2050, 1000), False, 176),
+])
+def test_planned_width_for_listed_workloads(lib, shape, c_tma, want):
+    assert mhr.gemm_testing_plan_pair_tile_n(*shape, CLUSTERS, c_tma) == want
+
+
+def test_planned_width_is_supported(lib):
+    rng = np.random.default_rng(11)
+    for _ in range(400):
+        M, N = (int(x) for x in rng.integers(1, 20000, size=2))
+        K = int(rng.integers(1, 9000))
+        clusters = int(rng.integers(1, 80))
+        for c_tma in (False, True):
+            bn = mhr.gemm_testing_plan_pair_tile_n(M, N, K, clusters, c_tma)
+            assert 128 <= bn <= 256 and bn % 16 == 0, (M, N, K, clusters, bn)
+            if c_tma:
+                assert bn % 32 == 0, (M, N, K, clusters, bn)
+
+
+def test_no_clusters_keeps_full_width(lib):
+    assert mhr.gemm_testing_plan_pair_tile_n(4096, 4096, 4096, 0, True) == 256
