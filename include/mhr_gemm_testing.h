@@ -135,6 +135,23 @@ int gemm_testing_set_pair_tile_n(int columns);
  */
 int gemm_testing_plan_pair_tile_n(int64_t M, int64_t N, int64_t K, int clusters, int c_tma);
 
+/*
+ * Forces the width of the single-CTA kernel's 3xTF32 output tiles (128 rows x
+ * `columns`, columns 128, 96, 64 or 32) for the following calls
+ * (process-wide); any other value, 0 included, restores the planner's choice.
+ * Calls that take the cluster split or the in-kernel split keep 128.
+ * Returns the previous setting.
+ */
+int gemm_testing_set_single_tile_n(int columns);
+
+/*
+ * The planner's choice of those columns for an M x N x K 3xTF32 problem on
+ * `sms` SMs, C written by TMA stores when c_tma is nonzero.  Host arithmetic
+ * only, as for gemm_testing_plan_pair_tile_n: smaller tiles spread a small
+ * problem over more SMs ("矩阵乘法 tiling", section 五, on the tile size).
+ */
+int gemm_testing_plan_single_tile_n(int64_t M, int64_t N, int64_t K, int sms, int c_tma);
+
 #ifdef __cplusplus
 }
 #endif

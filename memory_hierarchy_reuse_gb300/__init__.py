@@ -49,7 +49,8 @@ EXPORTS = ("gemm_f32", "gemm_f32_3xtf32", "gemm_bf16_f32acc", "gemm_f32_3xtf32_n
            "gemm_testing_set_raster_group", "gemm_testing_set_split_mode",
            "gemm_testing_last_launches", "gemm_testing_set_workspace_limit",
            "gemm_testing_set_zero_a_small", "gemm_testing_set_pair_tile_n",
-           "gemm_testing_plan_pair_tile_n")
+           "gemm_testing_plan_pair_tile_n", "gemm_testing_set_single_tile_n",
+           "gemm_testing_plan_single_tile_n")
 
 _lib = None
 
@@ -104,6 +105,10 @@ def load(path: str | None = None):
     lib.gemm_testing_set_pair_tile_n.restype = ctypes.c_int
     lib.gemm_testing_plan_pair_tile_n.argtypes = [i64, i64, i64, ctypes.c_int, ctypes.c_int]
     lib.gemm_testing_plan_pair_tile_n.restype = ctypes.c_int
+    lib.gemm_testing_set_single_tile_n.argtypes = [ctypes.c_int]
+    lib.gemm_testing_set_single_tile_n.restype = ctypes.c_int
+    lib.gemm_testing_plan_single_tile_n.argtypes = [i64, i64, i64, ctypes.c_int, ctypes.c_int]
+    lib.gemm_testing_plan_single_tile_n.restype = ctypes.c_int
     lib.gemm_testing_set_split_mode.argtypes = [ctypes.c_int]
     lib.gemm_testing_set_split_mode.restype = ctypes.c_int
     lib.gemm_testing_set_workspace_limit.argtypes = [ctypes.c_uint64]
@@ -268,3 +273,14 @@ def matmul(a, b, path: str = "f32", out=None, stream=None, lda=None, ldb=None, l
 
 # The same call under the name the C ABI's family uses: gemm(a, b, path).
 gemm = matmul
+
+
+def gemm_testing_set_single_tile_n(columns: int) -> int:
+    """Force the 3xTF32 single-CTA tiles' columns (128, 96, 64 or 32); 0
+    restores the planner (test hook)."""
+    return load().gemm_testing_set_single_tile_n(int(columns))
+
+
+def gemm_testing_plan_single_tile_n(M: int, N: int, K: int, sms: int, c_tma: bool) -> int:
+    """The 3xTF32 single-CTA tile columns the planner picks (host logic only)."""
+    return load().gemm_testing_plan_single_tile_n(M, N, K, int(sms), int(bool(c_tma)))

@@ -67,6 +67,7 @@ int g_pair_mode = 0;
 int g_raster_group = 0;
 int g_split_mode = 0;
 int g_pair_tile_n = 0;
+int g_single_tile_n = 0;
 uint64_t g_workspace_limit = UINT64_MAX;
 int g_zero_a_small = 0;
 cudaEvent_t g_main_start = nullptr, g_main_stop = nullptr;
@@ -247,6 +248,7 @@ DeviceCtl make_ctl(const DeviceState& st) {
   c.raster_group = g_raster_group;
   c.split_mode = g_split_mode;
   c.pair_tile_n = g_pair_tile_n;
+  c.single_tile_n = g_single_tile_n;
   return c;
 }
 
@@ -558,6 +560,17 @@ MHR_API int gemm_testing_set_pair_tile_n(int columns) {
   const int old = g_pair_tile_n;
   g_pair_tile_n = (columns >= 128 && columns <= 256 && columns % 16 == 0) ? columns : 0;
   return old;
+}
+
+MHR_API int gemm_testing_set_single_tile_n(int columns) {
+  std::lock_guard<std::mutex> g(g_mu);
+  const int old = g_single_tile_n;
+  g_single_tile_n = (columns == 32 || columns == 64 || columns == 96 || columns == 128) ? columns : 0;
+  return old;
+}
+
+MHR_API int gemm_testing_plan_single_tile_n(int64_t M, int64_t N, int64_t K, int sms, int c_tma) {
+  return tc::plan_single_tile_n(M, N, K, sms, c_tma != 0);
 }
 
 MHR_API int gemm_testing_plan_pair_tile_n(int64_t M, int64_t N, int64_t K, int clusters,

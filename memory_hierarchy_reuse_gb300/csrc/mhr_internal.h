@@ -20,6 +20,7 @@ struct DeviceCtl {
   int raster_group = 0;                // tile rows per raster group, 0 = default (tuning hook)
   int split_mode = 0;                  // 3xTF32: 0 auto, 1 split pre-pass, 2 in-kernel split (test hook)
   int pair_tile_n = 0;                 // 3xTF32 CTA-pair tile columns, 0 = planned (test hook)
+  int single_tile_n = 0;               // 3xTF32 single-CTA tile columns, 0 = planned (test hook)
 };
 
 cudaError_t launch_simt_f32(const float* A, const float* B, float* C, int64_t M, int64_t N,
@@ -92,6 +93,9 @@ namespace tc {
 // problem with up to `clusters` co-resident clusters; tc_gemm.cu gives the
 // cost model.
 int plan_pair_tile_n(int64_t M, int64_t N, int64_t K, int clusters, bool c_tma);
+// Columns of the single-CTA kernel's 3xTF32 tiles (128, 96, 64 or 32) on
+// `sms` SMs; tc_gemm.cu gives the cost model.
+int plan_single_tile_n(int64_t M, int64_t N, int64_t K, int sms, bool c_tma);
 }  // namespace tc
 
 // Whether C can be written with TMA stores: 16-byte aligned base and pitch,

@@ -356,9 +356,10 @@ struct TcMaps {
   bool c_even = false;
 };
 
-// tc_gemm_1cta.cu
+// tc_gemm_1cta.cu.  bn: KIND_3XTF32's tile columns (128, or 96, 64 or 32
+// with the B maps' boxes of bn rows; 0 = 128); the bf16 kind ignores it.
 cudaError_t launch_single_cta(int kind, const TcMaps& maps, float* C, int64_t M, int64_t N,
-                              int64_t K, int64_t ldc, bool c_tma, bool after_prepass,
+                              int64_t K, int64_t ldc, bool c_tma, bool after_prepass, int bn,
                               const DeviceCtl& ctl, cudaStream_t s);
 // tc_gemm_1cta.cu: KIND_3XTF32_SPLIT_TMA_A on the single-CTA kernel, for small
 // problems (one launch): maps.a0 is A's map (K-major boxes of 32 k x 128

@@ -72,6 +72,45 @@ int plan_pair_tile_n(int64_t M, int64_t N, int64_t K, int clusters, bool c_tma) 
   return best_t <= 0.95 * full_width ? best : PAIR_TILE_N;
 }
 
+// Tile width of the single-CTA 3xTF32 kernel (128 rows x bn, bn = 128, 96,
+// 64 or 32; it runs problems with too few 256 x 256 tiles to fill the CTA
+// pairs).  Narrower tiles put more SMs on a small problem: with every tile in
+// one round (or split into K halves when twice the tiles fit), a unit's time
+// is its K-blocks times the slower of two rates -- TMA filling the stage
+// (A's 32 KB plus 256 bn bytes of B at some 64 bytes per SM cycle, measured
+// on the 256^3 main loop) and the 12 MMAs of N = bn (6 bn cycles) -- plus
+// its last epilogue (about 20 cycles per column with TMA stores, 60 with
+// register stores).  The cluster split keeps whole tiles; bn = 128 unless a
+// narrower width is at least 5 % faster by this estimate.
+double single_cycles_estimate(int64_t M, int64_t N, int64_t K, int sms, bool c_tma, int bn) {
+  const int64_t tiles = ((M + 127) / 128) * ((N + bn - 1) / bn);
+  const int64_t kb = (K + 31) / 32;
+  const bool split = 2 * tiles <= sms && kb >= 4;
+  const int64_t units = split ? 2 * tiles : tiles;
+  const int64_t kb_unit = split ? kb - kb / 2 : kb;
+  const int64_t rounds = (units + sms - 1) / sms;
+  const double fill = (32768.0 + 256.0 * bn) / 64.0, mma = 6.0 * bn;
+  return static_cast<double>(rounds * kb_unit) * (fill > mma ? fill : mma) +
+         (c_tma ? 20.0 : 60.0) * bn;
+}
+
+int plan_single_tile_n(int64_t M, int64_t N, int64_t K, int sms, bool c_tma) {
+  if (sms < 1) return 128;
+  const int64_t tiles = ((M + 127) / 128) * ((N + 127) / 128);
+  if (2 * tiles <= sms && (K + 31) / 32 >= 64) return 128;  // the cluster split's domain
+  const double full_width = single_cycles_estimate(M, N, K, sms, c_tma, 128);
+  int best = 128;
+  double best_t = full_width;
+  for (int bn = 96; bn >= 32; bn -= 32) {
+    const double t = single_cycles_estimate(M, N, K, sms, c_tma, bn);
+    if (t < best_t) {
+      best_t = t;
+      best = bn;
+    }
+  }
+  return best_t <= 0.95 * full_width ? best : 128;
+}
+
 }  // namespace tc
 
 namespace {
@@ -95,7 +134,7 @@ cudaError_t launch_tc_any(int kind, const TcMaps& maps, float* C, int64_t M, int
   return tc_pair_chosen(kind, M, N, K, ctl)
              ? launch_cta_pair(kind, maps, C, M, N, K, ldc, c_tma, after_prepass, PAIR_TILE_N,
                                ctl, s)
-             : launch_single_cta(kind, maps, C, M, N, K, ldc, c_tma, after_prepass, ctl, s);
+             : launch_single_cta(kind, maps, C, M, N, K, ldc, c_tma, after_prepass, 0, ctl, s);
 }
 
 // C's map: the whole of C in boxes of 32 x 32 when TMA can store C.
@@ -141,15 +180,16 @@ cudaError_t launch_tc_3xtf32(const float* a_big, int64_t a_big_ld, const float* 
   const auto f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
   // The CTA-pair kernel's tiles are 256 x bn (each CTA loads bn / 2 rows of
-  // B^T per part); the single-CTA kernel's 128 x 128.  A tile width the
-  // planner would not give with TMA stores (one that is not whole 32-column
-  // chunks, forced by the test hook) writes C with register stores instead.
+  // B^T per part), the single-CTA kernel's 128 x bn (bn rows).  A tile width
+  // the planner would not give with TMA stores (one that is not whole
+  // 32-column chunks, forced by the test hook) writes C with register stores.
   const bool pair = tc_pair_chosen(KIND_3XTF32, M, N, K, ctl);
-  const int bn = !pair                ? PAIR_TILE_N
-                 : ctl.pair_tile_n > 0 ? ctl.pair_tile_n
-                                       : plan_pair_tile_n(M, N, K, ctl.sm_count / 2, c_tma);
+  const int bn = pair ? (ctl.pair_tile_n > 0 ? ctl.pair_tile_n
+                                             : plan_pair_tile_n(M, N, K, ctl.sm_count / 2, c_tma))
+                      : (ctl.single_tile_n > 0 ? ctl.single_tile_n
+                                               : plan_single_tile_n(M, N, K, ctl.sm_count, c_tma));
   const bool tma_c = c_tma && bn % 32 == 0;
-  const int b_box_rows = pair ? bn / 2 : 128;
+  const int b_box_rows = pair ? bn / 2 : bn;
   if (encode_tmap_2d(&mp.a0, f32, a_big, K, M, a_big_ld * 4, 32, 128, sw) != CUDA_SUCCESS ||
       encode_tmap_2d(&mp.a1, f32, a_small, K, M, Kp * 4, 32, 128, sw) != CUDA_SUCCESS ||
       encode_tmap_2d(&mp.b0, f32, bt_big, K, N, Kp * 4, 32, b_box_rows, sw) != CUDA_SUCCESS ||
@@ -158,7 +198,7 @@ cudaError_t launch_tc_3xtf32(const float* a_big, int64_t a_big_ld, const float* 
     return cudaErrorInvalidValue;
   if (!tma_c && !mp.c_even) mp.c = mp.a0;  // unused without TMA stores
   return pair ? launch_cta_pair(KIND_3XTF32, mp, C, M, N, K, ldc, tma_c, true, bn, ctl, s)
-              : launch_single_cta(KIND_3XTF32, mp, C, M, N, K, ldc, tma_c, true, ctl, s);
+              : launch_single_cta(KIND_3XTF32, mp, C, M, N, K, ldc, tma_c, true, bn, ctl, s);
 }
 
 cudaError_t launch_tc_3xtf32_split(const float* A, const float* B, float* C, int64_t M,

@@ -3,6 +3,7 @@
 //   3xTF32: 128 x 128 x 32 tiles, 3 stages of 64 KB, kind::tf32 M128 N128 K8.
 // Used for problems whose 256-row CTA-pair tiles would not keep the GPU busy.
 // The method and the warp roles are described in tc_common.cuh.
+#include <cstdio>
 #include <type_traits>
 
 #include "tc_common.cuh"
@@ -22,14 +23,19 @@ struct Cfg<KIND_BF16> {
   static constexpr int B_BOX_BYTES = 64 * BK * 2;          // 64 cols x 64 k = 8 KB
   static constexpr int B_BYTES = BK * BN * 2;              // 32 KB
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;    // 48 KB
+  static constexpr int MAX_STAGES = STAGES;
   static constexpr int INSTR_K = 16;
   static constexpr uint32_t IDESC = make_idesc(1, false, true, BM, BN);
   static constexpr uint32_t TMEM_COLS = 2 * BN;            // 512
 };
 
+// BN is the widest tile; with a pre-pass the kernel runs the width the host
+// planned (TcParams::bn: 128, 96, 64 or 32), and its ring holds as many
+// stages of 2 x 16 KB of A and 2 x bn x 128 bytes of B as fit in the same
+// 192 KB, up to MAX_STAGES (ring_stages below): four at bn = 32 and 64.
 template <>
 struct Cfg<KIND_3XTF32> {
-  static constexpr int BM = 128, BN = 128, BK = 32, STAGES = 3;
+  static constexpr int BM = 128, BN = 128, BK = 32, STAGES = 3, MAX_STAGES = 4;
   static constexpr int A_BYTES = BM * BK * 4;              // 16 KB each (big, small)
   static constexpr int B_BYTES = BN * BK * 4;              // 16 KB each (big, small)
   static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;  // 64 KB
@@ -44,6 +50,23 @@ struct Cfg<KIND_3XTF32> {
 // launch, no workspace.
 template <>
 struct Cfg<KIND_3XTF32_SPLIT_TMA_A> : Cfg<KIND_3XTF32> {};
+
+// Ring stages and bytes per stage for tiles of bn columns (KIND_3XTF32
+// outside the cluster split; every other case has the kind's fixed ring).
+template <int KIND>
+__host__ __device__ constexpr int ring_stage_bytes(int bn) {
+  return KIND == KIND_3XTF32 ? 2 * Cfg<KIND>::A_BYTES + 2 * bn * Cfg<KIND>::BK * 4
+                             : Cfg<KIND>::STAGE_BYTES;
+}
+template <int KIND>
+__host__ __device__ constexpr int ring_stages(int bn) {
+  return KIND == KIND_3XTF32
+             ? (Cfg<KIND>::STAGES * Cfg<KIND>::STAGE_BYTES / ring_stage_bytes<KIND>(bn) <
+                        Cfg<KIND>::MAX_STAGES
+                    ? Cfg<KIND>::STAGES * Cfg<KIND>::STAGE_BYTES / ring_stage_bytes<KIND>(bn)
+                    : Cfg<KIND>::MAX_STAGES)
+             : Cfg<KIND>::STAGES;
+}
 
 template <int KIND>
 __host__ __device__ constexpr int cta_threads() {
@@ -106,7 +129,7 @@ struct Layout {
   static constexpr int EPI_OFF = C::STAGES * C::STAGE_BYTES;
   static constexpr int BAR_OFF = EPI_OFF + EPI_BYTES;
   // full, empty, acc_full x2, acc_empty x2, drain, and the converters' stores
-  static constexpr int NUM_BARS = 3 * C::STAGES + 5;
+  static constexpr int NUM_BARS = 3 * C::MAX_STAGES + 5;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;   // tmem slot, abort flag
   static constexpr int USED = MISC_OFF + 16;
   static constexpr int ALLOC = USED + 1024;                 // slack for 1024-byte alignment
@@ -145,20 +168,24 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + L::BAR_OFF;
   auto full_bar = [&](uint32_t s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (Cf::STAGES + s); };
-  auto accf_bar = [&](uint32_t b) { return bar0 + 8u * (2 * Cf::STAGES + b); };
-  auto acce_bar = [&](uint32_t b) { return bar0 + 8u * (2 * Cf::STAGES + 2 + b); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * Cf::STAGES + 4);
+  auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (Cf::MAX_STAGES + s); };
+  auto accf_bar = [&](uint32_t b) { return bar0 + 8u * (2 * Cf::MAX_STAGES + b); };
+  auto acce_bar = [&](uint32_t b) { return bar0 + 8u * (2 * Cf::MAX_STAGES + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * Cf::MAX_STAGES + 4);
   // KIND_3XTF32_SPLIT_TMA_A: the converter warps' stores of stage s are done
-  auto cvt_bar = [&](uint32_t s) { return bar0 + 8u * (2 * Cf::STAGES + 5 + s); };
+  auto cvt_bar = [&](uint32_t s) { return bar0 + 8u * (2 * Cf::MAX_STAGES + 5 + s); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // The tile's columns (the cluster split runs whole tiles only), and the ring.
+  const int bn = KIND == KIND_3XTF32 && !CLUSTER ? p.bn : Cf::BN;
+  const uint32_t stages = static_cast<uint32_t>(ring_stages<KIND>(bn));
+  const uint32_t stage_bytes = static_cast<uint32_t>(ring_stage_bytes<KIND>(bn));
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < Cf::STAGES; ++s) {
+    for (int s = 0; s < Cf::MAX_STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
       if constexpr (KIND == KIND_3XTF32_SPLIT_TMA_A) mbar_init(cvt_bar(s), SPLIT_WARPS);
@@ -202,19 +229,19 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
         const Unit w = unit_1cta<CLUSTER>(u, p);
         int tm, tn;
         tile_coords(w.tile, p, tm, tn);
-        const int m0 = tm * Cf::BM, n0 = tn * Cf::BN;
+        const int m0 = tm * Cf::BM, n0 = tn * bn;
         for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-          const uint32_t s = it % Cf::STAGES, ph = (it / Cf::STAGES) & 1u;
+          const uint32_t s = it % stages, ph = (it / stages) & 1u;
           if (!mbar_wait_bounded(empty_bar(s), ph ^ 1u, limit, abort_flag)) {
             give_up_one(p, abort_flag, kErrTimeoutProducer);
             ok = false;
             break;
           }
-          const uint32_t st = sbase + s * Cf::STAGE_BYTES;
+          const uint32_t st = sbase + s * stage_bytes;
           const int k0 = kb * Cf::BK;
           // the split kind loads A alone (its converters fill the rest)
-          mbar_arrive_expect_tx(full_bar(s), KIND == KIND_3XTF32_SPLIT_TMA_A ? Cf::A_BYTES
-                                                                             : Cf::STAGE_BYTES);
+          mbar_arrive_expect_tx(full_bar(s),
+                                KIND == KIND_3XTF32_SPLIT_TMA_A ? Cf::A_BYTES : stage_bytes);
           const bool stall = p.inject_stall && blockIdx.x == 0 && it == 0;
           if (!stall) {
             if constexpr (KIND == KIND_3XTF32_SPLIT_TMA_A) {
@@ -229,7 +256,7 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
               tma_load_2d(st, &tmA0, full_bar(s), k0, m0);
               tma_load_2d(st + Cf::A_BYTES, &tmA1, full_bar(s), k0, m0);
               tma_load_2d(st + 2 * Cf::A_BYTES, &tmB0, full_bar(s), k0, n0);
-              tma_load_2d(st + 2 * Cf::A_BYTES + Cf::B_BYTES, &tmB1, full_bar(s), k0, n0);
+              tma_load_2d(st + 2 * Cf::A_BYTES + bn * Cf::BK * 4, &tmB1, full_bar(s), k0, n0);
             }
             inflight |= 1u << s;
           } else {
@@ -238,11 +265,11 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
         }
       }
       // Drain: every TMA this CTA issued must have landed before it exits.
-      for (uint32_t s = 0; s < static_cast<uint32_t>(Cf::STAGES) && s < it; ++s) {
+      for (uint32_t s = 0; s < stages && s < it; ++s) {
         if (!(inflight & (1u << s))) continue;
-        const uint32_t last = it - 1 - ((it - 1 - s) % Cf::STAGES);  // latest fill of stage s
+        const uint32_t last = it - 1 - ((it - 1 - s) % stages);  // latest fill of stage s
         volatile int never = 0;
-        if (!mbar_wait_bounded(full_bar(s), (last / Cf::STAGES) & 1u, limit, &never))
+        if (!mbar_wait_bounded(full_bar(s), (last / stages) & 1u, limit, &never))
           atomicOr(p.status, kErrTimeoutDrain);
       }
     }
@@ -253,6 +280,8 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
     if (lane == 0) {
       uint32_t it = 0, tcount = 0;
       bool ok = true;
+      const uint32_t idesc =
+          KIND == KIND_BF16 ? Cf::IDESC : make_idesc(2, false, false, Cf::BM, bn);
       for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++tcount) {
         const Unit w = unit_1cta<CLUSTER>(u, p);
         const uint32_t buf = tcount & 1u, aph = (tcount >> 1) & 1u;
@@ -263,7 +292,7 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
         tc_fence_after();  // the epilogue's TMEM reads precede these MMAs' writes
         const uint32_t d_tmem = tmem_base + buf * Cf::BN;
         for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-          const uint32_t s = it % Cf::STAGES, ph = (it / Cf::STAGES) & 1u;
+          const uint32_t s = it % stages, ph = (it / stages) & 1u;
           // the split kind: the converters' stores, which follow the A load
           if (!mbar_wait_bounded(KIND == KIND_3XTF32_SPLIT_TMA_A ? cvt_bar(s) : full_bar(s), ph,
                                  limit, abort_flag)) {
@@ -272,7 +301,7 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
             break;
           }
           tc_fence_after();
-          const uint32_t st = sbase + s * Cf::STAGE_BYTES;
+          const uint32_t st = sbase + s * stage_bytes;
           if constexpr (KIND == KIND_BF16) {
             // A: 128 rows x 128 B, K-major, 8-row groups 1024 B apart.
             // B: four 64-column boxes (8 KB apart) of 64 k-rows x 128 B,
@@ -281,13 +310,13 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
             for (int kk = 0; kk < Cf::BK / Cf::INSTR_K; ++kk) {
               const uint64_t ad = smem_desc_sw128(st + kk * 32, 16, 1024);
               const uint64_t bd = smem_desc_sw128(st + Cf::A_BYTES + kk * 2048, Cf::B_BOX_BYTES, 1024);
-              mma_f16(d_tmem, ad, bd, Cf::IDESC, (kb > w.kb0 || kk > 0) ? 1u : 0u);
+              mma_f16(d_tmem, ad, bd, idesc, (kb > w.kb0 || kk > 0) ? 1u : 0u);
             }
           } else {
             // All four operands K-major, 128 B rows (32 floats), 8-row groups
             // 1024 B apart; one instruction-K step (8 tf32) = 32 B.
             const uint32_t a_big = st, a_small = st + Cf::A_BYTES;
-            const uint32_t b_big = st + 2 * Cf::A_BYTES, b_small = b_big + Cf::B_BYTES;
+            const uint32_t b_big = st + 2 * Cf::A_BYTES, b_small = b_big + bn * Cf::BK * 4;
 #pragma unroll
             for (int kk = 0; kk < Cf::BK / Cf::INSTR_K; ++kk) {
               const uint32_t off = kk * 32;
@@ -295,9 +324,9 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
               const uint64_t asd = smem_desc_sw128(a_small + off, 16, 1024);
               const uint64_t bbd = smem_desc_sw128(b_big + off, 16, 1024);
               const uint64_t bsd = smem_desc_sw128(b_small + off, 16, 1024);
-              mma_tf32(d_tmem, asd, bbd, Cf::IDESC, (kb > w.kb0 || kk > 0) ? 1u : 0u);
-              mma_tf32(d_tmem, abd, bsd, Cf::IDESC, 1u);
-              mma_tf32(d_tmem, abd, bbd, Cf::IDESC, 1u);
+              mma_tf32(d_tmem, asd, bbd, idesc, (kb > w.kb0 || kk > 0) ? 1u : 0u);
+              mma_tf32(d_tmem, abd, bsd, idesc, 1u);
+              mma_tf32(d_tmem, abd, bbd, idesc, 1u);
             }
           }
           mma_commit(empty_bar(s));  // stage s may be refilled once these MMAs finish
@@ -338,13 +367,13 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
       BRegs r;
       if (g < total) load_b<VB>(r, p, ld, ct);
       for (int it = g; it < total; it += 2) {
-        const uint32_t s = it % Cf::STAGES, ph = (it / Cf::STAGES) & 1u;
+        const uint32_t s = it % stages, ph = (it / stages) & 1u;
         if (!warp_wait(empty_bar(s), ph ^ 1u, limit, abort_flag) ||
             !warp_wait(full_bar(s), ph, limit, abort_flag)) {
           give_up(p, abort_flag, kErrTimeoutProducer, lane);
           break;
         }
-        split_store_tma_a(r, sbase + s * Cf::STAGE_BYTES, so);
+        split_store_tma_a(r, sbase + s * stage_bytes, so);
         fence_proxy_async_smem();  // the stores, visible to the MMA's reads
         __syncwarp();
         if (lane == 0) mbar_arrive(cvt_bar(s));
@@ -375,7 +404,7 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
       tc_fence_after();
       int tm, tn;
       tile_coords(w.tile, p, tm, tn);
-      const int m0 = tm * Cf::BM, n0 = tn * Cf::BN;
+      const int m0 = tm * Cf::BM, n0 = tn * bn;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * Cf::BN;
       if constexpr (CLUSTER) {
         // this thread's row of the partial tile, into shared memory (a rank
@@ -400,13 +429,14 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
                                      __uint_as_float(r[4 * j + 3])));
         }
       } else {
+        const int col_end = n0 + bn < p.N ? n0 + bn : p.N;
 #pragma unroll 1
-        for (int c = 0; c < Cf::BN / 32; ++c) {
+        for (int c = 0; c < bn / 32; ++c) {
           uint32_t r[32];
           tmem_ld_32cols(taddr + c * 32, r);
           tmem_ld_wait();
           stage_and_store_chunk<TMA_STORE>(r, sbase + L::EPI_OFF, ew, chunk, lane, &tmC, p,
-                                           m0 + q * 32, n0 + c * 32, p.N, w.reduce);
+                                           m0 + q * 32, n0 + c * 32, col_end, w.reduce);
           ++chunk;
         }
       }
@@ -518,9 +548,11 @@ int cluster_split_size(const TcParams& p, cudaLaunchConfig_t cfg, const DeviceCt
 
 template <int KIND>
 cudaError_t launch_t(const TcMaps& mp, float* C, int64_t M, int64_t N, int64_t K, int64_t ldc,
-                     bool c_tma, bool after_prepass, const DeviceCtl& ctl, cudaStream_t s) {
+                     bool c_tma, bool after_prepass, int bn, const DeviceCtl& ctl,
+                     cudaStream_t s) {
   using Cf = Cfg<KIND>;
-  TcParams p = make_params(M, N, K, Cf::BM, Cf::BN, Cf::BK, C, ldc, ctl);
+  if (KIND != KIND_3XTF32 || bn <= 0) bn = Cf::BN;
+  TcParams p = make_params(M, N, K, Cf::BM, bn, Cf::BK, C, ldc, ctl);
   p.c_even = !c_tma && mp.c_even;
   cudaError_t e;
   cudaLaunchAttribute attr[2];
@@ -533,8 +565,9 @@ cudaError_t launch_t(const TcMaps& mp, float* C, int64_t M, int64_t N, int64_t K
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   // Few tiles with long K runs: a cluster of S CTAs per tile, each on one
-  // run of K-blocks, summing through distributed shared memory (see above).
-  const int S = cluster_split_size<KIND>(p, cfg, ctl);
+  // run of K-blocks, summing through distributed shared memory (see above;
+  // whole-width tiles only).
+  const int S = bn == Cf::BN ? cluster_split_size<KIND>(p, cfg, ctl) : 1;
   if (S > 1) {
     p.num_units = p.num_tiles * S;
     attr[1].id = cudaLaunchAttributeClusterDimension;
@@ -564,12 +597,16 @@ cudaError_t launch_t(const TcMaps& mp, float* C, int64_t M, int64_t N, int64_t K
     p.full_units = 0;
     p.num_units = 2 * p.num_tiles;
     p.kb_mid = p.num_kb / 2;
-    if ((e = launch_zero_split_tiles(p, Cf::BM, Cf::BN, after_prepass, s)) != cudaSuccess)
-      return e;
+    if ((e = launch_zero_split_tiles(p, Cf::BM, bn, after_prepass, s)) != cudaSuccess) return e;
   }
   const int grid = p.num_units < ctl.sm_count ? p.num_units : ctl.sm_count;
-  note_main_kernel(KIND == KIND_BF16 ? "tc_gemm_kernel<bf16>" : "tc_gemm_kernel<3xtf32>", grid,
-                   p.num_tiles);
+  char name[48];
+  if (KIND == KIND_3XTF32 && bn != Cf::BN)
+    snprintf(name, sizeof(name), "tc_gemm_kernel<3xtf32,n%d>", bn);
+  else
+    snprintf(name, sizeof(name), "%s",
+             KIND == KIND_BF16 ? "tc_gemm_kernel<bf16>" : "tc_gemm_kernel<3xtf32>");
+  note_main_kernel(name, grid, p.num_tiles);
   cfg.gridDim = dim3(grid);
   if (c_tma) {
     if ((e = prepare_kernel<KIND, true, false>()) != cudaSuccess) return e;
@@ -664,11 +701,11 @@ cudaError_t launch_single_cta_split(const TcMaps& maps, const float* A, const fl
 }
 
 cudaError_t launch_single_cta(int kind, const TcMaps& maps, float* C, int64_t M, int64_t N,
-                              int64_t K, int64_t ldc, bool c_tma, bool after_prepass,
+                              int64_t K, int64_t ldc, bool c_tma, bool after_prepass, int bn,
                               const DeviceCtl& ctl, cudaStream_t s) {
   return kind == KIND_BF16
-             ? launch_t<KIND_BF16>(maps, C, M, N, K, ldc, c_tma, after_prepass, ctl, s)
-             : launch_t<KIND_3XTF32>(maps, C, M, N, K, ldc, c_tma, after_prepass, ctl, s);
+             ? launch_t<KIND_BF16>(maps, C, M, N, K, ldc, c_tma, after_prepass, 0, ctl, s)
+             : launch_t<KIND_3XTF32>(maps, C, M, N, K, ldc, c_tma, after_prepass, bn, ctl, s);
 }
 
 }  // namespace tc

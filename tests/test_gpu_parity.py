@@ -321,6 +321,37 @@ def test_pair_kernel_narrow_tiles(mhr, bn):
         mhr.gemm_testing_set_cta_pair_mode(old)
 
 
+@pytest.mark.parametrize("bn", [128, 96, 64, 32])
+def test_single_cta_tile_widths(mhr, bn):
+    """The single-CTA 3xTF32 kernel at each tile width it can run (128 rows x
+    bn; each stage holds bn rows of each B part, the MMAs run with N = bn).
+    300 x 520 x 1000 (ragged, few tiles: K halves) and 1100 x 700 x 200 (with
+    32 columns, 9 x 22 tiles: more than one round). Integer inputs bit-exact
+    against the oracle through TMA stores (aligned C), register stores (odd
+    ldc) and the even-row mixed path (ldc 2 mod 4); real inputs within the
+    tolerance, bitwise repeatably."""
+    old = mhr.gemm_testing_set_cta_pair_mode(1)
+    old_n = mhr.gemm_testing_set_single_tile_n(bn)
+    try:
+        for M, N, K in ((300, 520, 1000), (1100, 700, 200)):
+            for ldc in (None, N + 1, N + 2):
+                A, B, _, _ = operands(M, N, K, 3801 + bn + K, "int", "3xtf32")
+                C = DeviceCall("3xtf32", A, B, ldc=ldc).run(mhr).result()
+                label = mhr.gemm_testing_last_main_kernel()
+                want = "tc_gemm_kernel<3xtf32" + ("> " if bn == 128 else f",n{bn}> ")
+                assert label.startswith(want), (label, want)
+                assert np.array_equal(C, oracle.gemm(A, B)), (M, N, K, ldc)
+            A, B, _, _ = operands(M, N, K, 3802 + bn + K, "normal", "3xtf32")
+            call = DeviceCall("3xtf32", A, B, ldc=N + 2)
+            C = call.run(mhr).result()
+            Cref, S = oracle.gemm(A, B, with_abs=True)
+            assert normalised_error(C, Cref, S) <= TOL["3xtf32"]
+            assert np.array_equal(call.run(mhr).result(), C)
+    finally:
+        mhr.gemm_testing_set_single_tile_n(old_n)
+        mhr.gemm_testing_set_cta_pair_mode(old)
+
+
 @pytest.mark.parametrize("path", ["3xtf32", "bf16"])
 def test_single_cta_few_tiles(mhr, path):
     """Few tiles on the single-CTA kernel. With long K runs (at least 16

@@ -1,13 +1,14 @@
-"""The tile-width planner of the 3xTF32 CTA-pair kernel (host arithmetic in
-libmhr_gemm.so, no GPU needed): which width it picks for the listed
-workloads on GB300's 76 co-resident CTA pairs, and that every pick is a width
-the kernel supports."""
+"""The tile-width planners of the 3xTF32 kernels (host arithmetic in
+libmhr_gemm.so, no GPU needed): which width they pick for the listed
+workloads on GB300 (152 SMs, 76 co-resident CTA pairs), and that every pick
+is a width the kernel supports."""
 import numpy as np
 import pytest
 
 import memory_hierarchy_reuse_gb300 as mhr
 
-CLUSTERS = 76  # 152 SMs in pairs
+SMS = 152
+CLUSTERS = SMS // 2  # CTA pairs
 
 
 @pytest.fixture(scope="module")
@@ -46,3 +47,30 @@ def test_planned_width_is_supported(lib):
 
 def test_no_clusters_keeps_full_width(lib):
     assert mhr.gemm_testing_plan_pair_tile_n(4096, 4096, 4096, 0, True) == 256
+
+
+@pytest.mark.parametrize("shape,want", [
+    # 256^3: 4 tiles of 128 columns in K halves keep 8 SMs busy; 16 tiles of 32
+    # columns in K halves keep 32 busy, each loading less and storing a
+    # quarter of the epilogue
+    ((256, 256, 256), 32),
+    ((300, 520, 1000), 32),
+    ((1024, 1024, 1024), 128),   # 64 tiles in K halves already fill 128 SMs
+    ((1536, 1536, 1536), 128),   # 144 tiles: one round
+    ((512, 512, 8192), 128),     # the cluster split's domain (whole tiles only)
+])
+def test_single_cta_planned_width(lib, shape, want):
+    for c_tma in (False, True):
+        assert mhr.gemm_testing_plan_single_tile_n(*shape, SMS, c_tma) == want
+
+
+def test_single_cta_planned_width_is_supported(lib):
+    rng = np.random.default_rng(12)
+    for _ in range(400):
+        M, N = (int(x) for x in rng.integers(1, 4000, size=2))
+        K = int(rng.integers(1, 9000))
+        sms = int(rng.integers(1, 160))
+        for c_tma in (False, True):
+            bn = mhr.gemm_testing_plan_single_tile_n(M, N, K, sms, c_tma)
+            assert bn in (32, 64, 96, 128), (M, N, K, sms, bn)
+    assert mhr.gemm_testing_plan_single_tile_n(256, 256, 256, 0, True) == 128
