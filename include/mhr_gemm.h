@@ -88,16 +88,18 @@ int gemm_f32(const float* A, const float* B, float* C, int64_t M, int64_t N, int
 /*
  * FP32-accurate path on the tensor cores: each operand is split as
  * x = big + small, where big keeps the top 11 significant bits of x
- * (rounded to nearest even for B; truncated for A, which is what the tensor
- * core reads from an fp32 operand) and small = tf32(x - big) (round to
- * nearest even), and C accumulates small*big + big*small + big*big with
- * tcgen05.mma kind::tf32 into a TMEM accumulator (the small*small term is
- * dropped).  A split pre-pass writes the tf32 operands into the library's
- * workspace (B transposed to K-major; A's big part is A itself when A is
- * 16-byte aligned with lda a multiple of 4; the workspace takes
- * 8 (M + N) K bytes in all), then a TMA + mbarrier ring feeds the tensor
- * cores.  If that workspace cannot
- * be allocated, converter warps of the CTA-pair kernel load A and B directly
+ * (truncated, which is what the tensor core reads from an fp32 operand) and
+ * small = tf32(x - big) (round to nearest even), and C accumulates
+ * small*big + big*small + big*big with tcgen05.mma kind::tf32 into a TMEM
+ * accumulator (the small*small term is dropped).  A split pre-pass writes
+ * the tf32 operands into the library's workspace (B transposed to K-major;
+ * A's big part is A itself when A is 16-byte aligned with lda a multiple of
+ * 4; the workspace takes 8 (M + N) K bytes in all), then a TMA + mbarrier
+ * ring feeds the tensor cores.  Small problems (M N <= 2^18 and K <= 2048,
+ * with A 16-byte aligned and lda a multiple of 4) skip the pre-pass: one
+ * launch of the single-CTA kernel stages A by TMA and splits on chip, with
+ * clusters of CTAs splitting K (no workspace).  If the workspace cannot be
+ * allocated, converter warps of the CTA-pair kernel load A and B directly
  * and split them on chip instead: the same MMAs in the same order, so the
  * same C bit for bit, at about 60 % of the speed on GB300.  Any alignment and
  * leading dimension are accepted.
@@ -124,9 +126,11 @@ int gemm_bf16_f32acc(const uint16_t* A, const uint16_t* B, float* C, int64_t M, 
  * fragment it), latency-critical loops (cudaMalloc and cudaFree synchronise
  * the device), and programs in which only one owner thread allocates.
  *
- * Same arguments, result and numerics as gemm_f32_3xtf32 (same kernels).  The
- * split operands live in a 64 MiB static device array inside the library
- * instead of the allocated workspace:
+ * Same arguments, result and numerics as gemm_f32_3xtf32 (same kernels; the
+ * small problems that gemm_f32_3xtf32 runs as one launch with the split
+ * inside run the same way here).  The split operands of the pre-pass live in
+ * a 64 MiB static device array inside the library instead of the allocated
+ * workspace:
  *   - problems for which 8 * Kp * (M + N) bytes exceed 64 MiB, Kp = K
  *     rounded up to a multiple of 4 (e.g. larger than M = N = K = 2048), are
  *     rejected with MHR_ERR_INVALID_ARG before any work is enqueued;

@@ -51,19 +51,22 @@ int gemm_testing_set_cta_pair_mode(int mode);
 
 /*
  * Chooses where gemm_f32_3xtf32 splits its operands into tf32 big and small
- * parts (process-wide): 0 = automatic (a pre-pass into the workspace, or
- * inside the CTA-pair kernel when the workspace cannot be allocated), 1 =
- * always a pre-pass, 2 = always inside a kernel: the single-CTA kernel's
- * one-launch form when the CTA-pair mode is 1 and A is 16-byte aligned with
- * lda a multiple of 4, else the CTA-pair kernel's (used whatever the CTA-pair
- * mode says).  Other values mean 0.  Pre-pass and in-kernel split give
- * bit-identical results for the same kernel.  Returns the previous mode.
+ * parts (process-wide): 0 = automatic (the single-CTA kernel's one-launch
+ * form for small problems -- M N <= 2^18, K <= 2048, A 16-byte aligned with
+ * lda a multiple of 4, unless the CTA-pair mode is 2 --, else a pre-pass
+ * into the workspace, or inside the CTA-pair kernel when the workspace
+ * cannot be allocated), 1 = always a pre-pass, 2 = always inside a kernel:
+ * the single-CTA kernel's one-launch form when the CTA-pair mode is 1 and A
+ * is aligned as above, else the CTA-pair kernel's (used whatever the
+ * CTA-pair mode says).  Other values mean 0.  Pre-pass and in-kernel split
+ * give bit-identical results for the same kernel and tile schedule.
+ * Returns the previous mode.
  */
 int gemm_testing_set_split_mode(int mode);
 
 /*
  * When `enable` is nonzero, gemm_f32_3xtf32 calls that split in a pre-pass
- * (split mode 0 or 1 with a workspace) clear A's small part after the split,
+ * (split mode 1, or 0 where it takes the pre-pass) clear A's small part after the split,
  * so the main kernel accumulates A_big * (B_big + B_small) only.  With B the
  * identity that exposes what the tensor core reads from an fp32 A operand
  * under kind::tf32 -- the library relies on it being A with the low 13 bits
@@ -138,9 +141,10 @@ int gemm_testing_plan_pair_tile_n(int64_t M, int64_t N, int64_t K, int clusters,
 /*
  * Forces the width of the single-CTA kernel's 3xTF32 output tiles (128 rows x
  * `columns`, columns 128, 96, 64 or 32) for the following calls
- * (process-wide); any other value, 0 included, restores the planner's choice.
- * Calls that take the cluster split or the in-kernel split keep 128.
- * Returns the previous setting.
+ * (process-wide); any other value, 0 included, restores the automatic
+ * choice.  Calls with a pre-pass that take the cluster split keep 128; the
+ * one-launch form (split inside) takes 128, 64 or 32 and splits K over
+ * clusters at any of them.  Returns the previous setting.
  */
 int gemm_testing_set_single_tile_n(int columns);
 

@@ -385,9 +385,9 @@ MHR_API int gemm_f32_3xtf32(const float* A, const float* B, float* C, int64_t M,
                                             &b_bytes) &&
                     !__builtin_add_overflow(a_bytes, b_bytes, &ws_bytes) &&
                     !__builtin_mul_overflow(ws_bytes, size_t{2}, &ws_bytes);
-  // In-kernel split forced with the single-CTA kernel forced: its one-launch
-  // form, when TMA can read A.
-  if (ctl.split_mode == 2 && ctl.pair_mode == 1 && a_serves_as_big(A, lda)) {
+  // Small problems (or the test hooks' choice): one launch of the single-CTA
+  // kernel with the split inside.
+  if (small_one_launch_chosen(A, lda, M, N, K, ctl)) {
     MainKernelEvents ev(s);
     return from_cuda(launch_tc_3xtf32_small(A, B, C, M, N, K, lda, ldb, ldc, c_tma, ctl, s));
   }

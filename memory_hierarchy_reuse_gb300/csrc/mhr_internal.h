@@ -87,6 +87,12 @@ cudaError_t launch_tc_3xtf32_small(const float* A, const float* B, float* C, int
 // tc_common.cuh) runs the CTA-pair kernel for this shape (else the
 // single-CTA kernel).
 bool tc_pair_chosen(int kind, int64_t M, int64_t N, int64_t K, const DeviceCtl& ctl);
+// Whether a 3xTF32 call runs as one launch of the single-CTA kernel with the
+// split inside (launch_tc_3xtf32_small): forced by the test hooks (split mode
+// 2 with the single-CTA kernel), or chosen for small problems (M N <= 2^18,
+// K <= 2048) in the automatic mode; A must be its own big part.
+bool small_one_launch_chosen(const float* A, int64_t lda, int64_t M, int64_t N, int64_t K,
+                             const DeviceCtl& ctl);
 namespace tc {
 // Columns of the CTA-pair kernel's 3xTF32 tiles (256, or a narrower multiple
 // of 16 -- of 32 when C is written by TMA -- down to 128) for an M x N x K

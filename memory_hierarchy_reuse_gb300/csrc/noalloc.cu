@@ -93,6 +93,10 @@ MHR_API int gemm_f32_3xtf32_noalloc(const float* A, const float* B, float* C, in
   cudaError_t e;
   if (K == 0) {
     e = launch_zero_fill(C, M, N, ldc, s);
+  } else if (small_one_launch_chosen(A, lda, M, N, K, ctl)) {  // as in gemm_f32_3xtf32
+    MainKernelEvents ev(s);
+    e = launch_tc_3xtf32_small(A, B, C, M, N, K, lda, ldb, ldc, c_tma_eligible(C, N, ldc), ctl,
+                               s);
   } else {
     float* scratch;
     if ((rc = scratch_address(dev, &scratch)) != MHR_OK) return rc;

@@ -15,6 +15,22 @@ bool tc_pair_chosen(int kind, int64_t M, int64_t N, int64_t K, const DeviceCtl& 
   return kind != tc::KIND_BF16 || K >= 2048 || pair_tiles >= 2 * clusters;
 }
 
+// Small 3xTF32 problems run as one launch with the split inside the
+// single-CTA kernel (no pre-pass, no zeroing, no workspace), on tiles of 128
+// rows x 128, 64 or 32 columns with a cluster per tile splitting K.  GB300,
+// whole calls, L2 flushed, against the split pre-pass path: 256^3 13.0
+// against 13.9 us, 512^3 15.1 / 16.8, 300 x 520 x 1000 19.1 / 22.1,
+// 256 x 512 x 1000 17.1 / 21.9, 128 x 128 x 1024 14.9 / 20.2, 256 x 256 x 2048
+// 19.1 / 23.3, 512 x 512 x 2048 25.3 / 25.3; the pre-pass path wins from 768^3
+// (20.4 against 21.2) and at 1024^3 (25.7 / 33.4), where each CTA's converter
+// warps would walk too many K-blocks.
+bool small_one_launch_chosen(const float* A, int64_t lda, int64_t M, int64_t N, int64_t K,
+                             const DeviceCtl& ctl) {
+  if (!a_serves_as_big(A, lda) || ctl.pair_mode == 2) return false;
+  if (ctl.split_mode == 2) return ctl.pair_mode == 1;
+  return ctl.split_mode == 0 && M * N <= (int64_t{1} << 18) && K <= 2048;
+}
+
 namespace tc {
 
 // Pair tile width for 3xTF32.  Each CTA of a pair computes 128 rows x bn

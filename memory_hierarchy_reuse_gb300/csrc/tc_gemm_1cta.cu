@@ -3,7 +3,9 @@
 //   3xTF32: 128 x 128 x 32 tiles, 3 stages of 64 KB, kind::tf32 M128 N128 K8.
 // Used for problems whose 256-row CTA-pair tiles would not keep the GPU busy.
 // The method and the warp roles are described in tc_common.cuh.
+#include <array>
 #include <cstdio>
+#include <map>
 #include <type_traits>
 
 #include "tc_common.cuh"
@@ -137,10 +139,12 @@ struct Layout {
   static_assert(C::BM * PART_LD<KIND> * 4 <= C::STAGES * C::STAGE_BYTES, "partial tile");
 };
 
-// The converter warps' walk over this CTA's units (A rows m0.., B columns
-// n0.., 128 each, and a K-block range).
+// The converter warps' walk over this CTA's units (A rows m0.., 128 of them,
+// B columns n0.., bn of them, and a K-block range).
 template <bool CLUSTER>
 struct SingleWalk {
+  int bn;
+  __device__ __forceinline__ int cols() const { return bn; }
   __device__ __forceinline__ bool box(const TcParams& p, int u, int& m0, int& nb0, int& kb0,
                                       int& kb1) const {
     if (u >= p.num_units) return false;
@@ -148,7 +152,7 @@ struct SingleWalk {
     int tm, tn;
     tile_coords(w.tile, p, tm, tn);
     m0 = tm * SPLIT_BOX_ROWS;
-    nb0 = tn * SPLIT_BOX_ROWS;
+    nb0 = tn * bn;
     kb0 = w.kb0;
     kb1 = w.kb1;
     return true;
@@ -179,8 +183,10 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // The tile's columns (the cluster split runs whole tiles only), and the ring.
-  const int bn = KIND == KIND_3XTF32 && !CLUSTER ? p.bn : Cf::BN;
+  // The tile's columns (with a pre-pass, the cluster split runs whole tiles
+  // only), and the ring.
+  const int bn = (KIND == KIND_3XTF32 && !CLUSTER) || KIND == KIND_3XTF32_SPLIT_TMA_A ? p.bn
+                                                                                     : Cf::BN;
   const uint32_t stages = static_cast<uint32_t>(ring_stages<KIND>(bn));
   const uint32_t stage_bytes = static_cast<uint32_t>(ring_stage_bytes<KIND>(bn));
 
@@ -346,7 +352,9 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
     const int g = (threadIdx.x - NUM_THREADS) / SPLIT_THREADS;
     const int ct = (threadIdx.x - NUM_THREADS) % SPLIT_THREADS;
     const StoreOffsets so(ct);
-    const SingleWalk<CLUSTER> walk;
+    const SingleWalk<CLUSTER> walk{bn};
+    // this thread's B columns 4 nb .. 4 nb + 3 lie inside the tile
+    const bool has_b = 4 * (((ct & 31) >> 3) + 4 * (ct >> 5)) < bn;
     const int stride = static_cast<int>(gridDim.x);
     auto convert = [&](auto vec_b) {
       constexpr bool VB = decltype(vec_b)::value;
@@ -373,7 +381,7 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
           give_up(p, abort_flag, kErrTimeoutProducer, lane);
           break;
         }
-        split_store_tma_a(r, sbase + s * stage_bytes, so);
+        split_store_tma_a(r, sbase + s * stage_bytes, so, bn * Cf::BK * 4, has_b);
         fence_proxy_async_smem();  // the stores, visible to the MMA's reads
         __syncwarp();
         if (lane == 0) mbar_arrive(cvt_bar(s));
@@ -412,7 +420,7 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
         const uint32_t prow = sbase + static_cast<uint32_t>((q * 32 + lane) * PART_LD<KIND> * 4);
         const bool has_k = w.kb1 > w.kb0;
 #pragma unroll 1
-        for (int c = 0; c < Cf::BN / 32; ++c) {
+        for (int c = 0; c < bn / 32; ++c) {
           uint32_t r[32];
           if (has_k) {
             tmem_ld_32cols(taddr + c * 32, r);
@@ -460,11 +468,11 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
     int tm, tn;
     tile_coords(static_cast<int>(blockIdx.x) / S, p, tm, tn);
     const int64_t m0 = static_cast<int64_t>(tm) * Cf::BM;
-    const int n0 = tn * Cf::BN;
+    const int n0 = tn * bn;
     const bool vec = (reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 && (p.ldc & 3) == 0;
-    for (int idx = threadIdx.x; idx < rows * (Cf::BN / 4); idx += cta_threads<KIND>()) {
-      const int r = rank * rows + idx / (Cf::BN / 4);
-      const int c = (idx % (Cf::BN / 4)) * 4;
+    for (int idx = threadIdx.x; idx < rows * (bn / 4); idx += cta_threads<KIND>()) {
+      const int r = rank * rows + idx / (bn / 4);
+      const int c = (idx % (bn / 4)) * 4;
       const uint32_t off = sbase + static_cast<uint32_t>((r * PART_LD<KIND> + c) * 4);
       // all loads first (their latencies overlap), then the sum in rank order
       float4 t[8];
@@ -634,7 +642,70 @@ cudaError_t launch_single_cta_split(const TcMaps& maps, const float* A, const fl
                                     cudaStream_t s) {
   constexpr int KIND = KIND_3XTF32_SPLIT_TMA_A;
   using Cf = Cfg<KIND>;
-  TcParams p = make_params(M, N, K, Cf::BM, Cf::BN, Cf::BK, C, ldc, ctl);
+  cudaError_t e;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(cta_threads<KIND>());
+  cfg.dynamicSmemBytes = Layout<KIND>::ALLOC;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if ((e = prepare_kernel<KIND, false, true>()) != cudaSuccess) return e;
+  // Clusters of c CTAs that fit on the GPU at once (c = 2, 4, 8): the
+  // occupancy query depends on the kernel and c only, so it is made once per
+  // device (calls are serialised by the library's lock).
+  static std::map<int, std::array<int, 9>> fit_cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  auto fit = fit_cache.emplace(dev, std::array<int, 9>{}).first;
+  auto clusters_fit = [&](int c) {
+    int& n = fit->second[c];
+    if (n == 0) {
+      attr[1].val.clusterDim.x = static_cast<unsigned>(c);
+      cfg.numAttrs = 2;
+      cfg.gridDim = dim3(static_cast<unsigned>(8 * c));
+      if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<KIND, false, true>, &cfg) !=
+          cudaSuccess) {
+        cudaGetLastError();
+        n = -1;
+      }
+      cfg.numAttrs = 1;
+    }
+    return n;
+  };
+  // With few tiles, a cluster of S CTAs per tile, each on one run of
+  // K-blocks, summing through distributed shared memory: the largest S in
+  // {8, 4, 2} that gives every rank a K-block and every CTA its own SM.
+  const int num_kb = static_cast<int>((K + Cf::BK - 1) / Cf::BK);
+  auto cluster_size = [&](int64_t tiles) {
+    for (int c = MHR_SMALL_MAX_CLUSTER; c >= 2; c /= 2)
+      if (tiles * c <= ctl.sm_count && num_kb >= c && clusters_fit(c) >= tiles) return c;
+    return 1;
+  };
+  // Tile width: the one that puts the most CTAs to work (128, 64 or 32
+  // columns; a tie goes to the wider tile), unless the test hook forces one.
+  // GB300, whole calls: 256^3 15.1 / 13.1 / 13.0 us at 128 / 64 / 32 columns,
+  // 512^3 18.7 / 15.1 / 17.1, 300 x 520 x 1000 19.1 / 19.2 / 23.1,
+  // 256 x 512 x 1000 19.1 / 19.1 / 17.1, 256 x 256 x 2048 25.2 / 19.1 / 23.0.
+  int bn = ctl.single_tile_n;
+  if (bn <= 0) {
+    int64_t best_grid = 0;
+    for (int w = Cf::BN; w >= 32; w /= 2) {
+      const int64_t tiles = ((M + Cf::BM - 1) / Cf::BM) * ((N + w - 1) / w);
+      const int c = cluster_size(tiles);
+      const int64_t grid = c > 1 ? tiles * c : (tiles < ctl.sm_count ? tiles : ctl.sm_count);
+      if (grid > best_grid) {
+        best_grid = grid;
+        bn = w;
+      }
+    }
+  }
+  TcParams p = make_params(M, N, K, Cf::BM, bn, Cf::BK, C, ldc, ctl);
   p.A = A;
   p.B = B;
   p.lda = lda;
@@ -642,50 +713,30 @@ cudaError_t launch_single_cta_split(const TcMaps& maps, const float* A, const fl
   p.vec_a = 1;  // the TMA map of A requires what the 16-byte loads do
   p.vec_b = (reinterpret_cast<uintptr_t>(B) % 16 == 0) && (ldb % 4 == 0);
   p.c_even = !c_tma && maps.c_even;
-  cudaError_t e;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(cta_threads<KIND>());
-  cfg.dynamicSmemBytes = Layout<KIND>::ALLOC;
-  cfg.stream = s;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  // With few tiles, a cluster of S CTAs per tile, each on one run of
-  // K-blocks, summing through distributed shared memory: the largest S in
-  // {8, 4, 2} that gives every rank a K-block and every CTA its own SM.
-  if ((e = prepare_kernel<KIND, false, true>()) != cudaSuccess) return e;
-  int S = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
-  for (int c = MHR_SMALL_MAX_CLUSTER; c >= 2 && S == 1; c /= 2) {
-    if (p.num_tiles * c > ctl.sm_count || p.num_kb < c) continue;
-    attr[1].val.clusterDim.x = static_cast<unsigned>(c);
-    cfg.numAttrs = 2;
-    cfg.gridDim = dim3(static_cast<unsigned>(p.num_tiles * c));
-    int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, tc_gemm_kernel<KIND, false, true>, &cfg) !=
-        cudaSuccess) {
-      cudaGetLastError();
-      continue;
-    }
-    if (clusters >= p.num_tiles) S = c;
-  }
+  const int S = cluster_size(p.num_tiles);
   if (S > 1) {
     attr[1].val.clusterDim.x = static_cast<unsigned>(S);
     p.num_units = p.num_tiles * S;
     cfg.numAttrs = 2;
     cfg.gridDim = dim3(static_cast<unsigned>(p.num_units));
-    note_main_kernel("tc_gemm_kernel<3xtf32,split,tma-a,cluster-K>", p.num_units, p.num_tiles);
+    char name[64];
+    if (bn == Cf::BN)
+      snprintf(name, sizeof(name), "tc_gemm_kernel<3xtf32,split,tma-a,cluster-K>");
+    else
+      snprintf(name, sizeof(name), "tc_gemm_kernel<3xtf32,split,tma-a,n%d,cluster-K>", bn);
+    note_main_kernel(name, p.num_units, p.num_tiles);
     e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<KIND, false, true>, maps.a0, maps.a1, maps.b0,
                            maps.b1, maps.c, p);
   } else {
     cfg.numAttrs = 1;
     const int grid = p.num_units < ctl.sm_count ? p.num_units : ctl.sm_count;
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    note_main_kernel("tc_gemm_kernel<3xtf32,split,tma-a>", grid, p.num_tiles);
+    char name[64];
+    if (bn == Cf::BN)
+      snprintf(name, sizeof(name), "tc_gemm_kernel<3xtf32,split,tma-a>");
+    else
+      snprintf(name, sizeof(name), "tc_gemm_kernel<3xtf32,split,tma-a,n%d>", bn);
+    note_main_kernel(name, grid, p.num_tiles);
     if (c_tma) {
       if ((e = prepare_kernel<KIND, true, false>()) != cudaSuccess) return e;
       e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<KIND, true, false>, maps.a0, maps.a1, maps.b0,

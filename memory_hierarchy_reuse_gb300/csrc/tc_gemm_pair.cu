@@ -117,6 +117,7 @@ __device__ __forceinline__ bool unit_boxes(const TcParams& p, int u, uint32_t ra
 // cluster + clusters, ...
 struct PairWalk {
   uint32_t rank;
+  __device__ __forceinline__ int cols() const { return PAIR_TILE_N / 2; }
   __device__ __forceinline__ bool box(const TcParams& p, int u, int& m0, int& nb0, int& kb0,
                                       int& kb1) const {
     return unit_boxes(p, u, rank, m0, nb0, kb0, kb1);
@@ -492,7 +493,7 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
           give_up_pair(kErrTimeoutProducer);
           break;
         }
-        split_store_tma_a(r, sbase + s * Cf::STAGE_BYTES, so);
+        split_store_tma_a(r, sbase + s * Cf::STAGE_BYTES, so, SPLIT_BOX_BYTES, true);
         fence_proxy_async_smem();  // the stores, visible to the pair's MMA reads
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(mapa_shared(full_bar(s), 0));

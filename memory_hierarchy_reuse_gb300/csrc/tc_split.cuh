@@ -3,8 +3,10 @@
 // the parts into a ring stage in the layout TMA gives the pre-split operands
 // (128-row x 128-byte K-major boxes, 128-byte swizzle).  Used by the CTA-pair
 // kernel (tc_gemm_pair.cu) and the single-CTA kernel (tc_gemm_1cta.cu); each
-// stage holds A_big, A_small, B_big^T and B_small^T boxes of SPLIT_BOX_BYTES,
-// in that order, for A rows m0 .. m0+127 and B columns nb0 .. nb0+127.
+// stage holds A_big, A_small, B_big^T and B_small^T boxes, in that order, for
+// A rows m0 .. m0+127 and B columns nb0 .. nb0+cols-1 (cols = 128, or the
+// single-CTA kernel's narrower tile width: the B boxes are then cols x 128
+// bytes).
 #pragma once
 
 #include <cstdint>
@@ -68,14 +70,16 @@ struct SplitRegs {
 // The next K-block whose loads a converter thread issues: pointers to its A
 // chunk 0 and its B row 4w at that K-block, and whether the unit's boxes lie
 // inside the matrices in M and N (only K is then checked, per block).  WALK
-// maps a work unit to this CTA's boxes (A rows m0.., B columns nb0.., each
-// 128 wide) and K-block range: bool box(p, u, m0, nb0, kb0, kb1).
+// maps a work unit to this CTA's boxes (A rows m0.., 128 of them, B columns
+// nb0.., walk.cols() of them) and K-block range: bool box(p, u, m0, nb0, kb0,
+// kb1).  has_b: the thread's 4 B columns lie inside the box (all threads when
+// it is 128 wide).
 template <class WALK>
 struct LoadCursor {
   const float* a;
   const float* b;
   int arow, bcol, u, kb, kb1;
-  bool valid, interior;
+  bool valid, interior, has_b;
 
   __device__ __forceinline__ void seek(const TcParams& p, const WALK& walk, int unit, int ct) {
     int m0, nb0;
@@ -85,7 +89,8 @@ struct LoadCursor {
     const int w = ct & 7, nb = ((ct & 31) >> 3) + 4 * (ct >> 5);
     arow = m0 + (ct >> 3);
     bcol = nb0 + 4 * nb;
-    interior = m0 + SPLIT_BOX_ROWS <= p.M && nb0 + SPLIT_BOX_ROWS <= p.N;
+    has_b = 4 * nb < walk.cols();
+    interior = m0 + SPLIT_BOX_ROWS <= p.M && nb0 + walk.cols() <= p.N;
     a = p.A + static_cast<int64_t>(arow) * p.lda + 32 * kb + 4 * w;
     b = p.B + static_cast<int64_t>(32 * kb + 4 * w) * p.ldb + bcol;
   }
@@ -109,12 +114,13 @@ struct LoadCursor {
 
 template <class WALK>
 struct PrefetchCursor {
-  int m0, nb0, u, kb, kb1;
+  int m0, nb0, u, kb, kb1, cols;
   bool valid;
 
   __device__ __forceinline__ void seek(const TcParams& p, const WALK& walk, int unit) {
     valid = walk.box(p, unit, m0, nb0, kb, kb1);
     u = unit;
+    cols = walk.cols();
   }
   __device__ __forceinline__ void seek_work(const TcParams& p, const WALK& walk, int unit,
                                             int stride) {
@@ -186,9 +192,9 @@ __device__ __forceinline__ void split_load(SplitRegs& r, const TcParams& p, cons
 
 // Pull one future K-block of this CTA's boxes into L2: each of the first 128
 // converter threads takes one row of the A box (128 bytes), each of the others
-// one 128-byte quarter of a row of the B box (32 rows x 512 bytes).  Both ends
-// of each piece are touched, in case it straddles two lines.  Addresses
-// outside the matrices are skipped.
+// one 128-byte quarter of a row of the B box (32 rows x up to 512 bytes).
+// Both ends of each piece are touched, in case it straddles two lines.
+// Addresses outside the matrices (or the box) are skipped.
 __device__ __forceinline__ void prefetch_l2(const float* a) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
 }
@@ -205,7 +211,7 @@ __device__ __forceinline__ void split_prefetch_l2(const TcParams& p, int ct, con
     prefetch_l2(a + (min(k0 + 31, p.K - 1) - k0));
   } else {
     const int q = ct - 128, k = k0 + (q >> 2), col = c.nb0 + 32 * (q & 3);
-    if (k >= p.K || col >= p.N) return;
+    if (k >= p.K || col >= p.N || 32 * (q & 3) >= c.cols) return;
     const float* b = p.B + static_cast<int64_t>(k) * p.ldb + col;
     prefetch_l2(b);
     prefetch_l2(b + (min(col + 31, p.N - 1) - col));
@@ -275,6 +281,7 @@ struct BRegs {
 
 template <bool VB, class CURSOR>
 __device__ __forceinline__ void load_b(BRegs& r, const TcParams& p, const CURSOR& c, int ct) {
+  if (!c.has_b) return;  // columns beyond a narrow box: nothing to load or store
   const int k0 = c.kb * 32;
   if (c.bcol + 4 <= p.N && k0 + 32 <= p.K) {
 #pragma unroll
@@ -296,14 +303,18 @@ __device__ __forceinline__ void load_b(BRegs& r, const TcParams& p, const CURSOR
   }
 }
 
-// A_small from the staged A box, and B_big^T, B_small^T from registers.
+// A_small from the staged A box, and B_big^T, B_small^T from registers (the
+// B_small^T box b_small_off bytes after B_big^T's: cols x 128; has_b as in
+// LoadCursor).
 __device__ __forceinline__ void split_store_tma_a(const BRegs& r, uint32_t st,
-                                                  const StoreOffsets& o) {
+                                                  const StoreOffsets& o, uint32_t b_small_off,
+                                                  bool has_b) {
 #pragma unroll
   for (int j = 0; j < SPLIT_CHUNKS; ++j) {
     const uint32_t off = o.a + j * 4096;
     st_shared_v4(st + SPLIT_BOX_BYTES + off, small4_tf32_trunc(ld_shared_v4(st + off)));
   }
+  if (!has_b) return;
   const float4 col[4] = {make_float4(r.b[0].x, r.b[1].x, r.b[2].x, r.b[3].x),
                          make_float4(r.b[0].y, r.b[1].y, r.b[2].y, r.b[3].y),
                          make_float4(r.b[0].z, r.b[1].z, r.b[2].z, r.b[3].z),
@@ -311,7 +322,7 @@ __device__ __forceinline__ void split_store_tma_a(const BRegs& r, uint32_t st,
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     st_shared_v4(st + 2 * SPLIT_BOX_BYTES + o.b[i], col[i]);
-    st_shared_v4(st + 2 * SPLIT_BOX_BYTES + SPLIT_BOX_BYTES + o.b[i], small4_tf32_trunc(col[i]));
+    st_shared_v4(st + 2 * SPLIT_BOX_BYTES + b_small_off + o.b[i], small4_tf32_trunc(col[i]));
   }
 }
 

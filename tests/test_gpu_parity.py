@@ -331,7 +331,8 @@ def test_single_cta_tile_widths(mhr, bn):
     ldc) and the even-row mixed path (ldc 2 mod 4); real inputs within the
     tolerance, bitwise repeatably."""
     old = mhr.gemm_testing_set_cta_pair_mode(1)
-    old_n = mhr.gemm_testing_set_single_tile_n(bn)
+    old_split = mhr.gemm_testing_set_split_mode(1)  # the split pre-pass (small problems would
+    old_n = mhr.gemm_testing_set_single_tile_n(bn)  # otherwise run as one launch)
     try:
         for M, N, K in ((300, 520, 1000), (1100, 700, 200)):
             for ldc in (None, N + 1, N + 2):
@@ -349,6 +350,7 @@ def test_single_cta_tile_widths(mhr, bn):
             assert np.array_equal(call.run(mhr).result(), C)
     finally:
         mhr.gemm_testing_set_single_tile_n(old_n)
+        mhr.gemm_testing_set_split_mode(old_split)
         mhr.gemm_testing_set_cta_pair_mode(old)
 
 
@@ -457,6 +459,63 @@ def test_single_cta_in_kernel_split_is_one_launch(mhr, shape):
     finally:
         mhr.gemm_testing_set_split_mode(old_split)
         mhr.gemm_testing_set_cta_pair_mode(old)
+
+
+@pytest.mark.parametrize("bn", [128, 96, 64, 32])
+def test_one_launch_tile_widths(mhr, bn):
+    """The one-launch form (single-CTA kernel, split inside) at each tile
+    width: converter warps write bn rows of B^T's parts, the MMAs run with
+    N = bn, and a cluster per tile splits K when the tiles are few (its
+    partial tiles bn columns wide). 256^3 (a cluster per tile), 300 x 520 x
+    1000 and 64 x 1000 x 300 (ragged tiles). Integer inputs bit-exact against
+    the oracle through TMA stores, register stores (odd ldc) and the even-row
+    path (ldc 2 mod 4); real inputs within the tolerance."""
+    old = mhr.gemm_testing_set_cta_pair_mode(1)
+    old_split = mhr.gemm_testing_set_split_mode(2)
+    old_n = mhr.gemm_testing_set_single_tile_n(bn)
+    try:
+        for M, N, K in ((256, 256, 256), (300, 520, 1000), (64, 1000, 300)):
+            for ldc in (None, N + 1, N + 2):
+                A, B, _, _ = operands(M, N, K, 3901 + bn + K, "int", "3xtf32")
+                C = DeviceCall("3xtf32", A, B, ldc=ldc).run(mhr).result()
+                label = mhr.gemm_testing_last_main_kernel()
+                want = "tc_gemm_kernel<3xtf32,split,tma-a" + ("" if bn == 128 else f",n{bn}")
+                assert label.startswith(want), (label, want)
+                assert mhr.gemm_testing_last_launches() == 1
+                assert np.array_equal(C, oracle.gemm(A, B)), (M, N, K, ldc, label)
+            A, B, _, _ = operands(M, N, K, 3902 + bn + K, "normal", "3xtf32")
+            C = DeviceCall("3xtf32", A, B, ldc=N + 2).run(mhr).result()
+            Cref, S = oracle.gemm(A, B, with_abs=True)
+            assert normalised_error(C, Cref, S) <= TOL["3xtf32"]
+    finally:
+        mhr.gemm_testing_set_single_tile_n(old_n)
+        mhr.gemm_testing_set_split_mode(old_split)
+        mhr.gemm_testing_set_cta_pair_mode(old)
+
+
+@pytest.mark.parametrize("shape,one_launch", [
+    ((256, 256, 256), True), ((512, 512, 512), True), ((300, 520, 1000), True),
+    ((256, 256, 2048), True), ((512, 512, 2052), False), ((1024, 1024, 1024), False)],
+    ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else str(v))
+def test_automatic_mode_runs_small_problems_as_one_launch(mhr, shape, one_launch):
+    """In the automatic mode, small 3xTF32 problems (M N <= 2^18, K <= 2048)
+    run as one launch of the single-CTA kernel with the split inside; larger
+    ones, and A one element off 16-byte alignment, take the split pre-pass.
+    Either way C matches the oracle bit for bit on integer inputs."""
+    M, N, K = shape
+    A, B, _, _ = operands(M, N, K, 3951 + K, "int", "3xtf32")
+    for offset in (0, 1):
+        call = DeviceCall("3xtf32", A, B, offset=offset)
+        C = call.run(mhr).result()
+        label = mhr.gemm_testing_last_main_kernel()
+        if one_launch and offset == 0:
+            assert label.startswith("tc_gemm_kernel<3xtf32,split,tma-a"), label
+            assert mhr.gemm_testing_last_launches() == 1
+        else:
+            assert ",split" not in label, label
+            assert mhr.gemm_testing_last_launches() >= 2  # the split pre-pass and the main kernel
+        assert np.array_equal(C, oracle.gemm(A, B)), (shape, offset, label)
+
 
 
 @pytest.mark.usefixtures("full_width_tiles")

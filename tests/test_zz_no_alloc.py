@@ -10,7 +10,8 @@ array instead of a cudaMalloc'd workspace.
 The tests call it through the C ABI and compare it with the allocating entry
 point, gemm_f32_3xtf32, which runs the same kernels in the same order -- so
 the two must agree bit for bit -- and with the CPU oracle. Two calls run back
-to back, so the second one runs over the scratch the first one left behind.
+to back: a small problem that both entry points run as one launch with the
+split inside (no scratch at all), then one that splits into the scratch.
 The limit is exercised at its exact edge (M = N = K = 2048 fills the array to
 its last byte), with an unaligned A (which makes the split write A's big part
 too), and one row beyond it on real buffers of that size, where the call must
