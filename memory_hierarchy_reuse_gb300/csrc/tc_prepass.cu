@@ -40,8 +40,13 @@ __global__ void pack_u16_kernel(const uint16_t* __restrict__ src, int64_t rows, 
 constexpr int SPLIT_THREADS = 256;
 constexpr int SPLIT_TILE = 64;
 
+// With 16- or 8-byte loads of B the kernel keeps to 64 registers, so four
+// blocks fit on an SM (the 8-byte form took 70, three blocks): fewer, fuller
+// passes for problems too small to fill HBM's queues, where every pass is a
+// round trip.  GB300, whole 3xTF32 calls in interleaved runs: 3000 x 2050 x
+// 1000 70.4 -> 68.4 us, 4096^3 441.1 us either way.
 template <bool VA, int VB>
-__global__ void __launch_bounds__(SPLIT_THREADS)
+__global__ void __launch_bounds__(SPLIT_THREADS, VB == 1 ? 1 : 4)
     split_vec_kernel(const float* __restrict__ A, const float* __restrict__ B, int64_t M,
                      int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t Kp, int a_blocks,
                      float* __restrict__ a_big, float* __restrict__ a_small,
