@@ -1,10 +1,12 @@
 """Seeded random sweep of every path variant against the oracle (GB300 only).
 
 Sixty cases with dimensions anywhere in 1..700, sixty with every dimension at
-or next to a tile boundary (1, 8, 16, ..., 512, each +-1), and twenty-four
-drawn onto the schedules that split or widen tiles. Each draws a path variant
-(SIMT fp32; 3xTF32 on the single-CTA kernel, on the CTA-pair kernel with the
-split pre-pass, and with the split on chip; bf16 on either kernel), a shape,
+or next to a tile boundary (1, 8, 16, ..., 512, each +-1), twenty-four drawn
+onto the schedules that split or widen tiles, and twenty-four small aligned
+problems in the automatic mode (one launch with the split inside, at the tile
+width it picks). Each draws a path variant (SIMT fp32; 3xTF32 in the automatic
+mode, on the single-CTA kernel, on the CTA-pair kernel with the split
+pre-pass, and with the split on chip; bf16 on either kernel), a shape,
 padded leading dimensions (0 to 9 extra elements), an element offset that
 breaks 16-byte alignment or not, and integer or real inputs. Integer inputs must
 match the oracle bit for bit, real ones within the path's tolerance; the
@@ -18,8 +20,8 @@ from parity_util import TOL, DeviceCall, normalised_error, operands
 pytestmark = pytest.mark.gpu
 
 # (path, CTA-pair mode, split mode)
-VARIANTS = [("f32", 0, 0), ("3xtf32", 1, 1), ("3xtf32", 1, 2), ("3xtf32", 2, 1), ("3xtf32", 2, 2),
-            ("bf16", 1, 0), ("bf16", 2, 0)]
+VARIANTS = [("f32", 0, 0), ("3xtf32", 0, 0), ("3xtf32", 1, 1), ("3xtf32", 1, 2), ("3xtf32", 2, 1),
+            ("3xtf32", 2, 2), ("bf16", 1, 0), ("bf16", 2, 0)]
 
 
 def cases(n=60, seed=20261202):
@@ -100,7 +102,28 @@ def aligned_split_cases(n=24, seed=20261205):
     return out
 
 
-@pytest.mark.parametrize("case", cases() + edge_cases() + schedule_cases() + aligned_split_cases(),
+def auto_small_cases(n=24, seed=20261206):
+    """Small 3xTF32 problems (M N <= 2^18, K <= 2048) with A 16-byte aligned
+    and lda a multiple of 4, in the automatic mode: one launch of the
+    single-CTA kernel with the split inside, on 128-, 64- or 32-column tiles
+    with clusters splitting K, whichever puts the most CTAs to work; B and C
+    at any padding."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        while True:
+            M, N = (int(x) for x in rng.integers(1, 700, 2))
+            if M * N <= 1 << 18:
+                break
+        K = 4 * int(rng.integers(1, 513))
+        pads = [4 * int(rng.integers(0, 3)), int(rng.integers(0, 10)), int(rng.integers(0, 10))]
+        dist = "int" if rng.random() < 0.5 else "normal"
+        out.append((("3xtf32", 0, 0), M, N, K, pads, 0, dist, 9800 + i))
+    return out
+
+
+@pytest.mark.parametrize("case", cases() + edge_cases() + schedule_cases() + aligned_split_cases() +
+                         auto_small_cases(),
                          ids=lambda c: f"{c[0][0]}-{c[0][1]}{c[0][2]}-{c[1]}x{c[2]}x{c[3]}-{c[6]}")
 def test_random_case(mhr, case):
     (path, pair_mode, split_mode), M, N, K, pads, offset, dist, seed = case
@@ -110,9 +133,13 @@ def test_random_case(mhr, case):
     try:
         C = DeviceCall(path, A, B, Ab, Bb, lda=K + pads[0], ldb=N + pads[1], ldc=N + pads[2],
                        offset=offset).run(mhr).result()
+        label = mhr.gemm_testing_last_main_kernel()
     finally:
         mhr.gemm_testing_set_split_mode(old_split)
         mhr.gemm_testing_set_cta_pair_mode(old_pair)
+    small_aligned = (offset == 0 and (K + pads[0]) % 4 == 0 and M * N <= 1 << 18 and K <= 2048)
+    if path == "3xtf32" and (pair_mode, split_mode) == (0, 0) and small_aligned:
+        assert label.startswith("tc_gemm_kernel<3xtf32,split,tma-a"), (case, label)
     if dist == "int":
         assert np.array_equal(C, oracle.gemm(A, B)), case
     else:
