@@ -98,8 +98,11 @@ struct TcParams {
   int64_t ldc;
   // C not TMA-aligned but its even rows are (16-byte aligned C, ldc even):
   // chunks wholly inside the tile and C store their even rows by TMA through
-  // a map over rows 0, 2, 4, ... and only the odd rows from registers.
-  int32_t c_even;
+  // a map over rows 0, 2, 4, ... (c_even), and their odd rows through a map
+  // over rows 1, 3, 5, ... whose base lies c_odd_shift columns (0, or 2 when
+  // ldc is 2 mod 4) left of each odd row's start, so that it is 16-byte
+  // aligned; -1: no odd-row map (the odd rows go out from registers).
+  int32_t c_even, c_odd_shift;
   uint32_t* status;
   uint64_t wait_limit_ns;
   int32_t inject_stall;
@@ -173,6 +176,36 @@ __device__ __forceinline__ void give_up(const TcParams& p, volatile int* abort_f
   __syncwarp();
 }
 
+// The odd-row part of an epilogue chunk under the even-row scheme
+// (TcParams::c_even): whether the odd rows go out by TMA through the odd-row
+// map, the chunk's columns 32 and 33 (the next chunk's first two, which a
+// box shifted by 2 columns also covers), and which of the chunk's first two
+// odd-row columns were written by the box of the chunk before it.
+struct OddRows {
+  bool tma = false;    // odd rows by one TMA store (or reduce-add) through tmC1
+  bool lead2 = false;  // columns 0-1 of the odd rows: written by the previous chunk's box
+  uint32_t e[2] = {0u, 0u};
+};
+
+// The odd-row plan of the chunk at col0 of a tile starting at n0.  With the
+// map shifted by 2 columns, a box covers columns col0 + 2 .. col0 + 33, so it
+// is used only when those lie inside the tile and C; the tile's first chunk
+// then writes its odd rows' columns 0-1 from registers, and every later chunk
+// finds them written.  Warp-uniform; TMEM columns col0 + 32 and + 33 of the
+// accumulator at taddr_next are loaded when the box needs them.
+__device__ __forceinline__ OddRows plan_odd_rows(const TcParams& p, int n0, int col0, int col_end,
+                                                 uint32_t taddr_next) {
+  OddRows o;
+  if (!p.c_even || p.c_odd_shift < 0) return o;
+  // the previous chunk (whole: this one starts inside the tile) had a box iff
+  // its columns 2 .. 33 lay inside the tile and C
+  o.lead2 = p.c_odd_shift == 2 && col0 > n0 && col0 + 2 <= col_end;
+  if (col0 + 32 > col_end) return o;
+  o.tma = col0 + 32 + p.c_odd_shift <= col_end;
+  if (o.tma && p.c_odd_shift == 2) tmem_ld_2cols(taddr_next, o.e);
+  return o;
+}
+
 // Epilogue of one 32 x 32 fp32 chunk held by a warp (lane = row, r[j] =
 // column j): write it into the warp's staging box in shared memory (128-byte
 // swizzle: 16-byte piece j of row r sits at position j ^ (r % 8), so both the
@@ -181,31 +214,50 @@ __device__ __forceinline__ void give_up(const TcParams& p, volatile int* abort_f
 // TMA-aligned -- store it two rows per warp instruction, masked to rows < M
 // and columns < col_end (atomic adds for split-K units).  col_end is N, or
 // the tile's last column + 1 when the tile is narrower than its last chunk
-// (the TMA path is used only for tiles that are whole chunks).
+// (the TMA path is used only for tiles that are whole chunks).  `odd`: the
+// odd rows' plan under the even-row scheme (plan_odd_rows).  The warp's two
+// staging boxes alternate; before reusing one, the warp waits until the bulk
+// group of the chunk two back has read it -- one group back when the chunk
+// just before committed one (prev_group), else none.  Returns whether this
+// chunk committed a bulk group.
 template <bool TMA_STORE>
-__device__ __forceinline__ void stage_and_store_chunk(const uint32_t (&r)[32], uint32_t epi_base,
+__device__ __forceinline__ bool stage_and_store_chunk(const uint32_t (&r)[32], uint32_t epi_base,
                                                       int ew, uint32_t chunk, int lane,
-                                                      const CUtensorMap* tmC, const TcParams& p,
+                                                      const CUtensorMap* tmC,
+                                                      const CUtensorMap* tmC1, const TcParams& p,
                                                       int row0, int col0, int col_end,
-                                                      bool reduce) {
+                                                      bool reduce, const OddRows& odd,
+                                                      bool prev_group) {
   const uint32_t stg = epi_base + (ew * 2 + (chunk & 1u)) * EPI_BUF_BYTES;
   const bool even_rows = !TMA_STORE && p.c_even;
   if (even_rows && col0 + 32 <= col_end) {
     // Even rows 0, 2, .., 30 of the chunk into the buffer's first 16 swizzled
     // rows, odd rows into the last 16; one TMA store (or reduce-add) writes
-    // the even half to rows row0 / 2 .. of the even-row map, and the odd half
-    // goes out from registers two rows per warp instruction as below.  A
-    // register chunk commits no bulk group, so wait for all of them: the
-    // buffer may have been handed to a store two or more groups back.
-    if (lane == 0) bulk_wait_group_read<0>();
+    // the even half to rows row0 / 2 .. of the even-row map.  The odd half
+    // goes out through the odd-row map (staged c_odd_shift columns on, the
+    // next chunk's first columns at the end) or from registers two rows per
+    // warp instruction as below.
+    if (lane == 0) {
+      if (prev_group)
+        bulk_wait_group_read<1>();
+      else
+        bulk_wait_group_read<0>();
+    }
     __syncwarp();
     const int brow = (lane >> 1) + (lane & 1) * 16;
     const uint32_t brow_addr = stg + brow * 128;
+    const bool shifted = odd.tma && p.c_odd_shift == 2 && (lane & 1);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const uint32_t a = brow_addr + ((j ^ (brow & 7)) << 4);
-      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(r[4 * j]),
-                   "r"(r[4 * j + 1]), "r"(r[4 * j + 2]), "r"(r[4 * j + 3])
+      // a shifted odd row holds columns 2 .. 33: r[2 ..], then the next
+      // chunk's two
+      const uint32_t v0 = shifted ? r[4 * j + 2] : r[4 * j];
+      const uint32_t v1 = shifted ? r[4 * j + 3] : r[4 * j + 1];
+      const uint32_t v2 = shifted ? (j < 7 ? r[4 * j + 4] : odd.e[0]) : r[4 * j + 2];
+      const uint32_t v3 = shifted ? (j < 7 ? r[4 * j + 5] : odd.e[1]) : r[4 * j + 3];
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v0), "r"(v1),
+                   "r"(v2), "r"(v3)
                    : "memory");
     }
     fence_proxy_async_smem();
@@ -215,7 +267,29 @@ __device__ __forceinline__ void stage_and_store_chunk(const uint32_t (&r)[32], u
         tma_reduce_add_2d(tmC, stg, col0, row0 / 2);
       else
         tma_store_2d(tmC, stg, col0, row0 / 2);
+      if (odd.tma) {
+        const int x = col0 + 2 * p.c_odd_shift;  // the odd map's column of col0 + shift
+        if (reduce)
+          tma_reduce_add_2d(tmC1, stg + 16 * 128, x, row0 / 2);
+        else
+          tma_store_2d(tmC1, stg + 16 * 128, x, row0 / 2);
+      }
       bulk_commit_group();
+    }
+    if (odd.tma) {
+      // a box shifted by 2 columns starts at the chunk's column 2: the tile's
+      // first chunk writes its odd rows' columns 0-1 itself (8-byte aligned:
+      // C 16-byte aligned, ldc 2 mod 4, col0 a multiple of 16)
+      if (p.c_odd_shift == 2 && !odd.lead2 && (lane & 1) && row0 + lane < p.M) {
+        float* dst = p.C + static_cast<int64_t>(row0 + lane) * p.ldc + col0;
+        const float2 v = make_float2(__uint_as_float(r[0]), __uint_as_float(r[1]));
+        if (reduce)
+          atomicAdd(reinterpret_cast<float2*>(dst), v);
+        else
+          *reinterpret_cast<float2*>(dst) = v;
+      }
+      __syncwarp();
+      return true;
     }
     const int half = lane >> 4;
     const int cp = (lane & 15) * 2;
@@ -233,7 +307,9 @@ __device__ __forceinline__ void stage_and_store_chunk(const uint32_t (&r)[32], u
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int row = row0 + 2 * (2 * i + half) + 1;
-      if (row < p.M) {
+      // (columns 0-1 of a chunk after one whose odd rows went out by TMA are
+      // written already: a reduce-add must not add them twice)
+      if (row < p.M && !(odd.lead2 && cp == 0)) {
         float* dst = p.C + static_cast<int64_t>(row) * p.ldc + col;  // 8-byte aligned: ldc even
         if (reduce)
           atomicAdd(reinterpret_cast<float2*>(dst), v[i]);
@@ -242,12 +318,15 @@ __device__ __forceinline__ void stage_and_store_chunk(const uint32_t (&r)[32], u
       }
     }
     __syncwarp();
-    return;
+    return true;
   }
   if (TMA_STORE) {
     if (lane == 0) bulk_wait_group_read<1>();  // the store that last used this buffer has read it
-  } else if (even_rows) {
-    if (lane == 0) bulk_wait_group_read<0>();  // (a chunk at the tile's edge; see above)
+  } else if (even_rows && lane == 0) {         // (a chunk at the tile's edge; see above)
+    if (prev_group)
+      bulk_wait_group_read<1>();
+    else
+      bulk_wait_group_read<0>();
   }
   __syncwarp();
   const uint32_t row_addr = stg + lane * 128;
@@ -268,6 +347,7 @@ __device__ __forceinline__ void stage_and_store_chunk(const uint32_t (&r)[32], u
         tma_store_2d(tmC, stg, col0, row0);
       bulk_commit_group();
     }
+    return true;
   } else {
     __syncwarp();
     // Two rows per step, two adjacent columns per lane: lanes 0-15 take row
@@ -292,7 +372,8 @@ __device__ __forceinline__ void stage_and_store_chunk(const uint32_t (&r)[32], u
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int row = row0 + 2 * i + half;
-      if (row < p.M && col < col_end) {
+      // (odd rows: see above; half = 1 is the odd rows)
+      if (row < p.M && col < col_end && !(odd.lead2 && half == 1 && cp == 0)) {
         float* dst = p.C + static_cast<int64_t>(row) * p.ldc + col;
         if (col + 1 < col_end && (reinterpret_cast<uintptr_t>(dst) & 7u) == 0) {
           if (reduce)
@@ -312,6 +393,7 @@ __device__ __forceinline__ void stage_and_store_chunk(const uint32_t (&r)[32], u
     }
     __syncwarp();  // the box is free for the next chunk
   }
+  return false;
 }
 
 // ------------------------------------------------------------------ host side
@@ -335,6 +417,7 @@ inline TcParams make_params(int64_t M, int64_t N, int64_t K, int tile_m, int til
   p.C = C;
   p.ldc = ldc;
   p.c_even = 0;
+  p.c_odd_shift = -1;
   p.status = ctl.status;
   p.wait_limit_ns = ctl.wait_limit_ns;
   p.inject_stall = ctl.inject_stall;
@@ -352,8 +435,9 @@ constexpr int PAIR_TILE_M = 256, PAIR_TILE_N = 256;
 // only) and C (unused without TMA stores).  c_even: `c` maps C's even rows
 // (boxes of 32 columns x 16 of those rows) for the register-store kernels.
 struct TcMaps {
-  CUtensorMap a0, a1, b0, b1, c;
+  CUtensorMap a0, a1, b0, b1, c, c1;
   bool c_even = false;
+  int c_odd_shift = -1;  // c1: C's odd rows (TcParams::c_odd_shift); -1: none
 };
 
 // tc_gemm_1cta.cu.  bn: KIND_3XTF32's tile columns (128, or 96, 64 or 32

@@ -155,18 +155,27 @@ cudaError_t launch_tc_any(int kind, const TcMaps& maps, float* C, int64_t M, int
 
 // C's map: the whole of C in boxes of 32 x 32 when TMA can store C.
 // Otherwise, when C is 16-byte aligned and ldc even (so that every other row
-// starts on a 16-byte boundary: the case of an ldc that is 2 mod 4), a map
-// over C's even rows (pitch 2 ldc, boxes of 32 columns x 16 rows) with which
-// the register-store kernels write half of each chunk by TMA (TcMaps::c_even).
+// starts on a 16-byte boundary: the case of an ldc that is 2 mod 4, or of N
+// not a multiple of 4), a map over C's even rows (pitch 2 ldc, boxes of 32
+// columns x 16 rows) with which the register-store kernels write half of
+// each chunk by TMA (TcMaps::c_even), and a map over the odd rows: row
+// 2 y + 1 starts ldc floats after row 2 y, so its base moves ldc % 4 columns
+// left, to the 16-byte boundary below (TcMaps::c_odd_shift; its first
+// columns then belong to the row above and are never written).
 CUresult encode_c_map(TcMaps* mp, float* C, int64_t M, int64_t N, int64_t ldc, bool c_tma) {
+  const auto f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
   mp->c_even = false;
-  if (c_tma)
-    return encode_tmap_2d(&mp->c, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, N, M, ldc * 4, 32, 32,
-                          CU_TENSOR_MAP_SWIZZLE_128B);
+  mp->c_odd_shift = -1;
+  if (c_tma) return encode_tmap_2d(&mp->c, f32, C, N, M, ldc * 4, 32, 32, sw);
   if ((reinterpret_cast<uintptr_t>(C) & 15u) == 0 && ldc % 2 == 0 &&
-      encode_tmap_2d(&mp->c, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, N, (M + 1) / 2, ldc * 8, 32, 16,
-                     CU_TENSOR_MAP_SWIZZLE_128B) == CUDA_SUCCESS)
+      encode_tmap_2d(&mp->c, f32, C, N, (M + 1) / 2, ldc * 8, 32, 16, sw) == CUDA_SUCCESS) {
     mp->c_even = true;
+    const int64_t shift = ldc % 4;  // 0 or 2
+    if (M >= 2 && encode_tmap_2d(&mp->c1, f32, C + ldc - shift, N + shift, M / 2, ldc * 8, 32,
+                                 16, sw) == CUDA_SUCCESS)
+      mp->c_odd_shift = static_cast<int>(shift);
+  }
   return CUDA_SUCCESS;
 }
 
@@ -185,6 +194,7 @@ cudaError_t launch_tc_bf16(const uint16_t* A, const uint16_t* B, float* C, int64
   mp.a1 = mp.a0;  // unused by the bf16 kernels
   mp.b1 = mp.b0;
   if (!c_tma && !mp.c_even) mp.c = mp.a0;  // unused without TMA stores
+  if (mp.c_odd_shift < 0) mp.c1 = mp.c;
   return launch_tc_any(KIND_BF16, mp, C, M, N, K, ldc, c_tma, after_prepass, ctl, s);
 }
 
@@ -213,6 +223,7 @@ cudaError_t launch_tc_3xtf32(const float* a_big, int64_t a_big_ld, const float* 
       encode_c_map(&mp, C, M, N, ldc, tma_c) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   if (!tma_c && !mp.c_even) mp.c = mp.a0;  // unused without TMA stores
+  if (mp.c_odd_shift < 0) mp.c1 = mp.c;
   return pair ? launch_cta_pair(KIND_3XTF32, mp, C, M, N, K, ldc, tma_c, true, bn, ctl, s)
               : launch_single_cta(KIND_3XTF32, mp, C, M, N, K, ldc, tma_c, true, bn, ctl, s);
 }

@@ -163,7 +163,8 @@ template <int KIND, bool TMA_STORE, bool CLUSTER>
 __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                    const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
-                   const __grid_constant__ CUtensorMap tmC, const TcParams p) {
+                   const __grid_constant__ CUtensorMap tmC,
+                   const __grid_constant__ CUtensorMap tmC1, const TcParams p) {
   using Cf = Cfg<KIND>;
   using L = Layout<KIND>;
   extern __shared__ uint8_t smem_raw[];
@@ -402,6 +403,7 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
     const int q = warp & 3;           // TMEM lane quarter this warp may access
     const int ew = warp - 2;          // epilogue warp index 0..3
     uint32_t tcount = 0, chunk = 0;
+    bool prev_group = false;  // the warp's previous chunk committed a bulk group
     for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++tcount) {
       const Unit w = unit_1cta<CLUSTER>(u, p);
       const uint32_t buf = tcount & 1u, aph = (tcount >> 1) & 1u;
@@ -442,9 +444,17 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
         for (int c = 0; c < bn / 32; ++c) {
           uint32_t r[32];
           tmem_ld_32cols(taddr + c * 32, r);
+          // (the converter kind, held to 80 registers, keeps its odd rows in
+          // registers)
+          const OddRows odd =
+              KIND == KIND_3XTF32_SPLIT_TMA_A
+                  ? OddRows{}
+                  : plan_odd_rows(p, n0, n0 + c * 32, col_end, taddr + c * 32 + 32);
           tmem_ld_wait();
-          stage_and_store_chunk<TMA_STORE>(r, sbase + L::EPI_OFF, ew, chunk, lane, &tmC, p,
-                                           m0 + q * 32, n0 + c * 32, col_end, w.reduce);
+          prev_group = stage_and_store_chunk<TMA_STORE>(r, sbase + L::EPI_OFF, ew, chunk, lane,
+                                                        &tmC, &tmC1, p, m0 + q * 32,
+                                                        n0 + c * 32, col_end, w.reduce, odd,
+                                                        prev_group);
           ++chunk;
         }
       }
@@ -562,6 +572,7 @@ cudaError_t launch_t(const TcMaps& mp, float* C, int64_t M, int64_t N, int64_t K
   if (KIND != KIND_3XTF32 || bn <= 0) bn = Cf::BN;
   TcParams p = make_params(M, N, K, Cf::BM, bn, Cf::BK, C, ldc, ctl);
   p.c_even = !c_tma && mp.c_even;
+  p.c_odd_shift = p.c_even ? mp.c_odd_shift : -1;
   cudaError_t e;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -588,7 +599,7 @@ cudaError_t launch_t(const TcMaps& mp, float* C, int64_t M, int64_t N, int64_t K
                                        : "tc_gemm_kernel<3xtf32,cluster-K>",
                      p.num_units, p.num_tiles);
     e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<KIND, false, true>, mp.a0, mp.a1, mp.b0, mp.b1,
-                           mp.c, p);
+                           mp.c, mp.c1, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
@@ -619,11 +630,11 @@ cudaError_t launch_t(const TcMaps& mp, float* C, int64_t M, int64_t N, int64_t K
   if (c_tma) {
     if ((e = prepare_kernel<KIND, true, false>()) != cudaSuccess) return e;
     e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<KIND, true, false>, mp.a0, mp.a1, mp.b0, mp.b1,
-                           mp.c, p);
+                           mp.c, mp.c1, p);
   } else {
     if ((e = prepare_kernel<KIND, false, false>()) != cudaSuccess) return e;
     e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<KIND, false, false>, mp.a0, mp.a1, mp.b0, mp.b1,
-                           mp.c, p);
+                           mp.c, mp.c1, p);
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -713,6 +724,7 @@ cudaError_t launch_single_cta_split(const TcMaps& maps, const float* A, const fl
   p.vec_a = 1;  // the TMA map of A requires what the 16-byte loads do
   p.vec_b = (reinterpret_cast<uintptr_t>(B) % 16 == 0) && (ldb % 4 == 0);
   p.c_even = !c_tma && maps.c_even;
+  p.c_odd_shift = -1;  // see the epilogue
   const int S = cluster_size(p.num_tiles);
   if (S > 1) {
     attr[1].val.clusterDim.x = static_cast<unsigned>(S);
@@ -726,7 +738,7 @@ cudaError_t launch_single_cta_split(const TcMaps& maps, const float* A, const fl
       snprintf(name, sizeof(name), "tc_gemm_kernel<3xtf32,split,tma-a,n%d,cluster-K>", bn);
     note_main_kernel(name, p.num_units, p.num_tiles);
     e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<KIND, false, true>, maps.a0, maps.a1, maps.b0,
-                           maps.b1, maps.c, p);
+                           maps.b1, maps.c, maps.c1, p);
   } else {
     cfg.numAttrs = 1;
     const int grid = p.num_units < ctl.sm_count ? p.num_units : ctl.sm_count;
@@ -740,11 +752,11 @@ cudaError_t launch_single_cta_split(const TcMaps& maps, const float* A, const fl
     if (c_tma) {
       if ((e = prepare_kernel<KIND, true, false>()) != cudaSuccess) return e;
       e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<KIND, true, false>, maps.a0, maps.a1, maps.b0,
-                             maps.b1, maps.c, p);
+                             maps.b1, maps.c, maps.c1, p);
     } else {
       if ((e = prepare_kernel<KIND, false, false>()) != cudaSuccess) return e;
       e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<KIND, false, false>, maps.a0, maps.a1, maps.b0,
-                             maps.b1, maps.c, p);
+                             maps.b1, maps.c, maps.c1, p);
     }
   }
   if (e != cudaSuccess) return e;

@@ -141,7 +141,8 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
                         const __grid_constant__ CUtensorMap tmA1,
                         const __grid_constant__ CUtensorMap tmB0,
                         const __grid_constant__ CUtensorMap tmB1,
-                        const __grid_constant__ CUtensorMap tmC, const TcParams p) {
+                        const __grid_constant__ CUtensorMap tmC,
+                        const __grid_constant__ CUtensorMap tmC1, const TcParams p) {
   using Cf = PairCfg<KIND>;
   using L = PairLayout<KIND>;
   extern __shared__ uint8_t smem_raw[];
@@ -426,6 +427,7 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
     const int q = warp & 3;
     const int ew = warp - 2;
     uint32_t tcount = 0, chunk = 0;
+    bool prev_group = false;  // the warp's previous chunk committed a bulk group
     for (int u = cluster; u < p.num_units; u += num_clusters, ++tcount) {
       const Unit w = unit_of(u, p);
       const uint32_t buf = tcount & 1u, aph = (tcount >> 1) & 1u;
@@ -448,9 +450,15 @@ __global__ void __launch_bounds__(pair_threads<KIND>(), 1)
       for (int c = 0; c < (bn + 31) / 32; ++c) {
         uint32_t r[32];
         tmem_ld_32cols(taddr + c * 32, r);
+        // (the converter kinds, held to 80 or 128 registers, keep their odd
+        // rows in registers)
+        const OddRows odd = has_converters<KIND>()
+                                ? OddRows{}
+                                : plan_odd_rows(p, n0, n0 + c * 32, col_end, taddr + c * 32 + 32);
         tmem_ld_wait();
-        stage_and_store_chunk<TMA_STORE>(r, sbase + L::EPI_OFF, ew, chunk, lane, &tmC, p,
-                                         m0 + q * 32, n0 + c * 32, col_end, w.reduce);
+        prev_group = stage_and_store_chunk<TMA_STORE>(r, sbase + L::EPI_OFF, ew, chunk, lane,
+                                                      &tmC, &tmC1, p, m0 + q * 32, n0 + c * 32,
+                                                      col_end, w.reduce, odd, prev_group);
         ++chunk;
       }
       tc_fence_before();
@@ -654,6 +662,7 @@ cudaError_t launch_pair_t(const TcMaps& mp, const TcParams& p, bool after_prepas
   // order, so results stay bit-reproducible.
   TcParams q = p;
   q.c_even = !TMA_STORE && mp.c_even;
+  q.c_odd_shift = q.c_even && !has_converters<KIND>() ? mp.c_odd_shift : -1;
   const int rem = p.num_tiles % clusters;
   if (p.num_tiles > clusters && rem > 0 && 2 * rem <= clusters && p.num_kb >= 2) {
     q.full_units = p.num_tiles - rem;
@@ -675,7 +684,7 @@ cudaError_t launch_pair_t(const TcMaps& mp, const TcParams& p, bool after_prepas
              : KIND == KIND_3XTF32_SPLIT_TMA_A ? "tc_gemm_pair_kernel<3xtf32,split,tma-a>"
                                                : "tc_gemm_pair_kernel<3xtf32,split>");
   note_main_kernel(name, 2 * clusters, p.num_tiles);
-  e = cudaLaunchKernelEx(&cfg, kern, mp.a0, mp.a1, mp.b0, mp.b1, mp.c, q);
+  e = cudaLaunchKernelEx(&cfg, kern, mp.a0, mp.a1, mp.b0, mp.b1, mp.c, mp.c1, q);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

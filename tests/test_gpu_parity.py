@@ -321,6 +321,65 @@ def test_pair_kernel_narrow_tiles(mhr, bn):
         mhr.gemm_testing_set_cta_pair_mode(old)
 
 
+# (path, CTA-pair mode, split mode, forced pair tile width)
+ODD_ROW_VARIANTS = [("3xtf32", 2, 1, 256), ("3xtf32", 2, 1, 176), ("3xtf32", 1, 1, 0),
+                    ("bf16", 2, 0, 0), ("bf16", 1, 0, 0)]
+
+
+@pytest.mark.parametrize("variant", ODD_ROW_VARIANTS,
+                         ids=["3xtf32-pair", "3xtf32-pair-n176", "3xtf32-1cta", "bf16-pair",
+                              "bf16-1cta"])
+def test_even_and_odd_row_maps(mhr, variant):
+    """C 16-byte aligned with an even ldc but not storable by TMA as a whole
+    (ldc 2 mod 4, or N not a multiple of 4): whole chunks store their even
+    rows through a map over rows 0, 2, 4, ... and their odd rows through a map
+    over rows 1, 3, 5, ... whose base lies ldc % 4 columns left of each odd
+    row (so a box starts 2 columns into the chunk and ends 2 into the next;
+    the tile's first 2 odd-row columns go out from registers). Odd and even
+    M, every N mod 4, ragged tiles. Integer inputs bit-exact against the
+    oracle; C's padding keeps its guard values; real inputs within the
+    tolerance."""
+    path, mode, split, bn = variant
+    old = mhr.gemm_testing_set_cta_pair_mode(mode)
+    old_split = mhr.gemm_testing_set_split_mode(split)
+    try:
+        with pair_tile_n(mhr, bn):
+            for M, N, K, ldc in ((300, 520, 200, 522), (301, 518, 200, 520), (300, 517, 200, 518),
+                                 (301, 515, 136, 516), (64, 1100, 72, 1102), (2, 298, 40, 300),
+                                 (1, 298, 40, 302)):
+                A, B, Ab, Bb = operands(M, N, K, 3551 + N + M, "int", path)
+                C = DeviceCall(path, A, B, Ab, Bb, ldc=ldc).run(mhr).result()
+                assert np.array_equal(C, oracle.gemm(A, B)), (M, N, K, ldc)
+            A, B, Ab, Bb = operands(300, 520, 200, 3552, "normal", path)
+            C = DeviceCall(path, A, B, Ab, Bb, ldc=522).run(mhr).result()
+            Cref, S = oracle.gemm(A, B, with_abs=True)
+            assert normalised_error(C, Cref, S) <= TOL[path]
+    finally:
+        mhr.gemm_testing_set_split_mode(old_split)
+        mhr.gemm_testing_set_cta_pair_mode(old)
+
+
+@pytest.mark.usefixtures("full_width_tiles")
+@pytest.mark.parametrize("path", ["3xtf32", "bf16"])
+def test_split_last_round_odd_row_map(mhr, path):
+    """The split last round (K halves reduce-added into zeroed C) through the
+    even- and odd-row maps: N = 254 with ldc = 256 (odd-row map unshifted) and
+    N = 252 with ldc = 254 (shifted by 2 columns); 3 more pair tiles than
+    clusters. Integer inputs: every addend is exact, so C matches the oracle
+    bit for bit, and no column is added twice."""
+    old = mhr.gemm_testing_set_cta_pair_mode(2)
+    try:
+        clusters = pair_clusters(mhr, path)
+        for N, ldc in ((254, 256), (252, 254)):
+            M, K = 256 * (clusters + 3), 320
+            A, B, Ab, Bb = operands(M, N, K, 3553 + N, "int", path)
+            C = DeviceCall(path, A, B, Ab, Bb, ldc=ldc).run(mhr).result()
+            assert f"tiles={clusters + 3}" in mhr.gemm_testing_last_main_kernel()
+            assert np.array_equal(C, oracle.gemm(A, B)), (N, ldc)
+    finally:
+        mhr.gemm_testing_set_cta_pair_mode(old)
+
+
 @pytest.mark.parametrize("bn", [128, 96, 64, 32])
 def test_single_cta_tile_widths(mhr, bn):
     """The single-CTA 3xTF32 kernel at each tile width it can run (128 rows x
