@@ -359,22 +359,29 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
     const int stride = static_cast<int>(gridDim.x);
     auto convert = [&](auto vec_b) {
       constexpr bool VB = decltype(vec_b)::value;
+      // The group's first loads go out before the rest of the set-up: on a
+      // small problem that set-up is most of the time to the first MMA.
+      LoadCursor<SingleWalk<CLUSTER>> ld;
+      ld.seek_work(p, walk, blockIdx.x, stride, ct);  // (a cluster rank's K run may be empty)
+      for (int d = 0; d < g; ++d) ld.advance(p, walk, stride, ct);
+      BRegs r;
+      if (ld.valid) load_b<VB>(r, p, ld, ct);
       int total = 0;  // how many K-blocks this CTA stores
       for (int u = blockIdx.x; u < p.num_units; u += stride) {
         const Unit w = unit_1cta<CLUSTER>(u, p);
         total += w.kb1 - w.kb0;
       }
-      LoadCursor<SingleWalk<CLUSTER>> ld;
-      ld.seek_work(p, walk, blockIdx.x, stride, ct);  // (a cluster rank's K run may be empty)
+      // L2 prefetches run SPLIT_PREFETCH K-blocks ahead of the loads; with at
+      // most one K-block per group there is nothing ahead to fetch.
+      const bool prefetch = total > 2;
       PrefetchCursor<SingleWalk<CLUSTER>> pf;
-      pf.seek_work(p, walk, blockIdx.x, stride);
-      for (int d = 0; d < g; ++d) ld.advance(p, walk, stride, ct);
-      for (int d = 0; d < g + 2 + SPLIT_PREFETCH; ++d) {
-        if (d >= g + 2 && ((d - g) & 1) == 0) split_prefetch_l2(p, ct, pf);
-        pf.advance(p, walk, stride);
+      if (prefetch) {
+        pf.seek_work(p, walk, blockIdx.x, stride);
+        for (int d = 0; d < g + 2 + SPLIT_PREFETCH; ++d) {
+          if (d >= g + 2 && ((d - g) & 1) == 0) split_prefetch_l2(p, ct, pf);
+          pf.advance(p, walk, stride);
+        }
       }
-      BRegs r;
-      if (g < total) load_b<VB>(r, p, ld, ct);
       for (int it = g; it < total; it += 2) {
         const uint32_t s = it % stages, ph = (it / stages) & 1u;
         if (!warp_wait(empty_bar(s), ph ^ 1u, limit, abort_flag) ||
@@ -389,9 +396,11 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
         ld.advance(p, walk, stride, ct);
         ld.advance(p, walk, stride, ct);
         if (it + 2 < total) load_b<VB>(r, p, ld, ct);
-        split_prefetch_l2(p, ct, pf);
-        pf.advance(p, walk, stride);
-        pf.advance(p, walk, stride);
+        if (prefetch) {
+          split_prefetch_l2(p, ct, pf);
+          pf.advance(p, walk, stride);
+          pf.advance(p, walk, stride);
+        }
       }
     };
     if (p.vec_b)
