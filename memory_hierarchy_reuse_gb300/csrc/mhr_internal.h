@@ -85,7 +85,7 @@ cudaError_t launch_tc_3xtf32_small(const float* A, const float* B, float* C, int
 
 // Whether the tensor-core path of `kind` (KIND_BF16 or KIND_3XTF32, in
 // tc_common.cuh) runs the CTA-pair kernel for this shape (else the
-// single-CTA kernel).
+// single-CTA kernel); for 3xTF32 this may be at a narrower planned width.
 bool tc_pair_chosen(int kind, int64_t M, int64_t N, int64_t K, const DeviceCtl& ctl);
 // Whether a 3xTF32 call runs as one launch of the single-CTA kernel with the
 // split inside (launch_tc_3xtf32_small): forced by the test hooks (split mode

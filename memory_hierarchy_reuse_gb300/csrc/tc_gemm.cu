@@ -11,7 +11,17 @@ bool tc_pair_chosen(int kind, int64_t M, int64_t N, int64_t K, const DeviceCtl& 
   const int64_t pair_tiles = ((M + tc::PAIR_TILE_M - 1) / tc::PAIR_TILE_M) *
                              ((N + tc::PAIR_TILE_N - 1) / tc::PAIR_TILE_N);
   const int64_t clusters = ctl.sm_count / 2;
-  if (2 * pair_tiles < clusters) return false;
+  if (2 * pair_tiles < clusters) {
+    // 3xTF32 also takes the pair kernel at a narrower planned width when
+    // those tiles fill at least 80 % of the clusters.  GB300, whole calls:
+    // 1536^3 47.8 -> 45.7 us, 2048 x 1024 x 1024 35.5 -> 33.5, 1024 x 2048 x
+    // 2048 60.1 -> 58.0 (128-column tiles); with fewer tiles (1024^3: 32 of
+    // them) the single-CTA kernel stays faster (26.3 against 33.4 us).
+    if (kind != tc::KIND_3XTF32 || ctl.pair_tile_n > 0) return false;
+    const int bn = tc::plan_pair_tile_n(M, N, K, static_cast<int>(clusters), true);
+    const int64_t tiles = ((M + tc::PAIR_TILE_M - 1) / tc::PAIR_TILE_M) * ((N + bn - 1) / bn);
+    return bn < tc::PAIR_TILE_N && 5 * tiles >= 4 * clusters;
+  }
   return kind != tc::KIND_BF16 || K >= 2048 || pair_tiles >= 2 * clusters;
 }
 
@@ -141,8 +151,9 @@ using namespace tc;
 // many shared-memory bytes per clock as the MMAs consume and runs the tensor
 // pipe near 57 % busy.  GB300 measurements, 3xTF32 calls: pair faster at
 // 2048^3 (1.2x), 2048 x 2048 x 1024 (1.13x), 3000 x 2048 x 1000 (1.12x),
-// 8192 x 1024 x 1024 (1.18x); 1-CTA faster at 1536^3 (36 pair tiles) and
-// 1024 x 1024 x 4096 (16).  bf16: 1-CTA (128 x 256 tiles) faster at
+// 8192 x 1024 x 1024 (1.18x); 1-CTA faster at 1536^3 with 256-column pair
+// tiles (36 of them; with the planner's 128-column ones, 72, the pair kernel
+// wins: tc_pair_chosen) and 1024 x 1024 x 4096 (16).  bf16: 1-CTA (128 x 256 tiles) faster at
 // 3000 x 2050 x 1000.  DeviceCtl::pair_mode forces one of them (tests).
 cudaError_t launch_tc_any(int kind, const TcMaps& maps, float* C, int64_t M, int64_t N, int64_t K,
                           int64_t ldc, bool c_tma, bool after_prepass, const DeviceCtl& ctl,

@@ -577,6 +577,39 @@ def test_automatic_mode_runs_small_problems_as_one_launch(mhr, shape, one_launch
 
 
 
+@pytest.mark.parametrize("shape", [(1536, 1536, 1024), (1024, 2048, 640), (1024, 1024, 1024),
+                                   (1280, 1280, 512)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_automatic_mode_narrow_pair_tiles(mhr, shape):
+    """3xTF32 shapes with too few 256 x 256 pair tiles for the CTA-pair kernel
+    still take it, at the planner's narrower width, when those tiles fill at
+    least 80 % of the clusters (1536 x 1536: 72 tiles of 256 x 128 on 76
+    clusters); with fewer the single-CTA kernel runs (1024 x 1024: 32).
+    Integer inputs bit-exact against the oracle on sampled entries."""
+    import re
+
+    import torch
+
+    M, N, K = shape
+    clusters = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    A, B, _, _ = operands(M, N, K, 3971 + K, "int", "3xtf32")
+    C = DeviceCall("3xtf32", A, B).run(mhr).result()
+    label = mhr.gemm_testing_last_main_kernel()
+    bn = mhr.gemm_testing_plan_pair_tile_n(M, N, K, clusters, True)
+    tiles = -(-M // 256) * -(-N // bn)
+    if 2 * (-(-M // 256)) * (-(-N // 256)) >= clusters:
+        want = "tc_gemm_pair_kernel<3xtf32"
+    elif bn < 256 and 5 * tiles >= 4 * clusters:
+        want = f"tc_gemm_pair_kernel<3xtf32,n{bn}>"
+    else:
+        want = "tc_gemm_kernel<3xtf32"
+    assert label.startswith(want), (label, want, bn, tiles)
+    assert int(re.search(r"tiles=(\d+)", label).group(1)) > 0
+    rows, cols = sample_indices(M, N, 3971, rows=(0, M // 2 + 1, M - 1), cols=(0, N - 1))
+    ref = oracle.gemm_entries(A, B, rows, cols, M, N, K)[0]
+    assert np.array_equal(C[rows, cols], ref)
+
+
 @pytest.mark.usefixtures("full_width_tiles")
 def test_workspace_fallback_splits_in_kernel(mhr):
     """Operands one element off 16-byte alignment cannot be their own big
