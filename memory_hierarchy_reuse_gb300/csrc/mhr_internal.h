@@ -99,6 +99,10 @@ namespace tc {
 // problem with up to `clusters` co-resident clusters; tc_gemm.cu gives the
 // cost model.
 int plan_pair_tile_n(int64_t M, int64_t N, int64_t K, int clusters, bool c_tma);
+// For 3xTF32 problems with too few 256 x 256 tiles for half of the clusters:
+// the CTA-pair tile columns (256, 192 or 128) that keep at least 80 % of the
+// clusters busy, counting K halves, or 0 (the single-CTA kernel runs).
+int few_tile_pair_width(int64_t M, int64_t N, int64_t K, int clusters);
 // Columns of the single-CTA kernel's 3xTF32 tiles (128, 96, 64 or 32) on
 // `sms` SMs; tc_gemm.cu gives the cost model.
 int plan_single_tile_n(int64_t M, int64_t N, int64_t K, int sms, bool c_tma);

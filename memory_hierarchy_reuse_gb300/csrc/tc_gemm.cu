@@ -11,17 +11,9 @@ bool tc_pair_chosen(int kind, int64_t M, int64_t N, int64_t K, const DeviceCtl& 
   const int64_t pair_tiles = ((M + tc::PAIR_TILE_M - 1) / tc::PAIR_TILE_M) *
                              ((N + tc::PAIR_TILE_N - 1) / tc::PAIR_TILE_N);
   const int64_t clusters = ctl.sm_count / 2;
-  if (2 * pair_tiles < clusters) {
-    // 3xTF32 also takes the pair kernel at a narrower planned width when
-    // those tiles fill at least 80 % of the clusters.  GB300, whole calls:
-    // 1536^3 47.8 -> 45.7 us, 2048 x 1024 x 1024 35.5 -> 33.5, 1024 x 2048 x
-    // 2048 60.1 -> 58.0 (128-column tiles); with fewer tiles (1024^3: 32 of
-    // them) the single-CTA kernel stays faster (26.3 against 33.4 us).
-    if (kind != tc::KIND_3XTF32 || ctl.pair_tile_n > 0) return false;
-    const int bn = tc::plan_pair_tile_n(M, N, K, static_cast<int>(clusters), true);
-    const int64_t tiles = ((M + tc::PAIR_TILE_M - 1) / tc::PAIR_TILE_M) * ((N + bn - 1) / bn);
-    return bn < tc::PAIR_TILE_N && 5 * tiles >= 4 * clusters;
-  }
+  if (2 * pair_tiles < clusters)  // 3xTF32: unless few_tile_pair_width finds a width
+    return kind == tc::KIND_3XTF32 && ctl.pair_tile_n == 0 &&
+           tc::few_tile_pair_width(M, N, K, static_cast<int>(clusters)) > 0;
   return kind != tc::KIND_BF16 || K >= 2048 || pair_tiles >= 2 * clusters;
 }
 
@@ -80,6 +72,27 @@ double pair_cycles_estimate(int64_t M, int64_t N, int64_t K, int clusters_max, b
   }
   const double epi_per_col = split ? (c_tma ? 20.0 : 58.0) : (c_tma ? 25.0 : 61.0);
   return rounds * tile + epi_per_col * bn;
+}
+
+// A 3xTF32 problem with too few 256 x 256 tiles for half of the clusters:
+// the widest CTA-pair tile (256, 192 or 128 columns) whose work units keep at
+// least 80 % of the clusters busy -- every tile split into two K halves when
+// twice the tiles fit on the clusters (the pair kernel does so from 32
+// K-blocks on) -- or 0, leaving the problem to the single-CTA kernel.  GB300,
+// whole calls against the single-CTA kernel: 1536^3 43.6 / 47.7 us and
+// 1024 x 2048 x 2048 52.8 / 60.0 (256 columns, 72 and 64 half-K units),
+// 1024 x 1024 x 4096 61.1 / 64.1 and 1024^3 26.2 / 26.2 (128 columns, 64
+// units); 768^3 (36 units of 128 columns) and 512 x 512 x 8192 (16) stay on
+// the single-CTA kernel.
+int few_tile_pair_width(int64_t M, int64_t N, int64_t K, int clusters) {
+  const int64_t kb = (K + 31) / 32;
+  const int64_t rows = (M + PAIR_TILE_M - 1) / PAIR_TILE_M;
+  for (const int bn : {256, 192, 128}) {
+    const int64_t tiles = rows * ((N + bn - 1) / bn);
+    const int64_t units = 2 * tiles <= clusters && kb >= 32 ? 2 * tiles : tiles;
+    if (units <= clusters && 5 * units >= 4 * static_cast<int64_t>(clusters)) return bn;
+  }
+  return 0;
 }
 
 int plan_pair_tile_n(int64_t M, int64_t N, int64_t K, int clusters, bool c_tma) {
@@ -221,8 +234,13 @@ cudaError_t launch_tc_3xtf32(const float* a_big, int64_t a_big_ld, const float* 
   // the planner would not give with TMA stores (one that is not whole
   // 32-column chunks, forced by the test hook) writes C with register stores.
   const bool pair = tc_pair_chosen(KIND_3XTF32, M, N, K, ctl);
-  const int bn = pair ? (ctl.pair_tile_n > 0 ? ctl.pair_tile_n
-                                             : plan_pair_tile_n(M, N, K, ctl.sm_count / 2, c_tma))
+  const int clusters = ctl.sm_count / 2;
+  const int few = few_tile_pair_width(M, N, K, clusters);
+  const int64_t tiles256 = ((M + PAIR_TILE_M - 1) / PAIR_TILE_M) * ((N + PAIR_TILE_N - 1) / PAIR_TILE_N);
+  const int bn = pair ? (ctl.pair_tile_n > 0                       ? ctl.pair_tile_n
+                         : 2 * tiles256 < clusters && few > 0 ? few
+                                                              : plan_pair_tile_n(M, N, K, clusters,
+                                                                                 c_tma))
                       : (ctl.single_tile_n > 0 ? ctl.single_tile_n
                                                : plan_single_tile_n(M, N, K, ctl.sm_count, c_tma));
   const bool tma_c = c_tma && bn % 32 == 0;

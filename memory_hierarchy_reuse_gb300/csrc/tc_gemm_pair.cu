@@ -655,7 +655,7 @@ cudaError_t launch_pair_t(const TcMaps& mp, const TcParams& p, bool after_prepas
   e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
   if (e != cudaSuccess) return e;
   if (max_clusters < 1) return cudaErrorInvalidConfiguration;
-  const int clusters = p.num_tiles < max_clusters ? p.num_tiles : max_clusters;
+  int clusters = p.num_tiles < max_clusters ? p.num_tiles : max_clusters;
   // A last round that would leave more than half of the clusters idle is
   // split along K: its tiles become two half-K units each, reduce-added into
   // C (zeroed first).  Two addends onto zero give the same sum in either
@@ -664,7 +664,20 @@ cudaError_t launch_pair_t(const TcMaps& mp, const TcParams& p, bool after_prepas
   q.c_even = !TMA_STORE && mp.c_even;
   q.c_odd_shift = q.c_even && !has_converters<KIND>() ? mp.c_odd_shift : -1;
   const int rem = p.num_tiles % clusters;
-  if (p.num_tiles > clusters && rem > 0 && 2 * rem <= clusters && p.num_kb >= 2) {
+  if (KIND != KIND_BF16 && 2 * p.num_tiles <= max_clusters && p.num_kb >= 32) {
+    // Few tiles (3xTF32): every tile becomes two half-K units, reduce-added
+    // into C (zeroed first), so that twice as many clusters work.  GB300,
+    // 1536^3: 60.0 -> 43.6 us per call with 256-column tiles; with fewer
+    // K-blocks the zeroing and the second add cost more than they save
+    // (1536 x 1536 x 512, 16 K-blocks: 25.2 against 23.2 us unsplit).
+    q.full_units = 0;
+    q.num_units = 2 * p.num_tiles;
+    q.kb_mid = p.num_kb / 2;
+    clusters = q.num_units;
+    if ((e = launch_zero_split_tiles(q, 2 * PairCfg<KIND>::BM, q.bn, after_prepass, s)) !=
+        cudaSuccess)
+      return e;
+  } else if (p.num_tiles > clusters && rem > 0 && 2 * rem <= clusters && p.num_kb >= 2) {
     q.full_units = p.num_tiles - rem;
     q.num_units = q.full_units + 2 * rem;
     q.kb_mid = p.num_kb / 2;
