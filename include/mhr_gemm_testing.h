@@ -43,7 +43,8 @@ int64_t gemm_testing_peek_status(void* stream);
 /*
  * Chooses the tensor-core kernel variant of the following calls
  * (process-wide): 0 = automatic (the CTA-pair kernel when its 256 x 256
- * tiles fill half of its clusters or, for 3xTF32, when tiles of 256, 192 or
+ * tiles fill half of its clusters -- for bf16 only with K >= 1536 or at
+ * least two tiles per cluster -- or, for 3xTF32, when tiles of 256, 192 or
  * 128 columns -- split into two K halves each where twice the tiles fit --
  * keep at least 80 % of them busy, else the single-CTA kernel), 1 = always the single-CTA
  * kernel, 2 = always the CTA-pair kernel.  Other values mean 0.  Returns the

@@ -14,7 +14,7 @@ bool tc_pair_chosen(int kind, int64_t M, int64_t N, int64_t K, const DeviceCtl& 
   if (2 * pair_tiles < clusters)  // 3xTF32: unless few_tile_pair_width finds a width
     return kind == tc::KIND_3XTF32 && ctl.pair_tile_n == 0 &&
            tc::few_tile_pair_width(M, N, K, static_cast<int>(clusters)) > 0;
-  return kind != tc::KIND_BF16 || K >= 2048 || pair_tiles >= 2 * clusters;
+  return kind != tc::KIND_BF16 || K >= 1536 || pair_tiles >= 2 * clusters;
 }
 
 // Small 3xTF32 problems run as one launch with the split inside the
@@ -159,15 +159,18 @@ using namespace tc;
 // 1-CTA or CTA-pair kernel.  The pair kernel moves half the shared-memory
 // bytes per FLOP; it is chosen once its 256 x 256 tiles occupy at least half
 // of the clusters, and for bf16 only when there is also enough work per tile
-// to amortise its prologue and epilogue (K >= 2048, or at least two rounds of
+// to amortise its prologue and epilogue (K >= 1536, or at least two rounds of
 // tiles).  3xTF32 needs no such margin: its 1-CTA tile, 128 x 128, reads as
 // many shared-memory bytes per clock as the MMAs consume and runs the tensor
 // pipe near 57 % busy.  GB300 measurements, 3xTF32 calls: pair faster at
 // 2048^3 (1.2x), 2048 x 2048 x 1024 (1.13x), 3000 x 2048 x 1000 (1.12x),
 // 8192 x 1024 x 1024 (1.18x); 1-CTA faster at 1536^3 with 256-column pair
 // tiles (36 of them; with the planner's 128-column ones, 72, the pair kernel
-// wins: tc_pair_chosen) and 1024 x 1024 x 4096 (16).  bf16: 1-CTA (128 x 256 tiles) faster at
-// 3000 x 2050 x 1000.  DeviceCtl::pair_mode forces one of them (tests).
+// wins: tc_pair_chosen) and 1024 x 1024 x 4096 (16).  bf16, against the 1-CTA kernel's
+// 128 x 256 tiles: pair faster at 2560 x 2560 x 1536 (27.3 / 29.3 us), 3000 x 2050 x 1536
+// (46.7 / 51.8) and 2304 x 2560 x 2000 (31.4 / 35.5), equal at 2048 x 2048 x 1536; 1-CTA
+// faster at 2048 x 2048 x 1280 (17.0 / 19.1) and 2560 x 2048 x 256 (15.0 / 19.1).
+// DeviceCtl::pair_mode forces one of them (tests).
 cudaError_t launch_tc_any(int kind, const TcMaps& maps, float* C, int64_t M, int64_t N, int64_t K,
                           int64_t ldc, bool c_tma, bool after_prepass, const DeviceCtl& ctl,
                           cudaStream_t s) {

@@ -615,6 +615,30 @@ def test_automatic_mode_narrow_pair_tiles(mhr, shape):
     assert np.array_equal(C[rows, cols], ref)
 
 
+@pytest.mark.parametrize("shape", [(2304, 2304, 1536), (2048, 2048, 1280), (1024, 2048, 2048),
+                                   (1024, 1024, 2048), (3000, 2050, 1000)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_automatic_mode_bf16(mhr, shape):
+    """bf16 takes the CTA-pair kernel when its 256 x 256 tiles fill half of
+    the clusters and there is enough work per tile: K >= 1536 or at least two
+    tiles per cluster; otherwise the single-CTA kernel's 128 x 256 tiles.
+    Integer inputs bit-exact against the oracle on sampled entries."""
+    import torch
+
+    M, N, K = shape
+    clusters = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    A, B, Ab, Bb = operands(M, N, K, 4211 + K, "int", "bf16")
+    C = DeviceCall("bf16", A, B, Ab, Bb).run(mhr).result()
+    label = mhr.gemm_testing_last_main_kernel()
+    tiles = -(-M // 256) * -(-N // 256)
+    pair = 2 * tiles >= clusters and (K >= 1536 or tiles >= 2 * clusters)
+    want = "tc_gemm_pair_kernel<bf16" if pair else "tc_gemm_kernel<bf16"
+    assert label.startswith(want), (label, want)
+    rows, cols = sample_indices(M, N, 4211, rows=(0, M // 2 + 1, M - 1), cols=(0, N - 1))
+    ref = oracle.gemm_entries(A, B, rows, cols, M, N, K)[0]
+    assert np.array_equal(C[rows, cols], ref)
+
+
 @pytest.mark.usefixtures("full_width_tiles")
 def test_workspace_fallback_splits_in_kernel(mhr):
     """Operands one element off 16-byte alignment cannot be their own big
