@@ -159,6 +159,28 @@ int gemm_testing_set_single_tile_n(int columns);
  */
 int gemm_testing_plan_single_tile_n(int64_t M, int64_t N, int64_t K, int sms, int c_tma);
 
+/*
+ * Chooses between gemm_f32's two SIMT kernels for the following calls
+ * (process-wide), where A, B and C are 16-byte aligned with leading
+ * dimensions multiples of 4 and M, N, K multiples of 128, 256 and 8:
+ * 0 = automatic (gemm_testing_plan_simt_wide), 1 = always the 128 x 128
+ * kernel, 2 = always the 128 x 256 kernel (on two K halves when that
+ * shortens its queue of blocks).  Other values mean 0.  Other problems take
+ * the 128 x 128 kernel whatever the mode.  Returns the previous mode.
+ */
+int gemm_testing_set_simt_wide_mode(int mode);
+
+/*
+ * The automatic choice for such a problem on `sms` SMs: 0 = the 128 x 128
+ * kernel, 1 = the 128 x 256 kernel, 2 = the 128 x 256 kernel on two K halves
+ * added into a zeroed C; 0 too for sizes that are not multiples of
+ * 128 x 256 x 8.  Host arithmetic only.  The estimate: a kernel's time
+ * follows the deepest queue of blocks on one SM, and a 128 x 256 block takes
+ * 11/6 of a 128 x 128 block's time (register tiling, "矩阵乘法 tiling",
+ * section 五: the wider block reuses each A value twice as often).
+ */
+int gemm_testing_plan_simt_wide(int64_t M, int64_t N, int64_t K, int sms);
+
 #ifdef __cplusplus
 }
 #endif

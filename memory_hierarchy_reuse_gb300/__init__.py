@@ -50,7 +50,8 @@ EXPORTS = ("gemm_f32", "gemm_f32_3xtf32", "gemm_bf16_f32acc", "gemm_f32_3xtf32_n
            "gemm_testing_last_launches", "gemm_testing_set_workspace_limit",
            "gemm_testing_set_zero_a_small", "gemm_testing_set_pair_tile_n",
            "gemm_testing_plan_pair_tile_n", "gemm_testing_set_single_tile_n",
-           "gemm_testing_plan_single_tile_n")
+           "gemm_testing_plan_single_tile_n", "gemm_testing_set_simt_wide_mode",
+           "gemm_testing_plan_simt_wide")
 
 _lib = None
 
@@ -109,6 +110,10 @@ def load(path: str | None = None):
     lib.gemm_testing_set_single_tile_n.restype = ctypes.c_int
     lib.gemm_testing_plan_single_tile_n.argtypes = [i64, i64, i64, ctypes.c_int, ctypes.c_int]
     lib.gemm_testing_plan_single_tile_n.restype = ctypes.c_int
+    lib.gemm_testing_set_simt_wide_mode.argtypes = [ctypes.c_int]
+    lib.gemm_testing_set_simt_wide_mode.restype = ctypes.c_int
+    lib.gemm_testing_plan_simt_wide.argtypes = [i64, i64, i64, ctypes.c_int]
+    lib.gemm_testing_plan_simt_wide.restype = ctypes.c_int
     lib.gemm_testing_set_split_mode.argtypes = [ctypes.c_int]
     lib.gemm_testing_set_split_mode.restype = ctypes.c_int
     lib.gemm_testing_set_workspace_limit.argtypes = [ctypes.c_uint64]
@@ -284,3 +289,15 @@ def gemm_testing_set_single_tile_n(columns: int) -> int:
 def gemm_testing_plan_single_tile_n(M: int, N: int, K: int, sms: int, c_tma: bool) -> int:
     """The 3xTF32 single-CTA tile columns the planner picks (host logic only)."""
     return load().gemm_testing_plan_single_tile_n(M, N, K, int(sms), int(bool(c_tma)))
+
+
+def gemm_testing_set_simt_wide_mode(mode: int) -> int:
+    """Choose gemm_f32's SIMT kernel for aligned 128 x 256 x 8 multiples: 0
+    automatic, 1 the 128 x 128 kernel, 2 the 128 x 256 kernel (test hook)."""
+    return load().gemm_testing_set_simt_wide_mode(int(mode))
+
+
+def gemm_testing_plan_simt_wide(M: int, N: int, K: int, sms: int) -> int:
+    """The automatic SIMT kernel choice: 0 128 x 128, 1 128 x 256, 2 128 x 256
+    on K halves (host logic only)."""
+    return load().gemm_testing_plan_simt_wide(M, N, K, int(sms))

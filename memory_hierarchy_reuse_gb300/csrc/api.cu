@@ -68,6 +68,7 @@ int g_raster_group = 0;
 int g_split_mode = 0;
 int g_pair_tile_n = 0;
 int g_single_tile_n = 0;
+int g_simt_wide_mode = 0;
 uint64_t g_workspace_limit = UINT64_MAX;
 int g_zero_a_small = 0;
 cudaEvent_t g_main_start = nullptr, g_main_stop = nullptr;
@@ -338,7 +339,7 @@ MHR_API int gemm_f32(const float* A, const float* B, float* C, int64_t M, int64_
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (K == 0) return from_cuda(launch_zero_fill(C, M, N, ldc, s));
   MainKernelEvents ev(s);
-  return from_cuda(launch_simt_f32(A, B, C, M, N, K, lda, ldb, ldc, s));
+  return from_cuda(launch_simt_f32(A, B, C, M, N, K, lda, ldb, ldc, g_simt_wide_mode, s));
 }
 
 MHR_API int gemm_f32_ladder(int rung, const float* A, const float* B, float* C, int64_t M,
@@ -567,6 +568,17 @@ MHR_API int gemm_testing_set_single_tile_n(int columns) {
   const int old = g_single_tile_n;
   g_single_tile_n = (columns == 32 || columns == 64 || columns == 96 || columns == 128) ? columns : 0;
   return old;
+}
+
+MHR_API int gemm_testing_set_simt_wide_mode(int mode) {
+  std::lock_guard<std::mutex> g(g_mu);
+  const int old = g_simt_wide_mode;
+  g_simt_wide_mode = (mode == 1 || mode == 2) ? mode : 0;
+  return old;
+}
+
+MHR_API int gemm_testing_plan_simt_wide(int64_t M, int64_t N, int64_t K, int sms) {
+  return simt_wide_plan(M, N, K, sms, 0);
 }
 
 MHR_API int gemm_testing_plan_single_tile_n(int64_t M, int64_t N, int64_t K, int sms, int c_tma) {

@@ -23,8 +23,15 @@ struct DeviceCtl {
   int single_tile_n = 0;               // 3xTF32 single-CTA tile columns, 0 = planned (test hook)
 };
 
+// wide_mode: 0 automatic, 1 never the 128 x 256 kernel, 2 that kernel
+// whenever the sizes allow (see simt_wide_plan).
 cudaError_t launch_simt_f32(const float* A, const float* B, float* C, int64_t M, int64_t N,
-                            int64_t K, int64_t lda, int64_t ldb, int64_t ldc, cudaStream_t s);
+                            int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int wide_mode,
+                            cudaStream_t s);
+// The SIMT kernel an M x N x K problem with 16-byte aligned operands takes on
+// `sms` SMs: 0 the 128 x 128 kernel, 1 the 128 x 256 kernel, 2 that kernel on
+// two K halves (host arithmetic only).
+int simt_wide_plan(int64_t M, int64_t N, int64_t K, int sms, int wide_mode);
 
 // The pages' ladder: rung 0 = one thread per output, 1 = 16 x 16 shared tiles,
 // 2 = 32 x 32 shared tiles.  Requires ceil(M / T) <= 65535.

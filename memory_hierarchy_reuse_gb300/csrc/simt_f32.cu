@@ -111,7 +111,12 @@ __device__ __forceinline__ float2 unpack2(uint64_t v) {
 // partial tiles, in rank order, and stores them.  One fixed order per
 // element: bit-reproducible, with no atomics and no zeroing of C.  Used when
 // the tiles alone would leave most SMs idle.
-template <bool VA, bool VB, bool VC, bool CLUSTER>
+//
+// WB, WC: the widest loads of B and stores of C that their alignment allows,
+// in floats (4: 16-byte aligned with a leading dimension a multiple of 4; 2:
+// 8-byte aligned with an even one; 1).  A column group of 4 starts at a
+// multiple of 4 from the tile's first column, so either width divides it.
+template <bool VA, int WB, int WC, bool CLUSTER>
 __global__ void __launch_bounds__(NT, 2)
     simt_f32_kernel(const float* __restrict__ A, const float* __restrict__ B,
                     float* __restrict__ C, int64_t M, int64_t N, int64_t K, int64_t lda,
@@ -177,9 +182,13 @@ __global__ void __launch_bounds__(NT, 2)
     }
     const int64_t kb = k0 + b_k;
     const float* bp = b_ptr + k0 * ldb;
-    if (VB && kb < K && b_col_g + 4 <= N) {
+    if (WB == 4 && kb < K && b_col_g + 4 <= N) {
       const float4 v = __ldg(reinterpret_cast<const float4*>(bp));
       rb[0] = v.x; rb[1] = v.y; rb[2] = v.z; rb[3] = v.w;
+    } else if (WB == 2 && kb < K && b_col_g + 4 <= N) {
+      const float2 v0 = __ldg(reinterpret_cast<const float2*>(bp));
+      const float2 v1 = __ldg(reinterpret_cast<const float2*>(bp + 2));
+      rb[0] = v0.x; rb[1] = v0.y; rb[2] = v1.x; rb[3] = v1.y;
     } else {
 #pragma unroll
       for (int i = 0; i < 4; ++i) rb[i] = (kb < K && b_col_g + i < N) ? __ldg(bp + i) : 0.f;
@@ -261,8 +270,11 @@ __global__ void __launch_bounds__(NT, 2)
       const int64_t row = m0 + r, col = n0 + c;
       if (row >= M) continue;
       float* crow = C + row * ldc;
-      if (VC && col + 4 <= N) {
+      if (WC == 4 && col + 4 <= N) {
         *reinterpret_cast<float4*>(crow + col) = v;
+      } else if (WC == 2 && col + 4 <= N) {
+        *reinterpret_cast<float2*>(crow + col) = make_float2(v.x, v.y);
+        *reinterpret_cast<float2*>(crow + col + 2) = make_float2(v.z, v.w);
       } else {
         const float w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -282,11 +294,20 @@ __global__ void __launch_bounds__(NT, 2)
         const int64_t col = n0 + h * 64 + tx * 4;
         const float4 v =
             make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2], acc[i][4 * h + 3]);
-        if (VC && col + 4 <= N) {
+        if (WC == 4 && col + 4 <= N) {
           if (k_mid > 0)
             atomicAdd(reinterpret_cast<float4*>(crow + col), v);
           else
             *reinterpret_cast<float4*>(crow + col) = v;
+        } else if (WC == 2 && col + 4 <= N) {
+          const float2 lo = make_float2(v.x, v.y), hi = make_float2(v.z, v.w);
+          if (k_mid > 0) {
+            atomicAdd(reinterpret_cast<float2*>(crow + col), lo);
+            atomicAdd(reinterpret_cast<float2*>(crow + col + 2), hi);
+          } else {
+            *reinterpret_cast<float2*>(crow + col) = lo;
+            *reinterpret_cast<float2*>(crow + col + 2) = hi;
+          }
         } else {
           const float w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -305,9 +326,10 @@ __global__ void __launch_bounds__(NT, 2)
 
 // ------------------------------------------------------------------ wide tiles
 //
-// Problems whose sizes are multiples of a 128 x 256 x 8 tile, with at least
-// half as many such tiles as SMs and every operand 16-byte aligned (leading
-// dimensions multiples of 4), take a wider tile: one block of 256 threads per SM, each thread an 8 x 16 register
+// Problems whose sizes are multiples of a 128 x 256 x 8 tile, with every
+// operand 16-byte aligned (leading dimensions multiples of 4), can take a
+// wider tile (simt_wide_plan decides, at the end of this file): one block of
+// 256 threads per SM, each thread an 8 x 16 register
 // block (rows {4ty..4ty+3, 64+4ty..64+4ty+3}, columns {64h+4tx..64h+4tx+3 :
 // h = 0..3}).  Every A value read from shared memory then feeds 16 FMAs and
 // every B value 8, so a k step issues 64 packed FMAs against 14 other
@@ -422,21 +444,24 @@ __global__ void zero_rows_v4_kernel(float* C, int64_t M, int64_t N, int64_t ldc)
     *reinterpret_cast<float4*>(C + (i / n4) * ldc + 4 * (i % n4)) = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-// Wide-tile launch, when the problem qualifies (see above); returns false
-// (launching nothing) when it does not.
+// Whether splitting every one of `blocks` tiles into two K halves shortens
+// the deepest queue of blocks on one SM by more than 7 % (see launch_t); each
+// half keeps at least 64 K steps.
+bool halves_pay(int64_t blocks, int64_t K, int sms) {
+  const int64_t whole = (blocks + sms - 1) / sms;
+  const int64_t halves = (2 * blocks + sms - 1) / sms;
+  return K >= 2 * 64 * BK && blocks < (int64_t{1} << 30) && halves < 2 * whole * 0.93;
+}
+
+// Wide-tile launch, when simt_wide_plan picks it; returns false (launching
+// nothing) when it does not.
 bool launch_wide(const float* A, const float* B, float* C, int64_t M, int64_t N, int64_t K,
-                 int64_t lda, int64_t ldb, int64_t ldc, int sms, cudaStream_t s,
+                 int64_t lda, int64_t ldb, int64_t ldc, int sms, int wide_mode, cudaStream_t s,
                  cudaError_t* err) {
-  if (M % BM || N % WBN || K % BK) return false;
+  const int plan = simt_wide_plan(M, N, K, sms, wide_mode);
+  if (plan == 0) return false;
   const int64_t tiles_m = M / BM, tiles_n = N / WBN, tiles = tiles_m * tiles_n;
-  // at least half a wave of tiles: at 2048^3 (128 tiles on 152 SMs) 316 us
-  // against 363 for the 128 x 128 kernel's 256 tiles two to an SM
-  if (2 * tiles < sms || tiles >= (int64_t{1} << 30)) return false;
-  // K halves when they shorten the busiest SM's queue (see launch_t)
-  const int64_t whole = (tiles + sms - 1) / sms;
-  const int64_t halves = (2 * tiles + sms - 1) / sms;
-  int64_t k_mid = 0;
-  if (K >= 2 * 64 * BK && halves < 2 * whole * 0.93) k_mid = (K / 2 + BK - 1) / BK * BK;
+  const int64_t k_mid = plan == 2 ? (K / 2 + BK - 1) / BK * BK : 0;
   if (k_mid > 0) {
     note_launch();
     zero_rows_v4_kernel<<<static_cast<unsigned>(4 * sms), 256, 0, s>>>(C, M, N, ldc);
@@ -451,9 +476,9 @@ bool launch_wide(const float* A, const float* B, float* C, int64_t M, int64_t N,
   return true;
 }
 
-template <bool VA, bool VB, bool VC>
+template <bool VA, int WB, int WC>
 cudaError_t launch_t(const float* A, const float* B, float* C, int64_t M, int64_t N, int64_t K,
-                     int64_t lda, int64_t ldb, int64_t ldc, cudaStream_t s) {
+                     int64_t lda, int64_t ldb, int64_t ldc, int wide_mode, cudaStream_t s) {
   const int64_t tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
   const int64_t tiles = tiles_m * tiles_n;
   // Split every tile along K when that shortens the busiest SM's queue.  On
@@ -469,7 +494,8 @@ cudaError_t launch_t(const float* A, const float* B, float* C, int64_t M, int64_
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cudaError_t e;
-  if (VA && VB && VC && launch_wide(A, B, C, M, N, K, lda, ldb, ldc, sms, s, &e)) return e;
+  if (VA && WB == 4 && WC == 4 && launch_wide(A, B, C, M, N, K, lda, ldb, ldc, sms, wide_mode, s, &e))
+    return e;
   // Few tiles (at most half as many as SMs): a cluster of S CTAs per tile,
   // the largest S in {8, 4, 2} that keeps one CTA per SM and at least two
   // K-steps per rank.
@@ -482,7 +508,7 @@ cudaError_t launch_t(const float* A, const float* B, float* C, int64_t M, int64_
         break;
       }
   if (cs > 1) {
-    auto kern = simt_f32_kernel<VA, VB, VC, true>;
+    auto kern = simt_f32_kernel<VA, WB, WC, true>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   RED_BYTES)) != cudaSuccess)
       return e;
@@ -505,41 +531,80 @@ cudaError_t launch_t(const float* A, const float* B, float* C, int64_t M, int64_
       return e;
     return cudaGetLastError();
   }
-  const int64_t whole = (tiles + sms - 1) / sms;
-  const int64_t halves = (2 * tiles + sms - 1) / sms;  // in half-block times
-  int64_t k_mid = 0;
-  if (K >= 2 * 64 * BK && tiles < (int64_t{1} << 30) && halves < 2 * whole * 0.93)
-    k_mid = (K / 2 + BK - 1) / BK * BK;
+  const int64_t k_mid = halves_pay(tiles, K, sms) ? (K / 2 + BK - 1) / BK * BK : 0;
   if (k_mid > 0 && (e = launch_zero_fill(C, M, N, ldc, s)) != cudaSuccess) return e;
   const int64_t blocks = k_mid > 0 ? 2 * tiles : tiles;
   note_main_kernel(k_mid > 0 ? "simt_f32_kernel<split-K>" : "simt_f32_kernel",
                    static_cast<int>(blocks), static_cast<int>(tiles));
-  simt_f32_kernel<VA, VB, VC, false><<<static_cast<unsigned>(blocks), NT, 0, s>>>(
+  simt_f32_kernel<VA, WB, WC, false><<<static_cast<unsigned>(blocks), NT, 0, s>>>(
       A, B, C, M, N, K, lda, ldb, ldc, tiles_m, tiles_n, k_mid);
   return cudaGetLastError();
 }
 
-inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// The widest access, in floats (4, 2 or 1), that every row of a matrix at `p`
+// with leading dimension `ld` allows.
+inline int vec_width(const void* p, int64_t ld) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  if ((a & 15u) == 0 && ld % 4 == 0) return 4;
+  if ((a & 7u) == 0 && ld % 2 == 0) return 2;
+  return 1;
+}
+
+template <bool VA, int WB>
+cudaError_t launch_wc(const float* A, const float* B, float* C, int64_t M, int64_t N, int64_t K,
+                      int64_t lda, int64_t ldb, int64_t ldc, int wc, int wide_mode,
+                      cudaStream_t s) {
+  switch (wc) {
+    case 4: return launch_t<VA, WB, 4>(A, B, C, M, N, K, lda, ldb, ldc, wide_mode, s);
+    case 2: return launch_t<VA, WB, 2>(A, B, C, M, N, K, lda, ldb, ldc, wide_mode, s);
+    default: return launch_t<VA, WB, 1>(A, B, C, M, N, K, lda, ldb, ldc, wide_mode, s);
+  }
+}
+
+template <bool VA>
+cudaError_t launch_wb(const float* A, const float* B, float* C, int64_t M, int64_t N, int64_t K,
+                      int64_t lda, int64_t ldb, int64_t ldc, int wb, int wc, int wide_mode,
+                      cudaStream_t s) {
+  switch (wb) {
+    case 4: return launch_wc<VA, 4>(A, B, C, M, N, K, lda, ldb, ldc, wc, wide_mode, s);
+    case 2: return launch_wc<VA, 2>(A, B, C, M, N, K, lda, ldb, ldc, wc, wide_mode, s);
+    default: return launch_wc<VA, 1>(A, B, C, M, N, K, lda, ldb, ldc, wc, wide_mode, s);
+  }
+}
 
 }  // namespace
 
+// The estimate behind the wide kernel's choice: the time of either kernel
+// follows the deepest queue of blocks on one SM, ceil(blocks / SMs) block
+// times (half block times with K halves), and a 128 x 256 block takes 11/6 of
+// a 128 x 128 block's time.  GB300, one kernel against the other on the same
+// shape: 4096^3 3.5 wide block times, 2188 us, against 7 narrow ones,
+// 2406 us (ratio 1.82); 2048^3 1.74; 4096 x 4096 x 1024 1.88; 8192^3 1.83.
+int simt_wide_plan(int64_t M, int64_t N, int64_t K, int sms, int wide_mode) {
+  if (wide_mode == 1 || sms < 1 || M % BM || N % WBN || K % BK) return 0;
+  const int64_t tiles = (M / BM) * (N / WBN);
+  if (tiles >= (int64_t{1} << 30)) return 0;
+  const bool split = halves_pay(tiles, K, sms);
+  if (wide_mode != 2) {
+    // fewer wide tiles than half the SMs: the 128 x 128 kernel spreads wider
+    if (2 * tiles < sms) return 0;
+    const int64_t wide_q = split ? (2 * tiles + sms - 1) / sms : 2 * ((tiles + sms - 1) / sms);
+    const int64_t narrow = 2 * tiles;
+    const int64_t narrow_q = halves_pay(narrow, K, sms) ? (2 * narrow + sms - 1) / sms
+                                                        : 2 * ((narrow + sms - 1) / sms);
+    if (11 * wide_q >= 6 * narrow_q) return 0;
+  }
+  return split ? 2 : 1;
+}
+
 // Requires M, N, K >= 1 and ceil(M/128) * ceil(N/128) < 2^31.  Validation is the caller's.
 cudaError_t launch_simt_f32(const float* A, const float* B, float* C, int64_t M, int64_t N,
-                            int64_t K, int64_t lda, int64_t ldb, int64_t ldc, cudaStream_t s) {
-  const bool va = aligned16(A) && (lda % 4) == 0;
-  const bool vb = aligned16(B) && (ldb % 4) == 0;
-  const bool vc = aligned16(C) && (ldc % 4) == 0;
-  const int key = (va ? 4 : 0) | (vb ? 2 : 0) | (vc ? 1 : 0);
-  switch (key) {
-    case 7: return launch_t<true, true, true>(A, B, C, M, N, K, lda, ldb, ldc, s);
-    case 6: return launch_t<true, true, false>(A, B, C, M, N, K, lda, ldb, ldc, s);
-    case 5: return launch_t<true, false, true>(A, B, C, M, N, K, lda, ldb, ldc, s);
-    case 4: return launch_t<true, false, false>(A, B, C, M, N, K, lda, ldb, ldc, s);
-    case 3: return launch_t<false, true, true>(A, B, C, M, N, K, lda, ldb, ldc, s);
-    case 2: return launch_t<false, true, false>(A, B, C, M, N, K, lda, ldb, ldc, s);
-    case 1: return launch_t<false, false, true>(A, B, C, M, N, K, lda, ldb, ldc, s);
-    default: return launch_t<false, false, false>(A, B, C, M, N, K, lda, ldb, ldc, s);
-  }
+                            int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int wide_mode,
+                            cudaStream_t s) {
+  const int wb = vec_width(B, ldb), wc = vec_width(C, ldc);
+  return vec_width(A, lda) == 4
+             ? launch_wb<true>(A, B, C, M, N, K, lda, ldb, ldc, wb, wc, wide_mode, s)
+             : launch_wb<false>(A, B, C, M, N, K, lda, ldb, ldc, wb, wc, wide_mode, s);
 }
 
 }  // namespace mhr

@@ -19,7 +19,8 @@ from parity_util import TOL, DeviceCall, normalised_error, operands
 
 pytestmark = pytest.mark.gpu
 
-# (path, CTA-pair mode, split mode)
+# (path, CTA-pair mode -- for f32 the SIMT kernel mode of gemm_testing_set_simt_wide_mode --,
+#  split mode)
 VARIANTS = [("f32", 0, 0), ("3xtf32", 0, 0), ("3xtf32", 1, 1), ("3xtf32", 1, 2), ("3xtf32", 2, 1),
             ("3xtf32", 2, 2), ("bf16", 1, 0), ("bf16", 2, 0)]
 
@@ -55,7 +56,8 @@ def edge_cases(n=60, seed=20261203):
 def schedule_cases(n=24, seed=20261204):
     """Shapes drawn to land on the schedules that split or widen tiles:
     aligned 128 x 256 x 8 multiples with 76-120 such tiles (the wide SIMT
-    kernel), few single-CTA tiles with long K (clusters of 4 or 8 CTAs summing
+    kernel, forced in every other such case, else the automatic choice
+    between it and the 128 x 128 kernel), few single-CTA tiles with long K (clusters of 4 or 8 CTAs summing
     through distributed shared memory, 3xTF32 and bf16), and few SIMT tiles
     (clusters of 2-8). Alignment-preserving pads for the wide kernel; any
     pads and offsets otherwise."""
@@ -71,7 +73,7 @@ def schedule_cases(n=24, seed=20261204):
                     break
             M, N, K = 128 * a, 256 * b, 8 * int(rng.integers(1, 34))
             pads = [4 * int(x) for x in rng.integers(0, 3, 3)]
-            out.append((("f32", 0, 0), M, N, K, pads, 0, dist, 9500 + i))
+            out.append((("f32", 2 if i % 8 == 0 else 0, 0), M, N, K, pads, 0, dist, 9500 + i))
             continue
         M, N = (int(x) for x in rng.integers(1, 401, 2))
         K = {1: int(rng.integers(2048, 4501)), 2: int(rng.integers(4096, 8401)),
@@ -128,7 +130,9 @@ def auto_small_cases(n=24, seed=20261206):
 def test_random_case(mhr, case):
     (path, pair_mode, split_mode), M, N, K, pads, offset, dist, seed = case
     A, B, Ab, Bb = operands(M, N, K, seed, dist, path)
-    old_pair = mhr.gemm_testing_set_cta_pair_mode(pair_mode)
+    simt = path == "f32"
+    old_pair = mhr.gemm_testing_set_cta_pair_mode(0 if simt else pair_mode)
+    old_wide = mhr.gemm_testing_set_simt_wide_mode(pair_mode if simt else 0)
     old_split = mhr.gemm_testing_set_split_mode(split_mode)
     try:
         C = DeviceCall(path, A, B, Ab, Bb, lda=K + pads[0], ldb=N + pads[1], ldc=N + pads[2],
@@ -136,10 +140,13 @@ def test_random_case(mhr, case):
         label = mhr.gemm_testing_last_main_kernel()
     finally:
         mhr.gemm_testing_set_split_mode(old_split)
+        mhr.gemm_testing_set_simt_wide_mode(old_wide)
         mhr.gemm_testing_set_cta_pair_mode(old_pair)
     small_aligned = (offset == 0 and (K + pads[0]) % 4 == 0 and M * N <= 1 << 18 and K <= 2048)
     if path == "3xtf32" and (pair_mode, split_mode) == (0, 0) and small_aligned:
         assert label.startswith("tc_gemm_kernel<3xtf32,split,tma-a"), (case, label)
+    if simt and pair_mode == 2 and offset == 0 and all(p % 4 == 0 for p in pads):
+        assert label.startswith("simt_f32_kernel<wide"), (case, label)
     if dist == "int":
         assert np.array_equal(C, oracle.gemm(A, B)), case
     else:

@@ -685,36 +685,74 @@ def test_simt_split_k(mhr):
     assert np.array_equal(call.run(mhr).result(), C)
 
 
-@pytest.mark.parametrize("shape,label", [
-    ((2048, 2560, 1032), "simt_f32_kernel<wide,split-K> grid=320 "),
-    ((2048, 4864, 64), "simt_f32_kernel<wide> grid=304 "),
-    ((2048, 4864 + 4, 64), "simt_f32_kernel grid="),
-    ((2048, 2560, 1032), "simt_f32_kernel<wide,split-K> grid=320 "),
-    ((2048, 2048, 512), "simt_f32_kernel<wide> grid=128 "),
-    ((1024, 2048, 512), "simt_f32_kernel grid=")],
-    ids=["160-tiles-split", "304-tiles", "ragged-n-standard", "160-tiles-padded-ld",
-         "128-tiles", "64-tiles-standard"])
-def test_simt_wide_tiles(mhr, shape, label, request):
-    """Aligned problems whose sizes are multiples of 128 x 256 x 8 and that
-    fill the SMs take the wide-tile SIMT kernel (8 x 16 outputs per thread,
-    no masks) when they have at least half as many such tiles as SMs: 160
-    tiles with K halves added into a zeroed C (K = 1032), 304 and 128 tiles
-    unsplit; N one vector wider, or 64 tiles, leave the shape to the masked
-    kernel.
-    The last case pads every leading dimension by a multiple of 4 with NaN in
-    the pads: a read outside the logical matrices poisons C, a write outside
+@pytest.mark.parametrize("shape,mode,label", [
+    ((2048, 2560, 1032), 2, "simt_f32_kernel<wide,split-K> grid=320 "),
+    ((2048, 2560, 1032), 0, "simt_f32_kernel<split-K> grid=640 "),
+    ((2048, 4864, 64), 0, "simt_f32_kernel<wide> grid=304 "),
+    ((2048, 4864 + 4, 64), 2, "simt_f32_kernel grid="),
+    ((2048, 2560, 1032), 2, "simt_f32_kernel<wide,split-K> grid=320 "),
+    ((2048, 2048, 512), 0, "simt_f32_kernel<wide> grid=128 "),
+    ((512, 4864, 1024), 0, "simt_f32_kernel<wide,split-K> grid=152 "),
+    ((2048, 2560, 1000), 0, "simt_f32_kernel grid=320 "),
+    ((2048, 2560, 1000), 2, "simt_f32_kernel<wide> grid=160 "),
+    ((1024, 2048, 512), 0, "simt_f32_kernel grid=")],
+    ids=["160-tiles-split-forced", "160-tiles-auto", "304-tiles", "ragged-n-standard",
+         "160-tiles-padded-ld", "128-tiles", "76-tiles-split", "k1000-auto", "k1000-forced",
+         "64-tiles-standard"])
+def test_simt_wide_tiles(mhr, shape, mode, label, request):
+    """Aligned problems whose sizes are multiples of 128 x 256 x 8 can take
+    the wide-tile SIMT kernel (8 x 16 outputs per thread, no masks), alone or
+    on K halves added into a zeroed C. The automatic choice takes it when its
+    queue of blocks per SM, at 11/6 of a 128 x 128 block's time per block, is
+    the shorter: 128 and 304 tiles unsplit, 76 tiles on K halves; 160 tiles
+    (two rounds) stay on the 128 x 128 kernel, split along K at K = 1032 and
+    whole at K = 1000. Mode 2 forces the wide kernel; N one vector wider, or
+    64 tiles, leave the shape to the masked kernel.
+    The padded case pads every leading dimension by a multiple of 4 with NaN
+    in the pads: a read outside the logical matrices poisons C, a write outside
     C breaks its guard band. Integer inputs bit-exact against the oracle,
     real inputs within tolerance and bitwise repeatable."""
     M, N, K = shape
     lds = {}
     if request.node.callspec.id.endswith("padded-ld"):
         lds = dict(lda=K + 4, ldb=N + 8, ldc=N + 4)
-    A, B, _, _ = operands(M, N, K, 3601 + K, "int", "f32")
-    C = DeviceCall("f32", A, B, **lds).run(mhr).result()
-    assert mhr.gemm_testing_last_main_kernel().startswith(label)
+    old = mhr.gemm_testing_set_simt_wide_mode(mode)
+    try:
+        A, B, _, _ = operands(M, N, K, 3601 + K, "int", "f32")
+        C = DeviceCall("f32", A, B, **lds).run(mhr).result()
+        assert mhr.gemm_testing_last_main_kernel().startswith(label)
+        assert np.array_equal(C, oracle.gemm(A, B))
+        A, B, _, _ = operands(M, N, K, 3602 + K, "normal", "f32")
+        call = DeviceCall("f32", A, B, **lds)
+        C = call.run(mhr).result()
+        Cref, S = oracle.gemm(A, B, with_abs=True)
+        assert normalised_error(C, Cref, S) <= TOL["f32"]
+        assert np.array_equal(call.run(mhr).result(), C)
+    finally:
+        mhr.gemm_testing_set_simt_wide_mode(old)
+
+
+@pytest.mark.parametrize("shape,ldb,ldc,offset", [
+    ((300, 522, 200), 522, 522, 0),      # B and C 8 bytes wide, A 16; ragged last group
+    ((300, 522, 200), 522, 522, 2),      # every operand 8-byte aligned only
+    ((300, 520, 200), 522, 521, 0),      # B 8 bytes wide, C scalar
+    ((300, 520, 200), 521, 522, 0),      # B scalar, C 8 bytes wide
+    ((1280, 2050, 1024), 2050, 2050, 0),  # K halves: 8-byte atomic adds into C
+    ((256, 258, 512), 258, 258, 0)],     # a cluster per tile, 8-byte stores of the sums
+    ids=["b2c2", "all8", "b2c1", "b1c2", "b2c2-split", "b2c2-cluster"])
+def test_simt_eight_byte_rows(mhr, shape, ldb, ldc, offset):
+    """Leading dimensions that are even but not multiples of 4 (C3's 2050),
+    or operands 8 bytes off 16-byte alignment, give the SIMT kernel 8-byte
+    loads of B and stores of C; odd ones scalar. Integer inputs bit-exact
+    against the oracle, real inputs within tolerance and bitwise repeatable;
+    the guard band of C's padding stays untouched."""
+    M, N, K = shape
+    A, B, _, _ = operands(M, N, K, 3701 + K, "int", "f32")
+    C = DeviceCall("f32", A, B, ldb=ldb, ldc=ldc, offset=offset).run(mhr).result()
+    assert mhr.gemm_testing_last_main_kernel().startswith("simt_f32_kernel")
     assert np.array_equal(C, oracle.gemm(A, B))
-    A, B, _, _ = operands(M, N, K, 3602 + K, "normal", "f32")
-    call = DeviceCall("f32", A, B, **lds)
+    A, B, _, _ = operands(M, N, K, 3702 + K, "normal", "f32")
+    call = DeviceCall("f32", A, B, ldb=ldb, ldc=ldc, offset=offset)
     C = call.run(mhr).result()
     Cref, S = oracle.gemm(A, B, with_abs=True)
     assert normalised_error(C, Cref, S) <= TOL["f32"]

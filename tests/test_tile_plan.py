@@ -1,7 +1,8 @@
-"""The tile-width planners of the 3xTF32 kernels (host arithmetic in
-libmhr_gemm.so, no GPU needed): which width they pick for the listed
-workloads on GB300 (152 SMs, 76 co-resident CTA pairs), and that every pick
-is a width the kernel supports."""
+"""The tile-width planners of the 3xTF32 kernels and the choice between the
+two SIMT fp32 kernels (host arithmetic in libmhr_gemm.so, no GPU needed):
+which width or kernel they pick for the listed workloads and for shapes
+measured on GB300 (152 SMs, 76 co-resident CTA pairs), and that every pick
+is one the kernels support."""
 import numpy as np
 import pytest
 
@@ -74,3 +75,44 @@ def test_single_cta_planned_width_is_supported(lib):
             bn = mhr.gemm_testing_plan_single_tile_n(M, N, K, sms, c_tma)
             assert bn in (32, 64, 96, 128), (M, N, K, sms, bn)
     assert mhr.gemm_testing_plan_single_tile_n(256, 256, 256, 0, True) == 128
+
+
+@pytest.mark.parametrize("shape,want", [
+    # GB300, whole calls, the 128 x 128 kernel against the 128 x 256 one:
+    ((4096, 4096, 4096), 2),   # 2407 / 2195 us
+    ((4096, 4096, 1024), 2),   # 613 / 578
+    ((2048, 2048, 2048), 1),   # 363 / 318
+    ((3072, 3072, 1000), 1),   # 347 / 314
+    ((3584, 2304, 512), 1),    # 185 / 167
+    ((8192, 8192, 8192), 1),
+    ((3072, 2048, 1000), 0),   # 265 / 310: 192 wide tiles, two rounds, K too short for halves
+    ((2560, 2560, 1000), 0),   # 265 / 314
+    ((2048, 2560, 2048), 0),   # 462 / 483
+    ((2048, 2560, 1032), 0),   # 245 / 254
+    ((1024, 2048, 512), 0),    # 64 wide tiles: fewer than half the SMs
+    ((3000, 2048, 1000), 0),   # not a multiple of 128 rows
+    ((2048, 2050, 1000), 0),
+    ((2048, 2048, 1001), 0),
+])
+def test_simt_wide_plan(lib, shape, want):
+    assert mhr.gemm_testing_plan_simt_wide(*shape, SMS) == want
+
+
+def test_simt_wide_plan_is_a_queue_model(lib):
+    """Whatever the shape and SM count, the wide kernel is chosen only where
+    its sizes allow it and its tiles fill at least half of the SMs, with K
+    halves only where each half keeps at least 64 steps of 8."""
+    rng = np.random.default_rng(13)
+    for _ in range(2000):
+        a, b = (int(x) for x in rng.integers(1, 64, size=2))
+        M, N, K = 128 * a, 256 * b, 8 * int(rng.integers(1, 1200))
+        sms = int(rng.integers(1, 200))
+        plan = mhr.gemm_testing_plan_simt_wide(M, N, K, sms)
+        assert plan in (0, 1, 2)
+        if plan == 2:
+            assert K >= 1024
+        if plan:
+            assert 2 * a * b >= sms, (M, N, K, sms)
+        assert mhr.gemm_testing_plan_simt_wide(M + 1, N, K, sms) == 0
+        assert mhr.gemm_testing_plan_simt_wide(M, N + 4, K, sms) == 0
+    assert mhr.gemm_testing_plan_simt_wide(4096, 4096, 4096, 0) == 0
