@@ -142,12 +142,16 @@ int gemm_testing_set_pair_tile_n(int columns);
 int gemm_testing_plan_pair_tile_n(int64_t M, int64_t N, int64_t K, int clusters, int c_tma);
 
 /*
- * Forces the width of the single-CTA kernel's 3xTF32 output tiles (128 rows x
- * `columns`, columns 128, 96, 64 or 32) for the following calls
- * (process-wide); any other value, 0 included, restores the automatic
- * choice.  Calls with a pre-pass that take the cluster split keep 128; the
- * one-launch form (split inside) takes 128, 64 or 32 and splits K over
- * clusters at any of them.  Returns the previous setting.
+ * Forces the width of the single-CTA kernel's output tiles (128 rows x
+ * `columns`) for the following calls (process-wide): 3xTF32 takes 128, 96, 64
+ * or 32, bf16 256 or 128; a width the kind lacks leaves that kind's automatic
+ * choice, and any other value, 0 included, restores the automatic choice for
+ * both.  3xTF32 calls with a pre-pass that take the cluster split keep 128;
+ * the one-launch form (split inside) takes 128, 64 or 32 and splits K over
+ * clusters at any of them; bf16 takes the cluster split at either width.
+ * Automatically, bf16 takes 128 columns when those tiles, split as the kernel
+ * splits them (a cluster per tile, or two K halves), put more CTAs to work in
+ * a single round of tiles.  Returns the previous setting.
  */
 int gemm_testing_set_single_tile_n(int columns);
 

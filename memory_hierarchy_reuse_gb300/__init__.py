@@ -281,8 +281,8 @@ gemm = matmul
 
 
 def gemm_testing_set_single_tile_n(columns: int) -> int:
-    """Force the 3xTF32 single-CTA tiles' columns (128, 96, 64 or 32); 0
-    restores the planner (test hook)."""
+    """Force the single-CTA tiles' columns (3xTF32: 128, 96, 64 or 32; bf16:
+    256 or 128); 0 restores the planners (test hook)."""
     return load().gemm_testing_set_single_tile_n(int(columns))
 
 

@@ -566,7 +566,10 @@ MHR_API int gemm_testing_set_pair_tile_n(int columns) {
 MHR_API int gemm_testing_set_single_tile_n(int columns) {
   std::lock_guard<std::mutex> g(g_mu);
   const int old = g_single_tile_n;
-  g_single_tile_n = (columns == 32 || columns == 64 || columns == 96 || columns == 128) ? columns : 0;
+  g_single_tile_n =
+      (columns == 32 || columns == 64 || columns == 96 || columns == 128 || columns == 256)
+          ? columns
+          : 0;
   return old;
 }
 

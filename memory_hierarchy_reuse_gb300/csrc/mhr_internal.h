@@ -20,7 +20,7 @@ struct DeviceCtl {
   int raster_group = 0;                // tile rows per raster group, 0 = default (tuning hook)
   int split_mode = 0;                  // 3xTF32: 0 auto, 1 split pre-pass, 2 in-kernel split (test hook)
   int pair_tile_n = 0;                 // 3xTF32 CTA-pair tile columns, 0 = planned (test hook)
-  int single_tile_n = 0;               // 3xTF32 single-CTA tile columns, 0 = planned (test hook)
+  int single_tile_n = 0;               // single-CTA tile columns, 0 = planned (test hook)
 };
 
 // wide_mode: 0 automatic, 1 never the 128 x 256 kernel, 2 that kernel

@@ -244,8 +244,9 @@ cudaError_t launch_tc_3xtf32(const float* a_big, int64_t a_big_ld, const float* 
                          : 2 * tiles256 < clusters && few > 0 ? few
                                                               : plan_pair_tile_n(M, N, K, clusters,
                                                                                  c_tma))
-                      : (ctl.single_tile_n > 0 ? ctl.single_tile_n
-                                               : plan_single_tile_n(M, N, K, ctl.sm_count, c_tma));
+                      : (ctl.single_tile_n > 0 && ctl.single_tile_n <= 128
+                             ? ctl.single_tile_n
+                             : plan_single_tile_n(M, N, K, ctl.sm_count, c_tma));
   const bool tma_c = c_tma && bn % 32 == 0;
   const int b_box_rows = pair ? bn / 2 : bn;
   if (encode_tmap_2d(&mp.a0, f32, a_big, K, M, a_big_ld * 4, 32, 128, sw) != CUDA_SUCCESS ||

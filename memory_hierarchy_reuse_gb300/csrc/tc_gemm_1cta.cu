@@ -27,7 +27,6 @@ struct Cfg<KIND_BF16> {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;    // 48 KB
   static constexpr int MAX_STAGES = STAGES;
   static constexpr int INSTR_K = 16;
-  static constexpr uint32_t IDESC = make_idesc(1, false, true, BM, BN);
   static constexpr uint32_t TMEM_COLS = 2 * BN;            // 512
 };
 
@@ -42,7 +41,6 @@ struct Cfg<KIND_3XTF32> {
   static constexpr int B_BYTES = BN * BK * 4;              // 16 KB each (big, small)
   static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;  // 64 KB
   static constexpr int INSTR_K = 8;
-  static constexpr uint32_t IDESC = make_idesc(2, false, false, BM, BN);
   static constexpr uint32_t TMEM_COLS = 2 * BN;            // 256
 };
 
@@ -186,8 +184,10 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
   const int lane = threadIdx.x & 31;
   // The tile's columns (with a pre-pass, the cluster split runs whole tiles
   // only), and the ring.
-  const int bn = (KIND == KIND_3XTF32 && !CLUSTER) || KIND == KIND_3XTF32_SPLIT_TMA_A ? p.bn
-                                                                                     : Cf::BN;
+  const int bn = (KIND == KIND_3XTF32 && !CLUSTER) || KIND == KIND_3XTF32_SPLIT_TMA_A ||
+                         KIND == KIND_BF16
+                     ? p.bn
+                     : Cf::BN;
   const uint32_t stages = static_cast<uint32_t>(ring_stages<KIND>(bn));
   const uint32_t stage_bytes = static_cast<uint32_t>(ring_stage_bytes<KIND>(bn));
 
@@ -247,16 +247,16 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
           const uint32_t st = sbase + s * stage_bytes;
           const int k0 = kb * Cf::BK;
           // the split kind loads A alone (its converters fill the rest)
-          mbar_arrive_expect_tx(full_bar(s),
-                                KIND == KIND_3XTF32_SPLIT_TMA_A ? Cf::A_BYTES : stage_bytes);
+          mbar_arrive_expect_tx(full_bar(s), KIND == KIND_3XTF32_SPLIT_TMA_A ? Cf::A_BYTES
+                                             : KIND == KIND_BF16 ? Cf::A_BYTES + bn * Cf::BK * 2
+                                                                 : stage_bytes);
           const bool stall = p.inject_stall && blockIdx.x == 0 && it == 0;
           if (!stall) {
             if constexpr (KIND == KIND_3XTF32_SPLIT_TMA_A) {
               tma_load_2d(st, &tmA0, full_bar(s), k0, m0);
             } else if constexpr (KIND == KIND_BF16) {
               tma_load_2d(st, &tmA0, full_bar(s), k0, m0);
-#pragma unroll
-              for (int j = 0; j < Cf::BN / 64; ++j)
+              for (int j = 0; j < bn / 64; ++j)
                 tma_load_2d(st + Cf::A_BYTES + j * Cf::B_BOX_BYTES, &tmB0, full_bar(s), n0 + 64 * j,
                             k0);
             } else {
@@ -287,8 +287,8 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
     if (lane == 0) {
       uint32_t it = 0, tcount = 0;
       bool ok = true;
-      const uint32_t idesc =
-          KIND == KIND_BF16 ? Cf::IDESC : make_idesc(2, false, false, Cf::BM, bn);
+      const uint32_t idesc = KIND == KIND_BF16 ? make_idesc(1, false, true, Cf::BM, bn)
+                                               : make_idesc(2, false, false, Cf::BM, bn);
       for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++tcount) {
         const Unit w = unit_1cta<CLUSTER>(u, p);
         const uint32_t buf = tcount & 1u, aph = (tcount >> 1) & 1u;
@@ -311,8 +311,8 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
           const uint32_t st = sbase + s * stage_bytes;
           if constexpr (KIND == KIND_BF16) {
             // A: 128 rows x 128 B, K-major, 8-row groups 1024 B apart.
-            // B: four 64-column boxes (8 KB apart) of 64 k-rows x 128 B,
-            //    MN-major: LBO = next 64 columns, SBO = next 8 k-rows.
+            // B: bn / 64 (4 or 2) 64-column boxes (8 KB apart) of 64 k-rows x
+            //    128 B, MN-major: LBO = next 64 columns, SBO = next 8 k-rows.
 #pragma unroll
             for (int kk = 0; kk < Cf::BK / Cf::INSTR_K; ++kk) {
               const uint64_t ad = smem_desc_sw128(st + kk * 32, 16, 1024);
@@ -558,19 +558,55 @@ int cluster_split_size(const TcParams& p, cudaLaunchConfig_t cfg, const DeviceCt
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  // Clusters of S CTAs that fit on the GPU at once: the occupancy query
+  // depends on the kernel and S only, so it is made once per device (calls
+  // are serialised by the library's lock).
+  static std::map<int, std::array<int, 9>> fit_cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  auto fit = fit_cache.emplace(dev, std::array<int, 9>{}).first;
   for (int S = 8; S >= 4; S /= 2) {
     if (p.num_tiles * S > ctl.sm_count || p.num_kb < 16 * S) continue;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(S);
-    cfg.gridDim = dim3(static_cast<unsigned>(p.num_tiles * S));
-    int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, tc_gemm_kernel<KIND, false, true>, &cfg) !=
-        cudaSuccess) {
-      cudaGetLastError();
-      continue;
+    int& clusters = fit->second[S];
+    if (clusters == 0) {
+      attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+      cfg.gridDim = dim3(static_cast<unsigned>(8 * S));
+      if (cudaOccupancyMaxActiveClusters(&clusters, tc_gemm_kernel<KIND, false, true>, &cfg) !=
+          cudaSuccess) {
+        cudaGetLastError();
+        clusters = -1;
+      }
     }
     if (clusters >= p.num_tiles) return S;
   }
   return 1;
+}
+
+// How many CTAs the single-CTA kernel puts to work on tiles of bn columns:
+// clusters for the cluster split, two K halves per tile when they all fit,
+// else one CTA per tile up to the SM count (as launch_t below decides).
+template <int KIND>
+int64_t working_ctas(int64_t M, int64_t N, int64_t K, float* C, int64_t ldc, int bn,
+                     bool after_prepass, cudaLaunchConfig_t cfg, const DeviceCtl& ctl) {
+  const TcParams q = make_params(M, N, K, Cfg<KIND>::BM, bn, Cfg<KIND>::BK, C, ldc, ctl);
+  const int S = cluster_split_size<KIND>(q, cfg, ctl);
+  if (S > 1) return q.num_tiles * S;
+  if (2 * q.num_tiles <= ctl.sm_count && q.num_kb >= (after_prepass ? 4 : 32))
+    return 2 * q.num_tiles;
+  return q.num_tiles < ctl.sm_count ? q.num_tiles : ctl.sm_count;
+}
+
+// bf16 tile columns, 256 or 128: 128 when its tiles, split as launch_t splits
+// them, put more CTAs to work in a single round.  An MMA of 128 columns reads
+// 32 KB of shared memory per 64-deep K-block against 48 KB for 256 columns
+// at half the work, so it only pays where it brings SMs that would idle.
+template <int KIND>
+int bf16_tile_n(int64_t M, int64_t N, int64_t K, float* C, int64_t ldc, bool after_prepass,
+                cudaLaunchConfig_t cfg, const DeviceCtl& ctl) {
+  const int64_t narrow = working_ctas<KIND>(M, N, K, C, ldc, 128, after_prepass, cfg, ctl);
+  const int64_t wide = working_ctas<KIND>(M, N, K, C, ldc, Cfg<KIND>::BN, after_prepass, cfg, ctl);
+  const int64_t tiles128 = ((M + Cfg<KIND>::BM - 1) / Cfg<KIND>::BM) * ((N + 127) / 128);
+  return narrow > wide && tiles128 <= ctl.sm_count ? 128 : Cfg<KIND>::BN;
 }
 
 template <int KIND>
@@ -578,10 +614,6 @@ cudaError_t launch_t(const TcMaps& mp, float* C, int64_t M, int64_t N, int64_t K
                      bool c_tma, bool after_prepass, int bn, const DeviceCtl& ctl,
                      cudaStream_t s) {
   using Cf = Cfg<KIND>;
-  if (KIND != KIND_3XTF32 || bn <= 0) bn = Cf::BN;
-  TcParams p = make_params(M, N, K, Cf::BM, bn, Cf::BK, C, ldc, ctl);
-  p.c_even = !c_tma && mp.c_even;
-  p.c_odd_shift = p.c_even ? mp.c_odd_shift : -1;
   cudaError_t e;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -592,10 +624,18 @@ cudaError_t launch_t(const TcMaps& mp, float* C, int64_t M, int64_t N, int64_t K
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  // bf16: 256 or 128 columns, forced or planned; 3xTF32: the width the
+  // caller planned (128, 96, 64 or 32)
+  if (KIND == KIND_BF16 && bn != 128 && bn != Cf::BN)
+    bn = bf16_tile_n<KIND>(M, N, K, C, ldc, after_prepass, cfg, ctl);
+  if ((KIND != KIND_3XTF32 && KIND != KIND_BF16) || bn <= 0 || bn > Cf::BN) bn = Cf::BN;
+  TcParams p = make_params(M, N, K, Cf::BM, bn, Cf::BK, C, ldc, ctl);
+  p.c_even = !c_tma && mp.c_even;
+  p.c_odd_shift = p.c_even ? mp.c_odd_shift : -1;
   // Few tiles with long K runs: a cluster of S CTAs per tile, each on one
   // run of K-blocks, summing through distributed shared memory (see above;
-  // whole-width tiles only).
-  const int S = bn == Cf::BN ? cluster_split_size<KIND>(p, cfg, ctl) : 1;
+  // 3xTF32 with whole-width tiles only).
+  const int S = bn == Cf::BN || KIND == KIND_BF16 ? cluster_split_size<KIND>(p, cfg, ctl) : 1;
   if (S > 1) {
     p.num_units = p.num_tiles * S;
     attr[1].id = cudaLaunchAttributeClusterDimension;
@@ -604,7 +644,8 @@ cudaError_t launch_t(const TcMaps& mp, float* C, int64_t M, int64_t N, int64_t K
     attr[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
     cfg.gridDim = dim3(static_cast<unsigned>(p.num_units));
-    note_main_kernel(KIND == KIND_BF16 ? "tc_gemm_kernel<bf16,cluster-K>"
+    note_main_kernel(KIND == KIND_BF16 ? (bn == Cf::BN ? "tc_gemm_kernel<bf16,cluster-K>"
+                                                       : "tc_gemm_kernel<bf16,n128,cluster-K>")
                                        : "tc_gemm_kernel<3xtf32,cluster-K>",
                      p.num_units, p.num_tiles);
     e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<KIND, false, true>, mp.a0, mp.a1, mp.b0, mp.b1,
@@ -629,8 +670,9 @@ cudaError_t launch_t(const TcMaps& mp, float* C, int64_t M, int64_t N, int64_t K
   }
   const int grid = p.num_units < ctl.sm_count ? p.num_units : ctl.sm_count;
   char name[48];
-  if (KIND == KIND_3XTF32 && bn != Cf::BN)
-    snprintf(name, sizeof(name), "tc_gemm_kernel<3xtf32,n%d>", bn);
+  if (bn != Cf::BN)
+    snprintf(name, sizeof(name), "tc_gemm_kernel<%s,n%d>",
+             KIND == KIND_BF16 ? "bf16" : "3xtf32", bn);
   else
     snprintf(name, sizeof(name), "%s",
              KIND == KIND_BF16 ? "tc_gemm_kernel<bf16>" : "tc_gemm_kernel<3xtf32>");
@@ -712,7 +754,7 @@ cudaError_t launch_single_cta_split(const TcMaps& maps, const float* A, const fl
   // GB300, whole calls: 256^3 15.1 / 13.1 / 13.0 us at 128 / 64 / 32 columns,
   // 512^3 18.7 / 15.1 / 17.1, 300 x 520 x 1000 19.1 / 19.2 / 23.1,
   // 256 x 512 x 1000 19.1 / 19.1 / 17.1, 256 x 256 x 2048 25.2 / 19.1 / 23.0.
-  int bn = ctl.single_tile_n;
+  int bn = ctl.single_tile_n <= Cf::BN ? ctl.single_tile_n : 0;
   if (bn <= 0) {
     int64_t best_grid = 0;
     for (int w = Cf::BN; w >= 32; w /= 2) {
@@ -776,7 +818,8 @@ cudaError_t launch_single_cta(int kind, const TcMaps& maps, float* C, int64_t M,
                               int64_t K, int64_t ldc, bool c_tma, bool after_prepass, int bn,
                               const DeviceCtl& ctl, cudaStream_t s) {
   return kind == KIND_BF16
-             ? launch_t<KIND_BF16>(maps, C, M, N, K, ldc, c_tma, after_prepass, 0, ctl, s)
+             ? launch_t<KIND_BF16>(maps, C, M, N, K, ldc, c_tma, after_prepass,
+                                   ctl.single_tile_n, ctl, s)
              : launch_t<KIND_3XTF32>(maps, C, M, N, K, ldc, c_tma, after_prepass, bn, ctl, s);
 }
 

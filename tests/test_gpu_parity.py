@@ -413,8 +413,9 @@ def test_single_cta_tile_widths(mhr, bn):
         mhr.gemm_testing_set_cta_pair_mode(old)
 
 
-@pytest.mark.parametrize("path", ["3xtf32", "bf16"])
-def test_single_cta_few_tiles(mhr, path):
+@pytest.mark.parametrize("path,width", [("3xtf32", 0), ("bf16", 256), ("bf16", 128)],
+                         ids=["3xtf32", "bf16-256", "bf16-128"])
+def test_single_cta_few_tiles(mhr, path, width):
     """Few tiles on the single-CTA kernel. With long K runs (at least 16
     K-blocks per rank) it runs a cluster of 8 or 4 CTAs per tile, each on one
     run of K-blocks, and sums the partial tiles through distributed shared
@@ -423,16 +424,19 @@ def test_single_cta_few_tiles(mhr, path):
     least 32 steps), every tile becomes two K halves reduce-added into a
     zeroed C. Cases: 4 tiles with 129-130 K-blocks (cluster of 8) and 65-66
     (cluster of 4, ragged runs), half the SM count in tiles (K halves) and one
-    more (no split); K ragged throughout. Integer inputs bit-exact against the
+    more (no split); K ragged throughout. bf16 at both of its tile widths,
+    256 and 128 columns (forced). Integer inputs bit-exact against the
     oracle through vector and scalar stores (ldc odd), real inputs within
     tolerance and bitwise repeatable."""
     import torch
 
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    tile_n = 256 if path == "bf16" else 128  # single-CTA tiles: 128 x tile_n
+    tile_n = width or 128  # single-CTA tiles: 128 x tile_n
     bk = 64 if path == "bf16" else 32
-    name = "tc_gemm_kernel<bf16" if path == "bf16" else "tc_gemm_kernel<3xtf32"
+    name = "tc_gemm_kernel<3xtf32" if path == "3xtf32" else (
+        "tc_gemm_kernel<bf16" if width == 256 else "tc_gemm_kernel<bf16,n128")
     old = mhr.gemm_testing_set_cta_pair_mode(1)
+    old_n = mhr.gemm_testing_set_single_tile_n(width)
     try:
         cases = [(4, bk * 128 + 40, f"{name},cluster-K> grid=32 "),
                  (4, bk * 64 + 40, f"{name},cluster-K> grid=16 "),
@@ -454,6 +458,7 @@ def test_single_cta_few_tiles(mhr, path):
             assert normalised_error(C, Cref, S) <= TOL[path]
             assert np.array_equal(call.run(mhr).result(), C)
     finally:
+        mhr.gemm_testing_set_single_tile_n(old_n)
         mhr.gemm_testing_set_cta_pair_mode(old)
 
 
@@ -635,6 +640,33 @@ def test_automatic_mode_bf16(mhr, shape):
     want = "tc_gemm_pair_kernel<bf16" if pair else "tc_gemm_kernel<bf16"
     assert label.startswith(want), (label, want)
     rows, cols = sample_indices(M, N, 4211, rows=(0, M // 2 + 1, M - 1), cols=(0, N - 1))
+    ref = oracle.gemm_entries(A, B, rows, cols, M, N, K)[0]
+    assert np.array_equal(C[rows, cols], ref)
+
+
+@pytest.mark.parametrize("shape,want", [
+    ((1024, 1024, 1024), "tc_gemm_kernel<bf16,n128> grid=64 "),
+    ((256, 256, 8192), "tc_gemm_kernel<bf16,n128,cluster-K> grid=32 "),
+    ((768, 768, 768), "tc_gemm_kernel<bf16,n128> grid=36 "),
+    ((1536, 2560, 512), "tc_gemm_kernel<bf16> grid=120 ")],
+    ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else "")
+def test_automatic_bf16_tile_width(mhr, shape, want):
+    """The single-CTA bf16 kernel takes 128-column tiles when they put more
+    CTAs to work in one round than 256-column ones: 1024^3 (64 tiles against
+    32), 256 x 256 x 8192 (4 tiles in clusters of 8 against 2), 768^3 (36
+    against 18); 1536 x 2560 x 512 keeps 256 columns (120 tiles; 240 narrow
+    ones would need two rounds on 152 SMs). Integer inputs bit-exact against
+    the oracle on sampled entries."""
+    import torch
+
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("tile counts stated for 152 SMs")
+    M, N, K = shape
+    A, B, Ab, Bb = operands(M, N, K, 4311 + K, "int", "bf16")
+    C = DeviceCall("bf16", A, B, Ab, Bb).run(mhr).result()
+    label = mhr.gemm_testing_last_main_kernel()
+    assert label.startswith(want), (label, want)
+    rows, cols = sample_indices(M, N, 4311, rows=(0, M // 2 + 1, M - 1), cols=(0, N - 1))
     ref = oracle.gemm_entries(A, B, rows, cols, M, N, K)[0]
     assert np.array_equal(C[rows, cols], ref)
 
