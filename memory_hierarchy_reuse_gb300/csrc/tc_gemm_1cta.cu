@@ -75,7 +75,8 @@ __host__ __device__ constexpr int cta_threads() {
 
 // ------------------------------------------------------------------ cluster split
 //
-// Few tiles: the kernel can run as clusters of S CTAs (2, 4 or 8), one
+// Few tiles: the kernel can run as clusters of S CTAs (2, 4 or 8; 16 for
+// 3xTF32, beyond the portable cluster size, with the kernel's opt-in), one
 // cluster per output tile.  Rank r takes the r-th run of ceil(num_kb / S)
 // K-blocks (trailing runs may be short or empty), accumulates it in TMEM as
 // usual, and its epilogue writes the partial 128 x BN fp32 tile into its own
@@ -85,6 +86,8 @@ __host__ __device__ constexpr int cta_threads() {
 // shared memory, in rank order, and stores them to C; a second barrier keeps
 // every partial tile alive until the peers have read it.  One fixed order
 // per element: bit-reproducible, with no zeroing of C and no atomics.
+template <int KIND>
+constexpr int MAX_CLUSTER = KIND == KIND_3XTF32 ? 16 : 8;
 
 __device__ __forceinline__ uint32_t cluster_ctas() {
   uint32_t r;
@@ -494,13 +497,13 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
       const int c = (idx % (bn / 4)) * 4;
       const uint32_t off = sbase + static_cast<uint32_t>((r * PART_LD<KIND> + c) * 4);
       // all loads first (their latencies overlap), then the sum in rank order
-      float4 t[8];
+      float4 t[MAX_CLUSTER<KIND>];
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
+      for (int k = 0; k < MAX_CLUSTER<KIND>; ++k)
         if (k < S) t[k] = ld_cluster_v4(mapa_shared(off, static_cast<uint32_t>(k)));
       float4 v = t[0];
 #pragma unroll
-      for (int k = 1; k < 8; ++k)
+      for (int k = 1; k < MAX_CLUSTER<KIND>; ++k)
         if (k < S) {
           v.x += t[k].x;
           v.y += t[k].y;
@@ -531,13 +534,23 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
 template <int KIND, bool TMA_STORE, bool CLUSTER>
 cudaError_t prepare_kernel() {
   // cudaFuncSetAttribute is per device; callers run it on every launch (cheap).
-  return cudaFuncSetAttribute(tc_gemm_kernel<KIND, TMA_STORE, CLUSTER>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<KIND>::ALLOC);
+  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<KIND, TMA_STORE, CLUSTER>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Layout<KIND>::ALLOC);
+  if (e == cudaSuccess && CLUSTER && MAX_CLUSTER<KIND> > 8)
+    e = cudaFuncSetAttribute(tc_gemm_kernel<KIND, TMA_STORE, CLUSTER>,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
 }
 
 // Cluster size for the cluster split of a problem with few tiles: the
-// largest S in {8, 4} with one CTA per SM for all tiles x S CTAs, at least
-// 16 K-blocks per rank, and every cluster co-resident; 1 = no cluster split.
+// largest S in {8, 4} (3xTF32: {16, 8, 4}) with one CTA per SM for all tiles
+// x S CTAs, at least 16 K-blocks per rank (8 at S = 16), and every cluster
+// co-resident; 1 = no cluster split.  Each rank pulls about one tile of
+// partial sums from its peers whatever S is, so a larger S shortens the K
+// runs at the same reduction cost: 3xTF32, 256 x 256 x 8192 37.5 -> 29.3 us
+// and 512 x 128 x 4136 27.3 -> 23.2 us with S = 16; bf16, at half the MMA
+// time per K-block, gained nothing from it (256 x 256 x 8192 17.1 / 17.0).
 // Measured on GB300 (whole calls), the split's fixed costs -- the cluster
 // launch, the partial tiles through shared memory, two cluster barriers --
 // pay off only on long K runs: 512 x 512 x 8192 3xTF32 95.9 -> 64.1 us (S =
@@ -561,12 +574,12 @@ int cluster_split_size(const TcParams& p, cudaLaunchConfig_t cfg, const DeviceCt
   // Clusters of S CTAs that fit on the GPU at once: the occupancy query
   // depends on the kernel and S only, so it is made once per device (calls
   // are serialised by the library's lock).
-  static std::map<int, std::array<int, 9>> fit_cache;
+  static std::map<int, std::array<int, 17>> fit_cache;
   int dev = 0;
   cudaGetDevice(&dev);
-  auto fit = fit_cache.emplace(dev, std::array<int, 9>{}).first;
-  for (int S = 8; S >= 4; S /= 2) {
-    if (p.num_tiles * S > ctl.sm_count || p.num_kb < 16 * S) continue;
+  auto fit = fit_cache.emplace(dev, std::array<int, 17>{}).first;
+  for (int S = MAX_CLUSTER<KIND>; S >= 4; S /= 2) {
+    if (p.num_tiles * S > ctl.sm_count || p.num_kb < (S > 8 ? 8 : 16) * S) continue;
     int& clusters = fit->second[S];
     if (clusters == 0) {
       attr[0].val.clusterDim.x = static_cast<unsigned>(S);

@@ -422,9 +422,10 @@ def test_single_cta_few_tiles(mhr, path, width):
     memory in rank order. Otherwise, when the halves of all tiles fit on the
     SMs at once (and, without a pre-pass to overlap the zeroing, K has at
     least 32 steps), every tile becomes two K halves reduce-added into a
-    zeroed C. Cases: 4 tiles with 129-130 K-blocks (cluster of 8) and 65-66
-    (cluster of 4, ragged runs), half the SM count in tiles (K halves) and one
-    more (no split); K ragged throughout. bf16 at both of its tile widths,
+    zeroed C. Cases: 4 tiles with 129-130 K-blocks (cluster of 8; of 16 for
+    3xTF32, whose ranks then run 9 K-blocks, and 10 such tiles in clusters of
+    8) and 65-66 (cluster of 4, ragged runs), half the SM count in tiles (K
+    halves) and one more (no split); K ragged throughout. bf16 at both of its tile widths,
     256 and 128 columns (forced). Integer inputs bit-exact against the
     oracle through vector and scalar stores (ldc odd), real inputs within
     tolerance and bitwise repeatable."""
@@ -438,10 +439,14 @@ def test_single_cta_few_tiles(mhr, path, width):
     old = mhr.gemm_testing_set_cta_pair_mode(1)
     old_n = mhr.gemm_testing_set_single_tile_n(width)
     try:
-        cases = [(4, bk * 128 + 40, f"{name},cluster-K> grid=32 "),
-                 (4, bk * 64 + 40, f"{name},cluster-K> grid=16 "),
+        cases = [(4, bk * 64 + 40, f"{name},cluster-K> grid=16 "),
                  (sms // 2, bk * 32 + 40, f"{name}> grid={sms} "),
                  (sms // 2 + 1, bk * 32 + 40, f"{name}> grid={sms // 2 + 1} ")]
+        if path == "3xtf32":  # clusters of 16, and of 8 where 16 would not fit
+            cases += [(4, bk * 128 + 40, f"{name},cluster-K> grid=64 "),
+                      (10, bk * 128 + 40, f"{name},cluster-K> grid=80 ")]
+        else:
+            cases += [(4, bk * 128 + 40, f"{name},cluster-K> grid=32 ")]
         for tiles, K, want in cases:
             M, N = 128 * tiles, tile_n
             for ldc in (None, N + 1, N + 2):
