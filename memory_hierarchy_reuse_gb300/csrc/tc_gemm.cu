@@ -240,13 +240,17 @@ cudaError_t launch_tc_3xtf32(const float* a_big, int64_t a_big_ld, const float* 
   const int clusters = ctl.sm_count / 2;
   const int few = few_tile_pair_width(M, N, K, clusters);
   const int64_t tiles256 = ((M + PAIR_TILE_M - 1) / PAIR_TILE_M) * ((N + PAIR_TILE_N - 1) / PAIR_TILE_N);
-  const int bn = pair ? (ctl.pair_tile_n > 0                       ? ctl.pair_tile_n
-                         : 2 * tiles256 < clusters && few > 0 ? few
-                                                              : plan_pair_tile_n(M, N, K, clusters,
-                                                                                 c_tma))
-                      : (ctl.single_tile_n > 0 && ctl.single_tile_n <= 128
-                             ? ctl.single_tile_n
-                             : plan_single_tile_n(M, N, K, ctl.sm_count, c_tma));
+  int bn;
+  if (pair) {
+    bn = ctl.pair_tile_n > 0                  ? ctl.pair_tile_n
+         : 2 * tiles256 < clusters && few > 0 ? few
+                                              : plan_pair_tile_n(M, N, K, clusters, c_tma);
+  } else if (ctl.single_tile_n > 0 && ctl.single_tile_n <= 128) {
+    bn = ctl.single_tile_n;
+  } else {
+    bn = plan_single_tile_n(M, N, K, ctl.sm_count, c_tma);
+    if (bn == 128) bn = single_cluster_tile_n(M, N, K, ctl);  // the cluster split's width
+  }
   const bool tma_c = c_tma && bn % 32 == 0;
   const int b_box_rows = pair ? bn / 2 : bn;
   if (encode_tmap_2d(&mp.a0, f32, a_big, K, M, a_big_ld * 4, 32, 128, sw) != CUDA_SUCCESS ||

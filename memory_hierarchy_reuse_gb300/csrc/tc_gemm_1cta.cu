@@ -187,10 +187,7 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
   const int lane = threadIdx.x & 31;
   // The tile's columns (with a pre-pass, the cluster split runs whole tiles
   // only), and the ring.
-  const int bn = (KIND == KIND_3XTF32 && !CLUSTER) || KIND == KIND_3XTF32_SPLIT_TMA_A ||
-                         KIND == KIND_BF16
-                     ? p.bn
-                     : Cf::BN;
+  const int bn = p.bn;
   const uint32_t stages = static_cast<uint32_t>(ring_stages<KIND>(bn));
   const uint32_t stage_bytes = static_cast<uint32_t>(ring_stage_bytes<KIND>(bn));
 
@@ -638,7 +635,7 @@ cudaError_t launch_t(const TcMaps& mp, float* C, int64_t M, int64_t N, int64_t K
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   // bf16: 256 or 128 columns, forced or planned; 3xTF32: the width the
-  // caller planned (128, 96, 64 or 32)
+  // caller planned (128, 96, 64 or 32; see single_cluster_tile_n)
   if (KIND == KIND_BF16 && bn != 128 && bn != Cf::BN)
     bn = bf16_tile_n<KIND>(M, N, K, C, ldc, after_prepass, cfg, ctl);
   if ((KIND != KIND_3XTF32 && KIND != KIND_BF16) || bn <= 0 || bn > Cf::BN) bn = Cf::BN;
@@ -646,9 +643,8 @@ cudaError_t launch_t(const TcMaps& mp, float* C, int64_t M, int64_t N, int64_t K
   p.c_even = !c_tma && mp.c_even;
   p.c_odd_shift = p.c_even ? mp.c_odd_shift : -1;
   // Few tiles with long K runs: a cluster of S CTAs per tile, each on one
-  // run of K-blocks, summing through distributed shared memory (see above;
-  // 3xTF32 with whole-width tiles only).
-  const int S = bn == Cf::BN || KIND == KIND_BF16 ? cluster_split_size<KIND>(p, cfg, ctl) : 1;
+  // run of K-blocks, summing through distributed shared memory (see above).
+  const int S = cluster_split_size<KIND>(p, cfg, ctl);
   if (S > 1) {
     p.num_units = p.num_tiles * S;
     attr[1].id = cudaLaunchAttributeClusterDimension;
@@ -657,10 +653,14 @@ cudaError_t launch_t(const TcMaps& mp, float* C, int64_t M, int64_t N, int64_t K
     attr[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
     cfg.gridDim = dim3(static_cast<unsigned>(p.num_units));
-    note_main_kernel(KIND == KIND_BF16 ? (bn == Cf::BN ? "tc_gemm_kernel<bf16,cluster-K>"
-                                                       : "tc_gemm_kernel<bf16,n128,cluster-K>")
-                                       : "tc_gemm_kernel<3xtf32,cluster-K>",
-                     p.num_units, p.num_tiles);
+    char cname[48];
+    if (bn == Cf::BN)
+      snprintf(cname, sizeof(cname), "tc_gemm_kernel<%s,cluster-K>",
+               KIND == KIND_BF16 ? "bf16" : "3xtf32");
+    else
+      snprintf(cname, sizeof(cname), "tc_gemm_kernel<%s,n%d,cluster-K>",
+               KIND == KIND_BF16 ? "bf16" : "3xtf32", bn);
+    note_main_kernel(cname, p.num_units, p.num_tiles);
     e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<KIND, false, true>, mp.a0, mp.a1, mp.b0, mp.b1,
                            mp.c, mp.c1, p);
     if (e != cudaSuccess) return e;
@@ -825,6 +825,25 @@ cudaError_t launch_single_cta_split(const TcMaps& maps, const float* A, const fl
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+// 3xTF32 after a pre-pass, where the planner keeps 128 columns for the
+// cluster split: 64 columns when those tiles, in their own clusters, put more
+// CTAs to work.  With more CTAs each rank's cluster is at least as large, so
+// its K run is no longer; but each 64-column unit still stages A's 32 KB of
+// both parts per K-block, as a 128-column one does, so the gain is small.
+// GB300, 512 x 512 x 8192: 32 tiles x clusters of 4 (128 CTAs) 64.1 us
+// against 16 x 4 (64 CTAs) 66.2 us.
+int single_cluster_tile_n(int64_t M, int64_t N, int64_t K, const DeviceCtl& ctl) {
+  constexpr int KIND = KIND_3XTF32;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = Layout<KIND>::ALLOC;
+  const TcParams p128 = make_params(M, N, K, Cfg<KIND>::BM, 128, Cfg<KIND>::BK, nullptr, N, ctl);
+  if (cluster_split_size<KIND>(p128, cfg, ctl) <= 1) return 128;
+  const int64_t wide = working_ctas<KIND>(M, N, K, nullptr, N, 128, true, cfg, ctl);
+  const int64_t narrow = working_ctas<KIND>(M, N, K, nullptr, N, 64, true, cfg, ctl);
+  return narrow > wide ? 64 : 128;
 }
 
 cudaError_t launch_single_cta(int kind, const TcMaps& maps, float* C, int64_t M, int64_t N,

@@ -413,8 +413,9 @@ def test_single_cta_tile_widths(mhr, bn):
         mhr.gemm_testing_set_cta_pair_mode(old)
 
 
-@pytest.mark.parametrize("path,width", [("3xtf32", 0), ("bf16", 256), ("bf16", 128)],
-                         ids=["3xtf32", "bf16-256", "bf16-128"])
+@pytest.mark.parametrize("path,width", [("3xtf32", 128), ("3xtf32", 64), ("bf16", 256),
+                                        ("bf16", 128)],
+                         ids=["3xtf32-128", "3xtf32-64", "bf16-256", "bf16-128"])
 def test_single_cta_few_tiles(mhr, path, width):
     """Few tiles on the single-CTA kernel. With long K runs (at least 16
     K-blocks per rank) it runs a cluster of 8 or 4 CTAs per tile, each on one
@@ -425,8 +426,8 @@ def test_single_cta_few_tiles(mhr, path, width):
     zeroed C. Cases: 4 tiles with 129-130 K-blocks (cluster of 8; of 16 for
     3xTF32, whose ranks then run 9 K-blocks, and 10 such tiles in clusters of
     8) and 65-66 (cluster of 4, ragged runs), half the SM count in tiles (K
-    halves) and one more (no split); K ragged throughout. bf16 at both of its tile widths,
-    256 and 128 columns (forced). Integer inputs bit-exact against the
+    halves) and one more (no split); K ragged throughout. 3xTF32 at 128 and
+    64 columns, bf16 at 256 and 128 (forced). Integer inputs bit-exact against the
     oracle through vector and scalar stores (ldc odd), real inputs within
     tolerance and bitwise repeatable."""
     import torch
@@ -434,8 +435,8 @@ def test_single_cta_few_tiles(mhr, path, width):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     tile_n = width or 128  # single-CTA tiles: 128 x tile_n
     bk = 64 if path == "bf16" else 32
-    name = "tc_gemm_kernel<3xtf32" if path == "3xtf32" else (
-        "tc_gemm_kernel<bf16" if width == 256 else "tc_gemm_kernel<bf16,n128")
+    full = 128 if path == "3xtf32" else 256
+    name = f"tc_gemm_kernel<{path}" + ("" if width == full else f",n{width}")
     old = mhr.gemm_testing_set_cta_pair_mode(1)
     old_n = mhr.gemm_testing_set_single_tile_n(width)
     try:
@@ -674,6 +675,34 @@ def test_automatic_bf16_tile_width(mhr, shape, want):
     rows, cols = sample_indices(M, N, 4311, rows=(0, M // 2 + 1, M - 1), cols=(0, N - 1))
     ref = oracle.gemm_entries(A, B, rows, cols, M, N, K)[0]
     assert np.array_equal(C[rows, cols], ref)
+
+
+def test_automatic_3xtf32_cluster_width(mhr):
+    """After a pre-pass, 3xTF32 problems in the cluster split's domain take
+    64-column tiles when those, in clusters of their own, put more CTAs to
+    work: 512 x 512 x 8192 runs 32 tiles in clusters of 4 (128 CTAs) instead
+    of 16 (64 CTAs); 256 x 512 x 4096 keeps 128 columns (8 tiles in clusters
+    of 8 against 16 narrow tiles in clusters of 4: as many CTAs). Integer
+    inputs bit-exact against the oracle on sampled entries."""
+    import torch
+
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("tile counts stated for 152 SMs")
+    old = mhr.gemm_testing_set_cta_pair_mode(1)
+    old_split = mhr.gemm_testing_set_split_mode(1)  # the pre-pass
+    try:
+        for (M, N, K), want in (((512, 512, 8192), "tc_gemm_kernel<3xtf32,n64,cluster-K> grid=128 "),
+                                ((256, 512, 4096), "tc_gemm_kernel<3xtf32,cluster-K> grid=64 ")):
+            A, B, _, _ = operands(M, N, K, 4411 + K, "int", "3xtf32")
+            C = DeviceCall("3xtf32", A, B).run(mhr).result()
+            label = mhr.gemm_testing_last_main_kernel()
+            assert label.startswith(want), (label, want)
+            rows, cols = sample_indices(M, N, 4411, rows=(0, M // 2 + 1, M - 1), cols=(0, N - 1))
+            ref = oracle.gemm_entries(A, B, rows, cols, M, N, K)[0]
+            assert np.array_equal(C[rows, cols], ref)
+    finally:
+        mhr.gemm_testing_set_split_mode(old_split)
+        mhr.gemm_testing_set_cta_pair_mode(old)
 
 
 @pytest.mark.usefixtures("full_width_tiles")
