@@ -146,9 +146,8 @@ int gemm_testing_plan_pair_tile_n(int64_t M, int64_t N, int64_t K, int clusters,
  * `columns`) for the following calls (process-wide): 3xTF32 takes 128, 96, 64
  * or 32, bf16 256 or 128; a width the kind lacks leaves that kind's automatic
  * choice, and any other value, 0 included, restores the automatic choice for
- * both.  3xTF32 calls with a pre-pass that take the cluster split plan 128,
- * or 64 where 64-column tiles in clusters put more CTAs to work, and take
- * any forced width; the one-launch form (split inside) takes 128, 64 or 32 and splits K over
+ * both.  3xTF32 calls with a pre-pass that take the cluster split plan 128
+ * and take any forced width; the one-launch form (split inside) takes 128, 64 or 32 and splits K over
  * clusters at any of them; bf16 takes the cluster split at either width.
  * Automatically, bf16 takes 128 columns when those tiles, split as the kernel
  * splits them (a cluster per tile, or two K halves), put more CTAs to work in

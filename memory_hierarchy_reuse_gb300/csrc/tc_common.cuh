@@ -447,10 +447,6 @@ struct TcMaps {
 cudaError_t launch_single_cta(int kind, const TcMaps& maps, float* C, int64_t M, int64_t N,
                               int64_t K, int64_t ldc, bool c_tma, bool after_prepass, int bn,
                               const DeviceCtl& ctl, cudaStream_t s);
-// tc_gemm_1cta.cu: KIND_3XTF32's tile columns after a pre-pass where the
-// width planner keeps 128 for the cluster split: 64 when 64-column tiles, in
-// clusters of their own, put more CTAs to work; else 128.
-int single_cluster_tile_n(int64_t M, int64_t N, int64_t K, const DeviceCtl& ctl);
 // tc_gemm_1cta.cu: KIND_3XTF32_SPLIT_TMA_A on the single-CTA kernel, for small
 // problems (one launch): maps.a0 is A's map (K-major boxes of 32 k x 128
 // rows), maps.c C's map when c_tma.

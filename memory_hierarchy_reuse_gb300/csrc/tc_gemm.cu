@@ -249,7 +249,6 @@ cudaError_t launch_tc_3xtf32(const float* a_big, int64_t a_big_ld, const float* 
     bn = ctl.single_tile_n;
   } else {
     bn = plan_single_tile_n(M, N, K, ctl.sm_count, c_tma);
-    if (bn == 128) bn = single_cluster_tile_n(M, N, K, ctl);  // the cluster split's width
   }
   const bool tma_c = c_tma && bn % 32 == 0;
   const int b_box_rows = pair ? bn / 2 : bn;

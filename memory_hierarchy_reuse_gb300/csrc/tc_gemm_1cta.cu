@@ -75,16 +75,17 @@ __host__ __device__ constexpr int cta_threads() {
 
 // ------------------------------------------------------------------ cluster split
 //
-// Few tiles: the kernel can run as clusters of S CTAs (2, 4 or 8; 16 for
+// Few tiles: the kernel can run as clusters of S CTAs (2 to 8; 16 for
 // 3xTF32, beyond the portable cluster size, with the kernel's opt-in), one
 // cluster per output tile.  Rank r takes the r-th run of ceil(num_kb / S)
 // K-blocks (trailing runs may be short or empty), accumulates it in TMEM as
 // usual, and its epilogue writes the partial 128 x BN fp32 tile into its own
 // shared memory, over the ring, which no longer holds operands once the
-// accumulator is complete.  After a cluster barrier rank r sums rows
-// [r * 128 / S, (r + 1) * 128 / S) of all S partial tiles through distributed
-// shared memory, in rank order, and stores them to C; a second barrier keeps
-// every partial tile alive until the peers have read it.  One fixed order
+// accumulator is complete.  After a cluster barrier rank r sums the r-th of
+// S equal runs of the tile's float4s (row-major; whole rows [r * 128 / S,
+// (r + 1) * 128 / S) when S divides 128) of all S partial tiles through
+// distributed shared memory, in rank order, and stores them to C; a second
+// barrier keeps every partial tile alive until the peers have read it.  One fixed order
 // per element: bit-reproducible, with no zeroing of C and no atomics.
 template <int KIND>
 constexpr int MAX_CLUSTER = KIND == KIND_3XTF32 ? 16 : 8;
@@ -483,15 +484,18 @@ __global__ void __launch_bounds__(cta_threads<KIND>(), 1)
     cluster_sync_all();  // every rank's partial tile is in its shared memory
     const int S = static_cast<int>(cluster_ctas());
     const int rank = static_cast<int>(cluster_ctarank());
-    const int rows = Cf::BM / S;
+    // rank r sums the r-th of S equal runs of the tile's float4s, row-major
+    const int quads = bn / 4;
+    const int end = (rank + 1) * (Cf::BM * quads) / S;
     int tm, tn;
     tile_coords(static_cast<int>(blockIdx.x) / S, p, tm, tn);
     const int64_t m0 = static_cast<int64_t>(tm) * Cf::BM;
     const int n0 = tn * bn;
     const bool vec = (reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 && (p.ldc & 3) == 0;
-    for (int idx = threadIdx.x; idx < rows * (bn / 4); idx += cta_threads<KIND>()) {
-      const int r = rank * rows + idx / (bn / 4);
-      const int c = (idx % (bn / 4)) * 4;
+    for (int idx = rank * (Cf::BM * quads) / S + static_cast<int>(threadIdx.x); idx < end;
+         idx += cta_threads<KIND>()) {
+      const int r = idx / quads;
+      const int c = (idx % quads) * 4;
       const uint32_t off = sbase + static_cast<uint32_t>((r * PART_LD<KIND> + c) * 4);
       // all loads first (their latencies overlap), then the sum in rank order
       float4 t[MAX_CLUSTER<KIND>];
@@ -541,9 +545,11 @@ cudaError_t prepare_kernel() {
 }
 
 // Cluster size for the cluster split of a problem with few tiles: the
-// largest S in {8, 4} (3xTF32: {16, 8, 4}) with one CTA per SM for all tiles
-// x S CTAs, at least 16 K-blocks per rank (8 at S = 16), and every cluster
-// co-resident; 1 = no cluster split.  Each rank pulls about one tile of
+// largest S in 8, 7, ..., 4 (3xTF32: 16 first) with one CTA per SM for all
+// tiles x S CTAs, at least 16 K-blocks per rank (8 at S = 16), and every
+// cluster co-resident; 1 = no cluster split.  Sizes between the powers of
+// two fit where the next power does not: 16 tiles of 128 x 128 take
+// clusters of 7 (112 CTAs) where sixteen clusters of 8 are more than fit.  Each rank pulls about one tile of
 // partial sums from its peers whatever S is, so a larger S shortens the K
 // runs at the same reduction cost: 3xTF32, 256 x 256 x 8192 37.5 -> 29.3 us
 // and 512 x 128 x 4136 27.3 -> 23.2 us with S = 16; bf16, at half the MMA
@@ -575,7 +581,7 @@ int cluster_split_size(const TcParams& p, cudaLaunchConfig_t cfg, const DeviceCt
   int dev = 0;
   cudaGetDevice(&dev);
   auto fit = fit_cache.emplace(dev, std::array<int, 17>{}).first;
-  for (int S = MAX_CLUSTER<KIND>; S >= 4; S /= 2) {
+  for (int S = MAX_CLUSTER<KIND>; S >= 4; S = S > 8 ? 8 : S - 1) {
     if (p.num_tiles * S > ctl.sm_count || p.num_kb < (S > 8 ? 8 : 16) * S) continue;
     int& clusters = fit->second[S];
     if (clusters == 0) {
@@ -635,7 +641,7 @@ cudaError_t launch_t(const TcMaps& mp, float* C, int64_t M, int64_t N, int64_t K
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   // bf16: 256 or 128 columns, forced or planned; 3xTF32: the width the
-  // caller planned (128, 96, 64 or 32; see single_cluster_tile_n)
+  // caller planned (128, 96, 64 or 32)
   if (KIND == KIND_BF16 && bn != 128 && bn != Cf::BN)
     bn = bf16_tile_n<KIND>(M, N, K, C, ldc, after_prepass, cfg, ctl);
   if ((KIND != KIND_3XTF32 && KIND != KIND_BF16) || bn <= 0 || bn > Cf::BN) bn = Cf::BN;
@@ -825,25 +831,6 @@ cudaError_t launch_single_cta_split(const TcMaps& maps, const float* A, const fl
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
-}
-
-// 3xTF32 after a pre-pass, where the planner keeps 128 columns for the
-// cluster split: 64 columns when those tiles, in their own clusters, put more
-// CTAs to work.  With more CTAs each rank's cluster is at least as large, so
-// its K run is no longer; but each 64-column unit still stages A's 32 KB of
-// both parts per K-block, as a 128-column one does, so the gain is small.
-// GB300, 512 x 512 x 8192: 32 tiles x clusters of 4 (128 CTAs) 64.1 us
-// against 16 x 4 (64 CTAs) 66.2 us.
-int single_cluster_tile_n(int64_t M, int64_t N, int64_t K, const DeviceCtl& ctl) {
-  constexpr int KIND = KIND_3XTF32;
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(NUM_THREADS);
-  cfg.dynamicSmemBytes = Layout<KIND>::ALLOC;
-  const TcParams p128 = make_params(M, N, K, Cfg<KIND>::BM, 128, Cfg<KIND>::BK, nullptr, N, ctl);
-  if (cluster_split_size<KIND>(p128, cfg, ctl) <= 1) return 128;
-  const int64_t wide = working_ctas<KIND>(M, N, K, nullptr, N, 128, true, cfg, ctl);
-  const int64_t narrow = working_ctas<KIND>(M, N, K, nullptr, N, 64, true, cfg, ctl);
-  return narrow > wide ? 64 : 128;
 }
 
 cudaError_t launch_single_cta(int kind, const TcMaps& maps, float* C, int64_t M, int64_t N,

@@ -677,13 +677,13 @@ def test_automatic_bf16_tile_width(mhr, shape, want):
     assert np.array_equal(C[rows, cols], ref)
 
 
-def test_automatic_3xtf32_cluster_width(mhr):
-    """After a pre-pass, 3xTF32 problems in the cluster split's domain take
-    64-column tiles when those, in clusters of their own, put more CTAs to
-    work: 512 x 512 x 8192 runs 32 tiles in clusters of 4 (128 CTAs) instead
-    of 16 (64 CTAs); 256 x 512 x 4096 keeps 128 columns (8 tiles in clusters
-    of 8 against 16 narrow tiles in clusters of 4: as many CTAs). Integer
-    inputs bit-exact against the oracle on sampled entries."""
+def test_automatic_3xtf32_cluster_sizes(mhr):
+    """After a pre-pass, 3xTF32 problems in the cluster split's domain run
+    128-column tiles in the largest clusters that fit: 512 x 512 x 8192 has
+    16 tiles, for which sixteen clusters of 8 do not fit at once, so it takes
+    clusters of 6 (96 CTAs), whose ranks each sum a sixth of the tile's
+    float4s rather than whole rows; 256 x 512 x 4096 (8 tiles) takes clusters
+    of 8. Integer inputs bit-exact against the oracle on sampled entries."""
     import torch
 
     if torch.cuda.get_device_properties(0).multi_processor_count != 152:
@@ -691,7 +691,7 @@ def test_automatic_3xtf32_cluster_width(mhr):
     old = mhr.gemm_testing_set_cta_pair_mode(1)
     old_split = mhr.gemm_testing_set_split_mode(1)  # the pre-pass
     try:
-        for (M, N, K), want in (((512, 512, 8192), "tc_gemm_kernel<3xtf32,n64,cluster-K> grid=128 "),
+        for (M, N, K), want in (((512, 512, 8192), "tc_gemm_kernel<3xtf32,cluster-K> grid=96 "),
                                 ((256, 512, 4096), "tc_gemm_kernel<3xtf32,cluster-K> grid=64 ")):
             A, B, _, _ = operands(M, N, K, 4411 + K, "int", "3xtf32")
             C = DeviceCall("3xtf32", A, B).run(mhr).result()
