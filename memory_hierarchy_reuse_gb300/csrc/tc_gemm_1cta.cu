@@ -598,6 +598,13 @@ int cluster_split_size(const TcParams& p, cudaLaunchConfig_t cfg, const DeviceCt
   return 1;
 }
 
+// Whether launch_t splits every tile into two K halves (see there): all the
+// halves fit on the SMs at once, and without a pre-pass to hide the zeroing
+// of C behind, K has at least 32 steps.
+inline bool k_halves_chosen(const TcParams& p, bool after_prepass, const DeviceCtl& ctl) {
+  return 2 * p.num_tiles <= ctl.sm_count && p.num_kb >= (after_prepass ? 4 : 32);
+}
+
 // How many CTAs the single-CTA kernel puts to work on tiles of bn columns:
 // clusters for the cluster split, two K halves per tile when they all fit,
 // else one CTA per tile up to the SM count (as launch_t below decides).
@@ -607,8 +614,7 @@ int64_t working_ctas(int64_t M, int64_t N, int64_t K, float* C, int64_t ldc, int
   const TcParams q = make_params(M, N, K, Cfg<KIND>::BM, bn, Cfg<KIND>::BK, C, ldc, ctl);
   const int S = cluster_split_size<KIND>(q, cfg, ctl);
   if (S > 1) return q.num_tiles * S;
-  if (2 * q.num_tiles <= ctl.sm_count && q.num_kb >= (after_prepass ? 4 : 32))
-    return 2 * q.num_tiles;
+  if (k_halves_chosen(q, after_prepass, ctl)) return 2 * q.num_tiles;
   return q.num_tiles < ctl.sm_count ? q.num_tiles : ctl.sm_count;
 }
 
@@ -681,7 +687,7 @@ cudaError_t launch_t(const TcMaps& mp, float* C, int64_t M, int64_t N, int64_t K
   // whole calls: 3xTF32 1024 x 1024 x 4096 95.9 -> 63.1 us, 1024^3 31.4 ->
   // 24.2, 256^3 15.0 -> 14.0; bf16 1024^3 (16 K-steps) 15.0 either way, 256^3
   // (4) 10.9 -> 13.0.
-  if (2 * p.num_tiles <= ctl.sm_count && p.num_kb >= (after_prepass ? 4 : 32)) {
+  if (k_halves_chosen(p, after_prepass, ctl)) {
     p.full_units = 0;
     p.num_units = 2 * p.num_tiles;
     p.kb_mid = p.num_kb / 2;
