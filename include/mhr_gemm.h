@@ -75,10 +75,12 @@ typedef enum mhr_status {
  * double-buffered shared-memory ring, each thread accumulating an 8 x 8
  * register block ("矩阵乘法 tiling", sections 四 and 五: thread coarsening,
  * accumulator in registers; "CUDA 编程系列之三", section 6: register tiling).
- * Aligned problems whose sizes are multiples of 128 x 256 x 8 and that fill
- * the SMs use 128 x 256 tiles with 8 x 16 register blocks; problems with few
- * tiles give each tile a cluster of CTAs that split K and sum their partial
- * tiles in distributed shared memory.  Every output is summed in one fixed
+ * Aligned problems whose sizes are multiples of 128 x 256 x 8 use 128 x 256
+ * tiles with 8 x 16 register blocks where that shortens the deepest queue of
+ * blocks on one SM; problems with few tiles give each tile a cluster of CTAs
+ * that split K and sum their partial tiles in distributed shared memory.
+ * Loads of B and stores of C are as wide as their alignment allows (16, 8
+ * or 4 bytes).  Every output is summed in one fixed
  * order per shape: results are bitwise repeatable.  Any alignment and any
  * leading dimension are accepted.
  */
