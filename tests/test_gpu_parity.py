@@ -418,17 +418,17 @@ def test_single_cta_tile_widths(mhr, bn):
                          ids=["3xtf32-128", "3xtf32-64", "bf16-256", "bf16-128"])
 def test_single_cta_few_tiles(mhr, path, width):
     """Few tiles on the single-CTA kernel. With long K runs (at least 16
-    K-blocks per rank) it runs a cluster of 8 or 4 CTAs per tile, each on one
-    run of K-blocks, and sums the partial tiles through distributed shared
-    memory in rank order. Otherwise, when the halves of all tiles fit on the
+    K-blocks per rank) it runs a cluster of 4 to 8 CTAs per tile (16 for
+    3xTF32 where they fit), each on one run of K-blocks, and sums the
+    partial tiles through distributed shared memory in rank order. Otherwise, when the halves of all tiles fit on the
     SMs at once (and, without a pre-pass to overlap the zeroing, K has at
     least 32 steps), every tile becomes two K halves reduce-added into a
     zeroed C. Cases: 4 tiles with 129-130 K-blocks (cluster of 8; of 16 for
     3xTF32, whose ranks then run 9 K-blocks, and 10 such tiles in clusters of
     8) and 65-66 (cluster of 4, ragged runs), half the SM count in tiles (K
     halves) and one more (no split); K ragged throughout. 3xTF32 at 128 and
-    64 columns, bf16 at 256 and 128 (forced). Integer inputs bit-exact against the
-    oracle through vector and scalar stores (ldc odd), real inputs within
+    64 columns, bf16 at 256 and 128 (forced). Integer inputs bit-exact
+    against the oracle through vector and scalar stores (ldc odd), real inputs within
     tolerance and bitwise repeatable."""
     import torch
 
