@@ -4,7 +4,8 @@ Sixty cases with dimensions anywhere in 1..700, sixty with every dimension at
 or next to a tile boundary (1, 8, 16, ..., 512, each +-1), twenty-four drawn
 onto the schedules that split or widen tiles, and twenty-four small aligned
 problems in the automatic mode (one launch with the split inside, at the tile
-width it picks). Each draws a path variant (SIMT fp32; 3xTF32 in the automatic
+width it picks); and sixty-four larger ones on the host's tiling choices
+(tiling_choice_cases), checked on sampled entries. Each draws a path variant (SIMT fp32; 3xTF32 in the automatic
 mode, on the single-CTA kernel, on the CTA-pair kernel with the split
 pre-pass, and with the split on chip; bf16 on either kernel), a shape,
 padded leading dimensions (0 to 9 extra elements), an element offset that
@@ -15,7 +16,7 @@ import numpy as np
 import pytest
 
 import oracle
-from parity_util import TOL, DeviceCall, normalised_error, operands
+from parity_util import TOL, DeviceCall, normalised_error, operands, sample_indices
 
 pytestmark = pytest.mark.gpu
 
@@ -152,3 +153,67 @@ def test_random_case(mhr, case):
     else:
         Cref, S = oracle.gemm(A, B, with_abs=True)
         assert normalised_error(C, Cref, S) <= TOL[path], case
+
+
+def tiling_choice_cases(n=64, seed=20261207):
+    """Shapes on the host's tiling choices, in the automatic mode of each:
+    bf16 on the single-CTA kernel (256- or 128-column tiles, clusters of 4 to
+    8 CTAs, K halves) or the pair kernel; 3xTF32 after the split pre-pass on
+    the single-CTA kernel with long K (clusters of up to 16); SIMT fp32 with
+    even pitches or 8-byte offsets (8-byte loads of B and stores of C); and
+    SIMT on aligned 128 x 256 x 8 multiples, automatic or with the wide
+    kernel forced."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        kind = i % 4
+        pads = [int(x) for x in rng.integers(0, 10, 3)]
+        offset = int(rng.choice([0, 0, 1, 2]))
+        if kind == 0:
+            v = ("bf16", 0, 0)
+            M, N = (int(x) for x in rng.integers(64, 1600, 2))
+            K = int(rng.integers(256, 9000))
+        elif kind == 1:
+            v = ("3xtf32", 1, 1)
+            M, N = (int(x) for x in rng.integers(32, 1100, 2))
+            K = int(rng.integers(1024, 9000))
+        elif kind == 2:
+            v = ("f32", 0, 0)
+            M, N, K = (int(x) for x in rng.integers(1, 1400, 3))
+            pads = [2 * int(x) for x in rng.integers(0, 4, 3)]
+        else:
+            v = ("f32", int(rng.choice([0, 2])), 0)
+            M, N = 128 * int(rng.integers(1, 20)), 256 * int(rng.integers(1, 10))
+            K = 8 * int(rng.integers(1, 200))
+            pads = [4 * int(x) for x in rng.integers(0, 3, 3)]
+            offset = 0
+        dist = "int" if rng.random() < 0.5 else "normal"
+        out.append((v, M, N, K, pads, offset, dist, 15000 + i))
+    return out
+
+
+@pytest.mark.parametrize("case", tiling_choice_cases(),
+                         ids=lambda c: f"{c[0][0]}-{c[0][1]}{c[0][2]}-{c[1]}x{c[2]}x{c[3]}-{c[6]}")
+def test_tiling_choice_case(mhr, case):
+    """As test_random_case, at sizes where the oracle is taken on sampled
+    entries (2048 random ones plus the first and last rows and columns):
+    integer inputs bit-exact, real ones within the path's tolerance."""
+    (path, mode, split_mode), M, N, K, pads, offset, dist, seed = case
+    A, B, Ab, Bb = operands(M, N, K, seed, dist, path)
+    simt = path == "f32"
+    old_pair = mhr.gemm_testing_set_cta_pair_mode(0 if simt else mode)
+    old_wide = mhr.gemm_testing_set_simt_wide_mode(mode if simt else 0)
+    old_split = mhr.gemm_testing_set_split_mode(split_mode)
+    try:
+        C = DeviceCall(path, A, B, Ab, Bb, lda=K + pads[0], ldb=N + pads[1], ldc=N + pads[2],
+                       offset=offset).run(mhr).result()
+    finally:
+        mhr.gemm_testing_set_split_mode(old_split)
+        mhr.gemm_testing_set_simt_wide_mode(old_wide)
+        mhr.gemm_testing_set_cta_pair_mode(old_pair)
+    r, c = sample_indices(M, N, seed, n_random=2048, rows=(0, M - 1), cols=(0, N - 1))
+    ref, S = oracle.gemm_entries(A, B, r, c, M, N, K)
+    if dist == "int":
+        assert np.array_equal(C[r, c], ref), case
+    else:
+        assert normalised_error(C[r, c], ref, S) <= TOL[path], case
